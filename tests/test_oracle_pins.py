@@ -1,0 +1,329 @@
+"""Pins for the CPU oracle: checks against things other than the oracle itself.
+
+Each check ties the oracle to an independent fact: torch's float8_e4m3fn cast,
+exact integer arithmetic, a numpy matmul formulation, closed forms, the
+pages' printed rule for UE8M0 scales, a hand-worked example, brute force over
+subsets, and invariances of the definition.  `test_oracle_mutations.py` shows
+that planted mistakes in the oracle fail these pins.
+"""
+import itertools
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+# ----------------------------------------------------------------------------
+# independent helpers (torch decode, numpy fp64 formulation)
+
+def torch_decode_e4m3(codes: np.ndarray) -> np.ndarray:
+    t = torch.from_numpy(np.ascontiguousarray(codes, dtype=np.uint8)).view(torch.float8_e4m3fn)
+    return t.to(torch.float64).numpy()
+
+
+def numpy_scores(p, rows=None):
+    """Scores from a different formulation: torch decode, fp64 matmul for all
+    heads at once, relu(s) = (s + |s|)/2, scale from 2**(e-127) via ldexp."""
+    rows = np.arange(p.rows) if rows is None else np.asarray(rows)
+    kd = torch_decode_e4m3(p.k)                       # [N, D]
+    e = p.scales_ue8m0[:, 0].astype(np.int64)
+    scale = np.ldexp(1.0, e - 127)
+    out = np.full((len(rows), p.keys), -np.inf)
+    for i, r in enumerate(rows):
+        qd = torch_decode_e4m3(p.q[r])               # [H, D]
+        s = qd @ kd.T                                 # [H, N], exact
+        relu = 0.5 * (s + np.abs(s))
+        val = scale * (p.weights[r].astype(np.float64) @ relu)
+        lo, hi = int(p.starts[r]), int(p.ends[r])
+        if hi > lo:
+            out[i, lo:hi] = val[lo:hi]
+    return out
+
+
+def tiny_problem(seed, rows, keys, topk, heads=synth.HEADS, dim=synth.HEAD_DIM):
+    return synth.random_small(seed, rows, keys, topk, heads=heads, dim=dim)
+
+
+def check_topk_against_scores(idx_row, scores_row, start, end, topk):
+    """idx_row must hold c = min(topk, n) distinct in-range relative indices,
+    then -1s, and every selected score must be >= every unselected score."""
+    n = max(0, end - start)
+    c = min(topk, n)
+    assert np.all(idx_row[c:] == -1)
+    sel = idx_row[:c]
+    assert np.all((sel >= 0) & (sel < n))
+    assert len(np.unique(sel)) == c
+    if c and c < n:
+        vis = scores_row[start:end]
+        mask = np.zeros(n, bool)
+        mask[sel] = True
+        assert vis[mask].min() >= vis[~mask].max()
+
+
+# ----------------------------------------------------------------------------
+# e4m3 table
+
+def test_e4m3_table_matches_torch_cast(lib=None):
+    tab = oracle.e4m3_table(lib=lib)
+    ref = torch_decode_e4m3(np.arange(256, dtype=np.uint8))
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(tab), nan)
+    assert set(np.nonzero(nan)[0].tolist()) == {0x7F, 0xFF}
+    assert np.array_equal(tab[~nan], ref[~nan])
+
+
+def test_e4m3_table_landmarks(lib=None):
+    tab = oracle.e4m3_table(lib=lib)
+    assert tab[0x7E] == 448.0 and tab[0xFE] == -448.0
+    assert tab[0x01] == 2.0 ** -9          # smallest subnormal
+    assert tab[0x08] == 2.0 ** -6          # smallest normal
+    assert tab[0x38] == 1.0
+    pos = tab[0x00:0x7F]
+    assert np.all(np.diff(pos) > 0)        # code order is value order
+    assert np.all(np.isclose(tab[0x80:0xFF], -tab[0x00:0x7F]) | (tab[0x80:0xFF] == 0))
+
+
+def test_quantizer_matches_torch_rne(lib=None):
+    rng = np.random.default_rng(5)
+    x = np.concatenate([rng.standard_normal(200000).astype(np.float32) * 4,
+                        rng.standard_normal(20000).astype(np.float32) * 1e-3,
+                        np.float32([0.0, -0.0, 448.0, -448.0, 2 ** -9, 2 ** -10, 3 * 2 ** -10,
+                                    1.0625, 1.1875, 300.0, 440.0])])
+    mine = synth.quantize_e4m3fn(x)
+    ref = torch.from_numpy(x).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(torch_decode_e4m3(mine), torch_decode_e4m3(ref))
+
+
+def test_quantizer_saturates(lib=None):
+    codes = synth.quantize_e4m3fn(np.float32([500.0, -1e4, 449.0]))
+    assert codes.tolist() == [0x7E, 0xFE, 0x7E]
+
+
+# ----------------------------------------------------------------------------
+# UE8M0
+
+def test_ue8m0_all_exponents_closed_form(lib=None):
+    e = np.arange(256, dtype=np.uint8)
+    got = oracle.ue8m0_decode(synth.ue8m0_bytes(e), lib=lib)
+    for ei in range(256):
+        if ei == 0:
+            want = 0.0
+        elif ei == 255:
+            want = math.inf
+        else:
+            want = math.ldexp(1.0, ei - 127)
+        assert got[ei] == np.float32(want), ei
+    # the bit-pattern rule for the whole range
+    assert np.array_equal(got.view(np.uint32), e.astype(np.uint32) << 23)
+
+
+def test_ue8m0_golden_examples(lib=None):
+    rows = [ln.split() for ln in open(os.path.join(GOLDEN, "ue8m0_examples.txt"))
+            if ln.strip() and not ln.startswith("#")]
+    e = np.array([int(r[0]) for r in rows], np.uint8)
+    got = oracle.ue8m0_decode(synth.ue8m0_bytes(e), lib=lib)
+    for (es, val, bits), g in zip(rows, got):
+        assert g == np.float32(float(val))
+        assert int(np.float32(g).view(np.uint32)) == int(bits, 16)
+
+
+# ----------------------------------------------------------------------------
+# exact dot products (integer brute force)
+
+def test_head_dots_exact_integer_bruteforce(lib=None):
+    p = tiny_problem(11, 3, 40, 8)
+    # every e4m3 value times 2^9 is an integer
+    qi = np.rint(torch_decode_e4m3(p.q) * 512).astype(np.int64)
+    ki = np.rint(torch_decode_e4m3(p.k) * 512).astype(np.int64)
+    assert np.array_equal(qi / 512.0, torch_decode_e4m3(p.q))
+    for r in range(p.rows):
+        for j in (0, 7, 39):
+            want = [sum(int(a) * int(b) for a, b in zip(qi[r, h], ki[j])) for h in range(p.heads)]
+            got = oracle.head_dots(p.q, p.k, r, j, lib=lib)
+            assert [int(v) for v in np.rint(np.ldexp(got, 18))] == want
+            assert np.array_equal(np.ldexp(np.array(want, dtype=np.float64), -18), got)
+
+
+def test_head_dots_extreme_codes_exact(lib=None):
+    # +-448 everywhere: 128 * 448^2 = 25690112 exactly
+    q = np.full((1, 2, 128), 0x7E, np.uint8)
+    q[0, 1] = 0xFE
+    k = np.full((1, 128), 0x7E, np.uint8)
+    got = oracle.head_dots(q, k, 0, 0, lib=lib)
+    assert got.tolist() == [128 * 448.0 ** 2, -128 * 448.0 ** 2]
+
+
+# ----------------------------------------------------------------------------
+# scores: independent formulation
+
+@pytest.mark.parametrize("seed", [1, 2])
+def test_scores_match_numpy_formulation(seed, lib=None):
+    p = tiny_problem(seed, 12, 700, 64)
+    _, s = oracle.run(p, want_topk=False, want_scores=True, lib=lib)
+    ref = numpy_scores(p)
+    assert np.array_equal(np.isinf(s), np.isinf(ref))
+    fin = np.isfinite(ref)
+    rowmax = np.max(np.where(fin, np.abs(ref), 0), axis=1, keepdims=True) + 1e-300
+    diff = np.abs(np.where(fin, s, 0.0) - np.where(fin, ref, 0.0))
+    assert np.all(diff <= 1e-12 * rowmax)
+
+
+def test_hand_example_golden(lib=None):
+    vals = {}
+    for ln in open(os.path.join(GOLDEN, "hand_example.txt")):
+        if ln.strip() and not ln.startswith("#"):
+            parts = ln.split()
+            vals[parts[0]] = parts[1:]
+    q = np.array([int(x, 16) for x in vals["q"]], np.uint8).reshape(1, 2, 2)
+    k = np.array([int(x, 16) for x in vals["k"]], np.uint8).reshape(5, 2)
+    w = np.array([float(x) for x in vals["w"]], np.float32).reshape(1, 2)
+    e = np.array([int(x) for x in vals["e"]], np.uint8)
+    s0, e0 = (int(x) for x in vals["range"])
+    tk = int(vals["topk"][0])
+    p = synth.Problem("hand", q, k, synth.ue8m0_bytes(e), w, np.int32([s0]), np.int32([e0]), tk)
+    idx, sc = oracle.run(p, want_scores=True, lib=lib)
+    assert sc[0, s0:e0].tolist() == [float(x) for x in vals["scores"]]
+    assert np.isneginf(sc[0, 0])
+    assert idx[0].tolist() == [int(x) for x in vals["expected"]]
+
+
+# ----------------------------------------------------------------------------
+# special case that reduces to a library routine: one head, positive weight
+
+def test_single_head_reduces_to_gemv_topk(lib=None):
+    p = tiny_problem(21, 6, 3000, 100)
+    p.weights[:] = 0
+    p.weights[:, 5] = 1.0
+    p.starts[:] = 0
+    p.ends[:] = p.keys
+    p.scales_ue8m0[:] = 127  # unit scales
+    idx = oracle.topk(p, lib=lib)
+    kd = torch_decode_e4m3(p.k)
+    for r in range(p.rows):
+        g = torch_decode_e4m3(p.q[r, 5]) @ kd.T
+        g = np.maximum(g, 0)
+        part = np.argpartition(-g, p.topk - 1)[: p.topk]
+        kth = np.sort(g)[::-1][p.topk - 1]
+        # same multiset of selected values; sets agree off the kth value
+        assert np.array_equal(np.sort(g[idx[r]]), np.sort(g[part]))
+        assert set(idx[r][g[idx[r]] > kth]) == set(part[g[part] > kth])
+
+
+# ----------------------------------------------------------------------------
+# brute force over subsets on tiny rows
+
+def test_bruteforce_subsets_tiny_rows(lib=None):
+    rng = np.random.default_rng(3)
+    for trial in range(30):
+        n = int(rng.integers(1, 10))
+        keys = n + 3
+        topk = int(rng.integers(1, n + 3))
+        p = tiny_problem(100 + trial, 1, keys, topk, heads=4, dim=8)
+        p.starts[:] = 2
+        p.ends[:] = 2 + n if 2 + n <= keys else keys
+        n = int(p.ends[0] - p.starts[0])
+        idx, _ = oracle.run(p, lib=lib)
+        sc = numpy_scores(p)[0, 2:2 + n]
+        c = min(topk, n)
+        best = max(itertools.combinations(range(n), c), key=lambda s: (sum(sc[list(s)]), [-x for x in s]))
+        got = sorted(idx[0, :c].tolist())
+        assert np.isclose(sum(sc[got]), sum(sc[list(best)]), rtol=0, atol=1e-12 * (1 + np.abs(sc).sum()))
+        check_topk_against_scores(idx[0], np.concatenate([np.zeros(2), sc]), 2, 2 + n, topk)
+
+
+# ----------------------------------------------------------------------------
+# structure: padding, relative indices, short rows
+
+@pytest.mark.parametrize("n", [0, 1, 511, 512, 513, 700])
+def test_row_lengths_around_topk(n, lib=None):
+    p = tiny_problem(7, 2, 800, 512)
+    p.starts[:] = [50, 0]
+    p.ends[:] = [50 + n, n]
+    idx, sc = oracle.run(p, want_scores=True, lib=lib)
+    for r in range(2):
+        check_topk_against_scores(idx[r], sc[r], int(p.starts[r]), int(p.ends[r]), 512)
+        if n <= 512:
+            assert sorted(idx[r, :n].tolist()) == list(range(n))
+
+
+def test_reversed_range_is_empty(lib=None):
+    p = tiny_problem(8, 1, 100, 16)
+    p.starts[:] = 60
+    p.ends[:] = 20
+    idx = oracle.topk(p, lib=lib)
+    assert np.all(idx == -1)
+
+
+def test_out_of_range_rejected(lib=None):
+    p = tiny_problem(9, 1, 100, 16)
+    p.starts[:] = 10
+    p.ends[:] = 101
+    with pytest.raises(ValueError):
+        oracle.topk(p, lib=lib)
+
+
+# ----------------------------------------------------------------------------
+# invariances of the definition
+
+def test_invariant_key_permutation_in_window(lib=None):
+    p = tiny_problem(31, 4, 900, 64)
+    p.starts[:] = 100
+    p.ends[:] = 800
+    base = oracle.topk(p, lib=lib)
+    rng = np.random.default_rng(0)
+    perm = rng.permutation(700)
+    p2 = synth.Problem("perm", p.q, p.k.copy(), p.scales_ue8m0.copy(), p.weights, p.starts, p.ends, p.topk)
+    p2.k[100:800] = p.k[100:800][perm]
+    p2.scales_ue8m0[100:800] = p.scales_ue8m0[100:800][perm]
+    got = oracle.topk(p2, lib=lib)
+    inv = np.argsort(perm)  # new position of old key t is inv[t]
+    for r in range(p.rows):
+        assert set(got[r].tolist()) == set(inv[base[r]].tolist())
+
+
+def test_invariant_power_of_two_scale(lib=None):
+    p = tiny_problem(32, 3, 600, 50)
+    _, s = oracle.run(p, want_scores=True, lib=lib)
+    p2 = synth.Problem("x2", p.q, p.k, p.scales_ue8m0 + 3, p.weights, p.starts, p.ends, p.topk)
+    idx2, s2 = oracle.run(p2, want_scores=True, lib=lib)
+    assert np.array_equal(s2, s * 8.0)
+    assert np.array_equal(idx2, oracle.topk(p, lib=lib))
+
+
+def test_invariant_shift_with_prepended_keys(lib=None):
+    p = tiny_problem(33, 3, 500, 40)
+    base = oracle.topk(p, lib=lib)
+    pad = 77
+    k2 = np.concatenate([np.full((pad, p.dim), 0x38, np.uint8), p.k])
+    g2 = np.concatenate([np.full((pad, 4), 127, np.uint8), p.scales_ue8m0])
+    p2 = synth.Problem("shift", p.q, k2, g2, p.weights, p.starts + pad, p.ends + pad, p.topk)
+    assert np.array_equal(oracle.topk(p2, lib=lib), base)
+
+
+def test_tiny_config_structure(lib=None):
+    p = synth.make("tiny_64x4096_k512")
+    idx, sc = oracle.run(p, want_scores=True, lib=lib)
+    for r in range(p.rows):
+        check_topk_against_scores(idx[r], sc[r], int(p.starts[r]), int(p.ends[r]), p.topk)
+
+
+def test_dense_budget_table_golden(lib=None):
+    """The dense baseline's chunking rule (rows per call = 2**27 / keys under a
+    512 MiB fp32 budget) and byte model reproduce the pages' table."""
+    from sparse_attention_indexer_relu_gb300 import plan
+    for ln in open(os.path.join(GOLDEN, "dense_logits_budget.txt")):
+        if not ln.strip() or ln.startswith("#"):
+            continue
+        keys, gib, calls, traffic = ln.split()
+        keys = int(keys)
+        assert plan.dense_logits_bytes(16384, keys) == int(gib) * 2 ** 30
+        assert plan.dense_logits_traffic_bytes(16384, keys) == int(traffic) * 2 ** 30
+        if calls != "-":
+            assert plan.dense_calls(16384, keys, 512 * 2 ** 20) == int(calls)
