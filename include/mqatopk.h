@@ -1,0 +1,161 @@
+/*
+ * mqatopk: fused FP8 MQA-logits + per-row top-k key selection for the prefill
+ * path of a sparse-attention indexer, for one GB300 GPU (sm_103a).
+ *
+ * Operation (vLLM API page `vllm.model_executor.kernels.attention.dsa.
+ * fused_mqa_topk`, `fused_mqa_topk_prefill` docstring; relu form of the score
+ * from vLLM pull request #60618, "What this PR does"): for every query row r
+ * and every key j in the row's visible range [starts[r], ends[r]),
+ *
+ *     s(r, j) = key_scales[j] * sum_{h<32} weights[r,h] * relu(q[r,h,:] . k[j,:])
+ *
+ * with q and k in FP8 e4m3fn (OCP "fn" flavour: bias 7, max 448, no inf) and
+ * head dimension 128.  out[r, :] receives the indices of the row's top-k keys
+ * relative to starts[r] (key - start), in no particular order, followed by -1
+ * when fewer than k keys are visible.  Ties at the k-th score may be broken
+ * either way.  The [rows, keys] logits matrix is never materialised.
+ *
+ * Conventions shared by every entry point
+ *  - All tensors are dense, contiguous, row-major, and live in DEVICE memory
+ *    of the current CUDA device unless stated otherwise.  The caller owns every
+ *    buffer, the workspace and the stream; the library never allocates device
+ *    memory and never synchronises a stream except in mqa_topk_get_status.
+ *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
+ *    Work is enqueued asynchronously on it.
+ *  - Return value: MQA_OK (0) or an MQA_ERR_* code.  Argument errors are
+ *    detected on the host before any work is enqueued.  Nothing throws.
+ *  - q, k, key_scales, weights, out (and logits) must be 16-byte aligned;
+ *    starts/ends 4-byte aligned.
+ *  - A row whose range is empty or reversed (end <= start) sees no key: its
+ *    output is all -1.  A non-empty range that leaves [0, keys) is clamped to
+ *    it on the device and MQA_DEV_RANGE_CLAMPED is recorded in the workspace
+ *    status word (fused path) or the dense path's status word.
+ */
+#ifndef MQATOPK_H_
+#define MQATOPK_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MQA_HEADS 32
+#define MQA_HEAD_DIM 128
+#define MQA_MAX_KEYS (1 << 24)
+
+/* Return codes. */
+#define MQA_OK 0
+#define MQA_ERR_INVALID_ARGUMENT 1 /* null pointer, bad size, bad topk */
+#define MQA_ERR_MISALIGNED 2       /* a pointer breaks the alignment rule */
+#define MQA_ERR_WORKSPACE_TOO_SMALL 3
+#define MQA_ERR_UNSUPPORTED_DEVICE 4 /* not a compute capability 10.3 device */
+#define MQA_ERR_CUDA 5               /* a CUDA runtime/driver call failed */
+#define MQA_ERR_NO_DEVICE 6          /* no CUDA device is visible */
+
+/* Device-side status bits (read with mqa_topk_get_status). */
+#define MQA_DEV_RANGE_CLAMPED 1 /* some row's range left [0, keys) */
+#define MQA_DEV_WAIT_TIMEOUT 2  /* a bounded wait expired: outputs are undefined */
+#define MQA_DEV_INTERNAL 4
+
+/* Per-call counters kept in the fused workspace (indices into `stats`). */
+#define MQA_STAT_STATUS 0
+#define MQA_STAT_ROWS_RESCANNED 1 /* rows recomputed by the exact rescan */
+#define MQA_STAT_COMPACTIONS 2    /* exact in-place candidate compactions */
+#define MQA_STAT_CANDIDATES 3     /* candidate records written by gated scans */
+#define MQA_STAT_GATED_ROWS 4     /* rows scanned behind a sampled gate */
+#define MQA_STAT_BLOCKS_DONE 5    /* 8-row blocks finished (scans + rescans) */
+#define MQA_STAT_SAMPLE_TILES 6   /* 128-key tiles scored for gate sampling */
+#define MQA_STAT_OVERFLOW_ROWS 7  /* gated rows whose candidates overflowed */
+#define MQA_STAT_UNDERFILL_ROWS 8 /* gated rows left with fewer than top-k */
+#define MQA_STATS_COUNT 9
+
+/* Test-only knobs for mqa_topk_prefill_debug.  Zero-initialise for defaults. */
+typedef struct mqa_topk_debug_options {
+  int force_gate;      /* 0: sampled gate; 1: gate at +inf (every non-empty row
+                          under-fills and is rescanned); 2: no gate (rows longer
+                          than the slab overflow and are rescanned) */
+  int slab_capacity;   /* candidate records per row; 0 = default (16384).  Must
+                          be >= topk + 256 and not above the capacity the
+                          workspace was sized for. */
+  int stall;           /* nonzero: the producer first waits on a barrier that
+                          nothing completes; the time limit ends the wait, the
+                          kernel unwinds and MQA_DEV_WAIT_TIMEOUT is recorded */
+  int wait_timeout_ms; /* bound on every device-side wait; 0 = default (4000) */
+  int max_ctas;        /* persistent CTAs; 0 = one per SM */
+} mqa_topk_debug_options;
+
+/* Bytes of workspace one mqa_topk_prefill call over `rows` rows needs on
+ * `device` (a CUDA device ordinal).  The size depends on the device's SM count
+ * and on min(rows, ...), not on keys: one persistent CTA per SM, two slabs of
+ * 8 rows x 16384 candidate records (8 B each) per CTA, plus a 256-byte header
+ * (workspace layout: pull request #60618, sections "Memory" and the workspace
+ * list of `get_fused_mqa_topk_workspaces` on the API page).
+ * Returns MQA_ERR_NO_DEVICE / MQA_ERR_CUDA when the device cannot be queried. */
+int mqa_topk_workspace_bytes(int device, int rows, size_t *bytes);
+
+/* Fused top-k prefill selection (the operation above), one kernel launch.
+ *  q          [rows, 32, 128] uint8 e4m3fn codes
+ *  k          [keys, 128] uint8 e4m3fn codes
+ *  key_scales [keys] fp32 (see mqa_ue8m0_decode)
+ *  weights    [rows, 32] fp32
+ *  starts, ends [rows] int32
+ *  out        [rows, topk] int32 (written)
+ *  rows >= 0 (0 is a no-op), 1 <= keys <= MQA_MAX_KEYS, topk in {512, 1024, 2048}
+ *  workspace  device buffer of at least mqa_topk_workspace_bytes(dev, rows)
+ *             bytes, 256-byte aligned; its header is reset on `stream` by
+ *             every call, so it may be reused by consecutive calls on one
+ *             stream but not by calls that overlap in time.
+ * The result is exact up to ties at the k-th score: a sampled per-row gate
+ * filters candidates, and any row the gate cannot serve (too many or too few
+ * candidates) is rescanned exactly. */
+int mqa_topk_prefill(const void *q, const void *k, const float *key_scales, const float *weights,
+                     const int32_t *starts, const int32_t *ends, int32_t *out, int rows, int keys, int topk,
+                     void *workspace, size_t workspace_bytes, void *stream);
+
+/* mqa_topk_prefill with test-only knobs (opt may be NULL). */
+int mqa_topk_prefill_debug(const void *q, const void *k, const float *key_scales, const float *weights,
+                           const int32_t *starts, const int32_t *ends, int32_t *out, int rows, int keys,
+                           int topk, void *workspace, size_t workspace_bytes, void *stream,
+                           const mqa_topk_debug_options *opt);
+
+/* UE8M0 -> fp32 key-scale decode (API page, `fused_mqa_topk_key_scales`
+ * docstring): scales is [keys, 4] uint8 whose first byte per key is the
+ * exponent e; out[j] is the fp32 with bit pattern e << 23 (2^(e-127) for
+ * 1 <= e <= 254).  keys >= 0. */
+int mqa_ue8m0_decode(const uint8_t *scales, float *out, int keys, void *stream);
+
+/* Debug: the scores themselves.  logits is [rows, keys] fp32, row-major;
+ * s(r, j) for keys in [starts[r], ends[r]) and -inf elsewhere.  Same inputs
+ * and limits as mqa_topk_prefill (topk unused); computed by the same tensor-
+ * core pipeline and score arithmetic as the fused path.  Needs no workspace
+ * beyond a 256-byte device header passed as `workspace` (counters/status). */
+int mqa_logits_debug(const void *q, const void *k, const float *key_scales, const float *weights,
+                     const int32_t *starts, const int32_t *ends, float *logits, int rows, int keys,
+                     void *workspace, size_t workspace_bytes, void *stream);
+
+/* Comparison baseline (dense path): materialise fp32 logits for as many rows
+ * as fit in logits_ws (logits_budget_bytes / (keys * 4) rows per call, as the
+ * dense path chunks under its logits budget in pull request #60618,
+ * "Motivation"), then select each row's top-k from them.  Same inputs and
+ * output convention as mqa_topk_prefill; `workspace` is a 256-byte header as
+ * for mqa_logits_debug.  logits_budget_bytes must hold at least one row. */
+int mqa_topk_dense_baseline(const void *q, const void *k, const float *key_scales, const float *weights,
+                            const int32_t *starts, const int32_t *ends, int32_t *out, int rows, int keys,
+                            int topk, void *logits_ws, size_t logits_budget_bytes, void *workspace,
+                            size_t workspace_bytes, void *stream);
+
+/* Read the status word and counters of the last call that used `workspace`.
+ * Synchronises `stream`.  status (host) receives the MQA_DEV_* bits; stats
+ * (host, nullable) receives MQA_STATS_COUNT int32 counters. */
+int mqa_topk_get_status(const void *workspace, int32_t *status, int32_t *stats, void *stream);
+
+/* Static description of a return code. */
+const char *mqa_topk_strerror(int code);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MQATOPK_H_ */

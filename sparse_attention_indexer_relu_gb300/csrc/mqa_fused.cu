@@ -1,0 +1,932 @@
+// Fused FP8 MQA-logits + per-row top-k for sm_103a (one persistent CTA per SM).
+//
+// What it computes (vLLM API page `vllm.model_executor.kernels.attention.dsa.
+// fused_mqa_topk`, `fused_mqa_topk_prefill` docstring; vLLM pull request
+// #60618, "What this PR does"): for each query row r and visible key j in
+// [start_r, end_r),
+//     s(r, j) = scale_j * sum_h w[r,h] * relu(q[r,h,:] . k[j,:])
+// with 32 heads of dimension 128 in FP8 e4m3, and the row's top-k keys as
+// indices relative to start_r (unordered, -1 padded).  The [rows, keys]
+// logits matrix never reaches HBM.  A second instantiation of the same
+// pipeline writes the logits instead (debug entry and dense baseline).
+//
+// CTA layout (512 threads):
+//   warp 0      producer: claims row blocks heaviest first, loads q (TMA) and
+//               per-row ranges/weights, streams 128-key K tiles (TMA) through a
+//               6-stage ring.
+//   warp 1      MMA issuer: per K tile, 4 x tcgen05.mma kind::f8f6f4
+//               (M = 128 keys, N = 8 rows x 32 heads, K = 32) into one of two
+//               256-column TMEM accumulators.
+//   warps 4-11  epilogue: TMEM -> registers (one key per thread), relu-weighted
+//               head sum, key scale, range mask; sampled gate; candidate
+//               emission to the block's slab; exact compaction on rescans.
+//   warps 12-15 selection: per finished block, exact radix top-k over each
+//               row's candidates, output write or rescan request.
+// Every wait is bounded by a time limit; on expiry the kernel records
+// MQA_DEV_WAIT_TIMEOUT in the workspace status word and unwinds.
+#include "mqa_internal.h"
+#include "ptx.cuh"
+
+#include <cfloat>
+#include <climits>
+
+namespace mqa {
+
+constexpr uint32_t kIdesc = idesc_f8_e4m3_f32(kTileKeys, kCols);
+constexpr int kEpiThreads = kEpiWarps * 32;
+constexpr int kEpiBarrier = 1;  // named barrier id for the epilogue warps
+
+struct JobInfo {
+  int block;      // row block (-1: no more work)
+  int mode;       // 0 gated scan, 1 exact rescan
+  int lo_t, nt;   // main tiles [lo_t, lo_t + nt)
+  int ns;         // sample tiles scored before the main tiles
+  uint32_t mask;  // rows taking part
+  int nrows;      // valid rows in the block
+  int pad;
+  int start[kBlockRows], end[kBlockRows];
+  alignas(16) float w[kBlockRows][kHeads];
+};
+
+struct SelSlot {  // what the selection warps need from a finished scan
+  int block, mode;
+  uint32_t mask;
+  int nrows;
+  int start[kBlockRows], n[kBlockRows], cnt[kBlockRows];
+  int gated[kBlockRows];
+};
+
+struct Smem {
+  alignas(1024) uint8_t kring[kKStages][kKTileBytes];
+  alignas(1024) uint8_t q[2][kQBytes];
+  JobInfo job[2];
+  SelSlot sel[2];
+  float tau[kBlockRows];
+  int cnt[kBlockRows];
+  uint32_t ref[kBlockRows];
+  int ref_frozen[kBlockRows];
+  int msample[kBlockRows];
+  int hist[kBlockRows][256];
+  int selhist[kSelWarps][256];
+  uint16_t order[kMaxSortBlocks];
+  uint64_t k_full[kKStages], k_empty[kKStages];
+  uint64_t t_full[2], t_empty[2];
+  uint64_t j_full[2], j_empty[2];
+  uint64_t s_full[2], s_empty[2];
+  uint64_t drain, stall_bar;
+  uint32_t tmem_base;
+  int abort_flag;
+  int fifo_block[8];
+  uint32_t fifo_mask[8];
+  int fifo_head, fifo_tail;
+  int retired;
+  int seldone[2];
+  uint32_t selfail[2];
+};
+
+size_t fused_smem_bytes() { return sizeof(Smem) + 1024; }
+
+__device__ __forceinline__ Smem &get_smem(uint8_t *raw) {
+  uintptr_t a = reinterpret_cast<uintptr_t>(raw);
+  a = (a + 1023) & ~uintptr_t(1023);
+  return *reinterpret_cast<Smem *>(a);
+}
+
+// ------------------------------------------------------------------ waits
+__device__ __forceinline__ bool aborted(Smem &S) { return *(volatile int *)&S.abort_flag != 0; }
+
+__device__ __noinline__ void raise_timeout(Smem &S, const FusedParams &p) {
+  *(volatile int *)&S.abort_flag = 1;
+  atomicOr(p.ws + kWsStatus, kDevWaitTimeout);
+}
+
+// Wait for the phase of `bar` with the given parity; false on abort/timeout.
+__device__ __forceinline__ bool wait_bar(Smem &S, uint64_t *bar, uint32_t parity, const FusedParams &p) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (;;) {
+    if (aborted(S)) return false;
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((long long)(globaltimer_ns() - t0) > p.timeout_ns) {
+      raise_timeout(S, p);
+      return false;
+    }
+  }
+}
+
+// Spin until *flag >= target (smem, written by another warp); false on abort/timeout.
+__device__ __forceinline__ bool wait_counter(Smem &S, int *flag, int target, const FusedParams &p) {
+  const uint64_t t0 = globaltimer_ns();
+  for (;;) {
+    if (*(volatile int *)flag >= target) return true;
+    if (aborted(S)) return false;
+    if ((long long)(globaltimer_ns() - t0) > p.timeout_ns) {
+      raise_timeout(S, p);
+      return false;
+    }
+    __nanosleep(64);
+  }
+}
+
+// ------------------------------------------------------------------ scoring
+// s = scale * sum_h w_h * max(acc_h, 0), accumulated in two packed fp32 pairs.
+// The same routine serves the fused and the logits instantiations, so both
+// produce bit-identical scores.
+__device__ __forceinline__ float relu_weighted_sum(const uint32_t (&v)[32], const float *w, float scale) {
+  float2 a0 = make_float2(0.f, 0.f), a1 = make_float2(0.f, 0.f);
+#pragma unroll
+  for (int h = 0; h < kHeads; h += 4) {
+    const float4 wv = *reinterpret_cast<const float4 *>(w + h);
+    const float2 r0 = make_float2(fmaxf(__uint_as_float(v[h]), 0.f), fmaxf(__uint_as_float(v[h + 1]), 0.f));
+    const float2 r1 = make_float2(fmaxf(__uint_as_float(v[h + 2]), 0.f), fmaxf(__uint_as_float(v[h + 3]), 0.f));
+    a0 = __ffma2_rn(r0, make_float2(wv.x, wv.y), a0);
+    a1 = __ffma2_rn(r1, make_float2(wv.z, wv.w), a1);
+  }
+  return ((a0.x + a0.y) + (a1.x + a1.y)) * scale;
+}
+
+// ------------------------------------------------------------------ sample gate bins
+// Distance d (in order-key units) below the row's reference maximum, binned on
+// a log scale with four sub-bins per power of two: bin 0 holds d == 0.
+__device__ __forceinline__ int dist_bin(uint32_t d) {
+  if (d == 0) return 0;
+  const int msb = 31 - __clz(d);
+  const uint32_t sub = msb >= 2 ? (d >> (msb - 2)) & 3u : (d << (2 - msb)) & 3u;
+  return 1 + 4 * msb + (int)sub;
+}
+// Smallest distance beyond bin b (every d in bins 0..b is below it).
+__device__ __forceinline__ uint64_t dist_bin_hi(int b) {
+  if (b == 0) return 1;
+  const int msb = (b - 1) >> 2, sub = (b - 1) & 3;
+  if (msb >= 2) return (uint64_t)(5 + sub) << (msb - 2);
+  return (uint64_t)((4 + sub) >> (2 - msb)) + 1;
+}
+
+// ------------------------------------------------------------------ warp radix select
+// Exact k-th largest order key among keys[0, n) (requires n > k >= 1), by
+// four 8-bit digit levels.  Returns the key T; *take_eq receives how many of
+// the keys equal to T belong to the top k (the rest of the top k is > T).
+__device__ uint32_t warp_radix_select(const uint32_t *keys, int n, int k, int *hist, int lane, int *take_eq) {
+  uint32_t prefix = 0;
+  int want = k;
+#pragma unroll 1
+  for (int level = 0; level < 4; ++level) {
+    const int shift = 24 - 8 * level;
+    const uint32_t hi_mask = level == 0 ? 0u : (0xFFFFFFFFu << (shift + 8));
+    for (int b = lane; b < 256; b += 32) hist[b] = 0;
+    __syncwarp();
+#pragma unroll 1
+    for (int i0 = 0; i0 < n; i0 += 32 * 8) {
+      uint32_t kk[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const int i = i0 + 32 * j + lane;
+        kk[j] = i < n ? __ldcg(keys + i) : 0u;
+      }
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const int i = i0 + 32 * j + lane;
+        if (i < n && (kk[j] & hi_mask) == prefix) atomicAdd(&hist[(kk[j] >> shift) & 255u], 1);
+      }
+    }
+    __syncwarp();
+    int c[8], tot = 0;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      c[j] = hist[255 - 8 * lane - j];
+      tot += c[j];
+    }
+    int incl = tot;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int v = __shfl_up_sync(0xFFFFFFFFu, incl, off);
+      if (lane >= off) incl += v;
+    }
+    const int excl = incl - tot;
+    const uint32_t bm = __ballot_sync(0xFFFFFFFFu, excl < want && want <= incl);
+    const int src = bm ? __ffs(bm) - 1 : 31;
+    int bin = 0, above = 0;
+    if (lane == src) {
+      int run = excl;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        if (run + c[j] >= want) {
+          bin = 255 - 8 * lane - j;
+          above = run;
+          break;
+        }
+        run += c[j];
+      }
+    }
+    bin = __shfl_sync(0xFFFFFFFFu, bin, src);
+    above = __shfl_sync(0xFFFFFFFFu, above, src);
+    want -= above;
+    prefix |= (uint32_t)bin << shift;
+    __syncwarp();
+  }
+  *take_eq = want;
+  return prefix;
+}
+
+// Stream keys/idx[0, n) once, keeping every key > T plus the first `take_eq`
+// keys equal to T (all keys when take_all).  Kept entries either go to
+// `out` as idx - base (-1 padding up to k is written by the caller) or are
+// compacted in place (stable; writes never overtake reads).  Returns the count.
+template <bool kCompact>
+__device__ int warp_emit(uint32_t *keys, int32_t *idx, int n, uint32_t T, int take_eq, bool take_all, int32_t *out,
+                         int base, int limit, int lane) {
+  int outc = 0, eq_seen = 0;
+  const uint32_t lt = lanemask_lt();
+#pragma unroll 1
+  for (int i0 = 0; i0 < n; i0 += 32 * 4) {
+    uint32_t kk[4];
+    int32_t ii[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int i = i0 + 32 * j + lane;
+      kk[j] = i < n ? __ldcg(keys + i) : 0u;
+      ii[j] = i < n ? __ldcg(idx + i) : 0;
+    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int i = i0 + 32 * j + lane;
+      const bool v = i < n;
+      const bool gt = v && (take_all || kk[j] > T);
+      const bool eq = v && !take_all && kk[j] == T;
+      const uint32_t beq = __ballot_sync(0xFFFFFFFFu, eq);
+      const int eq_rank = eq_seen + __popc(beq & lt);
+      const bool take = gt || (eq && eq_rank < take_eq);
+      const uint32_t bt = __ballot_sync(0xFFFFFFFFu, take);
+      if (take) {
+        const int pos = outc + __popc(bt & lt);
+        if (pos >= limit) {
+        } else if (kCompact) {
+          keys[pos] = kk[j];
+          idx[pos] = ii[j];
+        } else {
+          out[pos] = ii[j] - base;
+        }
+      }
+      outc += __popc(bt);
+      eq_seen += __popc(beq);
+    }
+  }
+  return outc < limit ? outc : limit;
+}
+
+// ------------------------------------------------------------------ heaviest-first order
+__device__ void build_order(Smem &S, const FusedParams &p) {
+  const int nb = p.nblocks;
+  if (nb > kMaxSortBlocks) return;  // fall back to descending block index
+  uint64_t *key = reinterpret_cast<uint64_t *>(&S.kring[0][0]);
+  int npow = 1;
+  while (npow < nb) npow <<= 1;
+  for (int b = threadIdx.x; b < npow; b += blockDim.x) {
+    uint64_t v = 0;
+    if (b < nb) {
+      long long wsum = 0;
+      for (int r = b * kBlockRows; r < min(p.rows, (b + 1) * kBlockRows); ++r) {
+        const int s = max(__ldg(p.starts + r), 0), e = min(__ldg(p.ends + r), p.keys);
+        wsum += e > s ? e - s : 0;
+      }
+      v = ((uint64_t)wsum << 32) | (uint32_t)(0xFFFFFFFFu - (uint32_t)b);
+    }
+    key[b] = v;
+  }
+  __syncthreads();
+  for (int k = 2; k <= npow; k <<= 1) {
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      for (int i = threadIdx.x; i < npow; i += blockDim.x) {
+        const int ixj = i ^ j;
+        if (ixj > i) {
+          const uint64_t a = key[i], b = key[ixj];
+          const bool desc = (i & k) == 0;
+          if (desc ? (a < b) : (a > b)) {
+            key[i] = b;
+            key[ixj] = a;
+          }
+        }
+      }
+      __syncthreads();
+    }
+  }
+  for (int b = threadIdx.x; b < nb; b += blockDim.x) S.order[b] = (uint16_t)(0xFFFFFFFFu - (uint32_t)key[b]);
+  __syncthreads();
+}
+
+__device__ __forceinline__ int sample_tile(const JobInfo &J, int u) {
+  return J.lo_t + (int)(((long long)(2 * u + 1) * J.nt) / (2LL * J.ns));
+}
+
+// ------------------------------------------------------------------ producer (warp 0)
+template <bool kLogits>
+__device__ void producer(Smem &S, const CUtensorMap *q_map, const CUtensorMap *k_map, const FusedParams &p,
+                         int lane) {
+  const uint64_t pol_k = policy_evict_last(), pol_q = policy_evict_first();
+  const int total_jobs = kLogits ? p.nblocks * p.key_chunks : p.nblocks;
+  const int ktiles_all = (p.keys + kTileKeys - 1) / kTileKeys;
+  int job_iter = 0, kcount = 0;
+  bool exhausted = false;
+  if (p.stall) {  // debug: a wait that nothing satisfies, ended by the time limit
+    bool ok = true;
+    if (lane == 0) ok = wait_bar(S, &S.stall_bar, 0, p);
+    ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+    if (!ok) return;
+  }
+  for (;;) {
+    const int slot = job_iter & 1;
+    bool ok = true;
+    if (lane == 0) ok = wait_bar(S, &S.j_empty[slot], ((job_iter >> 1) & 1) ^ 1, p);
+    ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+    if (!ok) return;
+    int block = -1, mode = 0, chunk = 0;
+    uint32_t mask = 0xFFu;
+    if (lane == 0) {
+      if (!kLogits) {
+        const int head = *(volatile int *)&S.fifo_head;
+        if (head != *(volatile int *)&S.fifo_tail) {
+          __threadfence_block();
+          block = S.fifo_block[head & 7];
+          mask = S.fifo_mask[head & 7];
+          mode = 1;
+          *(volatile int *)&S.fifo_head = head + 1;
+        }
+      }
+      if (block < 0 && !exhausted) {
+        const int i = atomicAdd(p.ws + kWsClaim, 1);
+        if (i < total_jobs) {
+          if (kLogits) {
+            block = i / p.key_chunks;
+            chunk = i % p.key_chunks;
+          } else {
+            block = p.nblocks <= kMaxSortBlocks ? (int)S.order[i] : p.nblocks - 1 - i;
+          }
+        } else {
+          exhausted = true;
+        }
+      }
+      if (!kLogits && block < 0 && exhausted) {
+        // Every issued job must retire (selection done) before the rescan
+        // queue can be declared empty.
+        if (wait_counter(S, &S.retired, job_iter, p)) {
+          __threadfence_block();
+          const int head = *(volatile int *)&S.fifo_head;
+          if (head != *(volatile int *)&S.fifo_tail) {
+            block = S.fifo_block[head & 7];
+            mask = S.fifo_mask[head & 7];
+            mode = 1;
+            *(volatile int *)&S.fifo_head = head + 1;
+          }
+        }
+      }
+    }
+    block = __shfl_sync(0xFFFFFFFFu, block, 0);
+    mode = __shfl_sync(0xFFFFFFFFu, mode, 0);
+    mask = __shfl_sync(0xFFFFFFFFu, mask, 0);
+    chunk = __shfl_sync(0xFFFFFFFFu, chunk, 0);
+    JobInfo &J = S.job[slot];
+    int ntiles = 0;
+    if (block >= 0) {
+      const int r0 = block * kBlockRows;
+      const int nrows = min(kBlockRows, p.rows - r0);
+      // rows and ranges (lanes 0..7), weights (all lanes: head = lane)
+      int s = 0, e = 0;
+      bool part = false;
+      if (lane < kBlockRows && lane < nrows) {
+        const int gr = r0 + lane;
+        s = __ldg(p.starts + gr);
+        e = __ldg(p.ends + gr);
+        if ((s < 0 || e > p.keys) && e > s) {
+          atomicOr(p.ws + kWsStatus, kDevRangeClamped);
+          s = max(s, 0);
+          e = min(e, p.keys);
+        }
+        if (e < s) e = s;
+        part = ((mask >> lane) & 1u) != 0;
+      }
+      const uint32_t pm = __ballot_sync(0xFFFFFFFFu, part);
+      if (lane < kBlockRows) {
+        J.start[lane] = s;
+        J.end[lane] = e;
+      }
+#pragma unroll
+      for (int r = 0; r < kBlockRows; ++r)
+        J.w[r][lane] = r < nrows ? __ldg(p.weights + (size_t)(r0 + r) * kHeads + lane) : 0.f;
+      // key range: the union of the taking-part rows' ranges
+      const bool live = part && e > s;
+      int lo = live ? s : INT_MAX, hi = live ? e : 0, len = live ? e - s : 0;
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) {
+        lo = min(lo, __shfl_xor_sync(0xFFFFFFFFu, lo, off));
+        hi = max(hi, __shfl_xor_sync(0xFFFFFFFFu, hi, off));
+        len = max(len, __shfl_xor_sync(0xFFFFFFFFu, len, off));
+      }
+      int lo_t = 0, nt = 0, ns = 0;
+      if (kLogits) {
+        const int tpc = (ktiles_all + p.key_chunks - 1) / p.key_chunks;
+        lo_t = chunk * tpc;
+        nt = max(0, min(ktiles_all, lo_t + tpc) - lo_t);
+      } else if (hi > lo) {
+        lo_t = lo / kTileKeys;
+        nt = (hi + kTileKeys - 1) / kTileKeys - lo_t;
+        if (mode == 0 && p.force_gate == 0 && len > p.cap) {
+          // sample about 32 gate-passing keys per row: tiles ~ 32 * L / (target * 128)
+          const long long L = (long long)(hi - lo);
+          long long want = (32LL * L + (long long)p.gate_target * kTileKeys - 1) /
+                           ((long long)p.gate_target * kTileKeys);
+          want = want < 4 ? 4 : (want > 64 ? 64 : want);
+          ns = (int)(want < nt ? want : nt);
+        }
+      }
+      if (lane == 0) {
+        J.block = block;
+        J.mode = mode;
+        J.lo_t = lo_t;
+        J.nt = nt;
+        J.ns = ns;
+        J.mask = kLogits ? ((1u << nrows) - 1u) : pm;
+        J.nrows = nrows;
+      }
+      ntiles = ns + nt;
+    } else if (lane == 0) {
+      J.block = -1;
+    }
+    __syncwarp();
+    if (lane == 0 && block >= 0 && ntiles > 0) {
+      mbar_arrive_expect_tx(&S.j_full[slot], kQBytes);
+      tma_load_2d(&S.q[slot][0], q_map, &S.j_full[slot], 0, block * kCols, pol_q);
+    } else {
+      mbar_arrive(&S.j_full[slot]);
+    }
+    if (block < 0) return;
+    if (lane == 0) {
+      const JobInfo &Jc = S.job[slot];
+      for (int u = 0; u < ntiles; ++u) {
+        const int tile = u < Jc.ns ? sample_tile(Jc, u) : Jc.lo_t + (u - Jc.ns);
+        const int stage = kcount % kKStages;
+        if (!wait_bar(S, &S.k_empty[stage], ((kcount / kKStages) & 1) ^ 1, p)) break;
+        mbar_arrive_expect_tx(&S.k_full[stage], kKTileBytes);
+        tma_load_2d(&S.kring[stage][0], k_map, &S.k_full[stage], 0, tile * kTileKeys, pol_k);
+        ++kcount;
+      }
+    }
+    kcount = __shfl_sync(0xFFFFFFFFu, kcount, 0);
+    if (aborted(S)) return;
+    ++job_iter;
+  }
+}
+
+// ------------------------------------------------------------------ MMA issuer (warp 1, lane 0)
+__device__ void mma_issuer(Smem &S, uint32_t tmem, const FusedParams &p) {
+  int job_iter = 0, kcount = 0, tcount = 0;
+  for (;;) {
+    const int slot = job_iter & 1;
+    if (!wait_bar(S, &S.j_full[slot], (job_iter >> 1) & 1, p)) break;
+    const JobInfo &J = S.job[slot];
+    if (J.block < 0) break;
+    const int ntiles = J.ns + J.nt;
+    const uint32_t b_base = smem_u32(&S.q[slot][0]);
+    bool ok = true;
+    for (int u = 0; u < ntiles && ok; ++u) {
+      const int stage = kcount % kKStages;
+      const int buf = tcount & 1;
+      ok = wait_bar(S, &S.k_full[stage], (kcount / kKStages) & 1, p) &&
+           wait_bar(S, &S.t_empty[buf], ((tcount >> 1) & 1) ^ 1, p);
+      if (!ok) break;
+      tc_fence_after();
+      const uint32_t a_base = smem_u32(&S.kring[stage][0]);
+      const uint32_t d = tmem + (uint32_t)(buf * kCols);
+#pragma unroll
+      for (int kk = 0; kk < kDim / 32; ++kk) {
+        umma_f8(d, sw128_kmajor_desc(a_base + 32 * kk), sw128_kmajor_desc(b_base + 32 * kk), kIdesc,
+                kk > 0 ? 1u : 0u);
+      }
+      umma_commit(&S.k_empty[stage]);
+      umma_commit(&S.t_full[buf]);
+      ++kcount;
+      ++tcount;
+    }
+    if (!ok) break;
+    umma_commit(&S.j_empty[slot]);
+    ++job_iter;
+  }
+  // Make sure no MMA is still writing TMEM when the CTA releases it.
+  umma_commit(&S.drain);
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait(&S.drain, 0)) {
+    if ((long long)(globaltimer_ns() - t0) > p.timeout_ns) {
+      raise_timeout(S, p);
+      break;
+    }
+  }
+}
+
+// ------------------------------------------------------------------ epilogue (warps 4-11)
+template <bool kLogits>
+__device__ void epilogue(Smem &S, uint32_t tmem, const FusedParams &p, int warp, int lane) {
+  const int ew = warp - kEpiWarp0;     // 0..7
+  const int quad = warp & 3;           // TMEM lane quadrant this warp may access
+  const int half = ew >> 2;            // rows 4*half .. 4*half+3
+  const uint32_t lane_addr = (uint32_t)(quad * 32) << 16;
+  const float NEG_INF = -INFINITY;
+  const int cap = p.cap;
+  int job_iter = 0, tcount = 0;
+  for (;;) {
+    const int slot = job_iter & 1;
+    bool ok = true;
+    if (lane == 0) ok = wait_bar(S, &S.j_full[slot], (job_iter >> 1) & 1, p);
+    ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+    if (bar_or(kEpiBarrier, kEpiThreads, !ok || aborted(S))) break;
+    const JobInfo &J = S.job[slot];
+    if (J.block < 0) {
+      // hand the end marker to the selection warps through the next slot
+      if (!kLogits && ew == 0 && lane == 0 && wait_bar(S, &S.s_empty[slot], ((job_iter >> 1) & 1) ^ 1, p)) {
+        S.sel[slot].block = -1;
+        mbar_arrive(&S.s_full[slot]);
+      }
+      break;
+    }
+    if (!kLogits) {
+      if (lane == 0) ok = wait_bar(S, &S.s_empty[slot], ((job_iter >> 1) & 1) ^ 1, p);
+      ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+      // per-row state for this scan: warp ew owns row ew
+      if (lane == 0) {
+        const int n = J.end[ew] - J.start[ew];
+        float t0 = NEG_INF;
+        if (J.ns == 0 && J.mode == 0 && p.force_gate == 1 && n > 0) t0 = INFINITY;
+        S.tau[ew] = t0;
+        S.cnt[ew] = 0;
+        S.ref[ew] = 0;
+        S.ref_frozen[ew] = 0;
+        S.msample[ew] = 0;
+      }
+      for (int b = lane; b < 256; b += 32) S.hist[ew][b] = 0;
+    }
+    if (bar_or(kEpiBarrier, kEpiThreads, !ok || aborted(S))) break;
+    int st[4], en[4];
+    bool act[4];
+    float tau[4];
+#pragma unroll
+    for (int rr = 0; rr < 4; ++rr) {
+      const int r = 4 * half + rr;
+      st[rr] = J.start[r];
+      en[rr] = J.end[r];
+      act[rr] = ((J.mask >> r) & 1u) != 0;
+      tau[rr] = kLogits ? NEG_INF : S.tau[r];
+    }
+    const int ns = J.ns, ntiles = J.ns + J.nt, mode = J.mode;
+    const int block = J.block;
+    uint32_t *slab_keys = p.slab + ((size_t)(blockIdx.x * kSlots + slot) * 2 * kBlockRows) * (size_t)cap;
+    int32_t *slab_idx = reinterpret_cast<int32_t *>(slab_keys + (size_t)kBlockRows * cap);
+    bool bail = false;
+    for (int u = 0; u < ntiles && !bail; ++u) {
+      const bool sampling = u < ns;
+      const int tile = sampling ? sample_tile(J, u) : J.lo_t + (u - ns);
+      const int key = tile * kTileKeys + quad * 32 + lane;
+      const float sc = key < p.keys ? __ldg(p.scales + key) : 0.f;
+      const int buf = tcount & 1;
+      ok = wait_bar(S, &S.t_full[buf], (tcount >> 1) & 1, p);
+      ok = __all_sync(0xFFFFFFFFu, ok);
+      tc_fence_after();
+      float sv[4];
+#pragma unroll
+      for (int rr = 0; rr < 4; ++rr) {
+        sv[rr] = NEG_INF;
+        if (act[rr] && ok) {
+          const int r = 4 * half + rr;
+          uint32_t v[32];
+          tmem_ld_32x32b_x32(tmem + lane_addr + (uint32_t)(buf * kCols + r * kHeads), v);
+          tmem_ld_wait();
+          const float s = relu_weighted_sum(v, &J.w[r][0], sc);
+          if (key >= st[rr] && key < en[rr]) sv[rr] = s;
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&S.t_empty[buf]);
+      ++tcount;
+      if (kLogits) {
+        if (key < p.keys) {
+#pragma unroll
+          for (int rr = 0; rr < 4; ++rr) {
+            if (act[rr]) {
+              const size_t row = (size_t)block * kBlockRows + 4 * half + rr;
+              p.logits[row * (size_t)p.keys + key] = sv[rr];
+            }
+          }
+        }
+        continue;
+      }
+      if (sampling) {
+        // step A: reference maximum from the row's first sample tile with visible keys
+#pragma unroll
+        for (int rr = 0; rr < 4; ++rr) {
+          const int r = 4 * half + rr;
+          if (act[rr] && !S.ref_frozen[r]) {
+            const uint32_t kv = sv[rr] > NEG_INF ? f2key(sv[rr]) : 0u;
+            const uint32_t m = __reduce_max_sync(0xFFFFFFFFu, kv);
+            if (lane == 0 && m) atomicMax(&S.ref[r], m);
+          }
+        }
+        if (bar_or(kEpiBarrier, kEpiThreads, aborted(S))) { bail = true; break; }
+        // step B: histogram of the distance below the reference
+#pragma unroll
+        for (int rr = 0; rr < 4; ++rr) {
+          const int r = 4 * half + rr;
+          if (act[rr]) {
+            const uint32_t ref = S.ref[r];
+            const bool vis = sv[rr] > NEG_INF;
+            if (ref && vis) {
+              const uint32_t kv = f2key(sv[rr]);
+              atomicAdd(&S.hist[r][dist_bin(kv < ref ? ref - kv : 0u)], 1);
+            }
+            const uint32_t bv = __ballot_sync(0xFFFFFFFFu, vis && ref != 0);
+            if (lane == 0 && bv) atomicAdd(&S.msample[r], __popc(bv));
+            if (quad == 0 && lane == 0) S.ref_frozen[r] = ref != 0;
+          }
+        }
+        if (bar_or(kEpiBarrier, kEpiThreads, aborted(S))) { bail = true; break; }
+        if (u == ns - 1) {
+          // gate for row ew from its sample histogram
+          const int r = ew;
+          const int n = J.end[r] - J.start[r];
+          float t = NEG_INF;
+          const int m = S.msample[r];
+          if (((J.mask >> r) & 1u) && n > cap && m > 0) {
+            const long long jwant = max(1LL, ((long long)m * p.gate_target + n - 1) / n);
+            int c[5], tot = 0;
+#pragma unroll
+            for (int j = 0; j < 5; ++j) {
+              c[j] = S.hist[r][5 * lane + j];
+              tot += c[j];
+            }
+            int incl = tot;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+              const int v = __shfl_up_sync(0xFFFFFFFFu, incl, off);
+              if (lane >= off) incl += v;
+            }
+            const int excl = incl - tot;
+            const uint32_t bm = __ballot_sync(0xFFFFFFFFu, excl < jwant && jwant <= incl);
+            if (bm) {
+              const int src = __ffs(bm) - 1;
+              int bin = 0;
+              if (lane == src) {
+                int run = excl;
+#pragma unroll
+                for (int j = 0; j < 5; ++j) {
+                  run += c[j];
+                  if (run >= jwant) { bin = 5 * lane + j; break; }
+                }
+              }
+              bin = __shfl_sync(0xFFFFFFFFu, bin, src);
+              const uint64_t dhi = dist_bin_hi(bin);
+              const uint32_t ref = S.ref[r];
+              if ((uint64_t)ref > dhi) t = key2f(ref - (uint32_t)dhi);
+            }
+          }
+          if (lane == 0) S.tau[r] = t;
+          if (bar_or(kEpiBarrier, kEpiThreads, aborted(S))) { bail = true; break; }
+#pragma unroll
+          for (int rr = 0; rr < 4; ++rr) tau[rr] = S.tau[4 * half + rr];
+          if (ew == 0 && lane == 0) atomicAdd(p.ws + kWsSampleTiles, ns);
+        }
+        continue;
+      }
+      // main scan: candidate emission
+#pragma unroll
+      for (int rr = 0; rr < 4; ++rr) {
+        const int r = 4 * half + rr;
+        const bool pass = sv[rr] > tau[rr];
+        const uint32_t bal = __ballot_sync(0xFFFFFFFFu, pass);
+        if (bal) {
+          const int leader = __ffs(bal) - 1;
+          int base = 0;
+          if (lane == leader) base = atomicAdd(&S.cnt[r], __popc(bal));
+          base = __shfl_sync(0xFFFFFFFFu, base, leader);
+          if (pass) {
+            const int pos = base + __popc(bal & lanemask_lt());
+            if (pos < cap) {
+              slab_keys[(size_t)r * cap + pos] = f2key(sv[rr]);
+              slab_idx[(size_t)r * cap + pos] = key;
+            }
+          }
+        }
+      }
+      if (mode == 1) {
+        // exact rescan: keep each row's slab bounded by compacting to its top-k
+        if (bar_or(kEpiBarrier, kEpiThreads, aborted(S))) { bail = true; break; }
+        const int r = ew;
+        if (((J.mask >> r) & 1u) && S.cnt[r] + kTileKeys > cap) {
+          int take_eq = 0;
+          const int n = S.cnt[r];
+          const uint32_t T = warp_radix_select(slab_keys + (size_t)r * cap, n, p.topk, &S.hist[r][0], lane, &take_eq);
+          warp_emit<true>(slab_keys + (size_t)r * cap, slab_idx + (size_t)r * cap, n, T, take_eq, false, nullptr, 0,
+                          p.topk, lane);
+          __syncwarp();
+          if (lane == 0) {
+            S.cnt[r] = p.topk;
+            S.tau[r] = key2f(T);
+            atomicAdd(p.ws + kWsCompactions, 1);
+          }
+        }
+        __threadfence_block();
+        if (bar_or(kEpiBarrier, kEpiThreads, aborted(S))) { bail = true; break; }
+#pragma unroll
+        for (int rr = 0; rr < 4; ++rr) tau[rr] = S.tau[4 * half + rr];
+      }
+    }
+    __threadfence_block();  // slab writes of every epilogue warp precede the hand-over
+    if (bar_or(kEpiBarrier, kEpiThreads, bail || aborted(S))) break;
+    if (!kLogits) {
+      if (ew == 0) {
+        SelSlot &Q = S.sel[slot];
+        if (lane < kBlockRows) {
+          Q.start[lane] = J.start[lane];
+          Q.n[lane] = J.end[lane] - J.start[lane];
+          Q.cnt[lane] = S.cnt[lane];
+          Q.gated[lane] = S.tau[lane] > NEG_INF;
+        }
+        if (lane == 0) {
+          Q.block = J.block;
+          Q.mode = J.mode;
+          Q.mask = J.mask;
+          Q.nrows = J.nrows;
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&S.s_full[slot]);
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&S.j_empty[slot]);
+    ++job_iter;
+  }
+}
+
+// ------------------------------------------------------------------ selection (warps 12-15)
+__device__ void selection(Smem &S, const FusedParams &p, int warp, int lane) {
+  const int sw = warp - kSelWarp0;
+  int *hist = &S.selhist[sw][0];
+  const int cap = p.cap;
+  int job_iter = 0;
+  for (;;) {
+    const int slot = job_iter & 1;
+    bool ok = true;
+    // A job reaches selection only after its scan; stop once the producer has
+    // ended and every issued scan has been handed over.
+    if (lane == 0) ok = wait_bar(S, &S.s_full[slot], (job_iter >> 1) & 1, p);
+    ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+    if (!ok) break;
+    const SelSlot &Q = S.sel[slot];
+    if (Q.block < 0) break;
+    uint32_t *slab_keys = p.slab + ((size_t)(blockIdx.x * kSlots + slot) * 2 * kBlockRows) * (size_t)cap;
+    int32_t *slab_idx = reinterpret_cast<int32_t *>(slab_keys + (size_t)kBlockRows * cap);
+    uint32_t fail = 0;
+    for (int r = sw; r < Q.nrows; r += kSelWarps) {
+      if (!((Q.mask >> r) & 1u)) continue;
+      const int n = Q.n[r], cnt = Q.cnt[r];
+      const int topk = p.topk;
+      if (Q.mode == 0) {
+        const bool over = cnt > cap;
+        const bool under = Q.gated[r] && cnt < min(topk, n);
+        if (lane == 0) {
+          if (Q.gated[r]) atomicAdd(p.ws + kWsGatedRows, 1);
+          atomicAdd(p.ws + kWsCandidates, min(cnt, cap));
+          if (over) atomicAdd(p.ws + kWsOverflowRows, 1);
+          if (under) atomicAdd(p.ws + kWsUnderfillRows, 1);
+        }
+        if (over || under) {
+          fail |= 1u << r;
+          continue;
+        }
+      } else if (lane == 0) {
+        atomicAdd(p.ws + kWsRowsRescanned, 1);
+      }
+      const int row = Q.block * kBlockRows + r;
+      int32_t *out = p.out + (size_t)row * topk;
+      uint32_t *kr = slab_keys + (size_t)r * cap;
+      int32_t *ir = slab_idx + (size_t)r * cap;
+      int wrote;
+      if (cnt <= topk) {
+        wrote = warp_emit<false>(kr, ir, cnt, 0u, 0, true, out, Q.start[r], topk, lane);
+      } else {
+        int take_eq = 0;
+        const uint32_t T = warp_radix_select(kr, cnt, topk, hist, lane, &take_eq);
+        wrote = warp_emit<false>(kr, ir, cnt, T, take_eq, false, out, Q.start[r], topk, lane);
+      }
+      for (int i = wrote + lane; i < topk; i += 32) out[i] = -1;
+    }
+    if (fail) atomicOr(&S.selfail[slot], fail);
+    __syncwarp();
+    if (lane == 0) {
+      __threadfence_block();
+      const int done = atomicAdd(&S.seldone[slot], 1);
+      if (done == kSelWarps - 1) {
+        const uint32_t fm = *(volatile uint32_t *)&S.selfail[slot];
+        if (fm) {
+          const int tail = S.fifo_tail;
+          S.fifo_block[tail & 7] = Q.block;
+          S.fifo_mask[tail & 7] = fm;
+          __threadfence_block();
+          *(volatile int *)&S.fifo_tail = tail + 1;
+        }
+        S.selfail[slot] = 0;
+        S.seldone[slot] = 0;
+        __threadfence_block();
+        atomicAdd(p.ws + kWsBlocksDone, 1);
+        atomicAdd(&S.retired, 1);
+      }
+      mbar_arrive(&S.s_empty[slot]);
+    }
+    ++job_iter;
+  }
+}
+
+// ------------------------------------------------------------------ kernel
+template <bool kLogits>
+__global__ void __launch_bounds__(kThreads, 1)
+    mqa_fused_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant__ CUtensorMap k_map,
+                     const FusedParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  Smem &S = get_smem(smem_raw);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kKStages; ++i) {
+      mbar_init(&S.k_full[i], 1);
+      mbar_init(&S.k_empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&S.t_full[i], 1);
+      mbar_init(&S.t_empty[i], kEpiWarps);
+      mbar_init(&S.j_full[i], 32);
+      mbar_init(&S.j_empty[i], 1 + kEpiWarps);
+      mbar_init(&S.s_full[i], 1);
+      mbar_init(&S.s_empty[i], kSelWarps);
+      S.seldone[i] = 0;
+      S.selfail[i] = 0;
+    }
+    mbar_init(&S.drain, 1);
+    mbar_init(&S.stall_bar, 1);
+    S.abort_flag = 0;
+    S.fifo_head = 0;
+    S.fifo_tail = 0;
+    S.retired = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&q_map);
+    tma_prefetch_desc(&k_map);
+  }
+  if (warp == 1) {
+    tmem_alloc(&S.tmem_base, 2 * kCols);
+    tmem_relinquish();
+  }
+  if (!kLogits) build_order(S, p);
+  // the order scratch shared the K ring with later TMA writes
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = S.tmem_base;
+
+  if (warp == 0) {
+    producer<kLogits>(S, &q_map, &k_map, p, lane);
+  } else if (warp == 1) {
+    if (lane == 0) mma_issuer(S, tmem, p);
+  } else if (warp >= kEpiWarp0 && warp < kSelWarp0) {
+    epilogue<kLogits>(S, tmem, p, warp, lane);
+  } else if (warp >= kSelWarp0) {
+    if (!kLogits) {
+      selection(S, p, warp, lane);
+    }
+  }
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, 2 * kCols);
+  }
+}
+
+static cudaError_t set_smem_attr(const void *fn) {
+  return cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)fused_smem_bytes());
+}
+
+cudaError_t launch_fused_topk(const CUtensorMap &q_map, const CUtensorMap &k_map, const FusedParams &p, int ctas,
+                              cudaStream_t stream) {
+  static cudaError_t attr = set_smem_attr((const void *)mqa_fused_kernel<false>);
+  if (attr != cudaSuccess) return attr;
+  mqa_fused_kernel<false><<<ctas, kThreads, fused_smem_bytes(), stream>>>(q_map, k_map, p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_logits(const CUtensorMap &q_map, const CUtensorMap &k_map, const FusedParams &p, int ctas,
+                          cudaStream_t stream) {
+  static cudaError_t attr = set_smem_attr((const void *)mqa_fused_kernel<true>);
+  if (attr != cudaSuccess) return attr;
+  mqa_fused_kernel<true><<<ctas, kThreads, fused_smem_bytes(), stream>>>(q_map, k_map, p);
+  return cudaGetLastError();
+}
+
+}  // namespace mqa

@@ -1,0 +1,87 @@
+// Internal definitions shared by the library's translation units (not part of
+// the public C ABI in include/mqatopk.h).
+#pragma once
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace mqa {
+
+constexpr int kHeads = 32;      // index heads per query row
+constexpr int kDim = 128;       // head dimension (bytes per fp8 row)
+constexpr int kBlockRows = 8;   // query rows per block (one TMEM accumulator group)
+constexpr int kTileKeys = 128;  // keys per tile (UMMA M, one TMEM lane per key)
+constexpr int kCols = kBlockRows * kHeads;  // 256 accumulator columns per tile (UMMA N)
+constexpr int kKStages = 6;     // K-tile ring depth
+constexpr int kQBytes = kCols * kDim;       // 32 KiB of q per block
+constexpr int kKTileBytes = kTileKeys * kDim;  // 16 KiB of k per tile
+
+constexpr int kEpiWarps = 8;    // two per TMEM lane quadrant; each owns 4 rows
+constexpr int kSelWarps = 4;    // candidate selection warps
+constexpr int kThreads = 512;   // warps 0-3 control, 4-11 epilogue, 12-15 selection
+constexpr int kEpiWarp0 = 4;
+constexpr int kSelWarp0 = 12;
+
+constexpr int kDefaultSlabCap = 16384;  // candidate records per row per slot
+constexpr int kSlots = 2;               // slab slots per CTA (scan one, select the other)
+constexpr int kMaxSortBlocks = 8192;    // heaviest-first order kept in smem up to this many blocks
+constexpr int kMaxKeys = 1 << 24;
+
+constexpr int kSampleBins = 160;        // 129 used, padded for the warp scan
+
+// Workspace header (int32 words), zeroed by the host before each launch.
+enum WsWord : int {
+  kWsClaim = 0,          // next entry of the heaviest-first block order
+  kWsStatus = 1,         // device status bits (MQA_DEV_*)
+  kWsRowsRescanned = 2,  // rows that took the exact rescan
+  kWsCompactions = 3,    // in-place slab compactions
+  kWsCandidates = 4,     // candidate records written by gated scans (sum over rows)
+  kWsGatedRows = 5,      // rows that used a sampled gate
+  kWsBlocksDone = 6,     // row blocks whose scan finished
+  kWsSampleTiles = 7,    // sample tiles scored
+  kWsOverflowRows = 8,   // rows whose candidates exceeded the slab
+  kWsUnderfillRows = 9,  // rows whose gated count fell below top-k
+  kWsWords = 64
+};
+constexpr size_t kWsHeaderBytes = 256;
+
+// Device status bits.
+constexpr int kDevRangeClamped = 1;
+constexpr int kDevWaitTimeout = 2;
+constexpr int kDevInternal = 4;
+
+struct FusedParams {
+  const float *scales;   // [keys] fp32
+  const float *weights;  // [rows, 32]
+  const int32_t *starts; // [rows]
+  const int32_t *ends;   // [rows]
+  int32_t *out;          // [rows, topk]   (top-k mode)
+  float *logits;         // [rows, keys]   (logits mode, row-chunk local)
+  int32_t *ws;           // workspace header (int32 words)
+  uint32_t *slab;        // slabs: [ctas][slots][rows 8][cap] keys, then same for indices
+  int rows;              // rows of this call
+  int row0;              // first global row (logits mode: chunk offset)
+  int keys;
+  int topk;
+  int nblocks;
+  int cap;               // slab capacity per row
+  int gate_target;       // expected candidates per gated row
+  int force_gate;        // 0 normal, 1 gate +inf, 2 gate -inf
+  int stall;             // debug: wait on a barrier nobody arrives on
+  int key_chunks;        // logits mode: key chunks per block
+  long long timeout_ns;  // bound on every wait
+};
+
+// Launchers (defined next to their kernels).
+cudaError_t launch_fused_topk(const CUtensorMap &q_map, const CUtensorMap &k_map, const FusedParams &p,
+                              int ctas, cudaStream_t stream);
+cudaError_t launch_logits(const CUtensorMap &q_map, const CUtensorMap &k_map, const FusedParams &p, int ctas,
+                          cudaStream_t stream);
+cudaError_t launch_ue8m0_decode(const uint8_t *scales, float *out, int keys, cudaStream_t stream);
+cudaError_t launch_dense_topk_rows(const float *logits, int rows, int keys, const int32_t *starts,
+                                   const int32_t *ends, int32_t *out, int topk, int32_t *ws_status,
+                                   cudaStream_t stream);
+size_t fused_smem_bytes();
+
+}  // namespace mqa

@@ -1,0 +1,342 @@
+// C ABI of the library (include/mqatopk.h): argument checks, workspace sizing,
+// TMA descriptor encoding and launches.  Host code only.
+#include "../../include/mqatopk.h"
+#include "mqa_internal.h"
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstring>
+#include <mutex>
+
+namespace {
+
+using namespace mqa;
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceInfo {
+  bool ok = false;
+  int sms = 0;
+  int major = 0, minor = 0;
+};
+
+std::mutex g_mu;
+DeviceInfo g_dev[kMaxDevices];
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn g_encode = nullptr;
+
+int device_info(int dev, DeviceInfo *out) {
+  if (dev < 0 || dev >= kMaxDevices) return MQA_ERR_INVALID_ARGUMENT;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_dev[dev].ok) {
+    int n = 0;
+    if (cudaGetDeviceCount(&n) != cudaSuccess || n <= 0) {
+      cudaGetLastError();
+      return MQA_ERR_NO_DEVICE;
+    }
+    if (dev >= n) return MQA_ERR_INVALID_ARGUMENT;
+    DeviceInfo d;
+    if (cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&d.major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&d.minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) {
+      cudaGetLastError();
+      return MQA_ERR_CUDA;
+    }
+    d.ok = true;
+    g_dev[dev] = d;
+  }
+  *out = g_dev[dev];
+  return MQA_OK;
+}
+
+int current_device_info(DeviceInfo *out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return MQA_ERR_NO_DEVICE;
+  }
+  int rc = device_info(dev, out);
+  if (rc != MQA_OK) return rc;
+  if (!(out->major == 10 && out->minor == 3)) return MQA_ERR_UNSUPPORTED_DEVICE;
+  return MQA_OK;
+}
+
+int get_encoder() {
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (g_encode) return MQA_OK;
+  void *fn = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+          cudaSuccess ||
+      q != cudaDriverEntryPointSuccess || !fn) {
+    cudaGetLastError();
+    return MQA_ERR_CUDA;
+  }
+  g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+  return MQA_OK;
+}
+
+// 2-D uint8 tensor [rows_outer, 128] with rows of 128 bytes, 128-byte swizzle.
+int encode_rows128(CUtensorMap *map, const void *base, uint64_t nrows, uint32_t box_rows) {
+  const cuuint64_t dims[2] = {(cuuint64_t)kDim, (cuuint64_t)nrows};
+  const cuuint64_t strides[1] = {(cuuint64_t)kDim};
+  const cuuint32_t box[2] = {(cuuint32_t)kDim, box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? MQA_OK : MQA_ERR_CUDA;
+}
+
+inline bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+int check_common(const void *q, const void *k, const float *scales, const float *weights, const int32_t *starts,
+                 const int32_t *ends, const void *out, int rows, int keys) {
+  if (rows < 0 || keys < 1 || keys > MQA_MAX_KEYS) return MQA_ERR_INVALID_ARGUMENT;
+  if (rows > 0 && (!q || !k || !scales || !weights || !starts || !ends || !out)) return MQA_ERR_INVALID_ARGUMENT;
+  if (rows > 0 && (!aligned(q, 16) || !aligned(k, 16) || !aligned(scales, 16) || !aligned(weights, 16) ||
+                   !aligned(out, 16) || !aligned(starts, 4) || !aligned(ends, 4)))
+    return MQA_ERR_MISALIGNED;
+  return MQA_OK;
+}
+
+bool valid_topk(int topk) { return topk == 512 || topk == 1024 || topk == 2048; }
+
+size_t slab_bytes(int ctas, int cap) {
+  return (size_t)ctas * kSlots * 2 * kBlockRows * (size_t)cap * sizeof(uint32_t);
+}
+
+int fused_ctas(const DeviceInfo &d, int rows) {
+  const int nb = (rows + kBlockRows - 1) / kBlockRows;
+  return nb < d.sms ? nb : d.sms;
+}
+
+cudaStream_t as_stream(void *s) { return reinterpret_cast<cudaStream_t>(s); }
+
+int run_fused(const void *q, const void *k, const float *scales, const float *weights, const int32_t *starts,
+              const int32_t *ends, int32_t *out, int rows, int keys, int topk, void *workspace,
+              size_t workspace_bytes, void *stream, const mqa_topk_debug_options *opt) {
+  int rc = check_common(q, k, scales, weights, starts, ends, out, rows, keys);
+  if (rc != MQA_OK) return rc;
+  if (!valid_topk(topk)) return MQA_ERR_INVALID_ARGUMENT;
+  if (!workspace) return MQA_ERR_INVALID_ARGUMENT;
+  if (!aligned(workspace, 256)) return MQA_ERR_MISALIGNED;
+  int cap = kDefaultSlabCap;
+  if (opt && opt->slab_capacity) {
+    cap = opt->slab_capacity;
+    if (cap < topk + 256 || cap > kDefaultSlabCap) return MQA_ERR_INVALID_ARGUMENT;
+  }
+  if (opt && (opt->force_gate < 0 || opt->force_gate > 2 || opt->wait_timeout_ms < 0 || opt->max_ctas < 0))
+    return MQA_ERR_INVALID_ARGUMENT;
+  if (rows == 0) return MQA_OK;
+  DeviceInfo d;
+  rc = current_device_info(&d);
+  if (rc != MQA_OK) return rc;
+  int ctas = fused_ctas(d, rows);
+  if (opt && opt->max_ctas && opt->max_ctas < ctas) ctas = opt->max_ctas;
+  if (workspace_bytes < kWsHeaderBytes + slab_bytes(ctas, cap)) return MQA_ERR_WORKSPACE_TOO_SMALL;
+  rc = get_encoder();
+  if (rc != MQA_OK) return rc;
+  CUtensorMap qm, km;
+  if (encode_rows128(&qm, q, (uint64_t)rows * kHeads, kCols) != MQA_OK ||
+      encode_rows128(&km, k, (uint64_t)keys, kTileKeys) != MQA_OK)
+    return MQA_ERR_CUDA;
+  FusedParams p;
+  std::memset(&p, 0, sizeof p);
+  p.scales = scales;
+  p.weights = weights;
+  p.starts = starts;
+  p.ends = ends;
+  p.out = out;
+  p.ws = reinterpret_cast<int32_t *>(workspace);
+  p.slab = reinterpret_cast<uint32_t *>(reinterpret_cast<uint8_t *>(workspace) + kWsHeaderBytes);
+  p.rows = rows;
+  p.keys = keys;
+  p.topk = topk;
+  p.nblocks = (rows + kBlockRows - 1) / kBlockRows;
+  p.cap = cap;
+  p.gate_target = 4 * topk < cap / 2 ? 4 * topk : cap / 2;
+  p.force_gate = opt ? opt->force_gate : 0;
+  p.stall = opt ? opt->stall : 0;
+  p.timeout_ns = (long long)((opt && opt->wait_timeout_ms) ? opt->wait_timeout_ms : 4000) * 1000000LL;
+  cudaStream_t st = as_stream(stream);
+  if (cudaMemsetAsync(workspace, 0, kWsHeaderBytes, st) != cudaSuccess) {
+    cudaGetLastError();
+    return MQA_ERR_CUDA;
+  }
+  if (launch_fused_topk(qm, km, p, ctas, st) != cudaSuccess) return MQA_ERR_CUDA;
+  return MQA_OK;
+}
+
+int run_logits_chunk(const DeviceInfo &d, const uint8_t *q, const void *k, const float *scales,
+                     const float *weights, const int32_t *starts, const int32_t *ends, float *logits, int rows,
+                     int keys, int32_t *ws, bool reset_header, cudaStream_t st) {
+  CUtensorMap qm, km;
+  if (encode_rows128(&qm, q, (uint64_t)rows * kHeads, kCols) != MQA_OK ||
+      encode_rows128(&km, k, (uint64_t)keys, kTileKeys) != MQA_OK)
+    return MQA_ERR_CUDA;
+  FusedParams p;
+  std::memset(&p, 0, sizeof p);
+  p.scales = scales;
+  p.weights = weights;
+  p.starts = starts;
+  p.ends = ends;
+  p.logits = logits;
+  p.ws = ws;
+  p.rows = rows;
+  p.keys = keys;
+  p.topk = 0;
+  p.nblocks = (rows + kBlockRows - 1) / kBlockRows;
+  p.cap = 0;
+  p.timeout_ns = 4000LL * 1000000LL;
+  // split each block's key range so that the grid stays full for few rows
+  const int ktiles = (keys + kTileKeys - 1) / kTileKeys;
+  int kc = 1;
+  while ((long long)p.nblocks * kc < 2LL * d.sms && ktiles / (kc * 2) >= 8) kc *= 2;
+  p.key_chunks = kc;
+  const long long jobs = (long long)p.nblocks * kc;
+  const int ctas = (int)(jobs < d.sms ? jobs : d.sms);
+  // the claim counter restarts for every launch; the status word persists
+  // across the chunks of one dense call
+  if (cudaMemsetAsync(ws, 0, reset_header ? kWsHeaderBytes : sizeof(int32_t), st) != cudaSuccess) {
+    cudaGetLastError();
+    return MQA_ERR_CUDA;
+  }
+  return launch_logits(qm, km, p, ctas, st) == cudaSuccess ? MQA_OK : MQA_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+int mqa_topk_workspace_bytes(int device, int rows, size_t *bytes) {
+  if (!bytes || rows < 0) return MQA_ERR_INVALID_ARGUMENT;
+  DeviceInfo d;
+  int rc = device_info(device, &d);
+  if (rc != MQA_OK) return rc;
+  *bytes = kWsHeaderBytes + slab_bytes(fused_ctas(d, rows), kDefaultSlabCap);
+  return MQA_OK;
+}
+
+int mqa_topk_prefill(const void *q, const void *k, const float *key_scales, const float *weights,
+                     const int32_t *starts, const int32_t *ends, int32_t *out, int rows, int keys, int topk,
+                     void *workspace, size_t workspace_bytes, void *stream) {
+  return run_fused(q, k, key_scales, weights, starts, ends, out, rows, keys, topk, workspace, workspace_bytes,
+                   stream, nullptr);
+}
+
+int mqa_topk_prefill_debug(const void *q, const void *k, const float *key_scales, const float *weights,
+                           const int32_t *starts, const int32_t *ends, int32_t *out, int rows, int keys,
+                           int topk, void *workspace, size_t workspace_bytes, void *stream,
+                           const mqa_topk_debug_options *opt) {
+  return run_fused(q, k, key_scales, weights, starts, ends, out, rows, keys, topk, workspace, workspace_bytes,
+                   stream, opt);
+}
+
+int mqa_ue8m0_decode(const uint8_t *scales, float *out, int keys, void *stream) {
+  if (keys < 0 || keys > MQA_MAX_KEYS) return MQA_ERR_INVALID_ARGUMENT;
+  if (keys == 0) return MQA_OK;
+  if (!scales || !out) return MQA_ERR_INVALID_ARGUMENT;
+  if (!aligned(scales, 16) || !aligned(out, 16)) return MQA_ERR_MISALIGNED;
+  DeviceInfo d;
+  int rc = current_device_info(&d);
+  if (rc != MQA_OK) return rc;
+  return launch_ue8m0_decode(scales, out, keys, as_stream(stream)) == cudaSuccess ? MQA_OK : MQA_ERR_CUDA;
+}
+
+int mqa_logits_debug(const void *q, const void *k, const float *key_scales, const float *weights,
+                     const int32_t *starts, const int32_t *ends, float *logits, int rows, int keys,
+                     void *workspace, size_t workspace_bytes, void *stream) {
+  int rc = check_common(q, k, key_scales, weights, starts, ends, logits, rows, keys);
+  if (rc != MQA_OK) return rc;
+  if (!workspace) return MQA_ERR_INVALID_ARGUMENT;
+  if (!aligned(workspace, 256)) return MQA_ERR_MISALIGNED;
+  if (workspace_bytes < kWsHeaderBytes) return MQA_ERR_WORKSPACE_TOO_SMALL;
+  if (rows == 0) return MQA_OK;
+  DeviceInfo d;
+  rc = current_device_info(&d);
+  if (rc != MQA_OK) return rc;
+  rc = get_encoder();
+  if (rc != MQA_OK) return rc;
+  return run_logits_chunk(d, reinterpret_cast<const uint8_t *>(q), k, key_scales, weights, starts, ends, logits,
+                          rows, keys, reinterpret_cast<int32_t *>(workspace), true, as_stream(stream));
+}
+
+int mqa_topk_dense_baseline(const void *q, const void *k, const float *key_scales, const float *weights,
+                            const int32_t *starts, const int32_t *ends, int32_t *out, int rows, int keys,
+                            int topk, void *logits_ws, size_t logits_budget_bytes, void *workspace,
+                            size_t workspace_bytes, void *stream) {
+  int rc = check_common(q, k, key_scales, weights, starts, ends, out, rows, keys);
+  if (rc != MQA_OK) return rc;
+  if (!valid_topk(topk) || !logits_ws || !workspace) return MQA_ERR_INVALID_ARGUMENT;
+  if (!aligned(logits_ws, 16)) return MQA_ERR_MISALIGNED;
+  if (!aligned(workspace, 256)) return MQA_ERR_MISALIGNED;
+  if (workspace_bytes < kWsHeaderBytes) return MQA_ERR_WORKSPACE_TOO_SMALL;
+  const size_t row_bytes = (size_t)keys * sizeof(float);
+  if (logits_budget_bytes < row_bytes) return MQA_ERR_WORKSPACE_TOO_SMALL;
+  if (rows == 0) return MQA_OK;
+  DeviceInfo d;
+  rc = current_device_info(&d);
+  if (rc != MQA_OK) return rc;
+  rc = get_encoder();
+  if (rc != MQA_OK) return rc;
+  const size_t per_call = logits_budget_bytes / row_bytes;
+  const int rows_per_call = per_call > (size_t)rows ? rows : (int)per_call;
+  cudaStream_t st = as_stream(stream);
+  float *L = reinterpret_cast<float *>(logits_ws);
+  int32_t *ws = reinterpret_cast<int32_t *>(workspace);
+  const uint8_t *qb = reinterpret_cast<const uint8_t *>(q);
+  for (int r0 = 0; r0 < rows; r0 += rows_per_call) {
+    const int nr = rows - r0 < rows_per_call ? rows - r0 : rows_per_call;
+    rc = run_logits_chunk(d, qb + (size_t)r0 * kHeads * kDim, k, key_scales, weights + (size_t)r0 * kHeads,
+                          starts + r0, ends + r0, L, nr, keys, ws, r0 == 0, st);
+    if (rc != MQA_OK) return rc;
+    if (launch_dense_topk_rows(L, nr, keys, starts + r0, ends + r0, out + (size_t)r0 * topk, topk,
+                               ws + kWsStatus, st) != cudaSuccess)
+      return MQA_ERR_CUDA;
+  }
+  return MQA_OK;
+}
+
+int mqa_topk_get_status(const void *workspace, int32_t *status, int32_t *stats, void *stream) {
+  if (!workspace || !status) return MQA_ERR_INVALID_ARGUMENT;
+  int32_t h[kWsWords];
+  cudaStream_t st = as_stream(stream);
+  if (cudaMemcpyAsync(h, workspace, sizeof h, cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+      cudaStreamSynchronize(st) != cudaSuccess) {
+    cudaGetLastError();
+    return MQA_ERR_CUDA;
+  }
+  *status = h[kWsStatus];
+  if (stats) {
+    stats[MQA_STAT_STATUS] = h[kWsStatus];
+    stats[MQA_STAT_ROWS_RESCANNED] = h[kWsRowsRescanned];
+    stats[MQA_STAT_COMPACTIONS] = h[kWsCompactions];
+    stats[MQA_STAT_CANDIDATES] = h[kWsCandidates];
+    stats[MQA_STAT_GATED_ROWS] = h[kWsGatedRows];
+    stats[MQA_STAT_BLOCKS_DONE] = h[kWsBlocksDone];
+    stats[MQA_STAT_SAMPLE_TILES] = h[kWsSampleTiles];
+    stats[MQA_STAT_OVERFLOW_ROWS] = h[kWsOverflowRows];
+    stats[MQA_STAT_UNDERFILL_ROWS] = h[kWsUnderfillRows];
+  }
+  return MQA_OK;
+}
+
+const char *mqa_topk_strerror(int code) {
+  switch (code) {
+    case MQA_OK: return "ok";
+    case MQA_ERR_INVALID_ARGUMENT: return "invalid argument";
+    case MQA_ERR_MISALIGNED: return "misaligned pointer";
+    case MQA_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
+    case MQA_ERR_UNSUPPORTED_DEVICE: return "unsupported device (needs compute capability 10.3)";
+    case MQA_ERR_CUDA: return "CUDA error";
+    case MQA_ERR_NO_DEVICE: return "no CUDA device";
+    default: return "unknown error";
+  }
+}
+
+}  // extern "C"

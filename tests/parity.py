@@ -1,0 +1,70 @@
+"""Helpers for comparing the CUDA path with the oracle.
+
+Pass rule for top-k (fixed by the target definition: exact top-k up to ties
+at the boundary): structure is bit-exact (c = min(topk, n) distinct in-range
+relative indices, then -1), a row with n <= topk returns exactly {0..n-1},
+and every key in the symmetric difference between the GPU set and the
+oracle set has an oracle score within 1e-4 * max|score| of the row's oracle
+k-th score.  Logits: |gpu - oracle| <= 1e-3 * max|score| per row, -inf
+exactly outside the row's range.
+"""
+import numpy as np
+
+TOPK_TIE_TOL = 1e-4
+LOGITS_TOL = 1e-3
+
+
+def to_device(p, dev="cuda"):
+    import torch
+    import sparse_attention_indexer_relu_gb300 as mqa
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+    q, k = t(p.q), t(p.k)
+    scales = mqa.ue8m0_decode(t(p.scales_ue8m0))
+    return q, k, scales, t(p.weights), t(p.starts), t(p.ends)
+
+
+def check_topk_rows(got, p, rows, scores, oracle_idx=None):
+    """got: [len(rows), topk] int32 (GPU), scores: oracle fp64 scores [len(rows), keys]."""
+    bad = []
+    for i, r in enumerate(rows):
+        s, e = int(p.starts[r]), int(p.ends[r])
+        n = max(0, e - s)
+        c = min(p.topk, n)
+        g = got[i]
+        if not np.all(g[c:] == -1):
+            bad.append((r, "padding"))
+            continue
+        sel = g[:c]
+        if np.any(sel < 0) or np.any(sel >= n) or len(np.unique(sel)) != c:
+            bad.append((r, "indices"))
+            continue
+        if n <= p.topk:
+            if set(sel.tolist()) != set(range(n)):
+                bad.append((r, "short row set"))
+            continue
+        vis = scores[i, s:e]
+        tol = TOPK_TIE_TOL * np.max(np.abs(vis))
+        order = np.argsort(-vis, kind="stable")
+        kth = vis[order[c - 1]]
+        want = set(order[:c].tolist())
+        diff = want ^ set(sel.tolist())
+        worst = max((abs(vis[j] - kth) for j in diff), default=0.0)
+        if worst > tol:
+            bad.append((r, f"tie rule: {len(diff)} keys differ, worst |S-kth| = {worst:.3g} > {tol:.3g}"))
+    return bad
+
+
+def check_logits_rows(got, p, rows, scores):
+    bad = []
+    for i, r in enumerate(rows):
+        ref = scores[i]
+        fin = np.isfinite(ref)
+        if not np.array_equal(np.isneginf(got[i]), ~fin):
+            bad.append((r, "-inf pattern"))
+            continue
+        if fin.any():
+            tol = LOGITS_TOL * np.max(np.abs(ref[fin]))
+            err = np.max(np.abs(got[i][fin] - ref[fin]))
+            if err > tol:
+                bad.append((r, f"max err {err:.3g} > {tol:.3g}"))
+    return bad

@@ -1,0 +1,171 @@
+"""Parity of the CUDA path (through the C ABI) with the CPU oracle."""
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from parity import check_logits_rows, check_topk_rows, to_device
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def mqa():
+    import torch
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    import sparse_attention_indexer_relu_gb300 as m
+    m.lib()
+    return m
+
+
+def run_fused(mqa, p, debug=None, workspace=None):
+    import torch
+    q, k, sc, w, s, e = to_device(p)
+    ws = workspace if workspace is not None else mqa.alloc_workspace(p.rows)
+    out = mqa.mqa_topk_prefill(q, k, sc, w, s, e, p.topk, workspace=ws, debug=debug)
+    status, stats = mqa.get_status(ws)
+    return out.cpu().numpy(), status, stats
+
+
+def assert_parity(p, got, rows=None):
+    rows = np.arange(p.rows) if rows is None else rows
+    _, scores = oracle.run(p, rows=rows, want_topk=False, want_scores=True)
+    bad = check_topk_rows(got[rows], p, rows, scores)
+    assert not bad, bad[:10]
+
+
+# ---------------------------------------------------------------- UE8M0 decode
+@pytest.mark.parametrize("keys", [1, 3, 256, 1001, 65536 + 5])
+def test_ue8m0_decode_bit_exact(mqa, keys):
+    import torch
+    rng = np.random.default_rng(keys)
+    e = rng.integers(0, 256, size=keys).astype(np.uint8)
+    e[: min(keys, 256)] = np.arange(min(keys, 256), dtype=np.uint8)
+    g = synth.ue8m0_bytes(e)
+    got = mqa.ue8m0_decode(torch.from_numpy(g).cuda()).cpu().numpy()
+    assert np.array_equal(got.view(np.uint32), oracle.ue8m0_decode(g).view(np.uint32))
+
+
+# ---------------------------------------------------------------- debug logits
+@pytest.mark.parametrize("name", ["tiny_64x4096_k512"])
+def test_logits_debug_config(mqa, name):
+    p = synth.make(name)
+    q, k, sc, w, s, e = to_device(p)
+    got = mqa.mqa_logits_debug(q, k, sc, w, s, e).cpu().numpy()
+    _, scores = oracle.run(p, want_topk=False, want_scores=True)
+    bad = check_logits_rows(got, p, np.arange(p.rows), scores)
+    assert not bad, bad[:10]
+
+
+@pytest.mark.parametrize("seed,rows,keys", [(1, 1, 1), (2, 5, 130), (3, 17, 999), (4, 40, 5000), (5, 9, 128)])
+def test_logits_debug_random(mqa, seed, rows, keys):
+    p = synth.random_small(seed, rows, keys, 512)
+    q, k, sc, w, s, e = to_device(p)
+    got = mqa.mqa_logits_debug(q, k, sc, w, s, e).cpu().numpy()
+    _, scores = oracle.run(p, want_topk=False, want_scores=True)
+    bad = check_logits_rows(got, p, np.arange(p.rows), scores)
+    assert not bad, bad[:10]
+
+
+# ---------------------------------------------------------------- fused top-k
+def test_fused_tiny_config(mqa):
+    p = synth.make("tiny_64x4096_k512")
+    got, status, stats = run_fused(mqa, p)
+    assert status == 0, stats
+    assert_parity(p, got)
+
+
+@pytest.mark.parametrize("seed,rows,keys,topk", [
+    (10, 1, 1, 512), (11, 3, 100, 512), (12, 8, 600, 512), (13, 9, 2100, 1024), (14, 40, 5000, 2048),
+    (15, 33, 4097, 512), (16, 16, 20000, 1024), (17, 25, 40000, 512),
+])
+def test_fused_random_ranges(mqa, seed, rows, keys, topk):
+    p = synth.random_small(seed, rows, keys, topk)
+    got, status, stats = run_fused(mqa, p)
+    assert status == 0, stats
+    assert_parity(p, got)
+
+
+@pytest.mark.parametrize("force_gate", [1, 2])
+def test_fused_forced_gate_rescans(mqa, force_gate):
+    """Gate forced to +inf (every row under-fills) or off (long rows overflow
+    a reduced slab): the exact rescan must still give the exact top-k."""
+    p = synth.random_small(21, 24, 30000, 512, empty_frac=0.0)
+    got, status, stats = run_fused(mqa, p, debug={"force_gate": force_gate, "slab_capacity": 2048})
+    assert status == 0, stats
+    assert stats["rows_rescanned"] > 0
+    if force_gate == 2:
+        assert stats["compactions"] > 0
+    assert_parity(p, got)
+
+
+def test_fused_small_slab_compaction_ties(mqa):
+    """Many exact ties (duplicated keys) with a small slab: compaction keeps
+    exactly top-k and the tie rule holds."""
+    p = synth.random_small(22, 16, 20000, 1024, empty_frac=0.0)
+    rng = np.random.default_rng(0)
+    dst = rng.choice(p.keys, p.keys // 2, replace=False)
+    src = rng.integers(0, 64, size=dst.size)
+    p.k[dst] = p.k[src]
+    p.scales_ue8m0[dst] = p.scales_ue8m0[src]
+    got, status, stats = run_fused(mqa, p, debug={"force_gate": 2, "slab_capacity": 1024 + 256})
+    assert status == 0, stats
+    assert_parity(p, got)
+
+
+def test_fused_single_cta(mqa):
+    """All blocks through one persistent CTA (job slots and slabs reused many times)."""
+    p = synth.random_small(23, 64, 9000, 512)
+    got, status, stats = run_fused(mqa, p, debug={"max_ctas": 1})
+    assert status == 0, stats
+    assert_parity(p, got)
+
+
+def test_workspace_reuse_two_calls(mqa):
+    p = synth.random_small(24, 20, 7000, 512)
+    ws = mqa.alloc_workspace(p.rows)
+    a, s1, _ = run_fused(mqa, p, workspace=ws)
+    b, s2, _ = run_fused(mqa, p, workspace=ws)
+    assert s1 == 0 and s2 == 0
+    assert_parity(p, a)
+    assert_parity(p, b)
+
+
+def test_bounded_wait_reports_timeout(mqa):
+    """A wait that nothing completes ends at the time limit with a status bit;
+    the context stays usable for the next call."""
+    p = synth.random_small(25, 8, 1000, 512)
+    _, status, _ = run_fused(mqa, p, debug={"stall": 1, "wait_timeout_ms": 200})
+    assert status & 2
+    got, status, _ = run_fused(mqa, p)
+    assert status == 0
+    assert_parity(p, got)
+
+
+def test_out_of_range_rows_clamped(mqa):
+    p = synth.random_small(26, 8, 3000, 512)
+    p.starts[0], p.ends[0] = -5, 700
+    p.starts[1], p.ends[1] = 2900, 3400
+    got, status, _ = run_fused(mqa, p)
+    assert status & 1
+    # the oracle rejects such rows; compare against the clamped problem
+    p.starts[0], p.ends[0] = 0, 700
+    p.starts[1], p.ends[1] = 2900, 3000
+    # indices are relative to the clamped start
+    assert_parity(p, got)
+
+
+# ---------------------------------------------------------------- dense baseline
+@pytest.mark.parametrize("budget_rows", [1000, 7, 1])
+def test_dense_baseline(mqa, budget_rows):
+    p = synth.random_small(30, 20, 6000, 512)
+    q, k, sc, w, s, e = to_device(p)
+    out = mqa.mqa_topk_dense_baseline(q, k, sc, w, s, e, p.topk, logits_budget_bytes=budget_rows * p.keys * 4)
+    assert_parity(p, out.cpu().numpy())
+
+
+def test_dense_matches_fused_tiny(mqa):
+    p = synth.make("tiny_64x4096_k512")
+    q, k, sc, w, s, e = to_device(p)
+    out = mqa.mqa_topk_dense_baseline(q, k, sc, w, s, e, p.topk).cpu().numpy()
+    assert_parity(p, out)
