@@ -1,0 +1,409 @@
+"""Benchmark: fused FP8 MQA-logits + per-row top-k prefill selection.
+
+One step = one `mqa_topk_prefill` call over one whole prefill chunk with its
+inputs resident in HBM (a single kernel launch after a 256-byte header reset).
+Default workload: 16,384 rows x 1,048,576 keys (causal tail), top-2048, q/k
+N(0,1) rounded to e4m3, weights N(0,1)/sqrt(32), UE8M0 exponents in
+[120, 127] -- the 1M-key top-2048 chunk.  Metric: scored (row, key) pairs/s
+(pairs = sum over rows of visible keys); rows/s alongside.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl fused|reference]
+                    [--workload NAME] [--no-e2e] [--no-dense] [--no-cpu]
+
+Under torchrun each rank runs the same chunk on its own GPU (independent
+replicas, weak scaling); rank 0 prints one JSON line.
+`--impl reference` times the CPU oracle (the reference arm of this build) on
+a bounded row sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+from sparse_attention_indexer_relu_gb300 import plan  # noqa: E402
+
+METRIC = "scored (row,key) pairs/s"
+UNIT = "pairs/s"
+DEFAULT_WORKLOAD = "r16k_1m_k2048"
+L2_BYTES = 129 * 10 ** 6
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+FP8_OVER_BF16 = 2.0  # nominal dense FP8 : BF16 tensor-core ratio
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def init_dist(ws, backend):
+    import torch.distributed as dist
+    if ws > 1 and not dist.is_initialized():
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist.init_process_group(backend=backend)
+    return dist
+
+
+def max_over_ranks(value: float, ws: int, device=None) -> float:
+    """Largest value over ranks (all_reduce MAX); identity for one rank."""
+    if ws <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(value: float, ws: int, device=None) -> float:
+    if ws <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+def barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        try:
+            d = json.load(open(path))
+            return d, "measured"
+        except Exception:
+            pass
+    return {}, "fallback"
+
+
+def fp8_peak_tflops():
+    d, src = load_peaks()
+    bf16 = None
+    for key in ("bf16_tflops", "bf16_dense_tflops", "bf16"):
+        if key in d and isinstance(d[key], (int, float)):
+            bf16 = float(d[key])
+            break
+    if bf16 is None:
+        bf16, src = FALLBACK_BF16_TFLOPS, "fallback"
+    return bf16 * FP8_OVER_BF16, src
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples during the timed region."""
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = os.path.join("/tmp", f"mqa_clocks_{os.getpid()}.csv")
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        if self.proc is None or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in open(self.path):
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ CPU oracle arm
+def oracle_sample(p, target_seconds: float):
+    """Time the oracle on a growing row sample until it has run ~target seconds."""
+    import oracle
+    vis = p.visible()
+    rng = np.random.default_rng(7)
+    order = rng.permutation(p.rows)
+    threads = oracle.default_threads()
+    done_rows, done_pairs, spent = 0, 0, 0.0
+    batch = max(1, threads)
+    while spent < target_seconds and done_rows < p.rows:
+        rows = np.sort(order[done_rows:done_rows + batch])
+        t0 = time.perf_counter()
+        oracle.run(p, rows=rows, want_topk=True, want_scores=False, nthreads=threads)
+        spent += time.perf_counter() - t0
+        done_rows += len(rows)
+        done_pairs += int(vis[rows].sum())
+        batch = min(batch * 2, 4 * threads)
+    return {"pairs": done_pairs, "rows": done_rows, "seconds": spent, "threads": threads}
+
+
+# ------------------------------------------------------------------ main
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="fused", choices=["fused", "reference"])
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(synth.CONFIGS))
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-dense", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    ws, rank, local = dist_env()
+
+    if args.impl == "reference":
+        return run_reference(args, ws, rank)
+
+    import torch
+    import sparse_attention_indexer_relu_gb300 as mqa
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    init_dist(ws, "nccl")
+    mqa.lib()
+
+    p = synth.make(args.workload)
+    pairs = p.pairs()
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+    q, k, w, s, e = t(p.q), t(p.k), t(p.weights), t(p.starts), t(p.ends)
+    groups = t(p.scales_ue8m0)
+    scales = mqa.ue8m0_decode(groups)
+    out = torch.empty((p.rows, p.topk), dtype=torch.int32, device=dev)
+    wsb = mqa.alloc_workspace(p.rows)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        mqa.mqa_topk_prefill(q, k, scales, w, s, e, p.topk, workspace=wsb, out=out)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    status, stats = mqa.get_status(wsb)
+    if status != 0:
+        raise RuntimeError(f"device status {status} {stats}")
+
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    with ClockSampler(torch.cuda.current_device()) as clk:
+        barrier(ws)
+        torch.cuda.synchronize()
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        for i in range(args.steps):
+            ev[i][0].record(stream)
+            step()
+            ev[i][1].record(stream)
+        t1.record(stream)
+        torch.cuda.synchronize()
+        barrier(ws)
+    total_ms = t0.elapsed_time(t1)
+    kernel_ms = [a.elapsed_time(b) for a, b in ev]
+    status, stats = mqa.get_status(wsb)
+    total_ms = max_over_ranks(total_ms, ws, dev)
+    ms_per_step = total_ms / args.steps
+    all_pairs = sum_over_ranks(float(pairs) * args.steps, ws, dev)
+    value = all_pairs / (total_ms / 1e3)
+    rows_per_s = sum_over_ranks(float(p.rows) * args.steps, ws, dev) / (total_ms / 1e3)
+
+    # roofline of the fused kernel (tensor-bound: 8192 flop per scored pair)
+    k_ms = statistics.mean(kernel_ms)
+    achieved = pairs * plan.FLOP_PER_PAIR / (k_ms / 1e3) / 1e12
+    peak, peak_src = fp8_peak_tflops()
+    traffic = load_traffic(args.workload)
+
+    result = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "fp8e4m3 in, fp32 accumulate/score", "data": "synthetic (seeded; no captures available)",
+        "config": {"workload": args.workload, "rows": p.rows, "keys": p.keys, "topk": p.topk, "pairs": pairs,
+                   "heads": 32, "head_dim": 128, "parallelism": f"replicas x{ws}",
+                   "l2": "inputs exceed L2 (q+k = %d MiB > 129 MB); no flush" % ((p.q.nbytes + p.k.nbytes) >> 20)},
+        "rows_per_s": rows_per_s,
+        "gpu_launches": args.steps,
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                     "frac": achieved / peak, "traffic": traffic,
+                     "peak_source": f"{peak_src} bf16 x {FP8_OVER_BF16:g} (nominal fp8:bf16)",
+                     "kernel_ms": k_ms, "flop_per_pair": plan.FLOP_PER_PAIR},
+        "clocks": clk.summary(),
+        "stats": stats,
+    }
+
+    if not args.no_dense and rank == 0:
+        result["dense_baseline"] = time_dense(mqa, torch, q, k, scales, w, s, e, p, pairs)
+    if not args.no_e2e:
+        result["e2e"] = time_e2e(mqa, torch, dev, p, pairs, args, ws)
+    if rank == 0 and not args.no_cpu:
+        cs = oracle_sample(p, args.cpu_seconds)
+        result["cpu_baseline"] = {"value": cs["pairs"] / cs["seconds"], "unit": UNIT, "cores": cs["threads"],
+                                  "kind": "oracle",
+                                  "sample": f"{cs['rows']} random rows of {args.workload} "
+                                            f"({cs['pairs']} pairs, {cs['seconds']:.1f} s, fp64 C oracle, "
+                                            f"full sort per row)"}
+    if rank == 0:
+        print(json.dumps(result))
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def load_traffic(workload):
+    """DRAM bytes per launch of the fused kernel from the committed ncu summary
+    (None when no capture matches the current kernel)."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    try:
+        d = json.load(open(path))
+        return d.get(workload)
+    except Exception:
+        return None
+
+
+def time_dense(mqa, torch, q, k, scales, w, s, e, p, pairs, reps=2):
+    budget = 512 * 2 ** 20
+    rows_per_call = max(1, min(p.rows, budget // (p.keys * 4)))
+    L = torch.empty(rows_per_call * p.keys, dtype=torch.float32, device=q.device)
+    hdr = torch.zeros(256, dtype=torch.uint8, device=q.device)
+    out = torch.empty((p.rows, p.topk), dtype=torch.int32, device=q.device)
+    f = lambda: mqa.mqa_topk_dense_baseline(q, k, scales, w, s, e, p.topk, logits_budget_bytes=budget,
+                                            logits_ws=L, workspace=hdr, out=out)
+    f()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(reps):
+        f()
+    b.record()
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / reps
+    return {"ms": ms, "value": pairs / (ms / 1e3), "unit": UNIT,
+            "calls": plan.dense_calls(p.rows, p.keys, budget), "logits_budget_mib": 512}
+
+
+def time_e2e(mqa, torch, dev, p, pairs, args, ws):
+    """Same metric through the public API from pinned host buffers: H2D of the
+    step's inputs, UE8M0 decode, fused call, D2H of the selected indices."""
+    pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()
+    hq, hk, hg, hw, hs, he = (pin(p.q), pin(p.k), pin(p.scales_ue8m0), pin(p.weights), pin(p.starts),
+                              pin(p.ends))
+    hout = torch.empty((p.rows, p.topk), dtype=torch.int32).pin_memory()
+    dq, dk, dg, dw, ds, de = (torch.empty_like(x, device=dev) for x in (hq, hk, hg, hw, hs, he))
+    sc = torch.empty(p.keys, dtype=torch.float32, device=dev)
+    dout = torch.empty((p.rows, p.topk), dtype=torch.int32, device=dev)
+    wsb = mqa.alloc_workspace(p.rows)
+    h2d = sum(x.numel() * x.element_size() for x in (hq, hk, hg, hw, hs, he))
+    d2h = hout.numel() * hout.element_size()
+
+    def step():
+        for d, h in ((dq, hq), (dk, hk), (dg, hg), (dw, hw), (ds, hs), (de, he)):
+            d.copy_(h, non_blocking=True)
+        mqa.ue8m0_decode(dg, out=sc)
+        mqa.mqa_topk_prefill(dq, dk, sc, dw, ds, de, p.topk, workspace=wsb, out=dout)
+        hout.copy_(dout, non_blocking=True)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    steps = max(3, args.steps // 2)
+    barrier(ws)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(steps):
+        step()
+    b.record()
+    torch.cuda.synchronize()
+    barrier(ws)
+    ms = max_over_ranks(a.elapsed_time(b), ws, dev)
+    value = sum_over_ranks(float(pairs) * steps, ws, dev) / (ms / 1e3)
+    return {"value": value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "ms_per_step": ms / steps, "steps": steps, "gpu_launches_per_step": 2}
+
+
+def run_reference(args, ws, rank):
+    """Reference arm: the CPU oracle on a bounded row sample per step."""
+    if ws > 1:
+        init_dist(ws, "gloo")
+        if rank != 0:
+            import torch.distributed as dist
+            dist.barrier()
+            dist.destroy_process_group()
+            return
+    p = synth.make(args.workload)
+    per_step = max(0.5, min(20.0, 90.0 / max(1, args.steps + args.warmup)))
+    for _ in range(args.warmup):
+        oracle_sample(p, per_step / 4)
+    tot_pairs, tot_rows, tot_s, threads = 0, 0, 0.0, 1
+    for _ in range(args.steps):
+        cs = oracle_sample(p, per_step)
+        tot_pairs += cs["pairs"]
+        tot_rows += cs["rows"]
+        tot_s += cs["seconds"]
+        threads = cs["threads"]
+    value = tot_pairs / tot_s
+    pp = p.pairs()
+    res = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": 1e3 * pp / value, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "fp64 (oracle)", "data": "synthetic (seeded; no captures available)",
+        "config": {"workload": args.workload, "rows": p.rows, "keys": p.keys, "topk": p.topk, "pairs": pp,
+                   "parallelism": "cpu oracle, rank 0"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
+                         "sample": f"{tot_rows} random rows over {args.steps} steps ({tot_pairs} pairs, "
+                                   f"{tot_s:.1f} s); ms_per_step extrapolates to the whole chunk"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(res))
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -77,8 +77,8 @@ typedef struct mqa_topk_debug_options {
                           under-fills and is rescanned); 2: no gate (rows longer
                           than the slab overflow and are rescanned) */
   int slab_capacity;   /* candidate records per row; 0 = default (16384).  Must
-                          be >= topk + 256 and not above the capacity the
-                          workspace was sized for. */
+                          be a multiple of 128, at least 4 * (topk + 64), and
+                          not above the default (the workspace is sized for it) */
   int stall;           /* nonzero: the producer first waits on a barrier that
                           nothing completes; the time limit ends the wait, the
                           kernel unwinds and MQA_DEV_WAIT_TIMEOUT is recorded */

@@ -10,18 +10,19 @@
 // logits matrix never reaches HBM.  A second instantiation of the same
 // pipeline writes the logits instead (debug entry and dense baseline).
 //
-// CTA layout (512 threads):
+// CTA layout (384 threads):
 //   warp 0      producer: claims row blocks heaviest first, loads q (TMA) and
 //               per-row ranges/weights, streams 128-key K tiles (TMA) through a
 //               6-stage ring.
 //   warp 1      MMA issuer: per K tile, 4 x tcgen05.mma kind::f8f6f4
 //               (M = 128 keys, N = 8 rows x 32 heads, K = 32) into one of two
 //               256-column TMEM accumulators.
+//   warps 2-3   selection: per finished block, exact radix top-k over each
+//               row's candidates, output write or rescan request.
 //   warps 4-11  epilogue: TMEM -> registers (one key per thread), relu-weighted
 //               head sum, key scale, range mask; sampled gate; candidate
-//               emission to the block's slab; exact compaction on rescans.
-//   warps 12-15 selection: per finished block, exact radix top-k over each
-//               row's candidates, output write or rescan request.
+//               emission to per-(row, quadrant) slab segments; exact
+//               compaction on rescans.
 // Every wait is bounded by a time limit; on expiry the kernel records
 // MQA_DEV_WAIT_TIMEOUT in the workspace status word and unwinds.
 #include "mqa_internal.h"
@@ -35,6 +36,7 @@ namespace mqa {
 constexpr uint32_t kIdesc = idesc_f8_e4m3_f32(kTileKeys, kCols);
 constexpr int kEpiThreads = kEpiWarps * 32;
 constexpr int kEpiBarrier = 1;  // named barrier id for the epilogue warps
+constexpr int kGateBins = 288;  // 257 two-sided distance bins, padded to 9 per lane
 
 struct JobInfo {
   int block;      // row block (-1: no more work)
@@ -52,8 +54,9 @@ struct SelSlot {  // what the selection warps need from a finished scan
   int block, mode;
   uint32_t mask;
   int nrows;
-  int start[kBlockRows], n[kBlockRows], cnt[kBlockRows];
+  int start[kBlockRows], n[kBlockRows];
   int gated[kBlockRows];
+  int segcnt[kBlockRows][kQuads];  // records appended per (row, quadrant segment)
 };
 
 struct Smem {
@@ -62,11 +65,11 @@ struct Smem {
   JobInfo job[2];
   SelSlot sel[2];
   float tau[kBlockRows];
-  int cnt[kBlockRows];
+  int segcnt[kBlockRows][kQuads];
   uint32_t ref[kBlockRows];
   int ref_frozen[kBlockRows];
   int msample[kBlockRows];
-  int hist[kBlockRows][256];
+  int hist[kBlockRows][kGateBins];
   int selhist[kSelWarps][256];
   uint16_t order[kMaxSortBlocks];
   uint64_t k_full[kKStages], k_empty[kKStages];
@@ -129,20 +132,29 @@ __device__ __forceinline__ bool wait_counter(Smem &S, int *flag, int target, con
 }
 
 // ------------------------------------------------------------------ scoring
-// s = scale * sum_h w_h * max(acc_h, 0), accumulated in two packed fp32 pairs.
-// The same routine serves the fused and the logits instantiations, so both
-// produce bit-identical scores.
-__device__ __forceinline__ float relu_weighted_sum(const uint32_t (&v)[32], const float *w, float scale) {
-  float2 a0 = make_float2(0.f, 0.f), a1 = make_float2(0.f, 0.f);
+// s = scale * sum_h w_h * relu(acc_h).  relu is formed as (x + |x|) / 2: a
+// packed FP add whose second operand carries an absolute-value modifier (FMA
+// pipe), with the 1/2 folded into the scale.  x + |x| is exactly 2x or 0 and
+// the halving is exact, so the result equals the plain relu form.  Four packed
+// accumulators keep the FMA chains short; the summation order is fixed, and
+// the fused and logits instantiations share this routine, so both produce
+// bit-identical scores.
+__device__ __forceinline__ float relu_weighted_sum(const uint32_t (&v)[32], const float *w, float half_scale) {
+  float2 a[4];
 #pragma unroll
-  for (int h = 0; h < kHeads; h += 4) {
-    const float4 wv = *reinterpret_cast<const float4 *>(w + h);
-    const float2 r0 = make_float2(fmaxf(__uint_as_float(v[h]), 0.f), fmaxf(__uint_as_float(v[h + 1]), 0.f));
-    const float2 r1 = make_float2(fmaxf(__uint_as_float(v[h + 2]), 0.f), fmaxf(__uint_as_float(v[h + 3]), 0.f));
-    a0 = __ffma2_rn(r0, make_float2(wv.x, wv.y), a0);
-    a1 = __ffma2_rn(r1, make_float2(wv.z, wv.w), a1);
+  for (int i = 0; i < 4; ++i) a[i] = make_float2(0.f, 0.f);
+#pragma unroll
+  for (int g = 0; g < kHeads / 4; ++g) {
+    const float4 wv = *reinterpret_cast<const float4 *>(w + 4 * g);
+    const float2 x0 = make_float2(__uint_as_float(v[4 * g]), __uint_as_float(v[4 * g + 1]));
+    const float2 x1 = make_float2(__uint_as_float(v[4 * g + 2]), __uint_as_float(v[4 * g + 3]));
+    const float2 r0 = __fadd2_rn(x0, make_float2(fabsf(x0.x), fabsf(x0.y)));
+    const float2 r1 = __fadd2_rn(x1, make_float2(fabsf(x1.x), fabsf(x1.y)));
+    a[(2 * g) & 3] = __ffma2_rn(r0, make_float2(wv.x, wv.y), a[(2 * g) & 3]);
+    a[(2 * g + 1) & 3] = __ffma2_rn(r1, make_float2(wv.z, wv.w), a[(2 * g + 1) & 3]);
   }
-  return ((a0.x + a0.y) + (a1.x + a1.y)) * scale;
+  const float2 t = __fadd2_rn(__fadd2_rn(a[0], a[1]), __fadd2_rn(a[2], a[3]));
+  return (t.x + t.y) * half_scale;
 }
 
 // ------------------------------------------------------------------ sample gate bins
@@ -154,6 +166,19 @@ __device__ __forceinline__ int dist_bin(uint32_t d) {
   const uint32_t sub = msb >= 2 ? (d >> (msb - 2)) & 3u : (d << (2 - msb)) & 3u;
   return 1 + 4 * msb + (int)sub;
 }
+// Smallest distance inside bin b (b >= 1).
+__device__ __forceinline__ uint32_t dist_bin_lo(int b) {
+  const int msb = (b - 1) >> 2, sub = (b - 1) & 3;
+  if (msb >= 2) return (uint32_t)(4 + sub) << (msb - 2);
+  return (uint32_t)((4 + sub) >> (2 - msb));
+}
+// Gate bins are two-sided around the reference key: bins 0..127 hold scores
+// above it (farther above = smaller bin), bin 128 the reference itself, bins
+// 129..256 scores below it (farther below = larger bin).  Bin order is
+// therefore descending score order.
+__device__ __forceinline__ int gate_bin(uint32_t key, uint32_t ref) {
+  return key > ref ? 128 - dist_bin(key - ref) : 128 + dist_bin(ref - key);
+}
 // Smallest distance beyond bin b (every d in bins 0..b is below it).
 __device__ __forceinline__ uint64_t dist_bin_hi(int b) {
   if (b == 0) return 1;
@@ -163,10 +188,20 @@ __device__ __forceinline__ uint64_t dist_bin_hi(int b) {
 }
 
 // ------------------------------------------------------------------ warp radix select
-// Exact k-th largest order key among keys[0, n) (requires n > k >= 1), by
-// four 8-bit digit levels.  Returns the key T; *take_eq receives how many of
-// the keys equal to T belong to the top k (the rest of the top k is > T).
-__device__ uint32_t warp_radix_select(const uint32_t *keys, int n, int k, int *hist, int lane, int *take_eq) {
+// A row's candidates live in kQuads segments (one per TMEM lane quadrant) of
+// `seg` records each; segment q holds c[q] valid records.
+struct RowSlab {
+  uint32_t *keys;  // [kQuads][seg]
+  int32_t *idx;    // [kQuads][seg]
+  int seg;
+  int c[kQuads];
+  __device__ int total() const { return c[0] + c[1] + c[2] + c[3]; }
+};
+
+// Exact k-th largest order key over the row's candidates (requires total > k
+// >= 1), by four 8-bit digit levels.  Returns the key T; *take_eq receives
+// how many keys equal to T belong to the top k (the rest of the top k is > T).
+__device__ uint32_t warp_radix_select(const RowSlab &R, int k, int *hist, int lane, int *take_eq) {
   uint32_t prefix = 0;
   int want = k;
 #pragma unroll 1
@@ -176,17 +211,22 @@ __device__ uint32_t warp_radix_select(const uint32_t *keys, int n, int k, int *h
     for (int b = lane; b < 256; b += 32) hist[b] = 0;
     __syncwarp();
 #pragma unroll 1
-    for (int i0 = 0; i0 < n; i0 += 32 * 8) {
-      uint32_t kk[8];
+    for (int q = 0; q < kQuads; ++q) {
+      const uint32_t *keys = R.keys + (size_t)q * R.seg;
+      const int n = R.c[q];
+#pragma unroll 1
+      for (int i0 = 0; i0 < n; i0 += 32 * 8) {
+        uint32_t kk[8];
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const int i = i0 + 32 * j + lane;
-        kk[j] = i < n ? __ldcg(keys + i) : 0u;
-      }
+        for (int j = 0; j < 8; ++j) {
+          const int i = i0 + 32 * j + lane;
+          kk[j] = i < n ? __ldcg(keys + i) : 0u;
+        }
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const int i = i0 + 32 * j + lane;
-        if (i < n && (kk[j] & hi_mask) == prefix) atomicAdd(&hist[(kk[j] >> shift) & 255u], 1);
+        for (int j = 0; j < 8; ++j) {
+          const int i = i0 + 32 * j + lane;
+          if (i < n && (kk[j] & hi_mask) == prefix) atomicAdd(&hist[(kk[j] >> shift) & 255u], 1);
+        }
       }
     }
     __syncwarp();
@@ -228,47 +268,55 @@ __device__ uint32_t warp_radix_select(const uint32_t *keys, int n, int k, int *h
   return prefix;
 }
 
-// Stream keys/idx[0, n) once, keeping every key > T plus the first `take_eq`
-// keys equal to T (all keys when take_all).  Kept entries either go to
-// `out` as idx - base (-1 padding up to k is written by the caller) or are
-// compacted in place (stable; writes never overtake reads).  Returns the count.
+// Stream the row's candidates once, keeping every key > T plus the first
+// `take_eq` keys equal to T (all keys when take_all).  Kept entries either go
+// to `out` as idx - base (the caller pads with -1) or are compacted into
+// segment 0 (stable; within segment 0 writes never overtake reads, and the
+// other segments are only read).  At most `limit` entries are kept.
 template <bool kCompact>
-__device__ int warp_emit(uint32_t *keys, int32_t *idx, int n, uint32_t T, int take_eq, bool take_all, int32_t *out,
-                         int base, int limit, int lane) {
+__device__ int warp_emit(const RowSlab &R, uint32_t T, int take_eq, bool take_all, int32_t *out, int base,
+                         int limit, int lane) {
   int outc = 0, eq_seen = 0;
   const uint32_t lt = lanemask_lt();
 #pragma unroll 1
-  for (int i0 = 0; i0 < n; i0 += 32 * 4) {
-    uint32_t kk[4];
-    int32_t ii[4];
+  for (int q = 0; q < kQuads; ++q) {
+    const uint32_t *keys = R.keys + (size_t)q * R.seg;
+    const int32_t *idx = R.idx + (size_t)q * R.seg;
+    const int n = R.c[q];
+#pragma unroll 1
+    for (int i0 = 0; i0 < n; i0 += 32 * 4) {
+      uint32_t kk[4];
+      int32_t ii[4];
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int i = i0 + 32 * j + lane;
-      kk[j] = i < n ? __ldcg(keys + i) : 0u;
-      ii[j] = i < n ? __ldcg(idx + i) : 0;
-    }
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int i = i0 + 32 * j + lane;
-      const bool v = i < n;
-      const bool gt = v && (take_all || kk[j] > T);
-      const bool eq = v && !take_all && kk[j] == T;
-      const uint32_t beq = __ballot_sync(0xFFFFFFFFu, eq);
-      const int eq_rank = eq_seen + __popc(beq & lt);
-      const bool take = gt || (eq && eq_rank < take_eq);
-      const uint32_t bt = __ballot_sync(0xFFFFFFFFu, take);
-      if (take) {
-        const int pos = outc + __popc(bt & lt);
-        if (pos >= limit) {
-        } else if (kCompact) {
-          keys[pos] = kk[j];
-          idx[pos] = ii[j];
-        } else {
-          out[pos] = ii[j] - base;
-        }
+      for (int j = 0; j < 4; ++j) {
+        const int i = i0 + 32 * j + lane;
+        kk[j] = i < n ? __ldcg(keys + i) : 0u;
+        ii[j] = i < n ? __ldcg(idx + i) : 0;
       }
-      outc += __popc(bt);
-      eq_seen += __popc(beq);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int i = i0 + 32 * j + lane;
+        const bool v = i < n;
+        const bool gt = v && (take_all || kk[j] > T);
+        const bool eq = v && !take_all && kk[j] == T;
+        const uint32_t beq = __ballot_sync(0xFFFFFFFFu, eq);
+        const int eq_rank = eq_seen + __popc(beq & lt);
+        const bool take = gt || (eq && eq_rank < take_eq);
+        const uint32_t bt = __ballot_sync(0xFFFFFFFFu, take);
+        if (take) {
+          const int pos = outc + __popc(bt & lt);
+          if (pos < limit) {
+            if (kCompact) {
+              R.keys[pos] = kk[j];
+              R.idx[pos] = ii[j];
+            } else {
+              out[pos] = ii[j] - base;
+            }
+          }
+        }
+        outc += __popc(bt);
+        eq_seen += __popc(beq);
+      }
     }
   }
   return outc < limit ? outc : limit;
@@ -315,7 +363,8 @@ __device__ void build_order(Smem &S, const FusedParams &p) {
 }
 
 __device__ __forceinline__ int sample_tile(const JobInfo &J, int u) {
-  return J.lo_t + (int)(((long long)(2 * u + 1) * J.nt) / (2LL * J.ns));
+  // (2u + 1) * nt < 2^31 for nt <= 2^17 tiles and u < 64
+  return J.lo_t + (int)((unsigned)((2 * u + 1) * J.nt) / (unsigned)(2 * J.ns));
 }
 
 // ------------------------------------------------------------------ producer (warp 0)
@@ -524,12 +573,13 @@ __device__ void mma_issuer(Smem &S, uint32_t tmem, const FusedParams &p) {
 // ------------------------------------------------------------------ epilogue (warps 4-11)
 template <bool kLogits>
 __device__ void epilogue(Smem &S, uint32_t tmem, const FusedParams &p, int warp, int lane) {
-  const int ew = warp - kEpiWarp0;     // 0..7
-  const int quad = warp & 3;           // TMEM lane quadrant this warp may access
-  const int half = ew >> 2;            // rows 4*half .. 4*half+3
+  const int ew = warp - kEpiWarp0;  // 0..7
+  const int quad = warp & 3;        // TMEM lane quadrant this warp may access
+  const int half = ew >> 2;         // rows 4*half .. 4*half+3
   const uint32_t lane_addr = (uint32_t)(quad * 32) << 16;
   const float NEG_INF = -INFINITY;
-  const int cap = p.cap;
+  const int cap = p.cap, seg = p.cap / kQuads;
+  const uint32_t lt = lanemask_lt();
   int job_iter = 0, tcount = 0;
   for (;;) {
     const int slot = job_iter & 1;
@@ -555,15 +605,14 @@ __device__ void epilogue(Smem &S, uint32_t tmem, const FusedParams &p, int warp,
         float t0 = NEG_INF;
         if (J.ns == 0 && J.mode == 0 && p.force_gate == 1 && n > 0) t0 = INFINITY;
         S.tau[ew] = t0;
-        S.cnt[ew] = 0;
         S.ref[ew] = 0;
         S.ref_frozen[ew] = 0;
         S.msample[ew] = 0;
       }
-      for (int b = lane; b < 256; b += 32) S.hist[ew][b] = 0;
+      for (int b = lane; b < kGateBins; b += 32) S.hist[ew][b] = 0;
     }
     if (bar_or(kEpiBarrier, kEpiThreads, !ok || aborted(S))) break;
-    int st[4], en[4];
+    int st[4], en[4], cnt[4];
     bool act[4];
     float tau[4];
 #pragma unroll
@@ -573,37 +622,66 @@ __device__ void epilogue(Smem &S, uint32_t tmem, const FusedParams &p, int warp,
       en[rr] = J.end[r];
       act[rr] = ((J.mask >> r) & 1u) != 0;
       tau[rr] = kLogits ? NEG_INF : S.tau[r];
+      cnt[rr] = 0;
     }
     const int ns = J.ns, ntiles = J.ns + J.nt, mode = J.mode;
     const int block = J.block;
     uint32_t *slab_keys = p.slab + ((size_t)(blockIdx.x * kSlots + slot) * 2 * kBlockRows) * (size_t)cap;
     int32_t *slab_idx = reinterpret_cast<int32_t *>(slab_keys + (size_t)kBlockRows * cap);
+    // this warp's segment of row r: slab_*[(r * kQuads + quad) * seg]
     bool bail = false;
+    auto tile_of = [&](int u) {
+      if (u < ns) return sample_tile(J, u);  // division only on the few sample tiles
+      return J.lo_t + (u - ns);
+    };
+    auto scale_of = [&](int u) {
+      const int kk = tile_of(u) * kTileKeys + quad * 32 + lane;
+      return (u < ntiles && kk < p.keys) ? 0.5f * __ldg(p.scales + kk) : 0.f;
+    };
+    float hsc_next = scale_of(0);
     for (int u = 0; u < ntiles && !bail; ++u) {
       const bool sampling = u < ns;
-      const int tile = sampling ? sample_tile(J, u) : J.lo_t + (u - ns);
+      const int tile = tile_of(u);
       const int key = tile * kTileKeys + quad * 32 + lane;
-      const float sc = key < p.keys ? __ldg(p.scales + key) : 0.f;
+      const float hsc = hsc_next;
+      hsc_next = scale_of(u + 1);  // one tile ahead: hides the global-load latency
       const int buf = tcount & 1;
+      // rows whose range covers the whole tile need no per-key mask (warp-uniform)
+      bool inside[4];
+      const int tile_lo = tile * kTileKeys;
+#pragma unroll
+      for (int rr = 0; rr < 4; ++rr) inside[rr] = tile_lo >= st[rr] && tile_lo + kTileKeys <= en[rr];
       ok = wait_bar(S, &S.t_full[buf], (tcount >> 1) & 1, p);
       ok = __all_sync(0xFFFFFFFFu, ok);
       tc_fence_after();
+      // two rows per TMEM round trip; the buffer goes back to the MMA as soon
+      // as the second pair is in registers
+      const uint32_t base = tmem + lane_addr + (uint32_t)(buf * kCols + (4 * half) * kHeads);
       float sv[4];
 #pragma unroll
-      for (int rr = 0; rr < 4; ++rr) {
-        sv[rr] = NEG_INF;
-        if (act[rr] && ok) {
-          const int r = 4 * half + rr;
-          uint32_t v[32];
-          tmem_ld_32x32b_x32(tmem + lane_addr + (uint32_t)(buf * kCols + r * kHeads), v);
-          tmem_ld_wait();
-          const float s = relu_weighted_sum(v, &J.w[r][0], sc);
-          if (key >= st[rr] && key < en[rr]) sv[rr] = s;
+      for (int pr = 0; pr < 2; ++pr) {
+        const int ra = 2 * pr, rb = 2 * pr + 1;
+        const bool la = act[ra] && ok, lb = act[rb] && ok;
+        uint32_t va[32], vb[32];
+        if (la) tmem_ld_32x32b_x32(base + (uint32_t)(ra * kHeads), va);
+        if (lb) tmem_ld_32x32b_x32(base + (uint32_t)(rb * kHeads), vb);
+        tmem_ld_wait();
+        if (pr == 1) {
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&S.t_empty[buf]);
+        }
+        sv[ra] = NEG_INF;
+        sv[rb] = NEG_INF;
+        if (la) {
+          const float s = relu_weighted_sum(va, &J.w[4 * half + ra][0], hsc);
+          if (inside[ra] || (key >= st[ra] && key < en[ra])) sv[ra] = s;
+        }
+        if (lb) {
+          const float s = relu_weighted_sum(vb, &J.w[4 * half + rb][0], hsc);
+          if (inside[rb] || (key >= st[rb] && key < en[rb])) sv[rb] = s;
         }
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&S.t_empty[buf]);
       ++tcount;
       if (kLogits) {
         if (key < p.keys) {
@@ -629,17 +707,14 @@ __device__ void epilogue(Smem &S, uint32_t tmem, const FusedParams &p, int warp,
           }
         }
         if (bar_or(kEpiBarrier, kEpiThreads, aborted(S))) { bail = true; break; }
-        // step B: histogram of the distance below the reference
+        // step B: histogram of the position relative to the reference
 #pragma unroll
         for (int rr = 0; rr < 4; ++rr) {
           const int r = 4 * half + rr;
           if (act[rr]) {
             const uint32_t ref = S.ref[r];
             const bool vis = sv[rr] > NEG_INF;
-            if (ref && vis) {
-              const uint32_t kv = f2key(sv[rr]);
-              atomicAdd(&S.hist[r][dist_bin(kv < ref ? ref - kv : 0u)], 1);
-            }
+            if (ref && vis) atomicAdd(&S.hist[r][gate_bin(f2key(sv[rr]), ref)], 1);
             const uint32_t bv = __ballot_sync(0xFFFFFFFFu, vis && ref != 0);
             if (lane == 0 && bv) atomicAdd(&S.msample[r], __popc(bv));
             if (quad == 0 && lane == 0) S.ref_frozen[r] = ref != 0;
@@ -654,17 +729,18 @@ __device__ void epilogue(Smem &S, uint32_t tmem, const FusedParams &p, int warp,
           const int m = S.msample[r];
           if (((J.mask >> r) & 1u) && n > cap && m > 0) {
             const long long jwant = max(1LL, ((long long)m * p.gate_target + n - 1) / n);
-            int c[5], tot = 0;
+            constexpr int kPer = kGateBins / 32;
+            int c[kPer], tot = 0;
 #pragma unroll
-            for (int j = 0; j < 5; ++j) {
-              c[j] = S.hist[r][5 * lane + j];
+            for (int j = 0; j < kPer; ++j) {
+              c[j] = S.hist[r][kPer * lane + j];
               tot += c[j];
             }
             int incl = tot;
 #pragma unroll
             for (int off = 1; off < 32; off <<= 1) {
-              const int v = __shfl_up_sync(0xFFFFFFFFu, incl, off);
-              if (lane >= off) incl += v;
+              const int vv = __shfl_up_sync(0xFFFFFFFFu, incl, off);
+              if (lane >= off) incl += vv;
             }
             const int excl = incl - tot;
             const uint32_t bm = __ballot_sync(0xFFFFFFFFu, excl < jwant && jwant <= incl);
@@ -674,15 +750,22 @@ __device__ void epilogue(Smem &S, uint32_t tmem, const FusedParams &p, int warp,
               if (lane == src) {
                 int run = excl;
 #pragma unroll
-                for (int j = 0; j < 5; ++j) {
+                for (int j = 0; j < kPer; ++j) {
                   run += c[j];
-                  if (run >= jwant) { bin = 5 * lane + j; break; }
+                  if (run >= jwant) { bin = kPer * lane + j; break; }
                 }
               }
               bin = __shfl_sync(0xFFFFFFFFu, bin, src);
-              const uint64_t dhi = dist_bin_hi(bin);
               const uint32_t ref = S.ref[r];
-              if ((uint64_t)ref > dhi) t = key2f(ref - (uint32_t)dhi);
+              if (bin >= 128) {
+                // pass every key whose distance below the reference is inside bins 128..bin
+                const uint64_t dhi = dist_bin_hi(bin - 128);
+                if ((uint64_t)ref > dhi) t = key2f(ref - (uint32_t)dhi);
+              } else {
+                // pass every key at least the lower edge of its bin above the reference
+                const uint64_t kt = (uint64_t)ref + dist_bin_lo(128 - bin) - 1;
+                t = kt >= 0xFFFFFFFFull ? INFINITY : key2f((uint32_t)kt);
+              }
             }
           }
           if (lane == 0) S.tau[r] = t;
@@ -693,39 +776,49 @@ __device__ void epilogue(Smem &S, uint32_t tmem, const FusedParams &p, int warp,
         }
         continue;
       }
-      // main scan: candidate emission
+      // main scan: append keys above the gate to this warp's segment of each row
+      // (a private counter per warp: no atomics)
 #pragma unroll
       for (int rr = 0; rr < 4; ++rr) {
-        const int r = 4 * half + rr;
         const bool pass = sv[rr] > tau[rr];
         const uint32_t bal = __ballot_sync(0xFFFFFFFFu, pass);
         if (bal) {
-          const int leader = __ffs(bal) - 1;
-          int base = 0;
-          if (lane == leader) base = atomicAdd(&S.cnt[r], __popc(bal));
-          base = __shfl_sync(0xFFFFFFFFu, base, leader);
-          if (pass) {
-            const int pos = base + __popc(bal & lanemask_lt());
-            if (pos < cap) {
-              slab_keys[(size_t)r * cap + pos] = f2key(sv[rr]);
-              slab_idx[(size_t)r * cap + pos] = key;
-            }
+          const int pos = cnt[rr] + __popc(bal & lt);
+          if (pass && pos < seg) {
+            const size_t o = (size_t)((4 * half + rr) * kQuads + quad) * seg + pos;
+            slab_keys[o] = f2key(sv[rr]);
+            slab_idx[o] = key;
           }
+          cnt[rr] += __popc(bal);
         }
       }
       if (mode == 1) {
-        // exact rescan: keep each row's slab bounded by compacting to its top-k
+        // exact rescan: keep each row's segments bounded by compacting the row
+        // to its top-k (into segment 0) before any segment can overflow
+        if (lane == 0) {
+#pragma unroll
+          for (int rr = 0; rr < 4; ++rr) S.segcnt[4 * half + rr][quad] = cnt[rr];
+        }
         if (bar_or(kEpiBarrier, kEpiThreads, aborted(S))) { bail = true; break; }
         const int r = ew;
-        if (((J.mask >> r) & 1u) && S.cnt[r] + kTileKeys > cap) {
+        RowSlab R;
+        R.keys = slab_keys + (size_t)r * kQuads * seg;
+        R.idx = slab_idx + (size_t)r * kQuads * seg;
+        R.seg = seg;
+        int mx = 0;
+#pragma unroll
+        for (int q = 0; q < kQuads; ++q) {
+          R.c[q] = S.segcnt[r][q];
+          mx = max(mx, R.c[q]);
+        }
+        if (((J.mask >> r) & 1u) && mx + 32 > seg) {
           int take_eq = 0;
-          const int n = S.cnt[r];
-          const uint32_t T = warp_radix_select(slab_keys + (size_t)r * cap, n, p.topk, &S.hist[r][0], lane, &take_eq);
-          warp_emit<true>(slab_keys + (size_t)r * cap, slab_idx + (size_t)r * cap, n, T, take_eq, false, nullptr, 0,
-                          p.topk, lane);
+          const uint32_t T = warp_radix_select(R, p.topk, &S.hist[r][0], lane, &take_eq);
+          warp_emit<true>(R, T, take_eq, false, nullptr, 0, p.topk, lane);
           __syncwarp();
           if (lane == 0) {
-            S.cnt[r] = p.topk;
+            S.segcnt[r][0] = p.topk;
+            for (int q = 1; q < kQuads; ++q) S.segcnt[r][q] = 0;
             S.tau[r] = key2f(T);
             atomicAdd(p.ws + kWsCompactions, 1);
           }
@@ -733,8 +826,15 @@ __device__ void epilogue(Smem &S, uint32_t tmem, const FusedParams &p, int warp,
         __threadfence_block();
         if (bar_or(kEpiBarrier, kEpiThreads, aborted(S))) { bail = true; break; }
 #pragma unroll
-        for (int rr = 0; rr < 4; ++rr) tau[rr] = S.tau[4 * half + rr];
+        for (int rr = 0; rr < 4; ++rr) {
+          tau[rr] = S.tau[4 * half + rr];
+          cnt[rr] = S.segcnt[4 * half + rr][quad];
+        }
       }
+    }
+    if (!kLogits && lane == 0) {
+#pragma unroll
+      for (int rr = 0; rr < 4; ++rr) S.segcnt[4 * half + rr][quad] = cnt[rr];
     }
     __threadfence_block();  // slab writes of every epilogue warp precede the hand-over
     if (bar_or(kEpiBarrier, kEpiThreads, bail || aborted(S))) break;
@@ -744,9 +844,9 @@ __device__ void epilogue(Smem &S, uint32_t tmem, const FusedParams &p, int warp,
         if (lane < kBlockRows) {
           Q.start[lane] = J.start[lane];
           Q.n[lane] = J.end[lane] - J.start[lane];
-          Q.cnt[lane] = S.cnt[lane];
           Q.gated[lane] = S.tau[lane] > NEG_INF;
         }
+        Q.segcnt[lane >> 2][lane & 3] = S.segcnt[lane >> 2][lane & 3];
         if (lane == 0) {
           Q.block = J.block;
           Q.mode = J.mode;
@@ -763,17 +863,15 @@ __device__ void epilogue(Smem &S, uint32_t tmem, const FusedParams &p, int warp,
   }
 }
 
-// ------------------------------------------------------------------ selection (warps 12-15)
+// ------------------------------------------------------------------ selection (warps 2-3)
 __device__ void selection(Smem &S, const FusedParams &p, int warp, int lane) {
   const int sw = warp - kSelWarp0;
   int *hist = &S.selhist[sw][0];
-  const int cap = p.cap;
+  const int cap = p.cap, seg = p.cap / kQuads;
   int job_iter = 0;
   for (;;) {
     const int slot = job_iter & 1;
     bool ok = true;
-    // A job reaches selection only after its scan; stop once the producer has
-    // ended and every issued scan has been handed over.
     if (lane == 0) ok = wait_bar(S, &S.s_full[slot], (job_iter >> 1) & 1, p);
     ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
     if (!ok) break;
@@ -784,14 +882,24 @@ __device__ void selection(Smem &S, const FusedParams &p, int warp, int lane) {
     uint32_t fail = 0;
     for (int r = sw; r < Q.nrows; r += kSelWarps) {
       if (!((Q.mask >> r) & 1u)) continue;
-      const int n = Q.n[r], cnt = Q.cnt[r];
+      const int n = Q.n[r];
       const int topk = p.topk;
+      RowSlab R;
+      R.keys = slab_keys + (size_t)r * kQuads * seg;
+      R.idx = slab_idx + (size_t)r * kQuads * seg;
+      R.seg = seg;
+      bool over = false;
+#pragma unroll
+      for (int q = 0; q < kQuads; ++q) {
+        R.c[q] = Q.segcnt[r][q];
+        over = over || R.c[q] > seg;
+      }
+      const int cnt = R.total();
       if (Q.mode == 0) {
-        const bool over = cnt > cap;
         const bool under = Q.gated[r] && cnt < min(topk, n);
         if (lane == 0) {
           if (Q.gated[r]) atomicAdd(p.ws + kWsGatedRows, 1);
-          atomicAdd(p.ws + kWsCandidates, min(cnt, cap));
+          atomicAdd(p.ws + kWsCandidates, cnt);
           if (over) atomicAdd(p.ws + kWsOverflowRows, 1);
           if (under) atomicAdd(p.ws + kWsUnderfillRows, 1);
         }
@@ -804,15 +912,13 @@ __device__ void selection(Smem &S, const FusedParams &p, int warp, int lane) {
       }
       const int row = Q.block * kBlockRows + r;
       int32_t *out = p.out + (size_t)row * topk;
-      uint32_t *kr = slab_keys + (size_t)r * cap;
-      int32_t *ir = slab_idx + (size_t)r * cap;
       int wrote;
       if (cnt <= topk) {
-        wrote = warp_emit<false>(kr, ir, cnt, 0u, 0, true, out, Q.start[r], topk, lane);
+        wrote = warp_emit<false>(R, 0u, 0, true, out, Q.start[r], topk, lane);
       } else {
         int take_eq = 0;
-        const uint32_t T = warp_radix_select(kr, cnt, topk, hist, lane, &take_eq);
-        wrote = warp_emit<false>(kr, ir, cnt, T, take_eq, false, out, Q.start[r], topk, lane);
+        const uint32_t T = warp_radix_select(R, topk, hist, lane, &take_eq);
+        wrote = warp_emit<false>(R, T, take_eq, false, out, Q.start[r], topk, lane);
       }
       for (int i = wrote + lane; i < topk; i += 32) out[i] = -1;
     }
@@ -894,12 +1000,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     producer<kLogits>(S, &q_map, &k_map, p, lane);
   } else if (warp == 1) {
     if (lane == 0) mma_issuer(S, tmem, p);
-  } else if (warp >= kEpiWarp0 && warp < kSelWarp0) {
+  } else if (warp >= kEpiWarp0) {
     epilogue<kLogits>(S, tmem, p, warp, lane);
-  } else if (warp >= kSelWarp0) {
-    if (!kLogits) {
-      selection(S, p, warp, lane);
-    }
+  } else if (warp >= kSelWarp0 && warp < kSelWarp0 + kSelWarps) {
+    if (!kLogits) selection(S, p, warp, lane);
   }
   __syncthreads();
   if (warp == 1) {

@@ -18,12 +18,13 @@ constexpr int kQBytes = kCols * kDim;       // 32 KiB of q per block
 constexpr int kKTileBytes = kTileKeys * kDim;  // 16 KiB of k per tile
 
 constexpr int kEpiWarps = 8;    // two per TMEM lane quadrant; each owns 4 rows
-constexpr int kSelWarps = 4;    // candidate selection warps
-constexpr int kThreads = 512;   // warps 0-3 control, 4-11 epilogue, 12-15 selection
+constexpr int kSelWarps = 2;    // candidate selection warps
+constexpr int kThreads = 384;   // warp 0 producer, 1 MMA, 2-3 selection, 4-11 epilogue
 constexpr int kEpiWarp0 = 4;
-constexpr int kSelWarp0 = 12;
+constexpr int kSelWarp0 = 2;
+constexpr int kQuads = 4;       // TMEM lane quadrants; each row's slab has one segment per quadrant
 
-constexpr int kDefaultSlabCap = 16384;  // candidate records per row per slot
+constexpr int kDefaultSlabCap = 16384;  // candidate records per row per slot (4 segments)
 constexpr int kSlots = 2;               // slab slots per CTA (scan one, select the other)
 constexpr int kMaxSortBlocks = 8192;    // heaviest-first order kept in smem up to this many blocks
 constexpr int kMaxKeys = 1 << 24;

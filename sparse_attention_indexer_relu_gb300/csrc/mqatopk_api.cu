@@ -128,7 +128,9 @@ int run_fused(const void *q, const void *k, const float *scales, const float *we
   int cap = kDefaultSlabCap;
   if (opt && opt->slab_capacity) {
     cap = opt->slab_capacity;
-    if (cap < topk + 256 || cap > kDefaultSlabCap) return MQA_ERR_INVALID_ARGUMENT;
+    // four per-quadrant segments, each able to hold top-k plus one tile's worth
+    if (cap % (kQuads * 32) != 0 || cap / kQuads < topk + 64 || cap > kDefaultSlabCap)
+      return MQA_ERR_INVALID_ARGUMENT;
   }
   if (opt && (opt->force_gate < 0 || opt->force_gate > 2 || opt->wait_timeout_ms < 0 || opt->max_ctas < 0))
     return MQA_ERR_INVALID_ARGUMENT;
@@ -159,7 +161,7 @@ int run_fused(const void *q, const void *k, const float *scales, const float *we
   p.topk = topk;
   p.nblocks = (rows + kBlockRows - 1) / kBlockRows;
   p.cap = cap;
-  p.gate_target = 4 * topk < cap / 2 ? 4 * topk : cap / 2;
+  p.gate_target = 3 * topk < cap / 2 ? 3 * topk : cap / 2;
   p.force_gate = opt ? opt->force_gate : 0;
   p.stall = opt ? opt->stall : 0;
   p.timeout_ns = (long long)((opt && opt->wait_timeout_ms) ? opt->wait_timeout_ms : 4000) * 1000000LL;

@@ -67,6 +67,20 @@ def quantize_e4m3fn(x: np.ndarray) -> np.ndarray:
     return (code.astype(np.uint8) | sign).astype(np.uint8)
 
 
+def quantize_e4m3fn_fast(x: np.ndarray) -> np.ndarray:
+    """Same codes as `quantize_e4m3fn` for large arrays: saturate to +-448,
+    then torch's round-to-nearest-even float8_e4m3fn cast (chunked)."""
+    import torch
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    out = np.empty(x.shape, dtype=np.uint8)
+    xf, of = x.reshape(-1), out.reshape(-1)
+    step = 1 << 24
+    for i in range(0, xf.size, step):
+        t = torch.from_numpy(xf[i:i + step]).clamp(-E4M3_MAX, E4M3_MAX)
+        of[i:i + step] = t.to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    return out
+
+
 def ue8m0_bytes(exponents: np.ndarray) -> np.ndarray:
     """Pack per-key exponents as the cache's [keys, 4] uint8 groups (4 equal bytes)."""
     e = np.asarray(exponents, dtype=np.uint8)
@@ -117,7 +131,8 @@ def _draw_core(rng, rows, keys, heads=HEADS, dim=HEAD_DIM, k_offset_dim0: float 
         kf[:, 0] += np.float32(k_offset_dim0)
     w = (rng.standard_normal((rows, heads), dtype=np.float32) / np.float32(math.sqrt(heads))).astype(np.float32)
     exps = rng.integers(120, 128, size=keys, dtype=np.int64).astype(np.uint8)
-    return quantize_e4m3fn(qf), quantize_e4m3fn(kf), w, exps
+    quant = quantize_e4m3fn if qf.size + kf.size <= (1 << 22) else quantize_e4m3fn_fast
+    return quant(qf), quant(kf), w, exps
 
 
 def causal_tail(rows: int, keys: int, base: int = 0):

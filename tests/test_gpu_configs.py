@@ -1,0 +1,75 @@
+"""Parity on the workload table's chunk shapes, in the launch configuration
+the benchmark times: every row is checked for structure, sampled rows against
+the oracle (exact top-k up to boundary ties)."""
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from parity import check_topk_rows, to_device
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def mqa():
+    import torch
+    assert torch.cuda.is_available()
+    import sparse_attention_indexer_relu_gb300 as m
+    m.lib()
+    return m
+
+
+def structure_all_rows(got, p):
+    n = np.maximum(p.ends.astype(np.int64) - p.starts.astype(np.int64), 0)
+    c = np.minimum(n, p.topk)
+    col = np.arange(p.topk)[None, :]
+    valid = col < c[:, None]
+    assert np.all(got[~valid] == -1), "padding"
+    g = np.where(valid, got, -1)
+    assert np.all((g[valid] >= 0) & (g[valid] < np.broadcast_to(n[:, None], g.shape)[valid])), "range"
+    srt = np.sort(np.where(valid, got, -1 - col), axis=1)
+    assert np.all(np.diff(srt, axis=1) != 0), "duplicates"
+
+
+CASES = [
+    ("r2048_32k_k512", 48),
+    ("r2048_32k_k2048", 48),
+    ("r16k_128k_k2048", 40),
+    ("r16k_128k_k2048_offset4", 40),
+    ("multi4_r16k_k1024", 48),
+    ("r16k_1m_k2048", 20),
+    ("r16k_1m_k2048_adversarial", 20),
+]
+
+
+@pytest.mark.parametrize("name,nsample", CASES)
+def test_config_parity(mqa, name, nsample):
+    p = synth.make(name)
+    q, k, sc, w, s, e = to_device(p)
+    ws = mqa.alloc_workspace(p.rows)
+    out = mqa.mqa_topk_prefill(q, k, sc, w, s, e, p.topk, workspace=ws)
+    status, stats = mqa.get_status(ws)
+    got = out.cpu().numpy()
+    assert status == 0, stats
+    structure_all_rows(got, p)
+    rows = synth.sample_rows(p, nsample)
+    if name.startswith("multi4"):
+        # every padded row of the 300-key request plus the samples
+        rows = np.unique(np.concatenate([rows, np.arange(64)]))
+    _, scores = oracle.run(p, rows=rows, want_topk=False, want_scores=True)
+    bad = check_topk_rows(got[rows], p, rows, scores)
+    assert not bad, (bad[:5], stats)
+    print(name, stats)
+
+
+@pytest.mark.parametrize("name", ["r2048_32k_k2048", "r16k_128k_k2048"])
+def test_config_dense_agrees(mqa, name):
+    p = synth.make(name)
+    q, k, sc, w, s, e = to_device(p)
+    dense = mqa.mqa_topk_dense_baseline(q, k, sc, w, s, e, p.topk).cpu().numpy()
+    structure_all_rows(dense, p)
+    rows = synth.sample_rows(p, 24)
+    _, scores = oracle.run(p, rows=rows, want_topk=False, want_scores=True)
+    bad = check_topk_rows(dense[rows], p, rows, scores)
+    assert not bad, bad[:5]

@@ -91,7 +91,7 @@ def test_fused_forced_gate_rescans(mqa, force_gate):
     """Gate forced to +inf (every row under-fills) or off (long rows overflow
     a reduced slab): the exact rescan must still give the exact top-k."""
     p = synth.random_small(21, 24, 30000, 512, empty_frac=0.0)
-    got, status, stats = run_fused(mqa, p, debug={"force_gate": force_gate, "slab_capacity": 2048})
+    got, status, stats = run_fused(mqa, p, debug={"force_gate": force_gate, "slab_capacity": 2560})
     assert status == 0, stats
     assert stats["rows_rescanned"] > 0
     if force_gate == 2:
@@ -108,7 +108,7 @@ def test_fused_small_slab_compaction_ties(mqa):
     src = rng.integers(0, 64, size=dst.size)
     p.k[dst] = p.k[src]
     p.scales_ue8m0[dst] = p.scales_ue8m0[src]
-    got, status, stats = run_fused(mqa, p, debug={"force_gate": 2, "slab_capacity": 1024 + 256})
+    got, status, stats = run_fused(mqa, p, debug={"force_gate": 2, "slab_capacity": 4608})
     assert status == 0, stats
     assert_parity(p, got)
 

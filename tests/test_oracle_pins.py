@@ -327,3 +327,10 @@ def test_dense_budget_table_golden(lib=None):
         assert plan.dense_logits_traffic_bytes(16384, keys) == int(traffic) * 2 ** 30
         if calls != "-":
             assert plan.dense_calls(16384, keys, 512 * 2 ** 20) == int(calls)
+
+
+def test_fast_quantizer_matches_reference(lib=None):
+    rng = np.random.default_rng(9)
+    x = np.concatenate([rng.standard_normal(300000).astype(np.float32) * 3,
+                        np.float32([1000.0, -700.0, 449.0, 2 ** -12, -2 ** -9])])
+    assert np.array_equal(synth.quantize_e4m3fn_fast(x), synth.quantize_e4m3fn(x))
