@@ -132,30 +132,50 @@ __device__ __forceinline__ bool wait_counter(Smem &S, int *flag, int target, con
 }
 
 // ------------------------------------------------------------------ scoring
-// s = scale * sum_h w_h * relu(acc_h).  relu is formed as (x + |x|) / 2: a
-// packed FP add whose second operand carries an absolute-value modifier (FMA
-// pipe), with the 1/2 folded into the scale.  x + |x| is exactly 2x or 0 and
-// the halving is exact, so the result equals the plain relu form.  Four packed
-// accumulators keep the FMA chains short; the summation order is fixed, and
-// the fused and logits instantiations share this routine, so both produce
-// bit-identical scores.
-__device__ __forceinline__ float relu_weighted_sum(const uint32_t (&v)[32], const float *w, float half_scale) {
-  float2 a[4];
-#pragma unroll
-  for (int i = 0; i < 4; ++i) a[i] = make_float2(0.f, 0.f);
-#pragma unroll
-  for (int g = 0; g < kHeads / 4; ++g) {
-    const float4 wv = *reinterpret_cast<const float4 *>(w + 4 * g);
-    const float2 x0 = make_float2(__uint_as_float(v[4 * g]), __uint_as_float(v[4 * g + 1]));
-    const float2 x1 = make_float2(__uint_as_float(v[4 * g + 2]), __uint_as_float(v[4 * g + 3]));
-    const float2 r0 = __fadd2_rn(x0, make_float2(fabsf(x0.x), fabsf(x0.y)));
-    const float2 r1 = __fadd2_rn(x1, make_float2(fabsf(x1.x), fabsf(x1.y)));
-    a[(2 * g) & 3] = __ffma2_rn(r0, make_float2(wv.x, wv.y), a[(2 * g) & 3]);
-    a[(2 * g + 1) & 3] = __ffma2_rn(r1, make_float2(wv.z, wv.w), a[(2 * g + 1) & 3]);
-  }
-  const float2 t = __fadd2_rn(__fadd2_rn(a[0], a[1]), __fadd2_rn(a[2], a[3]));
-  return (t.x + t.y) * half_scale;
+// Each epilogue thread reads one row's accumulators with two 16x256b TMEM
+// loads (lanes 0-15 and 16-31 of its warp's quadrant): 4 keys (A = g, B = g+8,
+// C = g+16, D = g+24 with g = lane/4) x 8 heads (8i + 2c, 8i + 2c + 1 for
+// i < 4, c = lane%4).  relu(x) is formed as (x + |x|): a packed FP add whose
+// second operand carries an absolute-value modifier (FMA pipe); the 1/2 is
+// folded into the key scale.  x + |x| is exactly 2x or 0 and the halving is
+// exact.  The 4 threads of a key group then reduce-scatter their partial head
+// sums so that every thread owns the full sum of one key.  The summation
+// order is fixed and the fused and logits instantiations share this code, so
+// both produce bit-identical scores.
+struct HeadW {
+  float2 w[4];  // weights of this thread's 8 heads of one row, as pairs
+};
+
+__device__ __forceinline__ float2 relu2(uint32_t a, uint32_t b) {
+  const float2 x = make_float2(__uint_as_float(a), __uint_as_float(b));
+  return __fadd2_rn(x, make_float2(fabsf(x.x), fabsf(x.y)));
 }
+
+// Full relu-weighted head sum of the key this thread owns (before scaling).
+__device__ __forceinline__ float row_head_sum(const uint32_t (&lo)[16], const uint32_t (&hi)[16], const HeadW &W,
+                                              int lane) {
+  float2 aA = make_float2(0.f, 0.f), aB = aA, aC = aA, aD = aA;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    aA = __ffma2_rn(relu2(lo[4 * i], lo[4 * i + 1]), W.w[i], aA);
+    aB = __ffma2_rn(relu2(lo[4 * i + 2], lo[4 * i + 3]), W.w[i], aB);
+    aC = __ffma2_rn(relu2(hi[4 * i], hi[4 * i + 1]), W.w[i], aC);
+    aD = __ffma2_rn(relu2(hi[4 * i + 2], hi[4 * i + 3]), W.w[i], aD);
+  }
+  const float pA = aA.x + aA.y, pB = aB.x + aB.y, pC = aC.x + aC.y, pD = aD.x + aD.y;
+  // round 1 (partner lane^1): even lanes keep keys A, B; odd lanes keep C, D
+  const bool odd = lane & 1;
+  const float s0 = odd ? pA : pC, s1 = odd ? pB : pD;
+  const float k0 = (odd ? pC : pA) + __shfl_xor_sync(0xFFFFFFFFu, s0, 1);
+  const float k1 = (odd ? pD : pB) + __shfl_xor_sync(0xFFFFFFFFu, s1, 1);
+  // round 2 (partner lane^2): lanes with bit 1 clear keep the first key
+  const bool second = lane & 2;
+  const float s = second ? k0 : k1;
+  return (second ? k1 : k0) + __shfl_xor_sync(0xFFFFFFFFu, s, 2);
+}
+
+// Key (0..31 within the warp's quadrant) whose sum row_head_sum leaves in `lane`.
+__device__ __forceinline__ int owned_key(int lane) { return (lane >> 2) + 8 * ((lane >> 1) & 1) + 16 * (lane & 1); }
 
 // ------------------------------------------------------------------ sample gate bins
 // Distance d (in order-key units) below the row's reference maximum, binned on
@@ -615,6 +635,7 @@ __device__ void epilogue(Smem &S, uint32_t tmem, const FusedParams &p, int warp,
     int st[4], en[4], cnt[4];
     bool act[4];
     float tau[4];
+    HeadW W[4];
 #pragma unroll
     for (int rr = 0; rr < 4; ++rr) {
       const int r = 4 * half + rr;
@@ -623,6 +644,9 @@ __device__ void epilogue(Smem &S, uint32_t tmem, const FusedParams &p, int warp,
       act[rr] = ((J.mask >> r) & 1u) != 0;
       tau[rr] = kLogits ? NEG_INF : S.tau[r];
       cnt[rr] = 0;
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        W[rr].w[i] = *reinterpret_cast<const float2 *>(&J.w[r][8 * i + 2 * (lane & 3)]);
     }
     const int ns = J.ns, ntiles = J.ns + J.nt, mode = J.mode;
     const int block = J.block;
@@ -634,17 +658,19 @@ __device__ void epilogue(Smem &S, uint32_t tmem, const FusedParams &p, int warp,
       if (u < ns) return sample_tile(J, u);  // division only on the few sample tiles
       return J.lo_t + (u - ns);
     };
-    auto scale_of = [&](int u) {
-      const int kk = tile_of(u) * kTileKeys + quad * 32 + lane;
-      return (u < ntiles && kk < p.keys) ? 0.5f * __ldg(p.scales + kk) : 0.f;
+    const int kown = quad * 32 + owned_key(lane);  // key of this thread within a tile
+    auto scale_of = [&](int u) {  // raw scale, consumed two tiles later
+      const int kk = tile_of(u) * kTileKeys + kown;
+      return (u < ntiles && kk < p.keys) ? __ldg(p.scales + kk) : 0.f;
     };
-    float hsc_next = scale_of(0);
+    float sc1 = scale_of(0), sc2 = scale_of(1);
     for (int u = 0; u < ntiles && !bail; ++u) {
       const bool sampling = u < ns;
       const int tile = tile_of(u);
-      const int key = tile * kTileKeys + quad * 32 + lane;
-      const float hsc = hsc_next;
-      hsc_next = scale_of(u + 1);  // one tile ahead: hides the global-load latency
+      const int key = tile * kTileKeys + kown;
+      const float hsc = 0.5f * sc1;
+      sc1 = sc2;
+      sc2 = scale_of(u + 2);  // two tiles ahead: hides the global-load latency
       const int buf = tcount & 1;
       // rows whose range covers the whole tile need no per-key mask (warp-uniform)
       bool inside[4];
@@ -662,9 +688,15 @@ __device__ void epilogue(Smem &S, uint32_t tmem, const FusedParams &p, int warp,
       for (int pr = 0; pr < 2; ++pr) {
         const int ra = 2 * pr, rb = 2 * pr + 1;
         const bool la = act[ra] && ok, lb = act[rb] && ok;
-        uint32_t va[32], vb[32];
-        if (la) tmem_ld_32x32b_x32(base + (uint32_t)(ra * kHeads), va);
-        if (lb) tmem_ld_32x32b_x32(base + (uint32_t)(rb * kHeads), vb);
+        uint32_t a_lo[16], a_hi[16], b_lo[16], b_hi[16];
+        if (la) {
+          tmem_ld_16x256b_x4(base + (uint32_t)(ra * kHeads), a_lo);
+          tmem_ld_16x256b_x4(base + (16u << 16) + (uint32_t)(ra * kHeads), a_hi);
+        }
+        if (lb) {
+          tmem_ld_16x256b_x4(base + (uint32_t)(rb * kHeads), b_lo);
+          tmem_ld_16x256b_x4(base + (16u << 16) + (uint32_t)(rb * kHeads), b_hi);
+        }
         tmem_ld_wait();
         if (pr == 1) {
           tc_fence_before();
@@ -674,11 +706,11 @@ __device__ void epilogue(Smem &S, uint32_t tmem, const FusedParams &p, int warp,
         sv[ra] = NEG_INF;
         sv[rb] = NEG_INF;
         if (la) {
-          const float s = relu_weighted_sum(va, &J.w[4 * half + ra][0], hsc);
+          const float s = row_head_sum(a_lo, a_hi, W[ra], lane) * hsc;
           if (inside[ra] || (key >= st[ra] && key < en[ra])) sv[ra] = s;
         }
         if (lb) {
-          const float s = relu_weighted_sum(vb, &J.w[4 * half + rb][0], hsc);
+          const float s = row_head_sum(b_lo, b_hi, W[rb], lane) * hsc;
           if (inside[rb] || (key >= st[rb] && key < en[rb])) sv[rb] = s;
         }
       }
