@@ -120,6 +120,30 @@ int mqa_topk_prefill_debug(const void *q, const void *k, const float *key_scales
                            int topk, void *workspace, size_t workspace_bytes, void *stream,
                            const mqa_topk_debug_options *opt);
 
+/* Allocation-free variant of mqa_topk_prefill (the pages have no counterpart;
+ * it exists for callers that cannot allocate device memory: code that runs
+ * while a stream is being captured into a CUDA graph in global capture mode,
+ * where cudaMalloc is not permitted; plugins whose host framework owns the
+ * whole device memory pool; latency-critical paths that must never wait on an
+ * allocator).  Same inputs, output and result as mqa_topk_prefill, but no
+ * workspace argument: the scratch is a static device array inside the library
+ * of 256 B + 8 CTAs x 2 slots x 8 rows x 16384 records x 8 B (16 MiB + 256 B),
+ * held by every GPU that loads the library until the process exits.  The call
+ * therefore runs on at most 8 persistent CTAs (slower than mqa_topk_prefill on
+ * big chunks).  Its scratch need does not grow with rows or keys, so every
+ * call that passes the argument checks fits; a need beyond the array would be
+ * rejected with MQA_ERR_WORKSPACE_TOO_SMALL.  It calls no cudaMalloc/cudaFree.
+ *  - The first call on each device resolves the array's device address
+ *    (cudaGetSymbolAddress) with that device current; make that first call
+ *    before any stream capture begins.
+ *  - Every call shares the one array and resets its header on `stream`.
+ *    Calls that overlap on the GPU (other streams, other host threads) race
+ *    on the scratch and give wrong results: serialise them.
+ *  - Device status and counters: not exposed (the scratch is internal). */
+int mqa_topk_prefill_noalloc(const void *q, const void *k, const float *key_scales, const float *weights,
+                             const int32_t *starts, const int32_t *ends, int32_t *out, int rows, int keys,
+                             int topk, void *stream);
+
 /* UE8M0 -> fp32 key-scale decode (API page, `fused_mqa_topk_key_scales`
  * docstring): scales is [keys, 4] uint8 whose first byte per key is the
  * exponent e; out[j] is the fp32 with bit pattern e << 23 (2^(e-127) for

@@ -30,8 +30,9 @@ STATUS_BITS = {1: "range_clamped", 2: "wait_timeout", 4: "internal"}
 STAT_NAMES = ("status", "rows_rescanned", "compactions", "candidates", "gated_rows", "blocks_done",
               "sample_tiles", "overflow_rows", "underfill_rows")
 
-EXPORTS = ("mqa_topk_workspace_bytes", "mqa_topk_prefill", "mqa_topk_prefill_debug", "mqa_ue8m0_decode",
-           "mqa_logits_debug", "mqa_topk_dense_baseline", "mqa_topk_get_status", "mqa_topk_strerror")
+EXPORTS = ("mqa_topk_workspace_bytes", "mqa_topk_prefill", "mqa_topk_prefill_debug", "mqa_topk_prefill_noalloc",
+           "mqa_ue8m0_decode", "mqa_logits_debug", "mqa_topk_dense_baseline", "mqa_topk_get_status",
+           "mqa_topk_strerror")
 
 
 class MQAError(RuntimeError):
@@ -62,6 +63,7 @@ def lib():
     common = [P, P, P, P, P, P, P, I, I]
     L.mqa_topk_prefill.argtypes = common + [I, P, S, P]
     L.mqa_topk_prefill_debug.argtypes = common + [I, P, S, P, ctypes.POINTER(DebugOptions)]
+    L.mqa_topk_prefill_noalloc.argtypes = common + [I, P]
     L.mqa_ue8m0_decode.argtypes = [P, P, I, P]
     L.mqa_logits_debug.argtypes = common + [P, S, P]
     L.mqa_topk_dense_baseline.argtypes = common + [I, P, S, P, S, P]
@@ -180,6 +182,22 @@ def mqa_topk_prefill(q, k, key_scales, weights, starts, ends, topk: int, workspa
         _check(lib().mqa_topk_prefill_debug(*args, ctypes.byref(opt)), "mqa_topk_prefill_debug")
     else:
         _check(lib().mqa_topk_prefill(*args), "mqa_topk_prefill")
+    return out
+
+
+def mqa_topk_prefill_noalloc(q, k, key_scales, weights, starts, ends, topk: int, out=None, stream=None):
+    """Fused top-k without a workspace: the library uses its own fixed static
+    device scratch (for callers that cannot allocate device memory).  Calls
+    must not overlap on the GPU; the first call on a device must precede any
+    stream capture."""
+    torch = _torch()
+    q, k, key_scales, weights, starts, ends, rows, keys = _inputs(q, k, key_scales, weights, starts, ends)
+    if out is None:
+        out = torch.empty((rows, int(topk)), dtype=torch.int32, device=q.device)
+    out = _as(out, torch.int32, (rows, int(topk)), "out")
+    _check(lib().mqa_topk_prefill_noalloc(_ptr(q), _ptr(k), _ptr(key_scales), _ptr(weights), _ptr(starts),
+                                          _ptr(ends), _ptr(out), rows, keys, int(topk), _stream(stream)),
+           "mqa_topk_prefill_noalloc")
     return out
 
 

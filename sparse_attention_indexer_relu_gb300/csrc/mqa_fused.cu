@@ -30,6 +30,7 @@
 
 #include <cfloat>
 #include <climits>
+#include <mutex>
 
 namespace mqa {
 
@@ -1043,6 +1044,32 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     tmem_dealloc(tmem, 2 * kCols);
   }
+}
+
+// ------------------------------------------------------------------ allocation-free scratch
+// Scratch for mqa_topk_prefill_noalloc: the 256-byte header plus the candidate
+// slabs of at most kStaticScratchCtas persistent CTAs, as a file-scope device
+// array.  Every GPU that loads the library holds it until the process exits.
+static __device__ __align__(256) uint8_t g_static_scratch[kStaticScratchBytes];
+
+cudaError_t static_scratch_address(void **ptr) {
+  // Host code cannot use the array's name as a device address: resolve it once
+  // per device, with that device current.
+  static std::mutex mu;
+  static void *addr[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lk(mu);
+  if (!addr[dev]) {
+    void *a = nullptr;
+    e = cudaGetSymbolAddress(&a, g_static_scratch);
+    if (e != cudaSuccess) return e;
+    addr[dev] = a;
+  }
+  *ptr = addr[dev];
+  return cudaSuccess;
 }
 
 static cudaError_t set_smem_attr(const void *fn) {

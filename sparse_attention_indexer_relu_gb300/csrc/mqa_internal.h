@@ -85,4 +85,11 @@ cudaError_t launch_dense_topk_rows(const float *logits, int rows, int keys, cons
                                    cudaStream_t stream);
 size_t fused_smem_bytes();
 
+// Allocation-free variant: a static device scratch sized for this many CTAs.
+constexpr int kStaticScratchCtas = 8;
+constexpr size_t kStaticScratchBytes =
+    kWsHeaderBytes + (size_t)kStaticScratchCtas * kSlots * 2 * kBlockRows * kDefaultSlabCap * sizeof(uint32_t);
+// Device address of the static scratch on the current device (resolved on first use).
+cudaError_t static_scratch_address(void **ptr);
+
 }  // namespace mqa

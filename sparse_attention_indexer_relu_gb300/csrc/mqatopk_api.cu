@@ -239,6 +239,34 @@ int mqa_topk_prefill_debug(const void *q, const void *k, const float *key_scales
                    stream, opt);
 }
 
+int mqa_topk_prefill_noalloc(const void *q, const void *k, const float *key_scales, const float *weights,
+                             const int32_t *starts, const int32_t *ends, int32_t *out, int rows, int keys,
+                             int topk, void *stream) {
+  int rc = check_common(q, k, key_scales, weights, starts, ends, out, rows, keys);
+  if (rc != MQA_OK) return rc;
+  if (!valid_topk(topk)) return MQA_ERR_INVALID_ARGUMENT;
+  if (rows == 0) return MQA_OK;
+  DeviceInfo d;
+  rc = current_device_info(&d);
+  if (rc != MQA_OK) return rc;
+  // The scratch need is set by the CTA count, which this entry caps; a call
+  // whose need exceeded the static array would be rejected here.
+  int ctas = fused_ctas(d, rows);
+  if (ctas > kStaticScratchCtas) ctas = kStaticScratchCtas;
+  const size_t need = kWsHeaderBytes + slab_bytes(ctas, kDefaultSlabCap);
+  if (need > kStaticScratchBytes) return MQA_ERR_WORKSPACE_TOO_SMALL;
+  void *scratch = nullptr;
+  if (static_scratch_address(&scratch) != cudaSuccess) {
+    cudaGetLastError();
+    return MQA_ERR_CUDA;
+  }
+  mqa_topk_debug_options opt;
+  std::memset(&opt, 0, sizeof opt);
+  opt.max_ctas = ctas;
+  return run_fused(q, k, key_scales, weights, starts, ends, out, rows, keys, topk, scratch, kStaticScratchBytes,
+                   stream, &opt);
+}
+
 int mqa_ue8m0_decode(const uint8_t *scales, float *out, int keys, void *stream) {
   if (keys < 0 || keys > MQA_MAX_KEYS) return MQA_ERR_INVALID_ARGUMENT;
   if (keys == 0) return MQA_OK;
