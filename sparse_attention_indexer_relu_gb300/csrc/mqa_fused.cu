@@ -43,7 +43,7 @@ struct JobInfo {
   int block;      // row block (-1: no more work)
   int mode;       // 0 gated scan, 1 exact rescan
   int lo_t, nt;   // main tiles [lo_t, lo_t + nt)
-  int ns;         // sample tiles scored before the main tiles
+  int ns;         // sample tiles; scored twice (coarse, then fine gate pass) before the main tiles
   uint32_t mask;  // rows taking part
   int nrows;      // valid rows in the block
   int pad;
@@ -63,6 +63,7 @@ struct SelSlot {  // what the selection warps need from a finished scan
 struct Smem {
   alignas(1024) uint8_t kring[kKStages][kKTileBytes];
   alignas(1024) uint8_t q[2][kQBytes];
+  alignas(128) float sring[kSStages][kTileKeys];  // key scales of the tiles in flight
   JobInfo job[2];
   SelSlot sel[2];
   float tau[kBlockRows];
@@ -70,10 +71,14 @@ struct Smem {
   uint32_t ref[kBlockRows];
   int ref_frozen[kBlockRows];
   int msample[kBlockRows];
+  // gate refinement: the coarse bin that holds the target sample rank
+  int g_on[kBlockRows], g_above[kBlockRows], g_j[kBlockRows];
+  uint32_t g_klo[kBlockRows], g_khi[kBlockRows];
   int hist[kBlockRows][kGateBins];
   int selhist[kSelWarps][256];
   uint16_t order[kMaxSortBlocks];
   uint64_t k_full[kKStages], k_empty[kKStages];
+  uint64_t sc_full[kSStages], sc_empty[kSStages];
   uint64_t t_full[2], t_empty[2];
   uint64_t j_full[2], j_empty[2];
   uint64_t s_full[2], s_empty[2];
@@ -177,6 +182,34 @@ __device__ __forceinline__ float row_head_sum(const uint32_t (&lo)[16], const ui
 
 // Key (0..31 within the warp's quadrant) whose sum row_head_sum leaves in `lane`.
 __device__ __forceinline__ int owned_key(int lane) { return (lane >> 2) + 8 * ((lane >> 1) & 1) + 16 * (lane & 1); }
+
+// Scaled head sums of this lane's key for the warp's 4 rows of one tile, read
+// from TMEM at `base` (the warp's quadrant, its first row); rows whose flag is
+// off give -inf.  All four rows are always loaded and summed (every TMEM
+// address here is in the allocation), so the code has no per-row branches.
+// The TMEM buffer is released (t_empty) once the last pair is in registers.
+__device__ __forceinline__ void score_rows(uint64_t *t_empty, uint32_t base, const bool (&act)[4],
+                                           const HeadW (&W)[4], float hsc, int lane, float (&out)[4]) {
+#pragma unroll
+  for (int pr = 0; pr < 2; ++pr) {
+    const int ra = 2 * pr, rb = 2 * pr + 1;
+    uint32_t a_lo[16], a_hi[16], b_lo[16], b_hi[16];
+    tmem_ld_16x256b_x4(base + (uint32_t)(ra * kHeads), a_lo);
+    tmem_ld_16x256b_x4(base + (16u << 16) + (uint32_t)(ra * kHeads), a_hi);
+    tmem_ld_16x256b_x4(base + (uint32_t)(rb * kHeads), b_lo);
+    tmem_ld_16x256b_x4(base + (16u << 16) + (uint32_t)(rb * kHeads), b_hi);
+    tmem_ld_wait();
+    if (pr == 1) {
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(t_empty);
+    }
+    const float sa = row_head_sum(a_lo, a_hi, W[ra], lane) * hsc;
+    const float sb = row_head_sum(b_lo, b_hi, W[rb], lane) * hsc;
+    out[ra] = act[ra] ? sa : -INFINITY;
+    out[rb] = act[rb] ? sb : -INFINITY;
+  }
+}
 
 // ------------------------------------------------------------------ sample gate bins
 // Distance d (in order-key units) below the row's reference maximum, binned on
@@ -390,8 +423,8 @@ __device__ __forceinline__ int sample_tile(const JobInfo &J, int u) {
 
 // ------------------------------------------------------------------ producer (warp 0)
 template <bool kLogits>
-__device__ void producer(Smem &S, const CUtensorMap *q_map, const CUtensorMap *k_map, const FusedParams &p,
-                         int lane) {
+__device__ void producer(Smem &S, const CUtensorMap *q_map, const CUtensorMap *k_map, const CUtensorMap *s_map,
+                         const FusedParams &p, int lane) {
   const uint64_t pol_k = policy_evict_last(), pol_q = policy_evict_first();
   const int total_jobs = kLogits ? p.nblocks * p.key_chunks : p.nblocks;
   const int ktiles_all = (p.keys + kTileKeys - 1) / kTileKeys;
@@ -517,7 +550,7 @@ __device__ void producer(Smem &S, const CUtensorMap *q_map, const CUtensorMap *k
         J.mask = kLogits ? ((1u << nrows) - 1u) : pm;
         J.nrows = nrows;
       }
-      ntiles = ns + nt;
+      ntiles = 2 * ns + nt;
     } else if (lane == 0) {
       J.block = -1;
     }
@@ -532,11 +565,16 @@ __device__ void producer(Smem &S, const CUtensorMap *q_map, const CUtensorMap *k
     if (lane == 0) {
       const JobInfo &Jc = S.job[slot];
       for (int u = 0; u < ntiles; ++u) {
-        const int tile = u < Jc.ns ? sample_tile(Jc, u) : Jc.lo_t + (u - Jc.ns);
+        const int tile = u < 2 * Jc.ns ? sample_tile(Jc, u < Jc.ns ? u : u - Jc.ns) : Jc.lo_t + (u - 2 * Jc.ns);
         const int stage = kcount % kKStages;
+        const int sst = kcount % kSStages;
         if (!wait_bar(S, &S.k_empty[stage], ((kcount / kKStages) & 1) ^ 1, p)) break;
         mbar_arrive_expect_tx(&S.k_full[stage], kKTileBytes);
         tma_load_2d(&S.kring[stage][0], k_map, &S.k_full[stage], 0, tile * kTileKeys, pol_k);
+        // the tile's key scales (zero past the last key), released by the epilogue
+        if (!wait_bar(S, &S.sc_empty[sst], ((kcount / kSStages) & 1) ^ 1, p)) break;
+        mbar_arrive_expect_tx(&S.sc_full[sst], kTileKeys * sizeof(float));
+        tma_load_1d(&S.sring[sst][0], s_map, &S.sc_full[sst], tile * kTileKeys, pol_k);
         ++kcount;
       }
     }
@@ -554,7 +592,7 @@ __device__ void mma_issuer(Smem &S, uint32_t tmem, const FusedParams &p) {
     if (!wait_bar(S, &S.j_full[slot], (job_iter >> 1) & 1, p)) break;
     const JobInfo &J = S.job[slot];
     if (J.block < 0) break;
-    const int ntiles = J.ns + J.nt;
+    const int ntiles = 2 * J.ns + J.nt;
     const uint32_t b_base = smem_u32(&S.q[slot][0]);
     bool ok = true;
     for (int u = 0; u < ntiles && ok; ++u) {
@@ -649,87 +687,45 @@ __device__ void epilogue(Smem &S, uint32_t tmem, const FusedParams &p, int warp,
       for (int i = 0; i < 4; ++i)
         W[rr].w[i] = *reinterpret_cast<const float2 *>(&J.w[r][8 * i + 2 * (lane & 3)]);
     }
-    const int ns = J.ns, ntiles = J.ns + J.nt, mode = J.mode;
+    const int ns = J.ns, ns2 = 2 * J.ns, ntiles = 2 * J.ns + J.nt, mode = J.mode;
     const int block = J.block;
     uint32_t *slab_keys = p.slab + ((size_t)(blockIdx.x * kSlots + slot) * 2 * kBlockRows) * (size_t)cap;
     int32_t *slab_idx = reinterpret_cast<int32_t *>(slab_keys + (size_t)kBlockRows * cap);
     // this warp's segment of row r: slab_*[(r * kQuads + quad) * seg]
     bool bail = false;
-    auto tile_of = [&](int u) {
-      if (u < ns) return sample_tile(J, u);  // division only on the few sample tiles
-      return J.lo_t + (u - ns);
-    };
     const int kown = quad * 32 + owned_key(lane);  // key of this thread within a tile
-    auto scale_of = [&](int u) {  // raw scale, consumed two tiles later
-      const int kk = tile_of(u) * kTileKeys + kown;
-      return (u < ntiles && kk < p.keys) ? __ldg(p.scales + kk) : 0.f;
-    };
-    float sc1 = scale_of(0), sc2 = scale_of(1);
-    for (int u = 0; u < ntiles && !bail; ++u) {
-      const bool sampling = u < ns;
-      const int tile = tile_of(u);
+    // One tile: wait for its accumulators and scales, score this lane's key for
+    // the warp's 4 rows (masked to each row's range), release TMEM and scales.
+    auto score_tile = [&](int tile, float (&sv)[4]) -> bool {
+      const int buf = tcount & 1, sst = tcount % kSStages;
       const int key = tile * kTileKeys + kown;
-      const float hsc = 0.5f * sc1;
-      sc1 = sc2;
-      sc2 = scale_of(u + 2);  // two tiles ahead: hides the global-load latency
-      const int buf = tcount & 1;
-      // rows whose range covers the whole tile need no per-key mask (warp-uniform)
-      bool inside[4];
       const int tile_lo = tile * kTileKeys;
-#pragma unroll
-      for (int rr = 0; rr < 4; ++rr) inside[rr] = tile_lo >= st[rr] && tile_lo + kTileKeys <= en[rr];
-      ok = wait_bar(S, &S.t_full[buf], (tcount >> 1) & 1, p);
+      bool ok = wait_bar(S, &S.t_full[buf], (tcount >> 1) & 1, p);
+      ok = wait_bar(S, &S.sc_full[sst], (tcount / kSStages) & 1, p) && ok;
       ok = __all_sync(0xFFFFFFFFu, ok);
       tc_fence_after();
-      // two rows per TMEM round trip; the buffer goes back to the MMA as soon
-      // as the second pair is in registers
+      const float hsc = 0.5f * S.sring[sst][kown];
       const uint32_t base = tmem + lane_addr + (uint32_t)(buf * kCols + (4 * half) * kHeads);
-      float sv[4];
+      float raw[4];
+      score_rows(&S.t_empty[buf], base, act, W, hsc, lane, raw);
+      if (lane == 0) mbar_arrive(&S.sc_empty[sst]);
 #pragma unroll
-      for (int pr = 0; pr < 2; ++pr) {
-        const int ra = 2 * pr, rb = 2 * pr + 1;
-        const bool la = act[ra] && ok, lb = act[rb] && ok;
-        uint32_t a_lo[16], a_hi[16], b_lo[16], b_hi[16];
-        if (la) {
-          tmem_ld_16x256b_x4(base + (uint32_t)(ra * kHeads), a_lo);
-          tmem_ld_16x256b_x4(base + (16u << 16) + (uint32_t)(ra * kHeads), a_hi);
-        }
-        if (lb) {
-          tmem_ld_16x256b_x4(base + (uint32_t)(rb * kHeads), b_lo);
-          tmem_ld_16x256b_x4(base + (16u << 16) + (uint32_t)(rb * kHeads), b_hi);
-        }
-        tmem_ld_wait();
-        if (pr == 1) {
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&S.t_empty[buf]);
-        }
-        sv[ra] = NEG_INF;
-        sv[rb] = NEG_INF;
-        if (la) {
-          const float s = row_head_sum(a_lo, a_hi, W[ra], lane) * hsc;
-          if (inside[ra] || (key >= st[ra] && key < en[ra])) sv[ra] = s;
-        }
-        if (lb) {
-          const float s = row_head_sum(b_lo, b_hi, W[rb], lane) * hsc;
-          if (inside[rb] || (key >= st[rb] && key < en[rb])) sv[rb] = s;
-        }
+      for (int rr = 0; rr < 4; ++rr) {
+        // rows whose range covers the whole tile need no per-key mask
+        const bool inside = tile_lo >= st[rr] && tile_lo + kTileKeys <= en[rr];
+        sv[rr] = (inside || (key >= st[rr] && key < en[rr])) ? raw[rr] : NEG_INF;
       }
       ++tcount;
-      if (kLogits) {
-        if (key < p.keys) {
-#pragma unroll
-          for (int rr = 0; rr < 4; ++rr) {
-            if (act[rr]) {
-              const size_t row = (size_t)block * kBlockRows + 4 * half + rr;
-              p.logits[row * (size_t)p.keys + key] = sv[rr];
-            }
-          }
-        }
-        continue;
-      }
-      if (sampling) {
-        // step A: reference maximum from the row's first sample tile with visible keys
+      return ok;
+    };
+    // ---- sample tiles: coarse then fine pass of the gate
+    for (int u = 0; u < ns2 && !bail; ++u) {
+      const int tile = sample_tile(J, u < ns ? u : u - ns);
+      float sv[4];
+      score_tile(tile, sv);
+      if (u < ns) {
+        // coarse pass, step A: reference maximum from the row's first sample
+        // tile with visible keys
 #pragma unroll
         for (int rr = 0; rr < 4; ++rr) {
           const int r = 4 * half + rr;
@@ -740,7 +736,7 @@ __device__ void epilogue(Smem &S, uint32_t tmem, const FusedParams &p, int warp,
           }
         }
         if (bar_or(kEpiBarrier, kEpiThreads, aborted(S))) { bail = true; break; }
-        // step B: histogram of the position relative to the reference
+        // step B: log-binned histogram of the position relative to the reference
 #pragma unroll
         for (int rr = 0; rr < 4; ++rr) {
           const int r = 4 * half + rr;
@@ -755,13 +751,14 @@ __device__ void epilogue(Smem &S, uint32_t tmem, const FusedParams &p, int warp,
         }
         if (bar_or(kEpiBarrier, kEpiThreads, aborted(S))) { bail = true; break; }
         if (u == ns - 1) {
-          // gate for row ew from its sample histogram
+          // coarse bin of row ew that holds the target sample rank j
           const int r = ew;
           const int n = J.end[r] - J.start[r];
-          float t = NEG_INF;
           const int m = S.msample[r];
+          int on = 0, above = 0, jw = 0;
+          uint32_t klo = 0, khi = 0;
           if (((J.mask >> r) & 1u) && n > cap && m > 0) {
-            const long long jwant = max(1LL, ((long long)m * p.gate_target + n - 1) / n);
+            jw = (int)max(1LL, ((long long)m * p.gate_target + n - 1) / n);
             constexpr int kPer = kGateBins / 32;
             int c[kPer], tot = 0;
 #pragma unroll
@@ -776,36 +773,126 @@ __device__ void epilogue(Smem &S, uint32_t tmem, const FusedParams &p, int warp,
               if (lane >= off) incl += vv;
             }
             const int excl = incl - tot;
-            const uint32_t bm = __ballot_sync(0xFFFFFFFFu, excl < jwant && jwant <= incl);
+            const uint32_t bm = __ballot_sync(0xFFFFFFFFu, excl < jw && jw <= incl);
             if (bm) {
               const int src = __ffs(bm) - 1;
-              int bin = 0;
+              int bin = 0, run_before = 0;
               if (lane == src) {
                 int run = excl;
 #pragma unroll
                 for (int j = 0; j < kPer; ++j) {
+                  if (run + c[j] >= jw) { bin = kPer * lane + j; run_before = run; break; }
                   run += c[j];
-                  if (run >= jwant) { bin = kPer * lane + j; break; }
                 }
               }
               bin = __shfl_sync(0xFFFFFFFFu, bin, src);
+              above = __shfl_sync(0xFFFFFFFFu, run_before, src);
               const uint32_t ref = S.ref[r];
-              if (bin >= 128) {
-                // pass every key whose distance below the reference is inside bins 128..bin
-                const uint64_t dhi = dist_bin_hi(bin - 128);
-                if ((uint64_t)ref > dhi) t = key2f(ref - (uint32_t)dhi);
-              } else {
-                // pass every key at least the lower edge of its bin above the reference
-                const uint64_t kt = (uint64_t)ref + dist_bin_lo(128 - bin) - 1;
-                t = kt >= 0xFFFFFFFFull ? INFINITY : key2f((uint32_t)kt);
+              if (bin == 128) {
+                klo = khi = ref;
+              } else if (bin > 128) {  // keys ref - d for d in [lo, hi)
+                const uint64_t lo = dist_bin_lo(bin - 128), hi = dist_bin_hi(bin - 128);
+                khi = ref - (uint32_t)lo;
+                klo = (uint64_t)ref >= hi - 1 ? ref - (uint32_t)(hi - 1) : 0u;
+              } else {  // keys ref + d for d in [lo, hi)
+                const uint64_t lo = dist_bin_lo(128 - bin), hi = dist_bin_hi(128 - bin);
+                klo = ref + (uint32_t)lo;
+                khi = (uint64_t)ref + hi - 1 > 0xFFFFFFFFull ? 0xFFFFFFFFu : ref + (uint32_t)(hi - 1);
               }
+              on = 1;
+            }
+          }
+          __syncwarp();
+          for (int b2 = lane; b2 < kGateBins; b2 += 32) S.hist[r][b2] = 0;
+          if (lane == 0) {
+            S.g_on[r] = on;
+            S.g_above[r] = above;
+            S.g_j[r] = jw;
+            S.g_klo[r] = klo;
+            S.g_khi[r] = khi;
+            S.tau[r] = NEG_INF;
+          }
+          if (bar_or(kEpiBarrier, kEpiThreads, aborted(S))) { bail = true; break; }
+          if (ew == 0 && lane == 0) atomicAdd(p.ws + kWsSampleTiles, ns2);
+        }
+        continue;
+      }
+      {
+        // fine pass over the same sample tiles: 256 linear sub-bins of the
+        // coarse bin, so the gate lands on the target sample rank
+#pragma unroll
+        for (int rr = 0; rr < 4; ++rr) {
+          const int r = 4 * half + rr;
+          if (act[rr] && S.g_on[r] && sv[rr] > NEG_INF) {
+            const uint32_t kv = f2key(sv[rr]), klo = S.g_klo[r], khi = S.g_khi[r];
+            if (kv >= klo && kv <= khi) {
+              const uint64_t width = (uint64_t)(khi - klo) + 1;
+              atomicAdd(&S.hist[r][(int)(((uint64_t)(khi - kv) * 256) / width)], 1);
+            }
+          }
+        }
+        if (u == ns2 - 1) {
+          if (bar_or(kEpiBarrier, kEpiThreads, aborted(S))) { bail = true; break; }
+          const int r = ew;
+          float t = NEG_INF;
+          if (S.g_on[r]) {
+            const int need = S.g_j[r] - S.g_above[r];
+            const uint32_t klo = S.g_klo[r], khi = S.g_khi[r];
+            int c[8], tot = 0;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              c[j] = S.hist[r][8 * lane + j];
+              tot += c[j];
+            }
+            int incl = tot;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+              const int vv = __shfl_up_sync(0xFFFFFFFFu, incl, off);
+              if (lane >= off) incl += vv;
+            }
+            const int excl = incl - tot;
+            const uint32_t bm = __ballot_sync(0xFFFFFFFFu, excl < need && need <= incl);
+            if (bm) {
+              const int src = __ffs(bm) - 1;
+              int sub = 0;
+              if (lane == src) {
+                int run = excl;
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                  run += c[j];
+                  if (run >= need) { sub = 8 * lane + j; break; }
+                }
+              }
+              sub = __shfl_sync(0xFFFFFFFFu, sub, src);
+              // pass every key inside sub-bins 0..sub (and everything above the coarse bin)
+              const uint64_t width = (uint64_t)(khi - klo) + 1;
+              const uint64_t drop = ((uint64_t)(sub + 1) * width + 255) / 256;
+              t = (uint64_t)khi >= drop ? key2f(khi - (uint32_t)drop) : NEG_INF;
             }
           }
           if (lane == 0) S.tau[r] = t;
           if (bar_or(kEpiBarrier, kEpiThreads, aborted(S))) { bail = true; break; }
 #pragma unroll
           for (int rr = 0; rr < 4; ++rr) tau[rr] = S.tau[4 * half + rr];
-          if (ew == 0 && lane == 0) atomicAdd(p.ws + kWsSampleTiles, ns);
+        }
+        continue;
+      }
+    }
+    // ---- main tiles
+    for (int u = ns2; u < ntiles && !bail; ++u) {
+      const int tile = J.lo_t + (u - ns2);
+      const int key = tile * kTileKeys + kown;
+      float sv[4];
+      score_tile(tile, sv);
+      if (kLogits) {
+        if (key < p.keys) {
+#pragma unroll
+          for (int rr = 0; rr < 4; ++rr) {
+            if (act[rr]) {
+              const size_t row = (size_t)block * kBlockRows + 4 * half + rr;
+              p.logits[row * (size_t)p.keys + key] = sv[rr];
+            }
+          }
         }
         continue;
       }
@@ -985,7 +1072,7 @@ __device__ void selection(Smem &S, const FusedParams &p, int warp, int lane) {
 template <bool kLogits>
 __global__ void __launch_bounds__(kThreads, 1)
     mqa_fused_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant__ CUtensorMap k_map,
-                     const FusedParams p) {
+                     const __grid_constant__ CUtensorMap s_map, const FusedParams p) {
   extern __shared__ uint8_t smem_raw[];
   Smem &S = get_smem(smem_raw);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -994,6 +1081,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = 0; i < kKStages; ++i) {
       mbar_init(&S.k_full[i], 1);
       mbar_init(&S.k_empty[i], 1);
+    }
+    for (int i = 0; i < kSStages; ++i) {
+      mbar_init(&S.sc_full[i], 1);
+      mbar_init(&S.sc_empty[i], kEpiWarps);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&S.t_full[i], 1);
@@ -1016,6 +1107,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&q_map);
     tma_prefetch_desc(&k_map);
+    tma_prefetch_desc(&s_map);
   }
   if (warp == 1) {
     tmem_alloc(&S.tmem_base, 2 * kCols);
@@ -1030,7 +1122,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = S.tmem_base;
 
   if (warp == 0) {
-    producer<kLogits>(S, &q_map, &k_map, p, lane);
+    producer<kLogits>(S, &q_map, &k_map, &s_map, p, lane);
   } else if (warp == 1) {
     if (lane == 0) mma_issuer(S, tmem, p);
   } else if (warp >= kEpiWarp0) {
@@ -1076,19 +1168,19 @@ static cudaError_t set_smem_attr(const void *fn) {
   return cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)fused_smem_bytes());
 }
 
-cudaError_t launch_fused_topk(const CUtensorMap &q_map, const CUtensorMap &k_map, const FusedParams &p, int ctas,
-                              cudaStream_t stream) {
+cudaError_t launch_fused_topk(const CUtensorMap &q_map, const CUtensorMap &k_map, const CUtensorMap &s_map,
+                              const FusedParams &p, int ctas, cudaStream_t stream) {
   static cudaError_t attr = set_smem_attr((const void *)mqa_fused_kernel<false>);
   if (attr != cudaSuccess) return attr;
-  mqa_fused_kernel<false><<<ctas, kThreads, fused_smem_bytes(), stream>>>(q_map, k_map, p);
+  mqa_fused_kernel<false><<<ctas, kThreads, fused_smem_bytes(), stream>>>(q_map, k_map, s_map, p);
   return cudaGetLastError();
 }
 
-cudaError_t launch_logits(const CUtensorMap &q_map, const CUtensorMap &k_map, const FusedParams &p, int ctas,
-                          cudaStream_t stream) {
+cudaError_t launch_logits(const CUtensorMap &q_map, const CUtensorMap &k_map, const CUtensorMap &s_map,
+                          const FusedParams &p, int ctas, cudaStream_t stream) {
   static cudaError_t attr = set_smem_attr((const void *)mqa_fused_kernel<true>);
   if (attr != cudaSuccess) return attr;
-  mqa_fused_kernel<true><<<ctas, kThreads, fused_smem_bytes(), stream>>>(q_map, k_map, p);
+  mqa_fused_kernel<true><<<ctas, kThreads, fused_smem_bytes(), stream>>>(q_map, k_map, s_map, p);
   return cudaGetLastError();
 }
 

@@ -14,6 +14,7 @@ constexpr int kBlockRows = 8;   // query rows per block (one TMEM accumulator gr
 constexpr int kTileKeys = 128;  // keys per tile (UMMA M, one TMEM lane per key)
 constexpr int kCols = kBlockRows * kHeads;  // 256 accumulator columns per tile (UMMA N)
 constexpr int kKStages = 6;     // K-tile ring depth
+constexpr int kSStages = 8;     // key-scale ring depth (held until the epilogue has read them)
 constexpr int kQBytes = kCols * kDim;       // 32 KiB of q per block
 constexpr int kKTileBytes = kTileKeys * kDim;  // 16 KiB of k per tile
 
@@ -75,10 +76,10 @@ struct FusedParams {
 };
 
 // Launchers (defined next to their kernels).
-cudaError_t launch_fused_topk(const CUtensorMap &q_map, const CUtensorMap &k_map, const FusedParams &p,
-                              int ctas, cudaStream_t stream);
-cudaError_t launch_logits(const CUtensorMap &q_map, const CUtensorMap &k_map, const FusedParams &p, int ctas,
-                          cudaStream_t stream);
+cudaError_t launch_fused_topk(const CUtensorMap &q_map, const CUtensorMap &k_map, const CUtensorMap &s_map,
+                              const FusedParams &p, int ctas, cudaStream_t stream);
+cudaError_t launch_logits(const CUtensorMap &q_map, const CUtensorMap &k_map, const CUtensorMap &s_map,
+                          const FusedParams &p, int ctas, cudaStream_t stream);
 cudaError_t launch_ue8m0_decode(const uint8_t *scales, float *out, int keys, cudaStream_t stream);
 cudaError_t launch_dense_topk_rows(const float *logits, int rows, int keys, const int32_t *starts,
                                    const int32_t *ends, int32_t *out, int topk, int32_t *ws_status,

@@ -92,6 +92,18 @@ int encode_rows128(CUtensorMap *map, const void *base, uint64_t nrows, uint32_t 
   return r == CUDA_SUCCESS ? MQA_OK : MQA_ERR_CUDA;
 }
 
+// 1-D fp32 tensor [n] read in boxes of 128 elements (out-of-range elements read as 0).
+int encode_scales(CUtensorMap *map, const float *base, uint64_t n) {
+  const cuuint64_t dims[1] = {(cuuint64_t)n};
+  const cuuint64_t strides[1] = {(cuuint64_t)(n * sizeof(float))};  // unused for rank 1
+  const cuuint32_t box[1] = {(cuuint32_t)kTileKeys};
+  const cuuint32_t estr[1] = {1};
+  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 1, const_cast<float *>(base), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? MQA_OK : MQA_ERR_CUDA;
+}
+
 inline bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 int check_common(const void *q, const void *k, const float *scales, const float *weights, const int32_t *starts,
@@ -143,9 +155,9 @@ int run_fused(const void *q, const void *k, const float *scales, const float *we
   if (workspace_bytes < kWsHeaderBytes + slab_bytes(ctas, cap)) return MQA_ERR_WORKSPACE_TOO_SMALL;
   rc = get_encoder();
   if (rc != MQA_OK) return rc;
-  CUtensorMap qm, km;
+  CUtensorMap qm, km, sm;
   if (encode_rows128(&qm, q, (uint64_t)rows * kHeads, kCols) != MQA_OK ||
-      encode_rows128(&km, k, (uint64_t)keys, kTileKeys) != MQA_OK)
+      encode_rows128(&km, k, (uint64_t)keys, kTileKeys) != MQA_OK || encode_scales(&sm, scales, keys) != MQA_OK)
     return MQA_ERR_CUDA;
   FusedParams p;
   std::memset(&p, 0, sizeof p);
@@ -170,16 +182,16 @@ int run_fused(const void *q, const void *k, const float *scales, const float *we
     cudaGetLastError();
     return MQA_ERR_CUDA;
   }
-  if (launch_fused_topk(qm, km, p, ctas, st) != cudaSuccess) return MQA_ERR_CUDA;
+  if (launch_fused_topk(qm, km, sm, p, ctas, st) != cudaSuccess) return MQA_ERR_CUDA;
   return MQA_OK;
 }
 
 int run_logits_chunk(const DeviceInfo &d, const uint8_t *q, const void *k, const float *scales,
                      const float *weights, const int32_t *starts, const int32_t *ends, float *logits, int rows,
                      int keys, int32_t *ws, bool reset_header, cudaStream_t st) {
-  CUtensorMap qm, km;
+  CUtensorMap qm, km, sm;
   if (encode_rows128(&qm, q, (uint64_t)rows * kHeads, kCols) != MQA_OK ||
-      encode_rows128(&km, k, (uint64_t)keys, kTileKeys) != MQA_OK)
+      encode_rows128(&km, k, (uint64_t)keys, kTileKeys) != MQA_OK || encode_scales(&sm, scales, keys) != MQA_OK)
     return MQA_ERR_CUDA;
   FusedParams p;
   std::memset(&p, 0, sizeof p);
@@ -208,7 +220,7 @@ int run_logits_chunk(const DeviceInfo &d, const uint8_t *q, const void *k, const
     cudaGetLastError();
     return MQA_ERR_CUDA;
   }
-  return launch_logits(qm, km, p, ctas, st) == cudaSuccess ? MQA_OK : MQA_ERR_CUDA;
+  return launch_logits(qm, km, sm, p, ctas, st) == cudaSuccess ? MQA_OK : MQA_ERR_CUDA;
 }
 
 }  // namespace
