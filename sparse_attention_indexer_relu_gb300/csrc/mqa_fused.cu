@@ -109,12 +109,23 @@ __device__ __noinline__ void raise_timeout(Smem &S, const FusedParams &p) {
   atomicOr(p.ws + kWsStatus, kDevWaitTimeout);
 }
 
+#ifndef MQA_BACKOFF_SCALE
+#define MQA_BACKOFF_SCALE 1
+#endif
+// Sleep between polls of a waiting role, so that warps which wait for long
+// stretches (producer, selection, MMA issuer) leave issue slots to the
+// epilogue warps that share their SM sub-partitions.
+constexpr unsigned kBackoffMma = 32 * MQA_BACKOFF_SCALE;
+constexpr unsigned kBackoffIdle = 256 * MQA_BACKOFF_SCALE;
+
 // Wait for the phase of `bar` with the given parity; false on abort/timeout.
-__device__ __forceinline__ bool wait_bar(Smem &S, uint64_t *bar, uint32_t parity, const FusedParams &p) {
+__device__ __forceinline__ bool wait_bar(Smem &S, uint64_t *bar, uint32_t parity, const FusedParams &p,
+                                         unsigned backoff_ns = 0) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   for (;;) {
     if (aborted(S)) return false;
+    if (backoff_ns) __nanosleep(backoff_ns);
     if (mbar_try_wait(bar, parity)) return true;
     if ((long long)(globaltimer_ns() - t0) > p.timeout_ns) {
       raise_timeout(S, p);
@@ -148,12 +159,22 @@ __device__ __forceinline__ bool wait_counter(Smem &S, int *flag, int target, con
 // sums so that every thread owns the full sum of one key.  The summation
 // order is fixed and the fused and logits instantiations share this code, so
 // both produce bit-identical scores.
+#ifndef MQA_RELU_ALU_CHUNKS
+#define MQA_RELU_ALU_CHUNKS 2
+#endif
+// Of a thread's 4 head-pair chunks per key, the first MQA_RELU_ALU_CHUNKS form
+// relu as max(x, 0) on the ALU pipe with pre-doubled weights (2w * max(x, 0));
+// the rest use x + |x| on the FMA pipe with w.  Both give 2 * w * relu(x)
+// exactly (one rounding of the same product), so the split only balances the
+// two pipes and leaves the scores bit-identical.
 struct HeadW {
-  float2 w[4];  // weights of this thread's 8 heads of one row, as pairs
+  float2 w[4];  // weights of this thread's 8 heads of one row, as pairs (doubled for ALU chunks)
 };
 
+template <int kChunk>
 __device__ __forceinline__ float2 relu2(uint32_t a, uint32_t b) {
   const float2 x = make_float2(__uint_as_float(a), __uint_as_float(b));
+  if (kChunk < MQA_RELU_ALU_CHUNKS) return make_float2(fmaxf(x.x, 0.f), fmaxf(x.y, 0.f));
   return __fadd2_rn(x, make_float2(fabsf(x.x), fabsf(x.y)));
 }
 
@@ -161,13 +182,16 @@ __device__ __forceinline__ float2 relu2(uint32_t a, uint32_t b) {
 __device__ __forceinline__ float row_head_sum(const uint32_t (&lo)[16], const uint32_t (&hi)[16], const HeadW &W,
                                               int lane) {
   float2 aA = make_float2(0.f, 0.f), aB = aA, aC = aA, aD = aA;
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    aA = __ffma2_rn(relu2(lo[4 * i], lo[4 * i + 1]), W.w[i], aA);
-    aB = __ffma2_rn(relu2(lo[4 * i + 2], lo[4 * i + 3]), W.w[i], aB);
-    aC = __ffma2_rn(relu2(hi[4 * i], hi[4 * i + 1]), W.w[i], aC);
-    aD = __ffma2_rn(relu2(hi[4 * i + 2], hi[4 * i + 3]), W.w[i], aD);
-  }
+#define MQA_HEAD_CHUNK(i)                                                    \
+  aA = __ffma2_rn(relu2<i>(lo[4 * i], lo[4 * i + 1]), W.w[i], aA);         \
+  aB = __ffma2_rn(relu2<i>(lo[4 * i + 2], lo[4 * i + 3]), W.w[i], aB);     \
+  aC = __ffma2_rn(relu2<i>(hi[4 * i], hi[4 * i + 1]), W.w[i], aC);         \
+  aD = __ffma2_rn(relu2<i>(hi[4 * i + 2], hi[4 * i + 3]), W.w[i], aD);
+  MQA_HEAD_CHUNK(0)
+  MQA_HEAD_CHUNK(1)
+  MQA_HEAD_CHUNK(2)
+  MQA_HEAD_CHUNK(3)
+#undef MQA_HEAD_CHUNK
   const float pA = aA.x + aA.y, pB = aB.x + aB.y, pC = aC.x + aC.y, pD = aD.x + aD.y;
   // round 1 (partner lane^1): even lanes keep keys A, B; odd lanes keep C, D
   const bool odd = lane & 1;
@@ -183,31 +207,37 @@ __device__ __forceinline__ float row_head_sum(const uint32_t (&lo)[16], const ui
 // Key (0..31 within the warp's quadrant) whose sum row_head_sum leaves in `lane`.
 __device__ __forceinline__ int owned_key(int lane) { return (lane >> 2) + 8 * ((lane >> 1) & 1) + 16 * (lane & 1); }
 
-// Scaled head sums of this lane's key for the warp's 4 rows of one tile, read
-// from TMEM at `base` (the warp's quadrant, its first row); rows whose flag is
-// off give -inf.  All four rows are always loaded and summed (every TMEM
-// address here is in the allocation), so the code has no per-row branches.
-// The TMEM buffer is released (t_empty) once the last pair is in registers.
-__device__ __forceinline__ void score_rows(uint64_t *t_empty, uint32_t base, const bool (&act)[4],
-                                           const HeadW (&W)[4], float hsc, int lane, float (&out)[4]) {
+// Scaled head sums of this lane's key for the warp's kRowsPerWarp rows of one
+// tile, read from TMEM at `base` (the warp's quadrant, its first row); rows
+// whose flag is off give -inf.  Every row is always loaded and summed (every
+// TMEM address here is in the allocation), so the code has no per-row
+// branches.  Rows are loaded kLoadRows at a time; the TMEM buffer is released
+// (t_empty) once the last group is in registers.
+constexpr int kLoadRows = kRowsPerWarp >= 4 ? 2 : 1;
+__device__ __forceinline__ void score_rows(uint64_t *t_empty, uint32_t base, const bool (&act)[kRowsPerWarp],
+                                           const HeadW (&W)[kRowsPerWarp], float hsc, int lane,
+                                           float (&out)[kRowsPerWarp]) {
 #pragma unroll
-  for (int pr = 0; pr < 2; ++pr) {
-    const int ra = 2 * pr, rb = 2 * pr + 1;
-    uint32_t a_lo[16], a_hi[16], b_lo[16], b_hi[16];
-    tmem_ld_16x256b_x4(base + (uint32_t)(ra * kHeads), a_lo);
-    tmem_ld_16x256b_x4(base + (16u << 16) + (uint32_t)(ra * kHeads), a_hi);
-    tmem_ld_16x256b_x4(base + (uint32_t)(rb * kHeads), b_lo);
-    tmem_ld_16x256b_x4(base + (16u << 16) + (uint32_t)(rb * kHeads), b_hi);
+  for (int g = 0; g < kRowsPerWarp / kLoadRows; ++g) {
+    uint32_t lo[kLoadRows][16], hi[kLoadRows][16];
+#pragma unroll
+    for (int j = 0; j < kLoadRows; ++j) {
+      const uint32_t col = (uint32_t)((g * kLoadRows + j) * kHeads);
+      tmem_ld_16x256b_x4(base + col, lo[j]);
+      tmem_ld_16x256b_x4(base + (16u << 16) + col, hi[j]);
+    }
     tmem_ld_wait();
-    if (pr == 1) {
+    if (g == kRowsPerWarp / kLoadRows - 1) {
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(t_empty);
     }
-    const float sa = row_head_sum(a_lo, a_hi, W[ra], lane) * hsc;
-    const float sb = row_head_sum(b_lo, b_hi, W[rb], lane) * hsc;
-    out[ra] = act[ra] ? sa : -INFINITY;
-    out[rb] = act[rb] ? sb : -INFINITY;
+#pragma unroll
+    for (int j = 0; j < kLoadRows; ++j) {
+      const int rr = g * kLoadRows + j;
+      const float sc = row_head_sum(lo[j], hi[j], W[rr], lane) * hsc;
+      out[rr] = act[rr] ? sc : -INFINITY;
+    }
   }
 }
 
@@ -439,7 +469,7 @@ __device__ void producer(Smem &S, const CUtensorMap *q_map, const CUtensorMap *k
   for (;;) {
     const int slot = job_iter & 1;
     bool ok = true;
-    if (lane == 0) ok = wait_bar(S, &S.j_empty[slot], ((job_iter >> 1) & 1) ^ 1, p);
+    if (lane == 0) ok = wait_bar(S, &S.j_empty[slot], ((job_iter >> 1) & 1) ^ 1, p, kBackoffIdle);
     ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
     if (!ok) return;
     int block = -1, mode = 0, chunk = 0;
@@ -568,11 +598,11 @@ __device__ void producer(Smem &S, const CUtensorMap *q_map, const CUtensorMap *k
         const int tile = u < 2 * Jc.ns ? sample_tile(Jc, u < Jc.ns ? u : u - Jc.ns) : Jc.lo_t + (u - 2 * Jc.ns);
         const int stage = kcount % kKStages;
         const int sst = kcount % kSStages;
-        if (!wait_bar(S, &S.k_empty[stage], ((kcount / kKStages) & 1) ^ 1, p)) break;
+        if (!wait_bar(S, &S.k_empty[stage], ((kcount / kKStages) & 1) ^ 1, p, kBackoffIdle)) break;
         mbar_arrive_expect_tx(&S.k_full[stage], kKTileBytes);
         tma_load_2d(&S.kring[stage][0], k_map, &S.k_full[stage], 0, tile * kTileKeys, pol_k);
         // the tile's key scales (zero past the last key), released by the epilogue
-        if (!wait_bar(S, &S.sc_empty[sst], ((kcount / kSStages) & 1) ^ 1, p)) break;
+        if (!wait_bar(S, &S.sc_empty[sst], ((kcount / kSStages) & 1) ^ 1, p, kBackoffIdle)) break;
         mbar_arrive_expect_tx(&S.sc_full[sst], kTileKeys * sizeof(float));
         tma_load_1d(&S.sring[sst][0], s_map, &S.sc_full[sst], tile * kTileKeys, pol_k);
         ++kcount;
@@ -589,7 +619,7 @@ __device__ void mma_issuer(Smem &S, uint32_t tmem, const FusedParams &p) {
   int job_iter = 0, kcount = 0, tcount = 0;
   for (;;) {
     const int slot = job_iter & 1;
-    if (!wait_bar(S, &S.j_full[slot], (job_iter >> 1) & 1, p)) break;
+    if (!wait_bar(S, &S.j_full[slot], (job_iter >> 1) & 1, p, kBackoffMma)) break;
     const JobInfo &J = S.job[slot];
     if (J.block < 0) break;
     const int ntiles = 2 * J.ns + J.nt;
@@ -598,8 +628,8 @@ __device__ void mma_issuer(Smem &S, uint32_t tmem, const FusedParams &p) {
     for (int u = 0; u < ntiles && ok; ++u) {
       const int stage = kcount % kKStages;
       const int buf = tcount & 1;
-      ok = wait_bar(S, &S.k_full[stage], (kcount / kKStages) & 1, p) &&
-           wait_bar(S, &S.t_empty[buf], ((tcount >> 1) & 1) ^ 1, p);
+      ok = wait_bar(S, &S.k_full[stage], (kcount / kKStages) & 1, p, kBackoffMma) &&
+           wait_bar(S, &S.t_empty[buf], ((tcount >> 1) & 1) ^ 1, p, kBackoffMma);
       if (!ok) break;
       tc_fence_after();
       const uint32_t a_base = smem_u32(&S.kring[stage][0]);
@@ -634,7 +664,8 @@ template <bool kLogits>
 __device__ void epilogue(Smem &S, uint32_t tmem, const FusedParams &p, int warp, int lane) {
   const int ew = warp - kEpiWarp0;  // 0..7
   const int quad = warp & 3;        // TMEM lane quadrant this warp may access
-  const int half = ew >> 2;         // rows 4*half .. 4*half+3
+  const int rbase = kRowsPerWarp * (ew >> 2);  // this warp's rows: rbase .. rbase + kRowsPerWarp - 1
+  const bool gate_warp = ew < kBlockRows;        // warps 0..7 also own row ew's gate / compaction
   const uint32_t lane_addr = (uint32_t)(quad * 32) << 16;
   const float NEG_INF = -INFINITY;
   const int cap = p.cap, seg = p.cap / kQuads;
@@ -659,7 +690,7 @@ __device__ void epilogue(Smem &S, uint32_t tmem, const FusedParams &p, int warp,
       if (lane == 0) ok = wait_bar(S, &S.s_empty[slot], ((job_iter >> 1) & 1) ^ 1, p);
       ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
       // per-row state for this scan: warp ew owns row ew
-      if (lane == 0) {
+      if (gate_warp && lane == 0) {
         const int n = J.end[ew] - J.start[ew];
         float t0 = NEG_INF;
         if (J.ns == 0 && J.mode == 0 && p.force_gate == 1 && n > 0) t0 = INFINITY;
@@ -668,24 +699,27 @@ __device__ void epilogue(Smem &S, uint32_t tmem, const FusedParams &p, int warp,
         S.ref_frozen[ew] = 0;
         S.msample[ew] = 0;
       }
-      for (int b = lane; b < kGateBins; b += 32) S.hist[ew][b] = 0;
+      if (gate_warp)
+        for (int b = lane; b < kGateBins; b += 32) S.hist[ew][b] = 0;
     }
     if (bar_or(kEpiBarrier, kEpiThreads, !ok || aborted(S))) break;
-    int st[4], en[4], cnt[4];
-    bool act[4];
-    float tau[4];
-    HeadW W[4];
+    int st[kRowsPerWarp], en[kRowsPerWarp], cnt[kRowsPerWarp];
+    bool act[kRowsPerWarp];
+    float tau[kRowsPerWarp];
+    HeadW W[kRowsPerWarp];
 #pragma unroll
-    for (int rr = 0; rr < 4; ++rr) {
-      const int r = 4 * half + rr;
+    for (int rr = 0; rr < kRowsPerWarp; ++rr) {
+      const int r = rbase + rr;
       st[rr] = J.start[r];
       en[rr] = J.end[r];
       act[rr] = ((J.mask >> r) & 1u) != 0;
       tau[rr] = kLogits ? NEG_INF : S.tau[r];
       cnt[rr] = 0;
 #pragma unroll
-      for (int i = 0; i < 4; ++i)
-        W[rr].w[i] = *reinterpret_cast<const float2 *>(&J.w[r][8 * i + 2 * (lane & 3)]);
+      for (int i = 0; i < 4; ++i) {
+        const float2 wv = *reinterpret_cast<const float2 *>(&J.w[r][8 * i + 2 * (lane & 3)]);
+        W[rr].w[i] = i < MQA_RELU_ALU_CHUNKS ? make_float2(2.f * wv.x, 2.f * wv.y) : wv;
+      }
     }
     const int ns = J.ns, ns2 = 2 * J.ns, ntiles = 2 * J.ns + J.nt, mode = J.mode;
     const int block = J.block;
@@ -696,7 +730,7 @@ __device__ void epilogue(Smem &S, uint32_t tmem, const FusedParams &p, int warp,
     const int kown = quad * 32 + owned_key(lane);  // key of this thread within a tile
     // One tile: wait for its accumulators and scales, score this lane's key for
     // the warp's 4 rows (masked to each row's range), release TMEM and scales.
-    auto score_tile = [&](int tile, float (&sv)[4]) -> bool {
+    auto score_tile = [&](int tile, float (&sv)[kRowsPerWarp]) -> bool {
       const int buf = tcount & 1, sst = tcount % kSStages;
       const int key = tile * kTileKeys + kown;
       const int tile_lo = tile * kTileKeys;
@@ -705,12 +739,12 @@ __device__ void epilogue(Smem &S, uint32_t tmem, const FusedParams &p, int warp,
       ok = __all_sync(0xFFFFFFFFu, ok);
       tc_fence_after();
       const float hsc = 0.5f * S.sring[sst][kown];
-      const uint32_t base = tmem + lane_addr + (uint32_t)(buf * kCols + (4 * half) * kHeads);
-      float raw[4];
+      const uint32_t base = tmem + lane_addr + (uint32_t)(buf * kCols + rbase * kHeads);
+      float raw[kRowsPerWarp];
       score_rows(&S.t_empty[buf], base, act, W, hsc, lane, raw);
       if (lane == 0) mbar_arrive(&S.sc_empty[sst]);
 #pragma unroll
-      for (int rr = 0; rr < 4; ++rr) {
+      for (int rr = 0; rr < kRowsPerWarp; ++rr) {
         // rows whose range covers the whole tile need no per-key mask
         const bool inside = tile_lo >= st[rr] && tile_lo + kTileKeys <= en[rr];
         sv[rr] = (inside || (key >= st[rr] && key < en[rr])) ? raw[rr] : NEG_INF;
@@ -721,14 +755,14 @@ __device__ void epilogue(Smem &S, uint32_t tmem, const FusedParams &p, int warp,
     // ---- sample tiles: coarse then fine pass of the gate
     for (int u = 0; u < ns2 && !bail; ++u) {
       const int tile = sample_tile(J, u < ns ? u : u - ns);
-      float sv[4];
+      float sv[kRowsPerWarp];
       score_tile(tile, sv);
       if (u < ns) {
         // coarse pass, step A: reference maximum from the row's first sample
         // tile with visible keys
 #pragma unroll
-        for (int rr = 0; rr < 4; ++rr) {
-          const int r = 4 * half + rr;
+        for (int rr = 0; rr < kRowsPerWarp; ++rr) {
+          const int r = rbase + rr;
           if (act[rr] && !S.ref_frozen[r]) {
             const uint32_t kv = sv[rr] > NEG_INF ? f2key(sv[rr]) : 0u;
             const uint32_t m = __reduce_max_sync(0xFFFFFFFFu, kv);
@@ -738,8 +772,8 @@ __device__ void epilogue(Smem &S, uint32_t tmem, const FusedParams &p, int warp,
         if (bar_or(kEpiBarrier, kEpiThreads, aborted(S))) { bail = true; break; }
         // step B: log-binned histogram of the position relative to the reference
 #pragma unroll
-        for (int rr = 0; rr < 4; ++rr) {
-          const int r = 4 * half + rr;
+        for (int rr = 0; rr < kRowsPerWarp; ++rr) {
+          const int r = rbase + rr;
           if (act[rr]) {
             const uint32_t ref = S.ref[r];
             const bool vis = sv[rr] > NEG_INF;
@@ -752,6 +786,7 @@ __device__ void epilogue(Smem &S, uint32_t tmem, const FusedParams &p, int warp,
         if (bar_or(kEpiBarrier, kEpiThreads, aborted(S))) { bail = true; break; }
         if (u == ns - 1) {
           // coarse bin of row ew that holds the target sample rank j
+          if (gate_warp) {
           const int r = ew;
           const int n = J.end[r] - J.start[r];
           const int m = S.msample[r];
@@ -812,6 +847,7 @@ __device__ void epilogue(Smem &S, uint32_t tmem, const FusedParams &p, int warp,
             S.g_khi[r] = khi;
             S.tau[r] = NEG_INF;
           }
+          }
           if (bar_or(kEpiBarrier, kEpiThreads, aborted(S))) { bail = true; break; }
           if (ew == 0 && lane == 0) atomicAdd(p.ws + kWsSampleTiles, ns2);
         }
@@ -821,8 +857,8 @@ __device__ void epilogue(Smem &S, uint32_t tmem, const FusedParams &p, int warp,
         // fine pass over the same sample tiles: 256 linear sub-bins of the
         // coarse bin, so the gate lands on the target sample rank
 #pragma unroll
-        for (int rr = 0; rr < 4; ++rr) {
-          const int r = 4 * half + rr;
+        for (int rr = 0; rr < kRowsPerWarp; ++rr) {
+          const int r = rbase + rr;
           if (act[rr] && S.g_on[r] && sv[rr] > NEG_INF) {
             const uint32_t kv = f2key(sv[rr]), klo = S.g_klo[r], khi = S.g_khi[r];
             if (kv >= klo && kv <= khi) {
@@ -833,6 +869,7 @@ __device__ void epilogue(Smem &S, uint32_t tmem, const FusedParams &p, int warp,
         }
         if (u == ns2 - 1) {
           if (bar_or(kEpiBarrier, kEpiThreads, aborted(S))) { bail = true; break; }
+          if (gate_warp) {
           const int r = ew;
           float t = NEG_INF;
           if (S.g_on[r]) {
@@ -871,9 +908,10 @@ __device__ void epilogue(Smem &S, uint32_t tmem, const FusedParams &p, int warp,
             }
           }
           if (lane == 0) S.tau[r] = t;
+          }
           if (bar_or(kEpiBarrier, kEpiThreads, aborted(S))) { bail = true; break; }
 #pragma unroll
-          for (int rr = 0; rr < 4; ++rr) tau[rr] = S.tau[4 * half + rr];
+          for (int rr = 0; rr < kRowsPerWarp; ++rr) tau[rr] = S.tau[rbase + rr];
         }
         continue;
       }
@@ -882,14 +920,14 @@ __device__ void epilogue(Smem &S, uint32_t tmem, const FusedParams &p, int warp,
     for (int u = ns2; u < ntiles && !bail; ++u) {
       const int tile = J.lo_t + (u - ns2);
       const int key = tile * kTileKeys + kown;
-      float sv[4];
+      float sv[kRowsPerWarp];
       score_tile(tile, sv);
       if (kLogits) {
         if (key < p.keys) {
 #pragma unroll
-          for (int rr = 0; rr < 4; ++rr) {
+          for (int rr = 0; rr < kRowsPerWarp; ++rr) {
             if (act[rr]) {
-              const size_t row = (size_t)block * kBlockRows + 4 * half + rr;
+              const size_t row = (size_t)block * kBlockRows + rbase + rr;
               p.logits[row * (size_t)p.keys + key] = sv[rr];
             }
           }
@@ -899,13 +937,13 @@ __device__ void epilogue(Smem &S, uint32_t tmem, const FusedParams &p, int warp,
       // main scan: append keys above the gate to this warp's segment of each row
       // (a private counter per warp: no atomics)
 #pragma unroll
-      for (int rr = 0; rr < 4; ++rr) {
+      for (int rr = 0; rr < kRowsPerWarp; ++rr) {
         const bool pass = sv[rr] > tau[rr];
         const uint32_t bal = __ballot_sync(0xFFFFFFFFu, pass);
         if (bal) {
           const int pos = cnt[rr] + __popc(bal & lt);
           if (pass && pos < seg) {
-            const size_t o = (size_t)((4 * half + rr) * kQuads + quad) * seg + pos;
+            const size_t o = (size_t)((rbase + rr) * kQuads + quad) * seg + pos;
             slab_keys[o] = f2key(sv[rr]);
             slab_idx[o] = key;
           }
@@ -917,9 +955,10 @@ __device__ void epilogue(Smem &S, uint32_t tmem, const FusedParams &p, int warp,
         // to its top-k (into segment 0) before any segment can overflow
         if (lane == 0) {
 #pragma unroll
-          for (int rr = 0; rr < 4; ++rr) S.segcnt[4 * half + rr][quad] = cnt[rr];
+          for (int rr = 0; rr < kRowsPerWarp; ++rr) S.segcnt[rbase + rr][quad] = cnt[rr];
         }
         if (bar_or(kEpiBarrier, kEpiThreads, aborted(S))) { bail = true; break; }
+        if (gate_warp) {
         const int r = ew;
         RowSlab R;
         R.keys = slab_keys + (size_t)r * kQuads * seg;
@@ -943,18 +982,19 @@ __device__ void epilogue(Smem &S, uint32_t tmem, const FusedParams &p, int warp,
             atomicAdd(p.ws + kWsCompactions, 1);
           }
         }
+        }
         __threadfence_block();
         if (bar_or(kEpiBarrier, kEpiThreads, aborted(S))) { bail = true; break; }
 #pragma unroll
-        for (int rr = 0; rr < 4; ++rr) {
-          tau[rr] = S.tau[4 * half + rr];
-          cnt[rr] = S.segcnt[4 * half + rr][quad];
+        for (int rr = 0; rr < kRowsPerWarp; ++rr) {
+          tau[rr] = S.tau[rbase + rr];
+          cnt[rr] = S.segcnt[rbase + rr][quad];
         }
       }
     }
     if (!kLogits && lane == 0) {
 #pragma unroll
-      for (int rr = 0; rr < 4; ++rr) S.segcnt[4 * half + rr][quad] = cnt[rr];
+      for (int rr = 0; rr < kRowsPerWarp; ++rr) S.segcnt[rbase + rr][quad] = cnt[rr];
     }
     __threadfence_block();  // slab writes of every epilogue warp precede the hand-over
     if (bar_or(kEpiBarrier, kEpiThreads, bail || aborted(S))) break;
@@ -992,7 +1032,7 @@ __device__ void selection(Smem &S, const FusedParams &p, int warp, int lane) {
   for (;;) {
     const int slot = job_iter & 1;
     bool ok = true;
-    if (lane == 0) ok = wait_bar(S, &S.s_full[slot], (job_iter >> 1) & 1, p);
+    if (lane == 0) ok = wait_bar(S, &S.s_full[slot], (job_iter >> 1) & 1, p, kBackoffIdle);
     ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
     if (!ok) break;
     const SelSlot &Q = S.sel[slot];

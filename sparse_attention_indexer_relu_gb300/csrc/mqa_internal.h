@@ -18,9 +18,14 @@ constexpr int kSStages = 8;     // key-scale ring depth (held until the epilogue
 constexpr int kQBytes = kCols * kDim;       // 32 KiB of q per block
 constexpr int kKTileBytes = kTileKeys * kDim;  // 16 KiB of k per tile
 
-constexpr int kEpiWarps = 8;    // two per TMEM lane quadrant; each owns 4 rows
+#ifndef MQA_ROWS_PER_WARP
+#define MQA_ROWS_PER_WARP 2
+#endif
+constexpr int kRowsPerWarp = MQA_ROWS_PER_WARP;  // rows of a block each epilogue warp scores
+constexpr int kQuadsC = 4;
+constexpr int kEpiWarps = kBlockRows * kQuadsC / kRowsPerWarp;  // per TMEM lane quadrant: 8 / kRowsPerWarp
 constexpr int kSelWarps = 2;    // candidate selection warps
-constexpr int kThreads = 384;   // warp 0 producer, 1 MMA, 2-3 selection, 4-11 epilogue
+constexpr int kThreads = (4 + kEpiWarps) * 32;  // warp 0 producer, 1 MMA, 2-3 selection, then epilogue
 constexpr int kEpiWarp0 = 4;
 constexpr int kSelWarp0 = 2;
 constexpr int kQuads = 4;       // TMEM lane quadrants; each row's slab has one segment per quadrant
