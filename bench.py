@@ -292,15 +292,32 @@ def main():
         dist.destroy_process_group()
 
 
+KERNEL_SOURCES = ("mqa_fused.cu", "ptx.cuh", "mqa_internal.h")
+
+
+def kernel_source_digest():
+    """sha256 over the fused kernel's source files, to tie a DRAM capture to
+    the exact kernel it was taken on."""
+    import hashlib
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "sparse_attention_indexer_relu_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()
+
+
 def load_traffic(workload):
-    """DRAM bytes per launch of the fused kernel from the committed ncu summary
-    (None when no capture matches the current kernel)."""
+    """DRAM bytes (read + write) per launch of the fused kernel from the
+    committed ncu summary; None when there is no capture for this workload or
+    the kernel's source has changed since it was taken."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(path):
         return None
     try:
         d = json.load(open(path))
-        return d.get(workload)
+        if d.get("kernel_source_sha256") != kernel_source_digest():
+            return None
+        return d.get("dram_bytes_per_launch", {}).get(workload)
     except Exception:
         return None
 
