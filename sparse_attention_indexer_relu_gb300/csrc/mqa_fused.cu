@@ -406,6 +406,211 @@ __device__ int warp_emit(const RowSlab &R, uint32_t T, int take_eq, bool take_al
   return outc < limit ? outc : limit;
 }
 
+// ------------------------------------------------------------------ selection over a key range
+// 16-byte loads in flight per lane in the selection warps' scans.
+#ifndef MQA_SEL_DEPTH
+#define MQA_SEL_DEPTH 4
+#endif
+constexpr int kSelDepth = MQA_SEL_DEPTH;
+
+// Smallest and largest order key of the row's candidates (one load-only pass).
+__device__ void warp_key_range(const RowSlab &R, int lane, uint32_t *kmin, uint32_t *kmax) {
+  uint32_t lo = 0xFFFFFFFFu, hi = 0u;
+#pragma unroll 1
+  for (int q = 0; q < kQuads; ++q) {
+    const uint32_t *keys = R.keys + (size_t)q * R.seg;
+    const int n = R.c[q], n4 = n & ~3;
+#pragma unroll 1
+    for (int i0 = 4 * lane; i0 < n4; i0 += 32 * 4 * kSelDepth) {
+      uint4 kk[kSelDepth];
+#pragma unroll
+      for (int j = 0; j < kSelDepth; ++j) {
+        const int i = i0 + 32 * 4 * j;
+        kk[j] = i < n4 ? __ldcg(reinterpret_cast<const uint4 *>(keys + i)) : make_uint4(0, 0, 0, 0);
+      }
+#pragma unroll
+      for (int j = 0; j < kSelDepth; ++j) {
+        if (i0 + 32 * 4 * j < n4) {
+          lo = min(min(lo, min(kk[j].x, kk[j].y)), min(kk[j].z, kk[j].w));
+          hi = max(max(hi, max(kk[j].x, kk[j].y)), max(kk[j].z, kk[j].w));
+        }
+      }
+    }
+    if (n4 + lane < n) {
+      const uint32_t v = __ldcg(keys + n4 + lane);
+      lo = min(lo, v);
+      hi = max(hi, v);
+    }
+  }
+  *kmin = __reduce_min_sync(0xFFFFFFFFu, lo);
+  *kmax = __reduce_max_sync(0xFFFFFFFFu, hi);
+}
+
+// Exact k-th largest order key of the row's candidates (total > k >= 1).
+// The candidates lie in [kmin, kmax] and share the binary prefix of those
+// two, so 8-bit radix digits start at the highest bit where they differ
+// (usually three levels; no pile-up of all keys in one bin).  Eight 16-byte
+// loads per lane are in flight per batch.
+__device__ uint32_t warp_select_range(const RowSlab &R, int k, int *hist, int lane, int *take_eq) {
+  uint32_t kmin, kmax;
+  warp_key_range(R, lane, &kmin, &kmax);
+  const uint32_t diff = kmin ^ kmax;
+  int hi = diff ? 32 - __clz(diff) : 0;  // bits [0, hi) vary among the candidates
+  uint32_t prefix = hi >= 32 ? 0u : (kmax & ~((1u << hi) - 1u));
+  int want = k;
+#pragma unroll 1
+  while (hi > 0) {
+    const int bits = hi >= 8 ? 8 : hi;
+    const int shift = hi - bits;
+    const uint32_t dmask = (1u << bits) - 1u;
+    const uint32_t hi_mask = hi >= 32 ? 0u : (0xFFFFFFFFu << hi);
+    for (int b = lane; b < 256; b += 32) hist[b] = 0;
+    __syncwarp();
+#pragma unroll 1
+    for (int q = 0; q < kQuads; ++q) {
+      const uint32_t *keys = R.keys + (size_t)q * R.seg;
+      const int n = R.c[q], n4 = n & ~3;
+#pragma unroll 1
+      for (int i0 = 4 * lane; i0 < n4; i0 += 32 * 4 * kSelDepth) {
+        uint4 kk[kSelDepth];
+#pragma unroll
+        for (int j = 0; j < kSelDepth; ++j) {
+          const int i = i0 + 32 * 4 * j;
+          kk[j] = i < n4 ? __ldcg(reinterpret_cast<const uint4 *>(keys + i)) : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int j = 0; j < kSelDepth; ++j) {
+          if (i0 + 32 * 4 * j < n4) {
+            const uint32_t v[4] = {kk[j].x, kk[j].y, kk[j].z, kk[j].w};
+#pragma unroll
+            for (int t = 0; t < 4; ++t)
+              if ((v[t] & hi_mask) == prefix) atomicAdd(&hist[(v[t] >> shift) & dmask], 1);
+          }
+        }
+      }
+      if (n4 + lane < n) {
+        const uint32_t v = __ldcg(keys + n4 + lane);
+        if ((v & hi_mask) == prefix) atomicAdd(&hist[(v >> shift) & dmask], 1);
+      }
+    }
+    __syncwarp();
+    int c[8], tot = 0;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      c[j] = hist[255 - 8 * lane - j];
+      tot += c[j];
+    }
+    int incl = tot;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int v = __shfl_up_sync(0xFFFFFFFFu, incl, off);
+      if (lane >= off) incl += v;
+    }
+    const int excl = incl - tot;
+    const uint32_t bm = __ballot_sync(0xFFFFFFFFu, excl < want && want <= incl);
+    const int src = bm ? __ffs(bm) - 1 : 31;
+    int bin = 0, above = 0;
+    if (lane == src) {
+      int run = excl;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        if (run + c[j] >= want) {
+          bin = 255 - 8 * lane - j;
+          above = run;
+          break;
+        }
+        run += c[j];
+      }
+    }
+    bin = __shfl_sync(0xFFFFFFFFu, bin, src);
+    above = __shfl_sync(0xFFFFFFFFu, above, src);
+    want -= above;
+    prefix |= (uint32_t)bin << shift;
+    hi = shift;
+    __syncwarp();
+  }
+  *take_eq = want;
+  return prefix;
+}
+
+// Write the row's top-k indices (idx - base) to out: every key > T plus
+// `take_eq` of the keys equal to T (all keys when take_all).  Which equal keys
+// are taken and the output order are free; 8 records per lane per batch.
+// Returns the number written (at most `limit`).
+__device__ int warp_emit_out(const RowSlab &R, uint32_t T, int take_eq, bool take_all, int32_t *out, int base,
+                             int limit, int lane) {
+  int outc = 0, eq_seen = 0;
+#pragma unroll 1
+  for (int q = 0; q < kQuads; ++q) {
+    const uint32_t *keys = R.keys + (size_t)q * R.seg;
+    const int32_t *idx = R.idx + (size_t)q * R.seg;
+    const int n = R.c[q];
+#pragma unroll 1
+    for (int i0 = 0; i0 < n; i0 += 32 * 8) {
+      uint32_t kk[8];
+      int32_t ii[8];
+#pragma unroll
+      for (int g = 0; g < 2; ++g) {
+        const int i = i0 + 32 * 4 * g + 4 * lane;
+        if (i + 3 < n) {
+          const uint4 kv = __ldcg(reinterpret_cast<const uint4 *>(keys + i));
+          const int4 iv = __ldcg(reinterpret_cast<const int4 *>(idx + i));
+          kk[4 * g] = kv.x; kk[4 * g + 1] = kv.y; kk[4 * g + 2] = kv.z; kk[4 * g + 3] = kv.w;
+          ii[4 * g] = iv.x; ii[4 * g + 1] = iv.y; ii[4 * g + 2] = iv.z; ii[4 * g + 3] = iv.w;
+        } else {
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            kk[4 * g + j] = i + j < n ? __ldcg(keys + i + j) : 0u;
+            ii[4 * g + j] = i + j < n ? __ldcg(idx + i + j) : 0;
+          }
+        }
+      }
+      bool gt[8], eq[8];
+      int neq = 0;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const bool v = i0 + 32 * 4 * (j >> 2) + 4 * lane + (j & 3) < n;
+        gt[j] = v && (take_all || kk[j] > T);
+        eq[j] = v && !take_all && kk[j] == T;
+        neq += eq[j];
+      }
+      int eq_incl = neq;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const int v = __shfl_up_sync(0xFFFFFFFFu, eq_incl, off);
+        if (lane >= off) eq_incl += v;
+      }
+      int eq_rank = eq_seen + eq_incl - neq;
+      int ntake = 0;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        if (eq[j]) {
+          eq[j] = eq_rank < take_eq;
+          ++eq_rank;
+        }
+        ntake += gt[j] || eq[j];
+      }
+      int t_incl = ntake;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const int v = __shfl_up_sync(0xFFFFFFFFu, t_incl, off);
+        if (lane >= off) t_incl += v;
+      }
+      int pos = outc + t_incl - ntake;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        if (gt[j] || eq[j]) {
+          if (pos < limit) out[pos] = ii[j] - base;
+          ++pos;
+        }
+      }
+      outc += __shfl_sync(0xFFFFFFFFu, t_incl, 31);
+      eq_seen += __shfl_sync(0xFFFFFFFFu, eq_incl, 31);
+    }
+  }
+  return outc < limit ? outc : limit;
+}
+
 // ------------------------------------------------------------------ heaviest-first order
 __device__ void build_order(Smem &S, const FusedParams &p) {
   const int nb = p.nblocks;
@@ -1074,11 +1279,11 @@ __device__ void selection(Smem &S, const FusedParams &p, int warp, int lane) {
       int32_t *out = p.out + (size_t)row * topk;
       int wrote;
       if (cnt <= topk) {
-        wrote = warp_emit<false>(R, 0u, 0, true, out, Q.start[r], topk, lane);
+        wrote = warp_emit_out(R, 0u, 0, true, out, Q.start[r], topk, lane);
       } else {
         int take_eq = 0;
-        const uint32_t T = warp_radix_select(R, topk, hist, lane, &take_eq);
-        wrote = warp_emit<false>(R, T, take_eq, false, out, Q.start[r], topk, lane);
+        const uint32_t T = warp_select_range(R, topk, hist, lane, &take_eq);
+        wrote = warp_emit_out(R, T, take_eq, false, out, Q.start[r], topk, lane);
       }
       for (int i = wrote + lane; i < topk; i += 32) out[i] = -1;
     }
