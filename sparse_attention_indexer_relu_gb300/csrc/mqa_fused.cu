@@ -160,7 +160,7 @@ __device__ __forceinline__ bool wait_counter(Smem &S, int *flag, int target, con
 // order is fixed and the fused and logits instantiations share this code, so
 // both produce bit-identical scores.
 #ifndef MQA_RELU_ALU_CHUNKS
-#define MQA_RELU_ALU_CHUNKS 2
+#define MQA_RELU_ALU_CHUNKS 1
 #endif
 // Of a thread's 4 head-pair chunks per key, the first MQA_RELU_ALU_CHUNKS form
 // relu as max(x, 0) on the ALU pipe with pre-doubled weights (2w * max(x, 0));
@@ -908,16 +908,20 @@ __device__ void epilogue(Smem &S, uint32_t tmem, const FusedParams &p, int warp,
         for (int b = lane; b < kGateBins; b += 32) S.hist[ew][b] = 0;
     }
     if (bar_or(kEpiBarrier, kEpiThreads, !ok || aborted(S))) break;
-    int st[kRowsPerWarp], en[kRowsPerWarp], cnt[kRowsPerWarp];
+    int cnt[kRowsPerWarp];
+    // tiles [f_lo, f_hi) lie inside the range of every active row of this warp
+    int f_lo = 0, f_hi = INT_MAX;
     bool act[kRowsPerWarp];
     float tau[kRowsPerWarp];
     HeadW W[kRowsPerWarp];
 #pragma unroll
     for (int rr = 0; rr < kRowsPerWarp; ++rr) {
       const int r = rbase + rr;
-      st[rr] = J.start[r];
-      en[rr] = J.end[r];
       act[rr] = ((J.mask >> r) & 1u) != 0;
+      if (act[rr]) {
+        f_lo = max(f_lo, (J.start[r] + kTileKeys - 1) / kTileKeys);
+        f_hi = min(f_hi, J.end[r] / kTileKeys);
+      }
       tau[rr] = kLogits ? NEG_INF : S.tau[r];
       cnt[rr] = 0;
 #pragma unroll
@@ -938,7 +942,6 @@ __device__ void epilogue(Smem &S, uint32_t tmem, const FusedParams &p, int warp,
     auto score_tile = [&](int tile, float (&sv)[kRowsPerWarp]) -> bool {
       const int buf = tcount & 1, sst = tcount % kSStages;
       const int key = tile * kTileKeys + kown;
-      const int tile_lo = tile * kTileKeys;
       bool ok = wait_bar(S, &S.t_full[buf], (tcount >> 1) & 1, p);
       ok = wait_bar(S, &S.sc_full[sst], (tcount / kSStages) & 1, p) && ok;
       ok = __all_sync(0xFFFFFFFFu, ok);
@@ -948,11 +951,16 @@ __device__ void epilogue(Smem &S, uint32_t tmem, const FusedParams &p, int warp,
       float raw[kRowsPerWarp];
       score_rows(&S.t_empty[buf], base, act, W, hsc, lane, raw);
       if (lane == 0) mbar_arrive(&S.sc_empty[sst]);
+      if (tile >= f_lo && tile < f_hi) {
+        // the tile lies inside every row's range: no per-key mask
 #pragma unroll
-      for (int rr = 0; rr < kRowsPerWarp; ++rr) {
-        // rows whose range covers the whole tile need no per-key mask
-        const bool inside = tile_lo >= st[rr] && tile_lo + kTileKeys <= en[rr];
-        sv[rr] = (inside || (key >= st[rr] && key < en[rr])) ? raw[rr] : NEG_INF;
+        for (int rr = 0; rr < kRowsPerWarp; ++rr) sv[rr] = raw[rr];
+      } else {
+#pragma unroll
+        for (int rr = 0; rr < kRowsPerWarp; ++rr) {
+          const int r = rbase + rr;
+          sv[rr] = (key >= J.start[r] && key < J.end[r]) ? raw[rr] : NEG_INF;
+        }
       }
       ++tcount;
       return ok;
