@@ -160,7 +160,7 @@ __device__ __forceinline__ bool wait_counter(Smem &S, int *flag, int target, con
 // order is fixed and the fused and logits instantiations share this code, so
 // both produce bit-identical scores.
 #ifndef MQA_RELU_ALU_CHUNKS
-#define MQA_RELU_ALU_CHUNKS 1
+#define MQA_RELU_ALU_CHUNKS 0
 #endif
 // Of a thread's 4 head-pair chunks per key, the first MQA_RELU_ALU_CHUNKS form
 // relu as max(x, 0) on the ALU pipe with pre-doubled weights (2w * max(x, 0));
@@ -208,14 +208,14 @@ __device__ __forceinline__ float row_head_sum(const uint32_t (&lo)[16], const ui
 __device__ __forceinline__ int owned_key(int lane) { return (lane >> 2) + 8 * ((lane >> 1) & 1) + 16 * (lane & 1); }
 
 // Scaled head sums of this lane's key for the warp's kRowsPerWarp rows of one
-// tile, read from TMEM at `base` (the warp's quadrant, its first row); rows
-// whose flag is off give -inf.  Every row is always loaded and summed (every
-// TMEM address here is in the allocation), so the code has no per-row
-// branches.  Rows are loaded kLoadRows at a time; the TMEM buffer is released
+// tile, read from TMEM at `base` (the warp's quadrant, its first row).  Every
+// row is always loaded and summed (every TMEM address here is in the
+// allocation), so the code has no per-row branches; the caller masks rows
+// that do not take part.  Rows are loaded kLoadRows at a time; the TMEM buffer is released
 // (t_empty) once the last group is in registers.
 constexpr int kLoadRows = kRowsPerWarp >= 4 ? 2 : 1;
-__device__ __forceinline__ void score_rows(uint64_t *t_empty, uint32_t base, const bool (&act)[kRowsPerWarp],
-                                           const HeadW (&W)[kRowsPerWarp], float hsc, int lane,
+__device__ __forceinline__ void score_rows(uint64_t *t_empty, uint32_t base, const HeadW (&W)[kRowsPerWarp],
+                                           float hsc, int lane,
                                            float (&out)[kRowsPerWarp]) {
 #pragma unroll
   for (int g = 0; g < kRowsPerWarp / kLoadRows; ++g) {
@@ -235,8 +235,7 @@ __device__ __forceinline__ void score_rows(uint64_t *t_empty, uint32_t base, con
 #pragma unroll
     for (int j = 0; j < kLoadRows; ++j) {
       const int rr = g * kLoadRows + j;
-      const float sc = row_head_sum(lo[j], hi[j], W[rr], lane) * hsc;
-      out[rr] = act[rr] ? sc : -INFINITY;
+      out[rr] = row_head_sum(lo[j], hi[j], W[rr], lane) * hsc;
     }
   }
 }
@@ -909,7 +908,8 @@ __device__ void epilogue(Smem &S, uint32_t tmem, const FusedParams &p, int warp,
     }
     if (bar_or(kEpiBarrier, kEpiThreads, !ok || aborted(S))) break;
     int cnt[kRowsPerWarp];
-    // tiles [f_lo, f_hi) lie inside the range of every active row of this warp
+    // tiles [f_lo, f_hi) lie inside the range of every row of this warp
+    // (none when one of its rows does not take part)
     int f_lo = 0, f_hi = INT_MAX;
     bool act[kRowsPerWarp];
     float tau[kRowsPerWarp];
@@ -918,10 +918,8 @@ __device__ void epilogue(Smem &S, uint32_t tmem, const FusedParams &p, int warp,
     for (int rr = 0; rr < kRowsPerWarp; ++rr) {
       const int r = rbase + rr;
       act[rr] = ((J.mask >> r) & 1u) != 0;
-      if (act[rr]) {
-        f_lo = max(f_lo, (J.start[r] + kTileKeys - 1) / kTileKeys);
-        f_hi = min(f_hi, J.end[r] / kTileKeys);
-      }
+      f_lo = max(f_lo, (J.start[r] + kTileKeys - 1) / kTileKeys);
+      f_hi = min(f_hi, act[rr] ? J.end[r] / kTileKeys : 0);
       tau[rr] = kLogits ? NEG_INF : S.tau[r];
       cnt[rr] = 0;
 #pragma unroll
@@ -949,7 +947,7 @@ __device__ void epilogue(Smem &S, uint32_t tmem, const FusedParams &p, int warp,
       const float hsc = 0.5f * S.sring[sst][kown];
       const uint32_t base = tmem + lane_addr + (uint32_t)(buf * kCols + rbase * kHeads);
       float raw[kRowsPerWarp];
-      score_rows(&S.t_empty[buf], base, act, W, hsc, lane, raw);
+      score_rows(&S.t_empty[buf], base, W, hsc, lane, raw);
       if (lane == 0) mbar_arrive(&S.sc_empty[sst]);
       if (tile >= f_lo && tile < f_hi) {
         // the tile lies inside every row's range: no per-key mask
@@ -959,7 +957,7 @@ __device__ void epilogue(Smem &S, uint32_t tmem, const FusedParams &p, int warp,
 #pragma unroll
         for (int rr = 0; rr < kRowsPerWarp; ++rr) {
           const int r = rbase + rr;
-          sv[rr] = (key >= J.start[r] && key < J.end[r]) ? raw[rr] : NEG_INF;
+          sv[rr] = (act[rr] && key >= J.start[r] && key < J.end[r]) ? raw[rr] : NEG_INF;
         }
       }
       ++tcount;
