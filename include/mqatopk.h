@@ -69,7 +69,12 @@ extern "C" {
 #define MQA_STAT_SAMPLE_TILES 6   /* 128-key tiles scored for gate sampling */
 #define MQA_STAT_OVERFLOW_ROWS 7  /* gated rows whose candidates overflowed */
 #define MQA_STAT_UNDERFILL_ROWS 8 /* gated rows left with fewer than top-k */
-#define MQA_STATS_COUNT 9
+#define MQA_STAT_SELECT_FALLBACK 9 /* gated rows whose threshold bin outgrew the
+                                      selection warp's shared-memory list and
+                                      took the slab-pass radix select */
+#define MQA_STAT_KERNEL_US 10     /* first CTA start to last CTA end, microseconds */
+#define MQA_STAT_END_SPREAD_US 11 /* first to last CTA end, microseconds (tail) */
+#define MQA_STATS_COUNT 12
 
 /* Test-only knobs for mqa_topk_prefill_debug.  Zero-initialise for defaults. */
 typedef struct mqa_topk_debug_options {

@@ -38,6 +38,8 @@ constexpr uint32_t kIdesc = idesc_f8_e4m3_f32(kTileKeys, kCols);
 constexpr int kEpiThreads = kEpiWarps * 32;
 constexpr int kEpiBarrier = 1;  // named barrier id for the epilogue warps
 constexpr int kGateBins = 288;  // 257 two-sided distance bins, padded to 9 per lane
+constexpr int kScoreBins = 128;  // linear score bins per gated row between the gate and the sample maximum
+constexpr int kSelList = 1024;   // threshold-bin records a selection warp holds in shared memory
 
 struct JobInfo {
   int block;      // row block (-1: no more work)
@@ -57,6 +59,8 @@ struct SelSlot {  // what the selection warps need from a finished scan
   int nrows;
   int start[kBlockRows], n[kBlockRows];
   int gated[kBlockRows];
+  float blo[kBlockRows], binv[kBlockRows];  // score-bin origin (the gate) and bins per unit score
+  int binned[kBlockRows];                    // mode-0 gated row: selected through score bins
   int segcnt[kBlockRows][kQuads];  // records appended per (row, quadrant segment)
 };
 
@@ -76,6 +80,10 @@ struct Smem {
   uint32_t g_klo[kBlockRows], g_khi[kBlockRows];
   int hist[kBlockRows][kGateBins];
   int selhist[kSelWarps][256];
+  uint32_t sel_lk[kSelWarps][kSelList];  // keys of the threshold bin's members
+  int32_t sel_li[kSelWarps][kSelList];   // and their key indices
+  uint32_t smax[kBlockRows];             // largest sample order key per row (current scan)
+  float binv[kBlockRows];                // score bins per unit score (current scan)
   uint16_t order[kMaxSortBlocks];
   uint64_t k_full[kKStages], k_empty[kKStages];
   uint64_t sc_full[kSStages], sc_empty[kSStages];
@@ -94,6 +102,7 @@ struct Smem {
 };
 
 size_t fused_smem_bytes() { return sizeof(Smem) + 1024; }
+static_assert(sizeof(Smem) + 1024 <= 232448, "shared memory above the 227 KB opt-in limit");
 
 __device__ __forceinline__ Smem &get_smem(uint8_t *raw) {
   uintptr_t a = reinterpret_cast<uintptr_t>(raw);
@@ -271,6 +280,11 @@ __device__ __forceinline__ uint64_t dist_bin_hi(int b) {
 }
 
 // ------------------------------------------------------------------ warp radix select
+#ifdef MQA_SEL_NOINLINE
+#define MQA_SEL_FN __noinline__
+#else
+#define MQA_SEL_FN
+#endif
 // A row's candidates live in kQuads segments (one per TMEM lane quadrant) of
 // `seg` records each; segment q holds c[q] valid records.
 struct RowSlab {
@@ -284,7 +298,7 @@ struct RowSlab {
 // Exact k-th largest order key over the row's candidates (requires total > k
 // >= 1), by four 8-bit digit levels.  Returns the key T; *take_eq receives
 // how many keys equal to T belong to the top k (the rest of the top k is > T).
-__device__ uint32_t warp_radix_select(const RowSlab &R, int k, int *hist, int lane, int *take_eq) {
+__device__ MQA_SEL_FN uint32_t warp_radix_select(const RowSlab &R, int k, int *hist, int lane, int *take_eq) {
   uint32_t prefix = 0;
   int want = k;
 #pragma unroll 1
@@ -357,7 +371,7 @@ __device__ uint32_t warp_radix_select(const RowSlab &R, int k, int *hist, int la
 // segment 0 (stable; within segment 0 writes never overtake reads, and the
 // other segments are only read).  At most `limit` entries are kept.
 template <bool kCompact>
-__device__ int warp_emit(const RowSlab &R, uint32_t T, int take_eq, bool take_all, int32_t *out, int base,
+__device__ MQA_SEL_FN int warp_emit(const RowSlab &R, uint32_t T, int take_eq, bool take_all, int32_t *out, int base,
                          int limit, int lane) {
   int outc = 0, eq_seen = 0;
   const uint32_t lt = lanemask_lt();
@@ -450,7 +464,7 @@ __device__ void warp_key_range(const RowSlab &R, int lane, uint32_t *kmin, uint3
 // two, so 8-bit radix digits start at the highest bit where they differ
 // (usually three levels; no pile-up of all keys in one bin).  Eight 16-byte
 // loads per lane are in flight per batch.
-__device__ uint32_t warp_select_range(const RowSlab &R, int k, int *hist, int lane, int *take_eq) {
+__device__ MQA_SEL_FN uint32_t warp_select_range(const RowSlab &R, int k, int *hist, int lane, int *take_eq) {
   uint32_t kmin, kmax;
   warp_key_range(R, lane, &kmin, &kmax);
   const uint32_t diff = kmin ^ kmax;
@@ -536,7 +550,7 @@ __device__ uint32_t warp_select_range(const RowSlab &R, int k, int *hist, int la
 // `take_eq` of the keys equal to T (all keys when take_all).  Which equal keys
 // are taken and the output order are free; 8 records per lane per batch.
 // Returns the number written (at most `limit`).
-__device__ int warp_emit_out(const RowSlab &R, uint32_t T, int take_eq, bool take_all, int32_t *out, int base,
+__device__ MQA_SEL_FN int warp_emit_out(const RowSlab &R, uint32_t T, int take_eq, bool take_all, int32_t *out, int base,
                              int limit, int lane) {
   int outc = 0, eq_seen = 0;
 #pragma unroll 1
@@ -608,6 +622,264 @@ __device__ int warp_emit_out(const RowSlab &R, uint32_t T, int take_eq, bool tak
     }
   }
   return outc < limit ? outc : limit;
+}
+
+// ------------------------------------------------------------------ binned selection
+// A gated row's candidates all score above its gate t.  Their scores are
+// counted into kScoreBins linear bins between t and the largest sample score
+// (scores above that share the top bin).  The count pass finds the bin B that
+// holds the k-th largest score; the order keys where bin B starts and ends
+// are then found by bisection (the bin is a monotone function of the key), and
+// one more pass writes every candidate above B straight to the output and
+// gathers B's members into shared memory, where an exact radix select over
+// those few records settles the rest.
+__device__ __forceinline__ int score_bin(float s, float lo, float inv) {
+  const float x = __fmul_rn(__fsub_rn(s, lo), inv);
+  return x >= (float)(kScoreBins - 1) ? kScoreBins - 1 : max(0, __float2int_rz(x));
+}
+
+// Smallest order key in [lo_key, kKeyPosInf] whose score bin is >= b
+// (kKeyPosInf + 1 when there is none).  Keys above +inf's are NaNs and are
+// never searched.
+constexpr uint32_t kKeyPosInf = 0xFF800000u;
+__device__ uint64_t first_key_of_bin(int b, uint32_t lo_key, float lo, float inv) {
+  uint64_t a = lo_key, z = (uint64_t)kKeyPosInf + 1;  // answer in [a, z]
+  while (a < z) {
+    const uint64_t m = (a + z) >> 1;
+    if (score_bin(key2f((uint32_t)m), lo, inv) >= b) z = m;
+    else a = m + 1;
+  }
+  return a;
+}
+
+// Count pass: score-bin histogram of the row's candidates into hist[kScoreBins].
+#ifndef MQA_HIST_DEPTH
+#define MQA_HIST_DEPTH 8
+#endif
+constexpr int kHistDepth = MQA_HIST_DEPTH;  // 16-byte key loads in flight per lane
+__device__ void score_hist(const RowSlab &R, float lo, float inv, int *hist, int lane) {
+  for (int b = lane; b < kScoreBins; b += 32) hist[b] = 0;
+  __syncwarp();
+#pragma unroll 1
+  for (int q = 0; q < kQuads; ++q) {
+    const uint32_t *keys = R.keys + (size_t)q * R.seg;
+    const int n = R.c[q], n4 = n & ~3;
+#pragma unroll 1
+    for (int i0 = 4 * lane; i0 < n4; i0 += 32 * 4 * kHistDepth) {
+      uint4 kk[kHistDepth];
+#pragma unroll
+      for (int j = 0; j < kHistDepth; ++j) {
+        const int i = i0 + 32 * 4 * j;
+        kk[j] = i < n4 ? __ldcg(reinterpret_cast<const uint4 *>(keys + i)) : make_uint4(0, 0, 0, 0);
+      }
+#pragma unroll
+      for (int j = 0; j < kHistDepth; ++j) {
+        if (i0 + 32 * 4 * j < n4) {
+          atomicAdd(&hist[score_bin(key2f(kk[j].x), lo, inv)], 1);
+          atomicAdd(&hist[score_bin(key2f(kk[j].y), lo, inv)], 1);
+          atomicAdd(&hist[score_bin(key2f(kk[j].z), lo, inv)], 1);
+          atomicAdd(&hist[score_bin(key2f(kk[j].w), lo, inv)], 1);
+        }
+      }
+    }
+    if (n4 + lane < n) atomicAdd(&hist[score_bin(key2f(__ldcg(keys + n4 + lane)), lo, inv)], 1);
+  }
+  __syncwarp();
+}
+
+// Exact top-k of a gated row (total > k >= 1, every candidate scoring above
+// lo) into out[0, k).  Returns the number written, or -1 (nothing written)
+// when the threshold bin holds more records than the shared-memory list.
+constexpr int kBinsPerLane = kScoreBins / 32;
+#ifndef MQA_PASS2_GROUPS
+#define MQA_PASS2_GROUPS 4
+#endif
+constexpr int kPass2Groups = MQA_PASS2_GROUPS;  // 16-byte key and index loads in flight per lane
+__device__ MQA_SEL_FN int warp_select_binned(const RowSlab &R, int k, float lo, float inv, int *hist, uint32_t *lk,
+                                  int32_t *li, int32_t *out, int base, int lane) {
+  score_hist(R, lo, inv, hist, lane);
+  // lane l owns bins kScoreBins-1 - kBinsPerLane*l - j: a prefix over lanes counts from the top
+  int c[kBinsPerLane], tot = 0;
+#pragma unroll
+  for (int j = 0; j < kBinsPerLane; ++j) {
+    c[j] = hist[kScoreBins - 1 - kBinsPerLane * lane - j];
+    tot += c[j];
+  }
+  int incl = tot;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int v = __shfl_up_sync(0xFFFFFFFFu, incl, off);
+    if (lane >= off) incl += v;
+  }
+  const int excl = incl - tot;
+  const uint32_t bm = __ballot_sync(0xFFFFFFFFu, excl < k && k <= incl);
+  const int src = bm ? __ffs(bm) - 1 : 31;
+  int B = 0, above = 0, nB = 0;
+  if (lane == src) {
+    int run = excl;
+#pragma unroll
+    for (int j = 0; j < kBinsPerLane; ++j) {
+      if (run + c[j] >= k) {
+        B = kScoreBins - 1 - kBinsPerLane * lane - j;
+        above = run;
+        nB = c[j];
+        break;
+      }
+      run += c[j];
+    }
+  }
+  B = __shfl_sync(0xFFFFFFFFu, B, src);
+  above = __shfl_sync(0xFFFFFFFFu, above, src);
+  nB = __shfl_sync(0xFFFFFFFFu, nB, src);
+  if (nB > kSelList || nB <= 0) return -1;
+  // order-key range [kb_lo, kb_hi) of bin B (kb_hi past every key when B is the top bin)
+  const uint32_t lo_key = f2key(lo);
+  const uint64_t kb_lo = first_key_of_bin(B, lo_key, lo, inv);
+  const uint64_t kb_hi = B == kScoreBins - 1 ? (uint64_t)kKeyPosInf + 1 : first_key_of_bin(B + 1, lo_key, lo, inv);
+  // pass 2: keys above B go out; B's members go to the list
+  int outc = 0, lc = 0;
+#pragma unroll 1
+  for (int q = 0; q < kQuads; ++q) {
+    const uint32_t *keys = R.keys + (size_t)q * R.seg;
+    const int32_t *idx = R.idx + (size_t)q * R.seg;
+    const int n = R.c[q];
+#pragma unroll 1
+    for (int i0 = 0; i0 < n; i0 += 32 * 4 * kPass2Groups) {
+      uint32_t kk[4 * kPass2Groups];
+      int32_t ii[4 * kPass2Groups];
+#pragma unroll
+      for (int gi = 0; gi < kPass2Groups; ++gi) {
+        const int i = i0 + 32 * 4 * gi + 4 * lane;
+        if (i + 3 < n) {
+          const uint4 kv = __ldcg(reinterpret_cast<const uint4 *>(keys + i));
+          const int4 iv = __ldcg(reinterpret_cast<const int4 *>(idx + i));
+          kk[4 * gi] = kv.x; kk[4 * gi + 1] = kv.y; kk[4 * gi + 2] = kv.z; kk[4 * gi + 3] = kv.w;
+          ii[4 * gi] = iv.x; ii[4 * gi + 1] = iv.y; ii[4 * gi + 2] = iv.z; ii[4 * gi + 3] = iv.w;
+        } else {
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            kk[4 * gi + j] = i + j < n ? __ldcg(keys + i + j) : 0u;
+            ii[4 * gi + j] = i + j < n ? __ldcg(idx + i + j) : 0;
+          }
+        }
+      }
+      // per-lane counts of (above B) and (in B), packed as up + (in << 16)
+      uint32_t up = 0, in = 0;
+#pragma unroll
+      for (int j = 0; j < 4 * kPass2Groups; ++j) {
+        const bool v = i0 + 32 * 4 * (j >> 2) + 4 * lane + (j & 3) < n;
+        if (v && kk[j] >= kb_hi) up |= 1u << j;
+        if (v && kk[j] >= kb_lo && kk[j] < kb_hi) in |= 1u << j;
+      }
+      const int packed = __popc(up) + (__popc(in) << 16);
+      int pincl = packed;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const int v = __shfl_up_sync(0xFFFFFFFFu, pincl, off);
+        if (lane >= off) pincl += v;
+      }
+      const int pexcl = pincl - packed;
+      int po = outc + (pexcl & 0xFFFF), pl = lc + (pexcl >> 16);
+#pragma unroll
+      for (int j = 0; j < 4 * kPass2Groups; ++j) {
+        if ((up >> j) & 1u) {
+          if (po < k) out[po] = ii[j] - base;
+          ++po;
+        }
+        if ((in >> j) & 1u) {
+          if (pl < kSelList) {
+            lk[pl] = kk[j];
+            li[pl] = ii[j];
+          }
+          ++pl;
+        }
+      }
+      const int ptot = __shfl_sync(0xFFFFFFFFu, pincl, 31);
+      outc += ptot & 0xFFFF;
+      lc += ptot >> 16;
+    }
+  }
+  __syncwarp();
+  lc = min(lc, kSelList);
+  // exact threshold among the list: the want-th largest key
+  const int want = k - above;
+  uint32_t kl = 0xFFFFFFFFu, kh = 0u;
+  for (int i = lane; i < lc; i += 32) {
+    kl = min(kl, lk[i]);
+    kh = max(kh, lk[i]);
+  }
+  kl = __reduce_min_sync(0xFFFFFFFFu, kl);
+  kh = __reduce_max_sync(0xFFFFFFFFu, kh);
+  const uint32_t diff = kl ^ kh;
+  int hb = diff ? 32 - __clz(diff) : 0;
+  uint32_t prefix = hb >= 32 ? 0u : (kh & ~((1u << hb) - 1u));
+  int w = want;
+#pragma unroll 1
+  while (hb > 0) {
+    const int bits = hb >= 8 ? 8 : hb;
+    const int shift = hb - bits;
+    const uint32_t dmask = (1u << bits) - 1u;
+    const uint32_t hi_mask = hb >= 32 ? 0u : (0xFFFFFFFFu << hb);
+    for (int b = lane; b < 256; b += 32) hist[b] = 0;
+    __syncwarp();
+    for (int i = lane; i < lc; i += 32) {
+      const uint32_t v = lk[i];
+      if ((v & hi_mask) == prefix) atomicAdd(&hist[(v >> shift) & dmask], 1);
+    }
+    __syncwarp();
+    int cc[8], t8 = 0;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      cc[j] = hist[255 - 8 * lane - j];
+      t8 += cc[j];
+    }
+    int in8 = t8;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int v = __shfl_up_sync(0xFFFFFFFFu, in8, off);
+      if (lane >= off) in8 += v;
+    }
+    const int ex8 = in8 - t8;
+    const uint32_t bm8 = __ballot_sync(0xFFFFFFFFu, ex8 < w && w <= in8);
+    const int s8 = bm8 ? __ffs(bm8) - 1 : 31;
+    int bin = 0, ab = 0;
+    if (lane == s8) {
+      int run = ex8;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        if (run + cc[j] >= w) {
+          bin = 255 - 8 * lane - j;
+          ab = run;
+          break;
+        }
+        run += cc[j];
+      }
+    }
+    bin = __shfl_sync(0xFFFFFFFFu, bin, s8);
+    ab = __shfl_sync(0xFFFFFFFFu, ab, s8);
+    w -= ab;
+    prefix |= (uint32_t)bin << shift;
+    hb = shift;
+    __syncwarp();
+  }
+  const uint32_t T = prefix;
+  // emit from the list: keys > T, then the first w keys equal to T
+  int eq_seen = 0;
+  const uint32_t ltm = lanemask_lt();
+  for (int i0 = 0; i0 < lc; i0 += 32) {
+    const int i = i0 + lane;
+    const bool v = i < lc;
+    const uint32_t key = v ? lk[i] : 0u;
+    const bool gt = v && key > T, eq = v && key == T;
+    const uint32_t eqm = __ballot_sync(0xFFFFFFFFu, eq);
+    const bool take = gt || (eq && eq_seen + __popc(eqm & ltm) < w);
+    const uint32_t tm = __ballot_sync(0xFFFFFFFFu, take);
+    const int pos = outc + __popc(tm & ltm);
+    if (take && pos < k) out[pos] = li[i] - base;
+    outc += __popc(tm);
+    eq_seen += __popc(eqm);
+  }
+  return outc < k ? outc : k;
 }
 
 // ------------------------------------------------------------------ heaviest-first order
@@ -902,6 +1174,8 @@ __device__ void epilogue(Smem &S, uint32_t tmem, const FusedParams &p, int warp,
         S.ref[ew] = 0;
         S.ref_frozen[ew] = 0;
         S.msample[ew] = 0;
+        S.smax[ew] = 0;
+        S.binv[ew] = 0.f;
       }
       if (gate_warp)
         for (int b = lane; b < kGateBins; b += 32) S.hist[ew][b] = 0;
@@ -1070,6 +1344,10 @@ __device__ void epilogue(Smem &S, uint32_t tmem, const FusedParams &p, int warp,
 #pragma unroll
         for (int rr = 0; rr < kRowsPerWarp; ++rr) {
           const int r = rbase + rr;
+          if (act[rr]) {
+            const uint32_t m = __reduce_max_sync(0xFFFFFFFFu, sv[rr] > NEG_INF ? f2key(sv[rr]) : 0u);
+            if (lane == 0 && m) atomicMax(&S.smax[r], m);
+          }
           if (act[rr] && S.g_on[r] && sv[rr] > NEG_INF) {
             const uint32_t kv = f2key(sv[rr]), klo = S.g_klo[r], khi = S.g_khi[r];
             if (kv >= klo && kv <= khi) {
@@ -1118,7 +1396,12 @@ __device__ void epilogue(Smem &S, uint32_t tmem, const FusedParams &p, int warp,
               t = (uint64_t)khi >= drop ? key2f(khi - (uint32_t)drop) : NEG_INF;
             }
           }
-          if (lane == 0) S.tau[r] = t;
+          if (lane == 0) {
+            S.tau[r] = t;
+            // linear score bins from the gate to the largest sample score
+            const float smax = S.smax[r] ? key2f(S.smax[r]) : NEG_INF;
+            S.binv[r] = (t > NEG_INF && smax > t) ? __fdiv_rn((float)kScoreBins, __fsub_rn(smax, t)) : 0.f;
+          }
           }
           if (bar_or(kEpiBarrier, kEpiThreads, aborted(S))) { bail = true; break; }
 #pragma unroll
@@ -1216,6 +1499,9 @@ __device__ void epilogue(Smem &S, uint32_t tmem, const FusedParams &p, int warp,
           Q.start[lane] = J.start[lane];
           Q.n[lane] = J.end[lane] - J.start[lane];
           Q.gated[lane] = S.tau[lane] > NEG_INF;
+          Q.blo[lane] = S.tau[lane];
+          Q.binv[lane] = S.binv[lane];
+          Q.binned[lane] = J.mode == 0 && S.tau[lane] > NEG_INF;
         }
         Q.segcnt[lane >> 2][lane & 3] = S.segcnt[lane >> 2][lane & 3];
         if (lane == 0) {
@@ -1235,7 +1521,12 @@ __device__ void epilogue(Smem &S, uint32_t tmem, const FusedParams &p, int warp,
 }
 
 // ------------------------------------------------------------------ selection (warps 2-3)
-__device__ void selection(Smem &S, const FusedParams &p, int warp, int lane) {
+#ifdef MQA_SELECTION_NOINLINE
+__device__ __noinline__
+#else
+__device__
+#endif
+void selection(Smem &S, const FusedParams &p, int warp, int lane) {
   const int sw = warp - kSelWarp0;
   int *hist = &S.selhist[sw][0];
   const int cap = p.cap, seg = p.cap / kQuads;
@@ -1287,9 +1578,16 @@ __device__ void selection(Smem &S, const FusedParams &p, int warp, int lane) {
       if (cnt <= topk) {
         wrote = warp_emit_out(R, 0u, 0, true, out, Q.start[r], topk, lane);
       } else {
-        int take_eq = 0;
-        const uint32_t T = warp_select_range(R, topk, hist, lane, &take_eq);
-        wrote = warp_emit_out(R, T, take_eq, false, out, Q.start[r], topk, lane);
+        wrote = -1;
+        if (Q.binned[r])
+          wrote = warp_select_binned(R, topk, Q.blo[r], Q.binv[r], hist, S.sel_lk[sw], S.sel_li[sw], out,
+                                     Q.start[r], lane);
+        if (wrote < 0) {
+          if (Q.binned[r] && lane == 0) atomicAdd(p.ws + kWsSelFallback, 1);
+          int take_eq = 0;
+          const uint32_t T = warp_select_range(R, topk, hist, lane, &take_eq);
+          wrote = warp_emit_out(R, T, take_eq, false, out, Q.start[r], topk, lane);
+        }
       }
       for (int i = wrote + lane; i < topk; i += 32) out[i] = -1;
     }
@@ -1327,7 +1625,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   Smem &S = get_smem(smem_raw);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-
+  if (threadIdx.x == 0 && !kLogits)
+    atomicMax(reinterpret_cast<unsigned long long *>(p.ws + kWsTStartMinInv), ~globaltimer_ns());
   if (threadIdx.x == 0) {
     for (int i = 0; i < kKStages; ++i) {
       mbar_init(&S.k_full[i], 1);
@@ -1382,6 +1681,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (!kLogits) selection(S, p, warp, lane);
   }
   __syncthreads();
+  if (threadIdx.x == 0 && !kLogits) {
+    const uint64_t t = globaltimer_ns();
+    atomicMax(reinterpret_cast<unsigned long long *>(p.ws + kWsTEndMinInv), ~t);
+    atomicMax(reinterpret_cast<unsigned long long *>(p.ws + kWsTEndMax), t);
+  }
   if (warp == 1) {
     __syncwarp();
     tc_fence_after();

@@ -49,6 +49,12 @@ enum WsWord : int {
   kWsSampleTiles = 7,    // sample tiles scored
   kWsOverflowRows = 8,   // rows whose candidates exceeded the slab
   kWsUnderfillRows = 9,  // rows whose gated count fell below top-k
+  kWsSelFallback = 10,   // gated rows selected by the slab-pass radix path
+  // 64-bit globaltimer stamps (word pairs, 8-byte aligned); minima are kept
+  // as UINT64_MAX - t so that every stamp is an atomicMax on a zeroed word
+  kWsTStartMinInv = 12,  // first CTA start
+  kWsTEndMinInv = 14,    // first CTA end
+  kWsTEndMax = 16,       // last CTA end
   kWsWords = 64
 };
 constexpr size_t kWsHeaderBytes = 256;

@@ -364,6 +364,14 @@ int mqa_topk_get_status(const void *workspace, int32_t *status, int32_t *stats, 
     stats[MQA_STAT_SAMPLE_TILES] = h[kWsSampleTiles];
     stats[MQA_STAT_OVERFLOW_ROWS] = h[kWsOverflowRows];
     stats[MQA_STAT_UNDERFILL_ROWS] = h[kWsUnderfillRows];
+    stats[MQA_STAT_SELECT_FALLBACK] = h[kWsSelFallback];
+    uint64_t t_start_inv, t_end_inv, t_end;
+    memcpy(&t_start_inv, h + kWsTStartMinInv, 8);
+    memcpy(&t_end_inv, h + kWsTEndMinInv, 8);
+    memcpy(&t_end, h + kWsTEndMax, 8);
+    const uint64_t t_start = ~t_start_inv, t_end_min = ~t_end_inv;
+    stats[MQA_STAT_KERNEL_US] = (t_end && t_end >= t_start) ? (int32_t)((t_end - t_start) / 1000) : 0;
+    stats[MQA_STAT_END_SPREAD_US] = (t_end && t_end >= t_end_min) ? (int32_t)((t_end - t_end_min) / 1000) : 0;
   }
   return MQA_OK;
 }

@@ -113,6 +113,37 @@ def test_fused_small_slab_compaction_ties(mqa):
     assert_parity(p, got)
 
 
+def test_fused_gated_logbin_selection(mqa):
+    """Rows longer than a reduced slab are gated; their top-k comes from the
+    two-pass log-bin selection (threshold bin gathered in shared memory)."""
+    p = synth.random_small(25, 48, 30000, 512, empty_frac=0.0)
+    got, status, stats = run_fused(mqa, p, debug={"slab_capacity": 4096})
+    assert status == 0, stats
+    assert stats["gated_rows"] > 0
+    assert stats["select_fallback"] == 0, stats
+    assert_parity(p, got)
+
+
+def test_fused_gated_tie_groups_take_fallback(mqa):
+    """Every key is a copy of one of 16 source keys (2048 copies each), so a
+    gated row's k-th score sits inside a tie group larger than the selection
+    warp's shared-memory list: the slab-pass radix select must take over and
+    still return an exact top-k under the tie rule."""
+    rows, keys, topk = 16, 32768, 2048
+    p = synth.random_small(26, rows, keys, topk, empty_frac=0.0)
+    src = np.repeat(np.arange(16), keys // 16)
+    np.random.default_rng(5).shuffle(src)
+    p.k = p.k[src].copy()
+    p.scales_ue8m0 = p.scales_ue8m0[src].copy()
+    p.starts = np.zeros(rows, np.int32)
+    p.ends = (keys - np.arange(rows)).astype(np.int32)
+    got, status, stats = run_fused(mqa, p)
+    assert status == 0, stats
+    assert stats["gated_rows"] == rows
+    assert stats["select_fallback"] > 0, stats
+    assert_parity(p, got)
+
+
 def test_fused_single_cta(mqa):
     """All blocks through one persistent CTA (job slots and slabs reused many times)."""
     p = synth.random_small(23, 64, 9000, 512)
