@@ -74,7 +74,9 @@ extern "C" {
                                       took the slab-pass radix select */
 #define MQA_STAT_KERNEL_US 10     /* first CTA start to last CTA end, microseconds */
 #define MQA_STAT_END_SPREAD_US 11 /* first to last CTA end, microseconds (tail) */
-#define MQA_STATS_COUNT 12
+#define MQA_STAT_SPLIT_BLOCKS 12  /* blocks whose key range several CTAs scanned
+                                     (key chunks merged by the last to finish) */
+#define MQA_STATS_COUNT 13
 
 /* Test-only knobs for mqa_topk_prefill_debug.  Zero-initialise for defaults. */
 typedef struct mqa_topk_debug_options {
@@ -93,10 +95,18 @@ typedef struct mqa_topk_debug_options {
 
 /* Bytes of workspace one mqa_topk_prefill call over `rows` rows needs on
  * `device` (a CUDA device ordinal).  The size depends on the device's SM count
- * and on min(rows, ...), not on keys: one persistent CTA per SM, two slabs of
- * 8 rows x 16384 candidate records (8 B each) per CTA, plus a 256-byte header
- * (workspace layout: pull request #60618, sections "Memory" and the workspace
- * list of `get_fused_mqa_topk_workspaces` on the API page).
+ * and on min(rows, ...), not on keys (workspace layout: pull request #60618,
+ * sections "Memory" and the workspace list of `get_fused_mqa_topk_workspaces`
+ * on the API page):
+ *  - a 256-byte header (claim counter, status, counters);
+ *  - one persistent CTA per SM (at most 8 per 8-row block), two slabs of
+ *    8 rows x 16384 candidate records (8 B each) per CTA;
+ *  - the key-range split arrays: for up to min(blocks, 2 x CTAs) blocks whose
+ *    key range several CTAs scan as chunks, a slab of 8 rows x (16384 + 512)
+ *    records (more per block at 4 or 8 chunks, for fewer blocks), the
+ *    per-chunk segment counts and a finished-chunk counter per block.
+ * A workspace below this size but at least the header plus the per-CTA slabs
+ * of min(blocks, SMs) CTAs still works: the call then splits no block. 
  * Returns MQA_ERR_NO_DEVICE / MQA_ERR_CUDA when the device cannot be queried. */
 int mqa_topk_workspace_bytes(int device, int rows, size_t *bytes);
 

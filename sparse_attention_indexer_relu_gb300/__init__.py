@@ -29,7 +29,7 @@ MQA_OK = 0
 STATUS_BITS = {1: "range_clamped", 2: "wait_timeout", 4: "internal"}
 STAT_NAMES = ("status", "rows_rescanned", "compactions", "candidates", "gated_rows", "blocks_done",
               "sample_tiles", "overflow_rows", "underfill_rows", "select_fallback",
-              "kernel_us", "end_spread_us")
+              "kernel_us", "end_spread_us", "split_blocks")
 
 EXPORTS = ("mqa_topk_workspace_bytes", "mqa_topk_prefill", "mqa_topk_prefill_debug", "mqa_topk_prefill_noalloc",
            "mqa_ue8m0_decode", "mqa_logits_debug", "mqa_topk_dense_baseline", "mqa_topk_get_status",

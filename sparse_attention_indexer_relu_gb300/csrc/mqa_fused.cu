@@ -48,7 +48,10 @@ struct JobInfo {
   int ns;         // sample tiles; scored twice (coarse, then fine gate pass) before the main tiles
   uint32_t mask;  // rows taking part
   int nrows;      // valid rows in the block
-  int pad;
+  int chunk;      // key chunk of a split block (-1: the whole block)
+  int nchunks;    // chunks the block is split into (1: not split)
+  int bs;         // split block index (its arrays in the split workspace)
+  int s_lo_t, s_nt;  // tiles [s_lo_t, s_lo_t + s_nt) the sample plan spans (the whole block)
   int start[kBlockRows], end[kBlockRows];
   alignas(16) float w[kBlockRows][kHeads];
 };
@@ -61,7 +64,9 @@ struct SelSlot {  // what the selection warps need from a finished scan
   int gated[kBlockRows];
   float blo[kBlockRows], binv[kBlockRows];  // score-bin origin (the gate) and bins per unit score
   int binned[kBlockRows];                    // mode-0 gated row: selected through score bins
-  int segcnt[kBlockRows][kQuads];  // records appended per (row, quadrant segment)
+  int split;    // candidates are in the split slab of block bs, nseg segments of seglen per row
+  int bs, nseg, seglen;
+  int segcnt[kBlockRows][kQuads * kMaxChunks];  // records appended per (row, segment)
 };
 
 struct Smem {
@@ -72,6 +77,7 @@ struct Smem {
   SelSlot sel[2];
   float tau[kBlockRows];
   int segcnt[kBlockRows][kQuads];
+  int nsplit, nchunks;  // key-range split plan: the last nsplit blocks of the order, nchunks chunks each
   uint32_t ref[kBlockRows];
   int ref_frozen[kBlockRows];
   int msample[kBlockRows];
@@ -285,14 +291,19 @@ __device__ __forceinline__ uint64_t dist_bin_hi(int b) {
 #else
 #define MQA_SEL_FN
 #endif
-// A row's candidates live in kQuads segments (one per TMEM lane quadrant) of
-// `seg` records each; segment q holds c[q] valid records.
+// A row's candidates live in nseg segments of `seg` records each (one per
+// TMEM lane quadrant, times the key chunks of a split block); segment q holds
+// c[q] valid records (c points to shared memory).
 struct RowSlab {
-  uint32_t *keys;  // [kQuads][seg]
-  int32_t *idx;    // [kQuads][seg]
-  int seg;
-  int c[kQuads];
-  __device__ int total() const { return c[0] + c[1] + c[2] + c[3]; }
+  uint32_t *keys;  // [nseg][seg]
+  int32_t *idx;    // [nseg][seg]
+  int seg, nseg;
+  const int *c;
+  __device__ int total() const {
+    int t = 0;
+    for (int q = 0; q < nseg; ++q) t += c[q];
+    return t;
+  }
 };
 
 // Exact k-th largest order key over the row's candidates (requires total > k
@@ -308,7 +319,7 @@ __device__ MQA_SEL_FN uint32_t warp_radix_select(const RowSlab &R, int k, int *h
     for (int b = lane; b < 256; b += 32) hist[b] = 0;
     __syncwarp();
 #pragma unroll 1
-    for (int q = 0; q < kQuads; ++q) {
+    for (int q = 0; q < R.nseg; ++q) {
       const uint32_t *keys = R.keys + (size_t)q * R.seg;
       const int n = R.c[q];
 #pragma unroll 1
@@ -376,7 +387,7 @@ __device__ MQA_SEL_FN int warp_emit(const RowSlab &R, uint32_t T, int take_eq, b
   int outc = 0, eq_seen = 0;
   const uint32_t lt = lanemask_lt();
 #pragma unroll 1
-  for (int q = 0; q < kQuads; ++q) {
+  for (int q = 0; q < R.nseg; ++q) {
     const uint32_t *keys = R.keys + (size_t)q * R.seg;
     const int32_t *idx = R.idx + (size_t)q * R.seg;
     const int n = R.c[q];
@@ -430,7 +441,7 @@ constexpr int kSelDepth = MQA_SEL_DEPTH;
 __device__ void warp_key_range(const RowSlab &R, int lane, uint32_t *kmin, uint32_t *kmax) {
   uint32_t lo = 0xFFFFFFFFu, hi = 0u;
 #pragma unroll 1
-  for (int q = 0; q < kQuads; ++q) {
+  for (int q = 0; q < R.nseg; ++q) {
     const uint32_t *keys = R.keys + (size_t)q * R.seg;
     const int n = R.c[q], n4 = n & ~3;
 #pragma unroll 1
@@ -480,7 +491,7 @@ __device__ MQA_SEL_FN uint32_t warp_select_range(const RowSlab &R, int k, int *h
     for (int b = lane; b < 256; b += 32) hist[b] = 0;
     __syncwarp();
 #pragma unroll 1
-    for (int q = 0; q < kQuads; ++q) {
+    for (int q = 0; q < R.nseg; ++q) {
       const uint32_t *keys = R.keys + (size_t)q * R.seg;
       const int n = R.c[q], n4 = n & ~3;
 #pragma unroll 1
@@ -554,7 +565,7 @@ __device__ MQA_SEL_FN int warp_emit_out(const RowSlab &R, uint32_t T, int take_e
                              int limit, int lane) {
   int outc = 0, eq_seen = 0;
 #pragma unroll 1
-  for (int q = 0; q < kQuads; ++q) {
+  for (int q = 0; q < R.nseg; ++q) {
     const uint32_t *keys = R.keys + (size_t)q * R.seg;
     const int32_t *idx = R.idx + (size_t)q * R.seg;
     const int n = R.c[q];
@@ -661,7 +672,7 @@ __device__ void score_hist(const RowSlab &R, float lo, float inv, int *hist, int
   for (int b = lane; b < kScoreBins; b += 32) hist[b] = 0;
   __syncwarp();
 #pragma unroll 1
-  for (int q = 0; q < kQuads; ++q) {
+  for (int q = 0; q < R.nseg; ++q) {
     const uint32_t *keys = R.keys + (size_t)q * R.seg;
     const int n = R.c[q], n4 = n & ~3;
 #pragma unroll 1
@@ -739,7 +750,7 @@ __device__ MQA_SEL_FN int warp_select_binned(const RowSlab &R, int k, float lo, 
   // pass 2: keys above B go out; B's members go to the list
   int outc = 0, lc = 0;
 #pragma unroll 1
-  for (int q = 0; q < kQuads; ++q) {
+  for (int q = 0; q < R.nseg; ++q) {
     const uint32_t *keys = R.keys + (size_t)q * R.seg;
     const int32_t *idx = R.idx + (size_t)q * R.seg;
     const int n = R.c[q];
@@ -883,6 +894,43 @@ __device__ MQA_SEL_FN int warp_select_binned(const RowSlab &R, int k, float lo, 
 }
 
 // ------------------------------------------------------------------ heaviest-first order
+// Key-range split plan (every CTA computes the same one).  The last blocks of
+// the claim order are cut into `nchunks` key chunks when that shortens the
+// final rounds: with few blocks all of them (idle SMs take the chunks), else
+// the blocks of the last partial wave plus one full wave before it.  Costs
+// are counted in units of the lightest block's scan; each chunk also scores
+// the block's whole sample again (fraction sfrac of a block).
+__device__ void plan_split(Smem &S, const FusedParams &p, long long w_light) {
+  const int nb = p.nblocks, ctas = gridDim.x;
+  const int cand = nb < ctas ? nb : (nb % ctas ? min(nb, nb % ctas + ctas) : 0);
+  if (cand == 0 || cand > p.split_max) return;
+  const long long L = w_light / kBlockRows;  // mean visible keys per row of the lightest block
+  const long long nt = (L + kTileKeys - 1) / kTileKeys;
+  if (nt < 8) return;  // too short to be worth a second sample pass
+  float sfrac = 0.f;
+  if (L > p.cap) {
+    long long want = (32LL * L + (long long)p.gate_target * kTileKeys - 1) / ((long long)p.gate_target * kTileKeys);
+    want = want < 4 ? 4 : (want > 64 ? 64 : want);
+    sfrac = 2.f * (float)(want < nt ? want : nt) / (float)nt;
+  }
+  const float base = (float)((cand + ctas - 1) / ctas);
+  float best = 0.97f * base;
+  int best_c = 1;
+  for (int c = 2; c <= kMaxChunks; c *= 2) {
+    if ((long long)cand * 2 * kBlockRows * split_row_capacity(p.cap, c) > p.split_words) break;
+    if (nt / c < 4) break;
+    const float cost = (float)(((long long)cand * c + ctas - 1) / ctas) * (1.f / c + sfrac);
+    if (cost < best) {
+      best = cost;
+      best_c = c;
+    }
+  }
+  if (best_c > 1) {
+    S.nsplit = cand;
+    S.nchunks = best_c;
+  }
+}
+
 __device__ void build_order(Smem &S, const FusedParams &p) {
   const int nb = p.nblocks;
   if (nb > kMaxSortBlocks) return;  // fall back to descending block index
@@ -919,12 +967,13 @@ __device__ void build_order(Smem &S, const FusedParams &p) {
     }
   }
   for (int b = threadIdx.x; b < nb; b += blockDim.x) S.order[b] = (uint16_t)(0xFFFFFFFFu - (uint32_t)key[b]);
+  if (threadIdx.x == 0 && p.split_max > 0) plan_split(S, p, (long long)(key[nb - 1] >> 32));
   __syncthreads();
 }
 
 __device__ __forceinline__ int sample_tile(const JobInfo &J, int u) {
   // (2u + 1) * nt < 2^31 for nt <= 2^17 tiles and u < 64
-  return J.lo_t + (int)((unsigned)((2 * u + 1) * J.nt) / (unsigned)(2 * J.ns));
+  return J.s_lo_t + (int)((unsigned)((2 * u + 1) * J.s_nt) / (unsigned)(2 * J.ns));
 }
 
 // ------------------------------------------------------------------ producer (warp 0)
@@ -932,7 +981,10 @@ template <bool kLogits>
 __device__ void producer(Smem &S, const CUtensorMap *q_map, const CUtensorMap *k_map, const CUtensorMap *s_map,
                          const FusedParams &p, int lane) {
   const uint64_t pol_k = policy_evict_last(), pol_q = policy_evict_first();
-  const int total_jobs = kLogits ? p.nblocks * p.key_chunks : p.nblocks;
+  // claim order: whole blocks, then nsplit blocks as nchunks consecutive key chunks each
+  const int nsplit = kLogits ? 0 : S.nsplit, nchunks = kLogits ? 1 : S.nchunks;
+  const int nwhole = p.nblocks - nsplit;
+  const int total_jobs = kLogits ? p.nblocks * p.key_chunks : nwhole + nsplit * nchunks;
   const int ktiles_all = (p.keys + kTileKeys - 1) / kTileKeys;
   int job_iter = 0, kcount = 0;
   bool exhausted = false;
@@ -948,7 +1000,7 @@ __device__ void producer(Smem &S, const CUtensorMap *q_map, const CUtensorMap *k
     if (lane == 0) ok = wait_bar(S, &S.j_empty[slot], ((job_iter >> 1) & 1) ^ 1, p, kBackoffIdle);
     ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
     if (!ok) return;
-    int block = -1, mode = 0, chunk = 0;
+    int block = -1, mode = 0, chunk = 0, kchunk = -1, bs = 0;
     uint32_t mask = 0xFFu;
     if (lane == 0) {
       if (!kLogits) {
@@ -968,7 +1020,13 @@ __device__ void producer(Smem &S, const CUtensorMap *q_map, const CUtensorMap *k
             block = i / p.key_chunks;
             chunk = i % p.key_chunks;
           } else {
-            block = p.nblocks <= kMaxSortBlocks ? (int)S.order[i] : p.nblocks - 1 - i;
+            int oi = i;
+            if (i >= nwhole) {  // a key chunk of a split block
+              bs = (i - nwhole) / nchunks;
+              kchunk = (i - nwhole) % nchunks;
+              oi = nwhole + bs;
+            }
+            block = p.nblocks <= kMaxSortBlocks ? (int)S.order[oi] : p.nblocks - 1 - oi;
           }
         } else {
           exhausted = true;
@@ -993,6 +1051,8 @@ __device__ void producer(Smem &S, const CUtensorMap *q_map, const CUtensorMap *k
     mode = __shfl_sync(0xFFFFFFFFu, mode, 0);
     mask = __shfl_sync(0xFFFFFFFFu, mask, 0);
     chunk = __shfl_sync(0xFFFFFFFFu, chunk, 0);
+    kchunk = __shfl_sync(0xFFFFFFFFu, kchunk, 0);
+    bs = __shfl_sync(0xFFFFFFFFu, bs, 0);
     JobInfo &J = S.job[slot];
     int ntiles = 0;
     if (block >= 0) {
@@ -1047,6 +1107,14 @@ __device__ void producer(Smem &S, const CUtensorMap *q_map, const CUtensorMap *k
           ns = (int)(want < nt ? want : nt);
         }
       }
+      // samples span the whole block; a key chunk scans its share of the tiles
+      const int s_lo_t = lo_t, s_nt = nt;
+      if (kchunk >= 0) {
+        const int tpc = (nt + nchunks - 1) / nchunks;
+        const int a = min(nt, kchunk * tpc), b = min(nt, a + tpc);
+        lo_t += a;
+        nt = b - a;
+      }
       if (lane == 0) {
         J.block = block;
         J.mode = mode;
@@ -1055,6 +1123,11 @@ __device__ void producer(Smem &S, const CUtensorMap *q_map, const CUtensorMap *k
         J.ns = ns;
         J.mask = kLogits ? ((1u << nrows) - 1u) : pm;
         J.nrows = nrows;
+        J.chunk = kchunk;
+        J.nchunks = kchunk >= 0 ? nchunks : 1;
+        J.bs = bs;
+        J.s_lo_t = s_lo_t;
+        J.s_nt = s_nt;
       }
       ntiles = 2 * ns + nt;
     } else if (lane == 0) {
@@ -1204,9 +1277,27 @@ __device__ void epilogue(Smem &S, uint32_t tmem, const FusedParams &p, int warp,
     }
     const int ns = J.ns, ns2 = 2 * J.ns, ntiles = 2 * J.ns + J.nt, mode = J.mode;
     const int block = J.block;
-    uint32_t *slab_keys = p.slab + ((size_t)(blockIdx.x * kSlots + slot) * 2 * kBlockRows) * (size_t)cap;
-    int32_t *slab_idx = reinterpret_cast<int32_t *>(slab_keys + (size_t)kBlockRows * cap);
-    // this warp's segment of row r: slab_*[(r * kQuads + quad) * seg]
+    // this warp's candidate segment of row rbase; row rbase + rr's is rr * row_stride further.
+    // Whole block: the CTA's slab slot, [rows][quadrant segments of seg].  Key
+    // chunk c of a split block: the split slab, [rows][chunks][quadrant segments].
+    uint32_t *seg_keys;
+    int32_t *seg_idx;
+    int row_stride, seglen;
+    if (J.chunk < 0) {
+      uint32_t *base = p.slab + ((size_t)(blockIdx.x * kSlots + slot) * 2 * kBlockRows) * (size_t)cap;
+      row_stride = cap;
+      seglen = seg;
+      seg_keys = base + (size_t)rbase * cap + quad * seg;
+      seg_idx = reinterpret_cast<int32_t *>(base + (size_t)kBlockRows * cap) + (size_t)rbase * cap + quad * seg;
+    } else {
+      const int rcap = (int)split_row_capacity(cap, J.nchunks);
+      uint32_t *base = p.split_slab + (size_t)J.bs * 2 * kBlockRows * rcap;
+      row_stride = rcap;
+      seglen = rcap / (kQuads * J.nchunks);
+      const int off = rbase * rcap + (J.chunk * kQuads + quad) * seglen;
+      seg_keys = base + off;
+      seg_idx = reinterpret_cast<int32_t *>(base + (size_t)kBlockRows * rcap) + off;
+    }
     bool bail = false;
     const int kown = quad * 32 + owned_key(lane);  // key of this thread within a tile
     // One tile: wait for its accumulators and scales, score this lane's key for
@@ -1436,10 +1527,10 @@ __device__ void epilogue(Smem &S, uint32_t tmem, const FusedParams &p, int warp,
         const uint32_t bal = __ballot_sync(0xFFFFFFFFu, pass);
         if (bal) {
           const int pos = cnt[rr] + __popc(bal & lt);
-          if (pass && pos < seg) {
-            const size_t o = (size_t)((rbase + rr) * kQuads + quad) * seg + pos;
-            slab_keys[o] = f2key(sv[rr]);
-            slab_idx[o] = key;
+          if (pass && pos < seglen) {
+            const int o = rr * row_stride + pos;
+            seg_keys[o] = f2key(sv[rr]);
+            seg_idx[o] = key;
           }
           cnt[rr] += __popc(bal);
         }
@@ -1454,16 +1545,17 @@ __device__ void epilogue(Smem &S, uint32_t tmem, const FusedParams &p, int warp,
         if (bar_or(kEpiBarrier, kEpiThreads, aborted(S))) { bail = true; break; }
         if (gate_warp) {
         const int r = ew;
+        // rescans are whole-block jobs: the CTA's slab slot
+        uint32_t *base = p.slab + ((size_t)(blockIdx.x * kSlots + slot) * 2 * kBlockRows) * (size_t)cap;
         RowSlab R;
-        R.keys = slab_keys + (size_t)r * kQuads * seg;
-        R.idx = slab_idx + (size_t)r * kQuads * seg;
+        R.keys = base + (size_t)r * cap;
+        R.idx = reinterpret_cast<int32_t *>(base + (size_t)kBlockRows * cap) + (size_t)r * cap;
         R.seg = seg;
+        R.nseg = kQuads;
+        R.c = &S.segcnt[r][0];
         int mx = 0;
 #pragma unroll
-        for (int q = 0; q < kQuads; ++q) {
-          R.c[q] = S.segcnt[r][q];
-          mx = max(mx, R.c[q]);
-        }
+        for (int q = 0; q < kQuads; ++q) mx = max(mx, S.segcnt[r][q]);
         if (((J.mask >> r) & 1u) && mx + 32 > seg) {
           int take_eq = 0;
           const uint32_t T = warp_radix_select(R, p.topk, &S.hist[r][0], lane, &take_eq);
@@ -1490,11 +1582,35 @@ __device__ void epilogue(Smem &S, uint32_t tmem, const FusedParams &p, int warp,
 #pragma unroll
       for (int rr = 0; rr < kRowsPerWarp; ++rr) S.segcnt[rbase + rr][quad] = cnt[rr];
     }
-    __threadfence_block();  // slab writes of every epilogue warp precede the hand-over
+    // slab writes of every epilogue warp precede the hand-over (device scope:
+    // another CTA may select a split block's candidates)
+    __threadfence();
     if (bar_or(kEpiBarrier, kEpiThreads, bail || aborted(S))) break;
     if (!kLogits) {
       if (ew == 0) {
         SelSlot &Q = S.sel[slot];
+        // A key chunk publishes its segment counts; the CTA that finishes the
+        // block's last chunk selects the block over every chunk's segments,
+        // the others hand the selection warps an empty job.
+        bool merge = true;
+        const int nseg = kQuads * J.nchunks;
+        if (J.chunk >= 0) {
+          int32_t *cnt_g = p.split_cnt + (size_t)J.bs * kBlockRows * 32;
+          cnt_g[(lane >> 2) * 32 + J.chunk * kQuads + (lane & 3)] = S.segcnt[lane >> 2][lane & 3];
+          __threadfence();
+          __syncwarp();
+          int old = 0;
+          if (lane == 0) old = atomicAdd(p.split_done + J.bs, 1);
+          old = __shfl_sync(0xFFFFFFFFu, old, 0);
+          merge = old == J.nchunks - 1;
+          if (merge) {
+            __threadfence();
+            for (int i = lane; i < kBlockRows * nseg; i += 32)
+              Q.segcnt[i / nseg][i % nseg] = __ldcg(cnt_g + (i / nseg) * 32 + i % nseg);
+          }
+        } else {
+          Q.segcnt[lane >> 2][lane & 3] = S.segcnt[lane >> 2][lane & 3];
+        }
         if (lane < kBlockRows) {
           Q.start[lane] = J.start[lane];
           Q.n[lane] = J.end[lane] - J.start[lane];
@@ -1503,12 +1619,16 @@ __device__ void epilogue(Smem &S, uint32_t tmem, const FusedParams &p, int warp,
           Q.binv[lane] = S.binv[lane];
           Q.binned[lane] = J.mode == 0 && S.tau[lane] > NEG_INF;
         }
-        Q.segcnt[lane >> 2][lane & 3] = S.segcnt[lane >> 2][lane & 3];
         if (lane == 0) {
           Q.block = J.block;
           Q.mode = J.mode;
           Q.mask = J.mask;
-          Q.nrows = J.nrows;
+          Q.nrows = merge ? J.nrows : 0;
+          Q.split = J.chunk >= 0;
+          Q.bs = J.bs;
+          Q.nseg = nseg;
+          Q.seglen = J.chunk >= 0 ? (int)(split_row_capacity(cap, J.nchunks) / nseg) : seg;
+          if (merge && J.chunk >= 0) atomicAdd(p.ws + kWsSplitBlocks, 1);
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&S.s_full[slot]);
@@ -1529,7 +1649,7 @@ __device__
 void selection(Smem &S, const FusedParams &p, int warp, int lane) {
   const int sw = warp - kSelWarp0;
   int *hist = &S.selhist[sw][0];
-  const int cap = p.cap, seg = p.cap / kQuads;
+  const int cap = p.cap;
   int job_iter = 0;
   for (;;) {
     const int slot = job_iter & 1;
@@ -1539,23 +1659,24 @@ void selection(Smem &S, const FusedParams &p, int warp, int lane) {
     if (!ok) break;
     const SelSlot &Q = S.sel[slot];
     if (Q.block < 0) break;
-    uint32_t *slab_keys = p.slab + ((size_t)(blockIdx.x * kSlots + slot) * 2 * kBlockRows) * (size_t)cap;
-    int32_t *slab_idx = reinterpret_cast<int32_t *>(slab_keys + (size_t)kBlockRows * cap);
+    // candidates: the CTA's slab slot, or the split slab of a merged split block
+    const int rcap = Q.split ? Q.nseg * Q.seglen : cap;
+    uint32_t *slab_keys = Q.split ? p.split_slab + (size_t)Q.bs * 2 * kBlockRows * rcap
+                                  : p.slab + ((size_t)(blockIdx.x * kSlots + slot) * 2 * kBlockRows) * (size_t)cap;
+    int32_t *slab_idx = reinterpret_cast<int32_t *>(slab_keys + (size_t)kBlockRows * rcap);
     uint32_t fail = 0;
     for (int r = sw; r < Q.nrows; r += kSelWarps) {
       if (!((Q.mask >> r) & 1u)) continue;
       const int n = Q.n[r];
       const int topk = p.topk;
       RowSlab R;
-      R.keys = slab_keys + (size_t)r * kQuads * seg;
-      R.idx = slab_idx + (size_t)r * kQuads * seg;
-      R.seg = seg;
+      R.keys = slab_keys + (size_t)r * rcap;
+      R.idx = slab_idx + (size_t)r * rcap;
+      R.seg = Q.seglen;
+      R.nseg = Q.nseg;
+      R.c = &Q.segcnt[r][0];
       bool over = false;
-#pragma unroll
-      for (int q = 0; q < kQuads; ++q) {
-        R.c[q] = Q.segcnt[r][q];
-        over = over || R.c[q] > seg;
-      }
+      for (int q = 0; q < R.nseg; ++q) over = over || R.c[q] > R.seg;
       const int cnt = R.total();
       if (Q.mode == 0) {
         const bool under = Q.gated[r] && cnt < min(topk, n);
@@ -1608,7 +1729,7 @@ void selection(Smem &S, const FusedParams &p, int warp, int lane) {
         S.selfail[slot] = 0;
         S.seldone[slot] = 0;
         __threadfence_block();
-        atomicAdd(p.ws + kWsBlocksDone, 1);
+        if (Q.nrows > 0) atomicAdd(p.ws + kWsBlocksDone, 1);
         atomicAdd(&S.retired, 1);
       }
       mbar_arrive(&S.s_empty[slot]);
@@ -1652,6 +1773,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     S.fifo_head = 0;
     S.fifo_tail = 0;
     S.retired = 0;
+    S.nsplit = 0;
+    S.nchunks = 1;
     fence_mbar_init();
   }
   if (warp == 0 && lane == 0) {

@@ -50,6 +50,7 @@ enum WsWord : int {
   kWsOverflowRows = 8,   // rows whose candidates exceeded the slab
   kWsUnderfillRows = 9,  // rows whose gated count fell below top-k
   kWsSelFallback = 10,   // gated rows selected by the slab-pass radix path
+  kWsSplitBlocks = 11,   // blocks whose key range was split across CTAs
   // 64-bit globaltimer stamps (word pairs, 8-byte aligned); minima are kept
   // as UINT64_MAX - t so that every stamp is an atomicMax on a zeroed word
   kWsTStartMinInv = 12,  // first CTA start
@@ -73,6 +74,12 @@ struct FusedParams {
   float *logits;         // [rows, keys]   (logits mode, row-chunk local)
   int32_t *ws;           // workspace header (int32 words)
   uint32_t *slab;        // slabs: [ctas][slots][rows 8][cap] keys, then same for indices
+  // Key-range split of the last blocks in claim order (disabled when split_max == 0):
+  uint32_t *split_slab;  // per split block: [rows 8][row capacity] keys, then same for indices
+  int32_t *split_cnt;    // per split block: [rows 8][32] records per (chunk, quadrant) segment
+  int32_t *split_done;   // per split block: chunks finished (zeroed with the header)
+  int split_max;         // split blocks the arrays above hold
+  long long split_words; // uint32 words of split_slab
   int rows;              // rows of this call
   int row0;              // first global row (logits mode: chunk offset)
   int keys;
@@ -96,6 +103,22 @@ cudaError_t launch_dense_topk_rows(const float *logits, int rows, int keys, cons
                                    const int32_t *ends, int32_t *out, int topk, int32_t *ws_status,
                                    cudaStream_t stream);
 size_t fused_smem_bytes();
+
+// Fused-op workspace layout: header, split-done counters, per-CTA slabs, split
+// slab, split counts (split_max == 0: header and slabs only).
+struct FusedLayout {
+  size_t done_off, slab_off, split_off, cnt_off, reset_bytes, total;
+  long long split_words;
+};
+constexpr int kMaxChunks = 8;  // key chunks a split block is cut into (a power of two)
+// Records per row a split block needs at `chunks` chunks: 4 * chunks
+// segments of max(cap / (4 chunks) + 64, cap / 8) records, so that one chunk
+// can hold a row's whole gated candidate set (at most cap / 2).
+__host__ __device__ inline long long split_row_capacity(int cap, int chunks) {
+  const long long a = cap / (4 * chunks) + 64, b = cap / 8;
+  return 4LL * chunks * (a > b ? a : b);
+}
+FusedLayout fused_layout(int ctas, int cap, int split_max);
 
 // Allocation-free variant: a static device scratch sized for this many CTAs.
 constexpr int kStaticScratchCtas = 8;

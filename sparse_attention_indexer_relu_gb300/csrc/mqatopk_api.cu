@@ -127,6 +127,42 @@ int fused_ctas(const DeviceInfo &d, int rows) {
   return nb < d.sms ? nb : d.sms;
 }
 
+// With the key-range split, few-block calls also use idle SMs (one CTA per
+// key chunk), and up to two waves' worth of blocks can be split.
+int fused_ctas_split(const DeviceInfo &d, int rows) {
+  const long long nb = (rows + kBlockRows - 1) / kBlockRows;
+  return nb * kMaxChunks < d.sms ? (int)(nb * kMaxChunks) : d.sms;
+}
+int split_max_blocks(int ctas, int rows) {
+  const int nb = (rows + kBlockRows - 1) / kBlockRows;
+  return nb < 2 * ctas ? nb : 2 * ctas;
+}
+
+}  // namespace
+
+FusedLayout mqa::fused_layout(int ctas, int cap, int split_max) {
+  FusedLayout L;
+  L.done_off = kWsHeaderBytes;
+  L.slab_off = L.done_off + (((size_t)split_max * sizeof(int32_t) + 255) / 256) * 256;
+  L.split_off = L.slab_off + slab_bytes(ctas, cap);
+  long long rc = 0;
+  if (split_max > 0) {
+    // the largest split set the device plan may choose (see plan_split)
+    const long long c2 = (long long)(split_max < 2 * ctas ? split_max : 2 * ctas) * split_row_capacity(cap, 2);
+    const long long c4 = (long long)(split_max < ctas / 4 ? split_max : ctas / 4) * split_row_capacity(cap, 4);
+    const long long c8 = (long long)(split_max < ctas / 8 ? split_max : ctas / 8) * split_row_capacity(cap, 8);
+    rc = c2 > c4 ? c2 : c4;
+    rc = rc > c8 ? rc : c8;
+  }
+  L.split_words = 2LL * kBlockRows * rc;
+  L.cnt_off = L.split_off + (size_t)L.split_words * sizeof(uint32_t);
+  L.total = L.cnt_off + (size_t)split_max * kBlockRows * 32 * sizeof(int32_t);
+  L.reset_bytes = L.slab_off;
+  return L;
+}
+
+namespace {
+
 cudaStream_t as_stream(void *s) { return reinterpret_cast<cudaStream_t>(s); }
 
 int run_fused(const void *q, const void *k, const float *scales, const float *weights, const int32_t *starts,
@@ -150,9 +186,19 @@ int run_fused(const void *q, const void *k, const float *scales, const float *we
   DeviceInfo d;
   rc = current_device_info(&d);
   if (rc != MQA_OK) return rc;
-  int ctas = fused_ctas(d, rows);
+  // key-range split when the workspace holds its arrays (mqa_topk_workspace_bytes
+  // sizes for it), else one CTA per block as far as SMs go
+  int ctas = fused_ctas_split(d, rows);
   if (opt && opt->max_ctas && opt->max_ctas < ctas) ctas = opt->max_ctas;
-  if (workspace_bytes < kWsHeaderBytes + slab_bytes(ctas, cap)) return MQA_ERR_WORKSPACE_TOO_SMALL;
+  int split_max = split_max_blocks(ctas, rows);
+  FusedLayout L = fused_layout(ctas, cap, split_max);
+  if (workspace_bytes < L.total) {
+    ctas = fused_ctas(d, rows);
+    if (opt && opt->max_ctas && opt->max_ctas < ctas) ctas = opt->max_ctas;
+    split_max = 0;
+    L = fused_layout(ctas, cap, 0);
+    if (workspace_bytes < L.total) return MQA_ERR_WORKSPACE_TOO_SMALL;
+  }
   rc = get_encoder();
   if (rc != MQA_OK) return rc;
   CUtensorMap qm, km, sm;
@@ -167,7 +213,15 @@ int run_fused(const void *q, const void *k, const float *scales, const float *we
   p.ends = ends;
   p.out = out;
   p.ws = reinterpret_cast<int32_t *>(workspace);
-  p.slab = reinterpret_cast<uint32_t *>(reinterpret_cast<uint8_t *>(workspace) + kWsHeaderBytes);
+  uint8_t *wsb = reinterpret_cast<uint8_t *>(workspace);
+  p.slab = reinterpret_cast<uint32_t *>(wsb + L.slab_off);
+  p.split_max = split_max;
+  if (split_max > 0) {
+    p.split_done = reinterpret_cast<int32_t *>(wsb + L.done_off);
+    p.split_slab = reinterpret_cast<uint32_t *>(wsb + L.split_off);
+    p.split_cnt = reinterpret_cast<int32_t *>(wsb + L.cnt_off);
+    p.split_words = L.split_words;
+  }
   p.rows = rows;
   p.keys = keys;
   p.topk = topk;
@@ -178,7 +232,7 @@ int run_fused(const void *q, const void *k, const float *scales, const float *we
   p.stall = opt ? opt->stall : 0;
   p.timeout_ns = (long long)((opt && opt->wait_timeout_ms) ? opt->wait_timeout_ms : 4000) * 1000000LL;
   cudaStream_t st = as_stream(stream);
-  if (cudaMemsetAsync(workspace, 0, kWsHeaderBytes, st) != cudaSuccess) {
+  if (cudaMemsetAsync(workspace, 0, L.reset_bytes, st) != cudaSuccess) {
     cudaGetLastError();
     return MQA_ERR_CUDA;
   }
@@ -232,7 +286,12 @@ int mqa_topk_workspace_bytes(int device, int rows, size_t *bytes) {
   DeviceInfo d;
   int rc = device_info(device, &d);
   if (rc != MQA_OK) return rc;
-  *bytes = kWsHeaderBytes + slab_bytes(fused_ctas(d, rows), kDefaultSlabCap);
+  if (rows == 0) {
+    *bytes = kWsHeaderBytes;
+    return MQA_OK;
+  }
+  const int ctas = fused_ctas_split(d, rows);
+  *bytes = fused_layout(ctas, kDefaultSlabCap, split_max_blocks(ctas, rows)).total;
   return MQA_OK;
 }
 
@@ -265,7 +324,7 @@ int mqa_topk_prefill_noalloc(const void *q, const void *k, const float *key_scal
   // whose need exceeded the static array would be rejected here.
   int ctas = fused_ctas(d, rows);
   if (ctas > kStaticScratchCtas) ctas = kStaticScratchCtas;
-  const size_t need = kWsHeaderBytes + slab_bytes(ctas, kDefaultSlabCap);
+  const size_t need = fused_layout(ctas, kDefaultSlabCap, 0).total;
   if (need > kStaticScratchBytes) return MQA_ERR_WORKSPACE_TOO_SMALL;
   void *scratch = nullptr;
   if (static_scratch_address(&scratch) != cudaSuccess) {
@@ -365,6 +424,7 @@ int mqa_topk_get_status(const void *workspace, int32_t *status, int32_t *stats, 
     stats[MQA_STAT_OVERFLOW_ROWS] = h[kWsOverflowRows];
     stats[MQA_STAT_UNDERFILL_ROWS] = h[kWsUnderfillRows];
     stats[MQA_STAT_SELECT_FALLBACK] = h[kWsSelFallback];
+    stats[MQA_STAT_SPLIT_BLOCKS] = h[kWsSplitBlocks];
     uint64_t t_start_inv, t_end_inv, t_end;
     memcpy(&t_start_inv, h + kWsTStartMinInv, 8);
     memcpy(&t_end_inv, h + kWsTEndMinInv, 8);

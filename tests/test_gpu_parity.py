@@ -144,6 +144,45 @@ def test_fused_gated_tie_groups_take_fallback(mqa):
     assert_parity(p, got)
 
 
+def _causal(p, keys):
+    p.starts = np.zeros(p.rows, np.int32)
+    p.ends = (keys - p.rows + 1 + np.arange(p.rows)).astype(np.int32)
+    return p
+
+
+def test_fused_key_split_few_blocks(mqa):
+    """Three row blocks on a GPU with many more SMs: each block's key range is
+    cut into chunks scanned by different CTAs, which share one sampled gate;
+    the CTA that finishes a block's last chunk selects over every chunk's
+    candidates.  The result must be the exact top-k."""
+    p = _causal(synth.random_small(27, 24, 60000, 2048, empty_frac=0.0), 60000)
+    got, status, stats = run_fused(mqa, p)
+    assert status == 0, stats
+    assert stats["split_blocks"] == 3, stats
+    assert stats["gated_rows"] == 24 and stats["rows_rescanned"] == 0, stats
+    assert_parity(p, got)
+
+
+def test_fused_key_split_ungated_rows(mqa):
+    """Split blocks whose rows are shorter than the slab: every chunk emits all
+    its keys, the merge selects exactly."""
+    p = _causal(synth.random_small(28, 16, 12000, 1024, empty_frac=0.0), 12000)
+    got, status, stats = run_fused(mqa, p)
+    assert status == 0, stats
+    assert stats["split_blocks"] == 2 and stats["gated_rows"] == 0, stats
+    assert_parity(p, got)
+
+
+def test_fused_key_split_overflow_rescans(mqa):
+    """No gate and a reduced slab: every chunk's segments overflow, the
+    merging CTA queues the block for an exact whole-block rescan."""
+    p = _causal(synth.random_small(29, 16, 40000, 512, empty_frac=0.0), 40000)
+    got, status, stats = run_fused(mqa, p, debug={"force_gate": 2, "slab_capacity": 2560})
+    assert status == 0, stats
+    assert stats["split_blocks"] == 2 and stats["rows_rescanned"] > 0, stats
+    assert_parity(p, got)
+
+
 def test_fused_single_cta(mqa):
     """All blocks through one persistent CTA (job slots and slabs reused many times)."""
     p = synth.random_small(23, 64, 9000, 512)
