@@ -306,6 +306,43 @@ struct RowSlab {
   }
 };
 
+// A row's candidates are visited in pieces of 128 records (32 lanes x 4),
+// numbered across segment boundaries, so that one batch of loads covers
+// several short segments (the key chunks of a split block) as readily as one
+// long segment.  Lane q (< nseg) holds segment q's record count and the
+// running piece counts; piece t lies in the segment whose inclusive piece
+// prefix first exceeds t, found by one ballot.
+struct PieceMap {
+  int cnt;    // lane q: records in segment q
+  int pexcl;  // lane q: pieces before segment q
+  int pincl;  // lane q: pieces up to and including segment q (INT_MAX past nseg)
+  int total;  // pieces in the row
+};
+__device__ __forceinline__ PieceMap piece_map(const RowSlab &R, int lane) {
+  PieceMap m;
+  m.cnt = lane < R.nseg ? R.c[lane] : 0;
+  const int np = (m.cnt + 127) >> 7;
+  int incl = np;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int v = __shfl_up_sync(0xFFFFFFFFu, incl, off);
+    if (lane >= off) incl += v;
+  }
+  m.pexcl = incl - np;
+  m.total = __shfl_sync(0xFFFFFFFFu, incl, 31);
+  m.pincl = lane < R.nseg ? incl : INT_MAX;
+  return m;
+}
+// Piece t: element offset of its first record in the row's slab and the
+// number of valid records in it (0 past the last piece).  Warp-uniform.
+__device__ __forceinline__ void piece_at(const RowSlab &R, const PieceMap &m, int t, int &at, int &lim) {
+  const int q = min(__popc(__ballot_sync(0xFFFFFFFFu, m.pincl <= t)), 31);
+  const int pe = __shfl_sync(0xFFFFFFFFu, m.pexcl, q), c = __shfl_sync(0xFFFFFFFFu, m.cnt, q);
+  const int off = (t - pe) << 7;
+  at = q * R.seg + off;
+  lim = t < m.total ? min(c - off, 128) : 0;
+}
+
 // Exact k-th largest order key over the row's candidates (requires total > k
 // >= 1), by four 8-bit digit levels.  Returns the key T; *take_eq receives
 // how many keys equal to T belong to the top k (the rest of the top k is > T).
@@ -440,30 +477,27 @@ constexpr int kSelDepth = MQA_SEL_DEPTH;
 // Smallest and largest order key of the row's candidates (one load-only pass).
 __device__ void warp_key_range(const RowSlab &R, int lane, uint32_t *kmin, uint32_t *kmax) {
   uint32_t lo = 0xFFFFFFFFu, hi = 0u;
+  const PieceMap pm = piece_map(R, lane);
 #pragma unroll 1
-  for (int q = 0; q < R.nseg; ++q) {
-    const uint32_t *keys = R.keys + (size_t)q * R.seg;
-    const int n = R.c[q], n4 = n & ~3;
-#pragma unroll 1
-    for (int i0 = 4 * lane; i0 < n4; i0 += 32 * 4 * kSelDepth) {
-      uint4 kk[kSelDepth];
+  for (int t0 = 0; t0 < pm.total; t0 += kSelDepth) {
+    int at[kSelDepth], lim[kSelDepth];
+    uint4 kk[kSelDepth];
 #pragma unroll
-      for (int j = 0; j < kSelDepth; ++j) {
-        const int i = i0 + 32 * 4 * j;
-        kk[j] = i < n4 ? __ldcg(reinterpret_cast<const uint4 *>(keys + i)) : make_uint4(0, 0, 0, 0);
-      }
+    for (int j = 0; j < kSelDepth; ++j) piece_at(R, pm, t0 + j, at[j], lim[j]);
 #pragma unroll
-      for (int j = 0; j < kSelDepth; ++j) {
-        if (i0 + 32 * 4 * j < n4) {
-          lo = min(min(lo, min(kk[j].x, kk[j].y)), min(kk[j].z, kk[j].w));
-          hi = max(max(hi, max(kk[j].x, kk[j].y)), max(kk[j].z, kk[j].w));
+    for (int j = 0; j < kSelDepth; ++j)
+      kk[j] = 4 * lane < lim[j] ? __ldcg(reinterpret_cast<const uint4 *>(R.keys + at[j] + 4 * lane))
+                                : make_uint4(0, 0, 0, 0);
+#pragma unroll
+    for (int j = 0; j < kSelDepth; ++j) {
+      const uint32_t v[4] = {kk[j].x, kk[j].y, kk[j].z, kk[j].w};
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+        if (4 * lane + t < lim[j]) {
+          lo = min(lo, v[t]);
+          hi = max(hi, v[t]);
         }
       }
-    }
-    if (n4 + lane < n) {
-      const uint32_t v = __ldcg(keys + n4 + lane);
-      lo = min(lo, v);
-      hi = max(hi, v);
     }
   }
   *kmin = __reduce_min_sync(0xFFFFFFFFu, lo);
@@ -490,31 +524,23 @@ __device__ MQA_SEL_FN uint32_t warp_select_range(const RowSlab &R, int k, int *h
     const uint32_t hi_mask = hi >= 32 ? 0u : (0xFFFFFFFFu << hi);
     for (int b = lane; b < 256; b += 32) hist[b] = 0;
     __syncwarp();
+    const PieceMap pm = piece_map(R, lane);
 #pragma unroll 1
-    for (int q = 0; q < R.nseg; ++q) {
-      const uint32_t *keys = R.keys + (size_t)q * R.seg;
-      const int n = R.c[q], n4 = n & ~3;
-#pragma unroll 1
-      for (int i0 = 4 * lane; i0 < n4; i0 += 32 * 4 * kSelDepth) {
-        uint4 kk[kSelDepth];
+    for (int t0 = 0; t0 < pm.total; t0 += kSelDepth) {
+      int at[kSelDepth], lim[kSelDepth];
+      uint4 kk[kSelDepth];
 #pragma unroll
-        for (int j = 0; j < kSelDepth; ++j) {
-          const int i = i0 + 32 * 4 * j;
-          kk[j] = i < n4 ? __ldcg(reinterpret_cast<const uint4 *>(keys + i)) : make_uint4(0, 0, 0, 0);
-        }
+      for (int j = 0; j < kSelDepth; ++j) piece_at(R, pm, t0 + j, at[j], lim[j]);
 #pragma unroll
-        for (int j = 0; j < kSelDepth; ++j) {
-          if (i0 + 32 * 4 * j < n4) {
-            const uint32_t v[4] = {kk[j].x, kk[j].y, kk[j].z, kk[j].w};
+      for (int j = 0; j < kSelDepth; ++j)
+        kk[j] = 4 * lane < lim[j] ? __ldcg(reinterpret_cast<const uint4 *>(R.keys + at[j] + 4 * lane))
+                                  : make_uint4(0, 0, 0, 0);
 #pragma unroll
-            for (int t = 0; t < 4; ++t)
-              if ((v[t] & hi_mask) == prefix) atomicAdd(&hist[(v[t] >> shift) & dmask], 1);
-          }
-        }
-      }
-      if (n4 + lane < n) {
-        const uint32_t v = __ldcg(keys + n4 + lane);
-        if ((v & hi_mask) == prefix) atomicAdd(&hist[(v >> shift) & dmask], 1);
+      for (int j = 0; j < kSelDepth; ++j) {
+        const uint32_t v[4] = {kk[j].x, kk[j].y, kk[j].z, kk[j].w};
+#pragma unroll
+        for (int t = 0; t < 4; ++t)
+          if (4 * lane + t < lim[j] && (v[t] & hi_mask) == prefix) atomicAdd(&hist[(v[t] >> shift) & dmask], 1);
       }
     }
     __syncwarp();
@@ -564,36 +590,31 @@ __device__ MQA_SEL_FN uint32_t warp_select_range(const RowSlab &R, int k, int *h
 __device__ MQA_SEL_FN int warp_emit_out(const RowSlab &R, uint32_t T, int take_eq, bool take_all, int32_t *out, int base,
                              int limit, int lane) {
   int outc = 0, eq_seen = 0;
+  const PieceMap pm = piece_map(R, lane);
 #pragma unroll 1
-  for (int q = 0; q < R.nseg; ++q) {
-    const uint32_t *keys = R.keys + (size_t)q * R.seg;
-    const int32_t *idx = R.idx + (size_t)q * R.seg;
-    const int n = R.c[q];
-#pragma unroll 1
-    for (int i0 = 0; i0 < n; i0 += 32 * 8) {
+  for (int t0 = 0; t0 < pm.total; t0 += 2) {
+    {
+      int at[2], lim[2];
       uint32_t kk[8];
       int32_t ii[8];
 #pragma unroll
-      for (int g = 0; g < 2; ++g) {
-        const int i = i0 + 32 * 4 * g + 4 * lane;
-        if (i + 3 < n) {
-          const uint4 kv = __ldcg(reinterpret_cast<const uint4 *>(keys + i));
-          const int4 iv = __ldcg(reinterpret_cast<const int4 *>(idx + i));
-          kk[4 * g] = kv.x; kk[4 * g + 1] = kv.y; kk[4 * g + 2] = kv.z; kk[4 * g + 3] = kv.w;
-          ii[4 * g] = iv.x; ii[4 * g + 1] = iv.y; ii[4 * g + 2] = iv.z; ii[4 * g + 3] = iv.w;
-        } else {
+      for (int g = 0; g < 2; ++g) piece_at(R, pm, t0 + g, at[g], lim[g]);
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            kk[4 * g + j] = i + j < n ? __ldcg(keys + i + j) : 0u;
-            ii[4 * g + j] = i + j < n ? __ldcg(idx + i + j) : 0;
-          }
+      for (int g = 0; g < 2; ++g) {
+        uint4 kv = make_uint4(0, 0, 0, 0);
+        int4 iv = make_int4(0, 0, 0, 0);
+        if (4 * lane < lim[g]) {
+          kv = __ldcg(reinterpret_cast<const uint4 *>(R.keys + at[g] + 4 * lane));
+          iv = __ldcg(reinterpret_cast<const int4 *>(R.idx + at[g] + 4 * lane));
         }
+        kk[4 * g] = kv.x; kk[4 * g + 1] = kv.y; kk[4 * g + 2] = kv.z; kk[4 * g + 3] = kv.w;
+        ii[4 * g] = iv.x; ii[4 * g + 1] = iv.y; ii[4 * g + 2] = iv.z; ii[4 * g + 3] = iv.w;
       }
       bool gt[8], eq[8];
       int neq = 0;
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
-        const bool v = i0 + 32 * 4 * (j >> 2) + 4 * lane + (j & 3) < n;
+        const bool v = 4 * lane + (j & 3) < lim[j >> 2];
         gt[j] = v && (take_all || kk[j] > T);
         eq[j] = v && !take_all && kk[j] == T;
         neq += eq[j];
@@ -667,33 +688,29 @@ __device__ uint64_t first_key_of_bin(int b, uint32_t lo_key, float lo, float inv
 #ifndef MQA_HIST_DEPTH
 #define MQA_HIST_DEPTH 8
 #endif
-constexpr int kHistDepth = MQA_HIST_DEPTH;  // 16-byte key loads in flight per lane
+constexpr int kHistDepth = MQA_HIST_DEPTH;  // pieces (16-byte loads per lane) in flight
 __device__ void score_hist(const RowSlab &R, float lo, float inv, int *hist, int lane) {
   for (int b = lane; b < kScoreBins; b += 32) hist[b] = 0;
   __syncwarp();
+  const PieceMap pm = piece_map(R, lane);
 #pragma unroll 1
-  for (int q = 0; q < R.nseg; ++q) {
-    const uint32_t *keys = R.keys + (size_t)q * R.seg;
-    const int n = R.c[q], n4 = n & ~3;
-#pragma unroll 1
-    for (int i0 = 4 * lane; i0 < n4; i0 += 32 * 4 * kHistDepth) {
-      uint4 kk[kHistDepth];
+  for (int t0 = 0; t0 < pm.total; t0 += kHistDepth) {
+    int at[kHistDepth], lim[kHistDepth];
+    uint4 kk[kHistDepth];
 #pragma unroll
-      for (int j = 0; j < kHistDepth; ++j) {
-        const int i = i0 + 32 * 4 * j;
-        kk[j] = i < n4 ? __ldcg(reinterpret_cast<const uint4 *>(keys + i)) : make_uint4(0, 0, 0, 0);
-      }
+    for (int j = 0; j < kHistDepth; ++j) piece_at(R, pm, t0 + j, at[j], lim[j]);
 #pragma unroll
-      for (int j = 0; j < kHistDepth; ++j) {
-        if (i0 + 32 * 4 * j < n4) {
-          atomicAdd(&hist[score_bin(key2f(kk[j].x), lo, inv)], 1);
-          atomicAdd(&hist[score_bin(key2f(kk[j].y), lo, inv)], 1);
-          atomicAdd(&hist[score_bin(key2f(kk[j].z), lo, inv)], 1);
-          atomicAdd(&hist[score_bin(key2f(kk[j].w), lo, inv)], 1);
-        }
-      }
+    for (int j = 0; j < kHistDepth; ++j)
+      kk[j] = 4 * lane < lim[j] ? __ldcg(reinterpret_cast<const uint4 *>(R.keys + at[j] + 4 * lane))
+                                : make_uint4(0, 0, 0, 0);
+#pragma unroll
+    for (int j = 0; j < kHistDepth; ++j) {
+      const int e = 4 * lane;
+      if (e < lim[j]) atomicAdd(&hist[score_bin(key2f(kk[j].x), lo, inv)], 1);
+      if (e + 1 < lim[j]) atomicAdd(&hist[score_bin(key2f(kk[j].y), lo, inv)], 1);
+      if (e + 2 < lim[j]) atomicAdd(&hist[score_bin(key2f(kk[j].z), lo, inv)], 1);
+      if (e + 3 < lim[j]) atomicAdd(&hist[score_bin(key2f(kk[j].w), lo, inv)], 1);
     }
-    if (n4 + lane < n) atomicAdd(&hist[score_bin(key2f(__ldcg(keys + n4 + lane)), lo, inv)], 1);
   }
   __syncwarp();
 }
@@ -749,66 +766,59 @@ __device__ MQA_SEL_FN int warp_select_binned(const RowSlab &R, int k, float lo, 
   const uint64_t kb_hi = B == kScoreBins - 1 ? (uint64_t)kKeyPosInf + 1 : first_key_of_bin(B + 1, lo_key, lo, inv);
   // pass 2: keys above B go out; B's members go to the list
   int outc = 0, lc = 0;
+  const PieceMap pm = piece_map(R, lane);
 #pragma unroll 1
-  for (int q = 0; q < R.nseg; ++q) {
-    const uint32_t *keys = R.keys + (size_t)q * R.seg;
-    const int32_t *idx = R.idx + (size_t)q * R.seg;
-    const int n = R.c[q];
-#pragma unroll 1
-    for (int i0 = 0; i0 < n; i0 += 32 * 4 * kPass2Groups) {
-      uint32_t kk[4 * kPass2Groups];
-      int32_t ii[4 * kPass2Groups];
+  for (int t0 = 0; t0 < pm.total; t0 += kPass2Groups) {
+    int at[kPass2Groups], lim[kPass2Groups];
+    uint32_t kk[4 * kPass2Groups];
+    int32_t ii[4 * kPass2Groups];
 #pragma unroll
-      for (int gi = 0; gi < kPass2Groups; ++gi) {
-        const int i = i0 + 32 * 4 * gi + 4 * lane;
-        if (i + 3 < n) {
-          const uint4 kv = __ldcg(reinterpret_cast<const uint4 *>(keys + i));
-          const int4 iv = __ldcg(reinterpret_cast<const int4 *>(idx + i));
-          kk[4 * gi] = kv.x; kk[4 * gi + 1] = kv.y; kk[4 * gi + 2] = kv.z; kk[4 * gi + 3] = kv.w;
-          ii[4 * gi] = iv.x; ii[4 * gi + 1] = iv.y; ii[4 * gi + 2] = iv.z; ii[4 * gi + 3] = iv.w;
-        } else {
+    for (int gi = 0; gi < kPass2Groups; ++gi) piece_at(R, pm, t0 + gi, at[gi], lim[gi]);
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            kk[4 * gi + j] = i + j < n ? __ldcg(keys + i + j) : 0u;
-            ii[4 * gi + j] = i + j < n ? __ldcg(idx + i + j) : 0;
-          }
-        }
+    for (int gi = 0; gi < kPass2Groups; ++gi) {
+      uint4 kv = make_uint4(0, 0, 0, 0);
+      int4 iv = make_int4(0, 0, 0, 0);
+      if (4 * lane < lim[gi]) {
+        kv = __ldcg(reinterpret_cast<const uint4 *>(R.keys + at[gi] + 4 * lane));
+        iv = __ldcg(reinterpret_cast<const int4 *>(R.idx + at[gi] + 4 * lane));
       }
-      // per-lane counts of (above B) and (in B), packed as up + (in << 16)
-      uint32_t up = 0, in = 0;
-#pragma unroll
-      for (int j = 0; j < 4 * kPass2Groups; ++j) {
-        const bool v = i0 + 32 * 4 * (j >> 2) + 4 * lane + (j & 3) < n;
-        if (v && kk[j] >= kb_hi) up |= 1u << j;
-        if (v && kk[j] >= kb_lo && kk[j] < kb_hi) in |= 1u << j;
-      }
-      const int packed = __popc(up) + (__popc(in) << 16);
-      int pincl = packed;
-#pragma unroll
-      for (int off = 1; off < 32; off <<= 1) {
-        const int v = __shfl_up_sync(0xFFFFFFFFu, pincl, off);
-        if (lane >= off) pincl += v;
-      }
-      const int pexcl = pincl - packed;
-      int po = outc + (pexcl & 0xFFFF), pl = lc + (pexcl >> 16);
-#pragma unroll
-      for (int j = 0; j < 4 * kPass2Groups; ++j) {
-        if ((up >> j) & 1u) {
-          if (po < k) out[po] = ii[j] - base;
-          ++po;
-        }
-        if ((in >> j) & 1u) {
-          if (pl < kSelList) {
-            lk[pl] = kk[j];
-            li[pl] = ii[j];
-          }
-          ++pl;
-        }
-      }
-      const int ptot = __shfl_sync(0xFFFFFFFFu, pincl, 31);
-      outc += ptot & 0xFFFF;
-      lc += ptot >> 16;
+      kk[4 * gi] = kv.x; kk[4 * gi + 1] = kv.y; kk[4 * gi + 2] = kv.z; kk[4 * gi + 3] = kv.w;
+      ii[4 * gi] = iv.x; ii[4 * gi + 1] = iv.y; ii[4 * gi + 2] = iv.z; ii[4 * gi + 3] = iv.w;
     }
+    // per-lane counts of (above B) and (in B), packed as up + (in << 16)
+    uint32_t up = 0, in = 0;
+#pragma unroll
+    for (int j = 0; j < 4 * kPass2Groups; ++j) {
+      const bool v = 4 * lane + (j & 3) < lim[j >> 2];
+      if (v && kk[j] >= kb_hi) up |= 1u << j;
+      if (v && kk[j] >= kb_lo && kk[j] < kb_hi) in |= 1u << j;
+    }
+    const int packed = __popc(up) + (__popc(in) << 16);
+    int pincl = packed;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int v = __shfl_up_sync(0xFFFFFFFFu, pincl, off);
+      if (lane >= off) pincl += v;
+    }
+    const int pexcl = pincl - packed;
+    int po = outc + (pexcl & 0xFFFF), pl = lc + (pexcl >> 16);
+#pragma unroll
+    for (int j = 0; j < 4 * kPass2Groups; ++j) {
+      if ((up >> j) & 1u) {
+        if (po < k) out[po] = ii[j] - base;
+        ++po;
+      }
+      if ((in >> j) & 1u) {
+        if (pl < kSelList) {
+          lk[pl] = kk[j];
+          li[pl] = ii[j];
+        }
+        ++pl;
+      }
+    }
+    const int ptot = __shfl_sync(0xFFFFFFFFu, pincl, 31);
+    outc += ptot & 0xFFFF;
+    lc += ptot >> 16;
   }
   __syncwarp();
   lc = min(lc, kSelList);
