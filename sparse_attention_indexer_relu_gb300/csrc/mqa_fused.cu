@@ -66,7 +66,7 @@ struct SelSlot {  // what the selection warps need from a finished scan
   int binned[kBlockRows];                    // mode-0 gated row: selected through score bins
   int split;    // candidates are in the split slab of block bs, nseg segments of seglen per row
   int bs, nseg, seglen;
-  int segcnt[kBlockRows][kQuads * kMaxChunks];  // records appended per (row, segment)
+  int segcnt[kBlockRows][32];  // records per (row, segment): 4 quadrant segments, or one run per key chunk
 };
 
 struct Smem {
@@ -1218,6 +1218,45 @@ __device__ void mma_issuer(Smem &S, uint32_t tmem, const FusedParams &p) {
   }
 }
 
+// One row of a finished key chunk: move the records of quadrant segments 1..3
+// down behind segment 0's, so the chunk's candidates form one run.  Returns
+// the run's length, or 4 * seglen + 1 when a quadrant segment overflowed.
+// Out of line: it runs once per chunk and keeps its registers out of the
+// epilogue's tile loop.
+__device__ __noinline__ int pack_chunk_row(uint32_t *keys_r, int32_t *idx_r, const int *segcnt, int seglen,
+                                           int lane) {
+  int dst = segcnt[0];
+  if (dst > seglen) return kQuads * seglen + 1;
+  for (int q = 1; q < kQuads; ++q) {
+    const int n = segcnt[q];
+    if (n > seglen) return kQuads * seglen + 1;
+    // 128 records per round, all read before any is written: the run lies
+    // below the source, so a round's writes never reach records still unread
+    for (int i0 = 0; i0 < n; i0 += 128) {
+      uint32_t kv[4];
+      int32_t iv[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int i = i0 + 32 * j + lane;
+        kv[j] = i < n ? __ldcg(keys_r + q * seglen + i) : 0u;
+        iv[j] = i < n ? __ldcg(idx_r + q * seglen + i) : 0;
+      }
+      __syncwarp();
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int i = i0 + 32 * j + lane;
+        if (i < n) {
+          keys_r[dst + i] = kv[j];
+          idx_r[dst + i] = iv[j];
+        }
+      }
+      __syncwarp();
+    }
+    dst += n;
+  }
+  return dst;
+}
+
 // ------------------------------------------------------------------ epilogue (warps 4-11)
 template <bool kLogits>
 __device__ void epilogue(Smem &S, uint32_t tmem, const FusedParams &p, int warp, int lane) {
@@ -1596,19 +1635,38 @@ __device__ void epilogue(Smem &S, uint32_t tmem, const FusedParams &p, int warp,
     // another CTA may select a split block's candidates)
     __threadfence();
     if (bar_or(kEpiBarrier, kEpiThreads, bail || aborted(S))) break;
+    if (!kLogits && J.chunk >= 0) {
+      // A key chunk publishes its rows' segment counts.  Up to 8 chunks keep
+      // the four quadrant segments (at most 32 per row); past that each row's
+      // quadrant segments are packed into one run per chunk (warp ew packs row
+      // ew), and a row whose quadrant segment overflowed publishes a length
+      // past the run's room.
+      if (J.nchunks <= 8) {
+        if (ew == 0)
+          p.split_cnt[((size_t)J.bs * kBlockRows + (lane >> 2)) * 32 + J.chunk * kQuads + (lane & 3)] =
+              S.segcnt[lane >> 2][lane & 3];
+      } else if (gate_warp) {
+        const int r = ew, rcap = row_stride;
+        uint32_t *keys_r = p.split_slab + (size_t)J.bs * 2 * kBlockRows * rcap + (size_t)r * rcap +
+                           (size_t)J.chunk * kQuads * seglen;
+        const int n = pack_chunk_row(keys_r, reinterpret_cast<int32_t *>(keys_r + (size_t)kBlockRows * rcap),
+                                     &S.segcnt[r][0], seglen, lane);
+        if (lane == 0) p.split_cnt[((size_t)J.bs * kBlockRows + r) * 32 + J.chunk] = n;
+      }
+      __threadfence();
+      if (bar_or(kEpiBarrier, kEpiThreads, aborted(S))) break;
+    }
     if (!kLogits) {
       if (ew == 0) {
         SelSlot &Q = S.sel[slot];
-        // A key chunk publishes its segment counts; the CTA that finishes the
-        // block's last chunk selects the block over every chunk's segments,
-        // the others hand the selection warps an empty job.
+        // The CTA that finishes a split block's last chunk selects the block
+        // over every chunk's run (one segment per chunk); the others hand the
+        // selection warps an empty job.
         bool merge = true;
-        const int nseg = kQuads * J.nchunks;
+        const bool packed = J.chunk >= 0 && J.nchunks > 8;
+        const int nseg = J.chunk < 0 ? kQuads : (packed ? J.nchunks : kQuads * J.nchunks);
         if (J.chunk >= 0) {
           int32_t *cnt_g = p.split_cnt + (size_t)J.bs * kBlockRows * 32;
-          cnt_g[(lane >> 2) * 32 + J.chunk * kQuads + (lane & 3)] = S.segcnt[lane >> 2][lane & 3];
-          __threadfence();
-          __syncwarp();
           int old = 0;
           if (lane == 0) old = atomicAdd(p.split_done + J.bs, 1);
           old = __shfl_sync(0xFFFFFFFFu, old, 0);
@@ -1637,7 +1695,7 @@ __device__ void epilogue(Smem &S, uint32_t tmem, const FusedParams &p, int warp,
           Q.split = J.chunk >= 0;
           Q.bs = J.bs;
           Q.nseg = nseg;
-          Q.seglen = J.chunk >= 0 ? (int)(split_row_capacity(cap, J.nchunks) / nseg) : seg;
+          Q.seglen = J.chunk < 0 ? seg : (packed ? kQuads * seglen : seglen);
           if (merge && J.chunk >= 0) atomicAdd(p.ws + kWsSplitBlocks, 1);
         }
         __syncwarp();

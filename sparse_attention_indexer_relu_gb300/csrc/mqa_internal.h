@@ -110,7 +110,7 @@ struct FusedLayout {
   size_t done_off, slab_off, split_off, cnt_off, reset_bytes, total;
   long long split_words;
 };
-constexpr int kMaxChunks = 8;  // key chunks a split block is cut into (a power of two)
+constexpr int kMaxChunks = 32;  // key chunks a split block is cut into (a power of two)
 // Records per row a split block needs at `chunks` chunks: 4 * chunks
 // segments of max(cap / (4 chunks) + 64, cap / 8) records, so that one chunk
 // can hold a row's whole gated candidate set (at most cap / 2).

@@ -150,9 +150,11 @@ FusedLayout mqa::fused_layout(int ctas, int cap, int split_max) {
     // the largest split set the device plan may choose (see plan_split)
     const long long c2 = (long long)(split_max < 2 * ctas ? split_max : 2 * ctas) * split_row_capacity(cap, 2);
     const long long c4 = (long long)(split_max < ctas / 4 ? split_max : ctas / 4) * split_row_capacity(cap, 4);
-    const long long c8 = (long long)(split_max < ctas / 8 ? split_max : ctas / 8) * split_row_capacity(cap, 8);
     rc = c2 > c4 ? c2 : c4;
-    rc = rc > c8 ? rc : c8;
+    for (int c = 8; c <= kMaxChunks; c *= 2) {
+      const long long cc = (long long)(split_max < ctas / c ? split_max : ctas / c) * split_row_capacity(cap, c);
+      rc = rc > cc ? rc : cc;
+    }
   }
   L.split_words = 2LL * kBlockRows * rc;
   L.cnt_off = L.split_off + (size_t)L.split_words * sizeof(uint32_t);

@@ -186,7 +186,8 @@ def make_multi(name, contexts, row_split, topk, seed=0) -> Problem:
 
 
 # The chunk shapes of the workload table: 16,384-row prefill chunks at top-2048
-# with 32K..1M keys, multi-request chunks, the 512/1024/2048 top-k set.
+# with 32K..1M keys, multi-request chunks, the 512/1024/2048 top-k set; and
+# decode batches of few rows per request.
 CONFIGS = {
     "tiny_64x4096_k512": lambda: make_single("tiny_64x4096_k512", 64, 4096, 512),
     "r2048_32k_k512": lambda: make_single("r2048_32k_k512", 2048, 32768, 512),
@@ -199,6 +200,14 @@ CONFIGS = {
     "r16k_1m_k2048": lambda: make_single("r16k_1m_k2048", 16384, 1 << 20, 2048),
     "r16k_1m_k2048_adversarial": lambda: make_single("r16k_1m_k2048_adversarial", 16384, 1 << 20, 2048,
                                                      dup_frac=0.25, scaled_row_frac=0.01),
+    # Decode batches: each request verifies K + 1 = 8 query rows (speculative
+    # K = 7) against its own context; row t of a request sees its context up to
+    # N - 8 + t + 1 keys (the multi-request layout with 8 rows per request).
+    "decode_b32_s8_64k_k2048": lambda: make_multi("decode_b32_s8_64k_k2048", (65536,) * 32, (8,) * 32, 2048),
+    "decode_b4_s8_256k_k2048": lambda: make_multi("decode_b4_s8_256k_k2048", (262144,) * 4, (8,) * 4, 2048),
+    "decode_b64_s8_mixed_k512": lambda: make_multi(
+        "decode_b64_s8_mixed_k512", tuple((4096, 8192, 16384, 32768, 65536, 131072)[i % 6] for i in range(64)),
+        (8,) * 64, 512),
 }
 
 

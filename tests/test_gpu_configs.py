@@ -40,6 +40,9 @@ CASES = [
     ("multi4_r16k_k1024", 48),
     ("r16k_1m_k2048", 20),
     ("r16k_1m_k2048_adversarial", 20),
+    ("decode_b32_s8_64k_k2048", 48),
+    ("decode_b4_s8_256k_k2048", 32),
+    ("decode_b64_s8_mixed_k512", 64),
 ]
 
 

@@ -174,10 +174,11 @@ def test_fused_key_split_ungated_rows(mqa):
 
 
 def test_fused_key_split_overflow_rescans(mqa):
-    """No gate and a reduced slab: every chunk's segments overflow, the
-    merging CTA queues the block for an exact whole-block rescan."""
+    """No gate and a reduced slab on 4 CTAs (2 blocks of 2 key chunks each):
+    every chunk's segments overflow, the merging CTA queues the block for an
+    exact whole-block rescan."""
     p = _causal(synth.random_small(29, 16, 40000, 512, empty_frac=0.0), 40000)
-    got, status, stats = run_fused(mqa, p, debug={"force_gate": 2, "slab_capacity": 2560})
+    got, status, stats = run_fused(mqa, p, debug={"force_gate": 2, "slab_capacity": 2560, "max_ctas": 4})
     assert status == 0, stats
     assert stats["split_blocks"] == 2 and stats["rows_rescanned"] > 0, stats
     assert_parity(p, got)
