@@ -103,8 +103,10 @@ struct Smem {
   uint32_t fifo_mask[8];
   int fifo_head, fifo_tail;
   int retired;
-  int seldone[2];
+  int seldone[2];    // rows finished over all uses of the selection slot
+  int selnext[2];    // rows claimed over all uses of the selection slot
   uint32_t selfail[2];
+  int prod_parked;   // the producer has issued its last job and waits for every job to retire
 };
 
 size_t fused_smem_bytes() { return sizeof(Smem) + 1024; }
@@ -918,7 +920,7 @@ __device__ void plan_split(Smem &S, const FusedParams &p, long long w_light) {
   const long long nt = (L + kTileKeys - 1) / kTileKeys;
   if (nt < 8) return;  // too short to be worth a second sample pass
   float sfrac = 0.f;
-  if (L > p.cap) {
+  if (L > p.gate_min) {
     long long want = (32LL * L + (long long)p.gate_target * kTileKeys - 1) / ((long long)p.gate_target * kTileKeys);
     want = want < 4 ? 4 : (want > 64 ? 64 : want);
     sfrac = 2.f * (float)(want < nt ? want : nt) / (float)nt;
@@ -1045,6 +1047,11 @@ __device__ void producer(Smem &S, const CUtensorMap *q_map, const CUtensorMap *k
       if (!kLogits && block < 0 && exhausted) {
         // Every issued job must retire (selection done) before the rescan
         // queue can be declared empty.
+        // Parked: no more claims and, until every issued job has retired, no
+        // more TMA writes, so the epilogue warps may use the K ring and q
+        // buffers as scratch to help select the last blocks' rows.
+        *(volatile int *)&S.prod_parked = 1;
+        __threadfence_block();
         if (wait_counter(S, &S.retired, job_iter, p)) {
           __threadfence_block();
           const int head = *(volatile int *)&S.fifo_head;
@@ -1053,6 +1060,8 @@ __device__ void producer(Smem &S, const CUtensorMap *q_map, const CUtensorMap *k
             mask = S.fifo_mask[head & 7];
             mode = 1;
             *(volatile int *)&S.fifo_head = head + 1;
+            *(volatile int *)&S.prod_parked = 0;
+            __threadfence_block();
           }
         }
       }
@@ -1108,7 +1117,7 @@ __device__ void producer(Smem &S, const CUtensorMap *q_map, const CUtensorMap *k
       } else if (hi > lo) {
         lo_t = lo / kTileKeys;
         nt = (hi + kTileKeys - 1) / kTileKeys - lo_t;
-        if (mode == 0 && p.force_gate == 0 && len > p.cap) {
+        if (mode == 0 && p.force_gate == 0 && len > p.gate_min) {
           // sample about 32 gate-passing keys per row: tiles ~ 32 * L / (target * 128)
           const long long L = (long long)(hi - lo);
           long long want = (32LL * L + (long long)p.gate_target * kTileKeys - 1) /
@@ -1256,6 +1265,15 @@ __device__ __noinline__ int pack_chunk_row(uint32_t *keys_r, int32_t *idx_r, con
   }
   return dst;
 }
+
+// Selection work shared by the selection warps and, at the end, the epilogue
+// warps (defined with the selection below).
+__device__ void work_slot_rows(Smem &S, const FusedParams &p, int slot, int use, int *hist, uint32_t *lk,
+                               int32_t *li, int lane);
+// Scratch of one helping epilogue warp: a 256-bin histogram and the list.
+constexpr int kHelperScratchBytes = 1024 + 8 * kSelList;
+static_assert(kEpiWarps * kHelperScratchBytes <= (int)(sizeof(Smem::kring) + sizeof(Smem::q)),
+              "helper scratch exceeds the K ring and q buffers");
 
 // ------------------------------------------------------------------ epilogue (warps 4-11)
 template <bool kLogits>
@@ -1417,7 +1435,7 @@ __device__ void epilogue(Smem &S, uint32_t tmem, const FusedParams &p, int warp,
           const int m = S.msample[r];
           int on = 0, above = 0, jw = 0;
           uint32_t klo = 0, khi = 0;
-          if (((J.mask >> r) & 1u) && n > cap && m > 0) {
+          if (((J.mask >> r) & 1u) && n > p.gate_min && m > 0) {
             jw = (int)max(1LL, ((long long)m * p.gate_target + n - 1) / n);
             constexpr int kPer = kGateBins / 32;
             int c[kPer], tot = 0;
@@ -1701,6 +1719,16 @@ __device__ void epilogue(Smem &S, uint32_t tmem, const FusedParams &p, int warp,
         __syncwarp();
         if (lane == 0) mbar_arrive(&S.s_full[slot]);
       }
+      // Once the producer has parked, the epilogue warps help select the
+      // block just handed over, with scratch in the idle K ring and q buffers.
+      const bool parked =
+          bar_or(kEpiBarrier, kEpiThreads, ew == 0 && lane == 0 && *(volatile int *)&S.prod_parked != 0);
+      if (parked) {
+        uint8_t *scr = &S.kring[0][0] + (size_t)ew * kHelperScratchBytes;
+        work_slot_rows(S, p, slot, job_iter >> 1, reinterpret_cast<int *>(scr),
+                       reinterpret_cast<uint32_t *>(scr + 1024), reinterpret_cast<int32_t *>(scr + 1024 + 4 * kSelList),
+                       lane);
+      }
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&S.j_empty[slot]);
@@ -1708,85 +1736,92 @@ __device__ void epilogue(Smem &S, uint32_t tmem, const FusedParams &p, int warp,
   }
 }
 
-// ------------------------------------------------------------------ selection (warps 2-3)
-#ifdef MQA_SELECTION_NOINLINE
-__device__ __noinline__
-#else
-__device__
-#endif
-void selection(Smem &S, const FusedParams &p, int warp, int lane) {
-  const int sw = warp - kSelWarp0;
-  int *hist = &S.selhist[sw][0];
-  const int cap = p.cap;
-  int job_iter = 0;
-  for (;;) {
-    const int slot = job_iter & 1;
-    bool ok = true;
-    if (lane == 0) ok = wait_bar(S, &S.s_full[slot], (job_iter >> 1) & 1, p, kBackoffIdle);
-    ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
-    if (!ok) break;
-    const SelSlot &Q = S.sel[slot];
-    if (Q.block < 0) break;
-    // candidates: the CTA's slab slot, or the split slab of a merged split block
-    const int rcap = Q.split ? Q.nseg * Q.seglen : cap;
-    uint32_t *slab_keys = Q.split ? p.split_slab + (size_t)Q.bs * 2 * kBlockRows * rcap
-                                  : p.slab + ((size_t)(blockIdx.x * kSlots + slot) * 2 * kBlockRows) * (size_t)cap;
-    int32_t *slab_idx = reinterpret_cast<int32_t *>(slab_keys + (size_t)kBlockRows * rcap);
-    uint32_t fail = 0;
-    for (int r = sw; r < Q.nrows; r += kSelWarps) {
-      if (!((Q.mask >> r) & 1u)) continue;
-      const int n = Q.n[r];
-      const int topk = p.topk;
-      RowSlab R;
-      R.keys = slab_keys + (size_t)r * rcap;
-      R.idx = slab_idx + (size_t)r * rcap;
-      R.seg = Q.seglen;
-      R.nseg = Q.nseg;
-      R.c = &Q.segcnt[r][0];
-      bool over = false;
-      for (int q = 0; q < R.nseg; ++q) over = over || R.c[q] > R.seg;
-      const int cnt = R.total();
-      if (Q.mode == 0) {
-        const bool under = Q.gated[r] && cnt < min(topk, n);
-        if (lane == 0) {
-          if (Q.gated[r]) atomicAdd(p.ws + kWsGatedRows, 1);
-          atomicAdd(p.ws + kWsCandidates, cnt);
-          if (over) atomicAdd(p.ws + kWsOverflowRows, 1);
-          if (under) atomicAdd(p.ws + kWsUnderfillRows, 1);
-        }
-        if (over || under) {
-          fail |= 1u << r;
-          continue;
-        }
-      } else if (lane == 0) {
-        atomicAdd(p.ws + kWsRowsRescanned, 1);
-      }
-      const int row = Q.block * kBlockRows + r;
-      int32_t *out = p.out + (size_t)row * topk;
-      int wrote;
-      if (cnt <= topk) {
-        wrote = warp_emit_out(R, 0u, 0, true, out, Q.start[r], topk, lane);
-      } else {
-        wrote = -1;
-        if (Q.binned[r])
-          wrote = warp_select_binned(R, topk, Q.blo[r], Q.binv[r], hist, S.sel_lk[sw], S.sel_li[sw], out,
-                                     Q.start[r], lane);
-        if (wrote < 0) {
-          if (Q.binned[r] && lane == 0) atomicAdd(p.ws + kWsSelFallback, 1);
-          int take_eq = 0;
-          const uint32_t T = warp_select_range(R, topk, hist, lane, &take_eq);
-          wrote = warp_emit_out(R, T, take_eq, false, out, Q.start[r], topk, lane);
-        }
-      }
-      for (int i = wrote + lane; i < topk; i += 32) out[i] = -1;
+// ------------------------------------------------------------------ per-row selection work
+// Row r of the block in selection slot `slot`: its top-k indices go to out,
+// or (returns true) the row must be rescanned.  hist (256 ints) and the list
+// lk/li (kSelList records) are the calling warp's scratch.
+__device__ bool select_row(Smem &S, const FusedParams &p, int slot, int r, int *hist, uint32_t *lk, int32_t *li,
+                           int lane) {
+  const SelSlot &Q = S.sel[slot];
+  if (r >= Q.nrows || !((Q.mask >> r) & 1u)) return false;
+  const int cap = p.cap, topk = p.topk, n = Q.n[r];
+  // candidates: the CTA's slab slot, or the split slab of a merged split block
+  const int rcap = Q.split ? Q.nseg * Q.seglen : cap;
+  uint32_t *slab_keys = Q.split ? p.split_slab + (size_t)Q.bs * 2 * kBlockRows * rcap
+                                : p.slab + ((size_t)(blockIdx.x * kSlots + slot) * 2 * kBlockRows) * (size_t)cap;
+  int32_t *slab_idx = reinterpret_cast<int32_t *>(slab_keys + (size_t)kBlockRows * rcap);
+  RowSlab R;
+  R.keys = slab_keys + (size_t)r * rcap;
+  R.idx = slab_idx + (size_t)r * rcap;
+  R.seg = Q.seglen;
+  R.nseg = Q.nseg;
+  R.c = &Q.segcnt[r][0];
+  bool over = false;
+  for (int q = 0; q < R.nseg; ++q) over = over || R.c[q] > R.seg;
+  const int cnt = R.total();
+  if (Q.mode == 0) {
+    const bool under = Q.gated[r] && cnt < min(topk, n);
+    if (lane == 0) {
+      if (Q.gated[r]) atomicAdd(p.ws + kWsGatedRows, 1);
+      atomicAdd(p.ws + kWsCandidates, cnt);
+      if (over) atomicAdd(p.ws + kWsOverflowRows, 1);
+      if (under) atomicAdd(p.ws + kWsUnderfillRows, 1);
     }
-    if (fail) atomicOr(&S.selfail[slot], fail);
+    if (over || under) return true;
+  } else if (lane == 0) {
+    atomicAdd(p.ws + kWsRowsRescanned, 1);
+  }
+  int32_t *out = p.out + (size_t)(Q.block * kBlockRows + r) * topk;
+  int wrote;
+  if (cnt <= topk) {
+    wrote = warp_emit_out(R, 0u, 0, true, out, Q.start[r], topk, lane);
+  } else {
+    wrote = -1;
+    if (Q.binned[r]) wrote = warp_select_binned(R, topk, Q.blo[r], Q.binv[r], hist, lk, li, out, Q.start[r], lane);
+    if (wrote < 0) {
+      if (Q.binned[r] && lane == 0) atomicAdd(p.ws + kWsSelFallback, 1);
+      int take_eq = 0;
+      const uint32_t T = warp_select_range(R, topk, hist, lane, &take_eq);
+      wrote = warp_emit_out(R, T, take_eq, false, out, Q.start[r], topk, lane);
+    }
+  }
+  for (int i = wrote + lane; i < topk; i += 32) out[i] = -1;
+  return false;
+}
+
+// Work on the rows of selection slot `slot` in its use-th use until none is
+// left.  Every warp that helps claims rows one at a time through a bounded
+// counter (it never passes this use's last row, so it needs no reset and a
+// late claimer can never take a row of a later use); the warp that finishes
+// the use's last row queues failed rows for a rescan, retires the job and
+// releases the slot.
+__device__ void work_slot_rows(Smem &S, const FusedParams &p, int slot, int use, int *hist, uint32_t *lk,
+                               int32_t *li, int lane) {
+  const int base = use * kBlockRows;
+  for (;;) {
+    int r = -1;
+    if (lane == 0) {
+      int v = *(volatile int *)&S.selnext[slot];
+      while (v < base + kBlockRows) {
+        const int w = atomicCAS(&S.selnext[slot], v, v + 1);
+        if (w == v) {
+          r = v - base;
+          break;
+        }
+        v = w;
+      }
+    }
+    r = __shfl_sync(0xFFFFFFFFu, r, 0);
+    if (r < 0) break;
+    const bool fail = select_row(S, p, slot, r, hist, lk, li, lane);
     __syncwarp();
     if (lane == 0) {
+      if (fail) atomicOr(&S.selfail[slot], 1u << r);
       __threadfence_block();
       const int done = atomicAdd(&S.seldone[slot], 1);
-      if (done == kSelWarps - 1) {
-        const uint32_t fm = *(volatile uint32_t *)&S.selfail[slot];
+      if (done == base + kBlockRows - 1) {
+        const SelSlot &Q = S.sel[slot];
+        const uint32_t fm = atomicExch(&S.selfail[slot], 0u);
         if (fm) {
           const int tail = S.fifo_tail;
           S.fifo_block[tail & 7] = Q.block;
@@ -1794,14 +1829,27 @@ void selection(Smem &S, const FusedParams &p, int warp, int lane) {
           __threadfence_block();
           *(volatile int *)&S.fifo_tail = tail + 1;
         }
-        S.selfail[slot] = 0;
-        S.seldone[slot] = 0;
         __threadfence_block();
         if (Q.nrows > 0) atomicAdd(p.ws + kWsBlocksDone, 1);
         atomicAdd(&S.retired, 1);
+        mbar_arrive(&S.s_empty[slot]);
       }
-      mbar_arrive(&S.s_empty[slot]);
     }
+  }
+}
+
+// ------------------------------------------------------------------ selection (warps 2-3)
+__device__ void selection(Smem &S, const FusedParams &p, int warp, int lane) {
+  const int sw = warp - kSelWarp0;
+  int job_iter = 0;
+  for (;;) {
+    const int slot = job_iter & 1;
+    bool ok = true;
+    if (lane == 0) ok = wait_bar(S, &S.s_full[slot], (job_iter >> 1) & 1, p, kBackoffIdle);
+    ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+    if (!ok) break;
+    if (S.sel[slot].block < 0) break;
+    work_slot_rows(S, p, slot, job_iter >> 1, &S.selhist[sw][0], S.sel_lk[sw], S.sel_li[sw], lane);
     ++job_iter;
   }
 }
@@ -1831,8 +1879,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&S.j_full[i], 32);
       mbar_init(&S.j_empty[i], 1 + kEpiWarps);
       mbar_init(&S.s_full[i], 1);
-      mbar_init(&S.s_empty[i], kSelWarps);
+      mbar_init(&S.s_empty[i], 1);  // released by the warp that finishes the slot's last row
       S.seldone[i] = 0;
+      S.selnext[i] = 0;
       S.selfail[i] = 0;
     }
     mbar_init(&S.drain, 1);
@@ -1843,6 +1892,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     S.retired = 0;
     S.nsplit = 0;
     S.nchunks = 1;
+    S.prod_parked = 0;
     fence_mbar_init();
   }
   if (warp == 0 && lane == 0) {

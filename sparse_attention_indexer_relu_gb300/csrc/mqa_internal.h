@@ -87,6 +87,7 @@ struct FusedParams {
   int nblocks;
   int cap;               // slab capacity per row
   int gate_target;       // expected candidates per gated row
+  int gate_min;          // rows seeing more keys than this are gated (2 x gate_target)
   int force_gate;        // 0 normal, 1 gate +inf, 2 gate -inf
   int stall;             // debug: wait on a barrier nobody arrives on
   int key_chunks;        // logits mode: key chunks per block

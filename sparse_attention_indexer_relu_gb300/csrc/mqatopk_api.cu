@@ -230,6 +230,9 @@ int run_fused(const void *q, const void *k, const float *scales, const float *we
   p.nblocks = (rows + kBlockRows - 1) / kBlockRows;
   p.cap = cap;
   p.gate_target = 3 * topk < cap / 2 ? 3 * topk : cap / 2;
+  // gate every row that would otherwise bring more than twice the target
+  // candidates to the selection (and every row the slab cannot hold)
+  p.gate_min = 2 * p.gate_target;
   p.force_gate = opt ? opt->force_gate : 0;
   p.stall = opt ? opt->stall : 0;
   p.timeout_ns = (long long)((opt && opt->wait_timeout_ms) ? opt->wait_timeout_ms : 4000) * 1000000LL;

@@ -164,9 +164,10 @@ def test_fused_key_split_few_blocks(mqa):
 
 
 def test_fused_key_split_ungated_rows(mqa):
-    """Split blocks whose rows are shorter than the slab: every chunk emits all
-    its keys, the merge selects exactly."""
-    p = _causal(synth.random_small(28, 16, 12000, 1024, empty_frac=0.0), 12000)
+    """Split blocks whose rows see too few keys to be gated (at most twice the
+    gate's target, 6144 at top-2048): every chunk emits all its keys, the merge
+    selects exactly."""
+    p = _causal(synth.random_small(28, 16, 12000, 2048, empty_frac=0.0), 12000)
     got, status, stats = run_fused(mqa, p)
     assert status == 0, stats
     assert stats["split_blocks"] == 2 and stats["gated_rows"] == 0, stats
