@@ -129,6 +129,23 @@ int mqa_topk_prefill(const void *q, const void *k, const float *key_scales, cons
                      const int32_t *starts, const int32_t *ends, int32_t *out, int rows, int keys, int topk,
                      void *workspace, size_t workspace_bytes, void *stream);
 
+/* Workspace bytes for mqa_topk_prefill_ex with `heads` index heads (32 or
+ * 64) per query row.  Same contents as mqa_topk_workspace_bytes; with 64 heads
+ * a block holds 4 rows instead of 8. */
+int mqa_topk_workspace_bytes_ex(int device, int rows, int heads, size_t *bytes);
+
+/* mqa_topk_prefill for 32 or 64 index heads per query row (the pages list
+ * DeepSeek-V3.2's 64 index heads as not yet supported by their kernel: PR
+ * #60618, section "Limitations of this PR -- TODOs").  q is [rows, heads, 128] uint8 e4m3fn, weights
+ * [rows, heads] fp32; everything else as mqa_topk_prefill.  A 256-column
+ * accumulator tile holds 8 rows of 32 heads or 4 rows of 64, so the kernel is
+ * compiled once per head count.  opt (nullable) carries the test-only knobs of
+ * mqa_topk_prefill_debug.  heads other than 32 or 64: MQA_ERR_INVALID_ARGUMENT. */
+int mqa_topk_prefill_ex(const void *q, const void *k, const float *key_scales, const float *weights,
+                        const int32_t *starts, const int32_t *ends, int32_t *out, int rows, int keys, int topk,
+                        int heads, void *workspace, size_t workspace_bytes, void *stream,
+                        const mqa_topk_debug_options *opt);
+
 /* mqa_topk_prefill with test-only knobs (opt may be NULL). */
 int mqa_topk_prefill_debug(const void *q, const void *k, const float *key_scales, const float *weights,
                            const int32_t *starts, const int32_t *ends, int32_t *out, int rows, int keys,

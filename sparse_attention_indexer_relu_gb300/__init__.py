@@ -31,7 +31,8 @@ STAT_NAMES = ("status", "rows_rescanned", "compactions", "candidates", "gated_ro
               "sample_tiles", "overflow_rows", "underfill_rows", "select_fallback",
               "kernel_us", "end_spread_us", "split_blocks")
 
-EXPORTS = ("mqa_topk_workspace_bytes", "mqa_topk_prefill", "mqa_topk_prefill_debug", "mqa_topk_prefill_noalloc",
+EXPORTS = ("mqa_topk_workspace_bytes", "mqa_topk_workspace_bytes_ex", "mqa_topk_prefill", "mqa_topk_prefill_ex",
+           "mqa_topk_prefill_debug", "mqa_topk_prefill_noalloc",
            "mqa_ue8m0_decode", "mqa_logits_debug", "mqa_topk_dense_baseline", "mqa_topk_get_status",
            "mqa_topk_strerror")
 
@@ -61,9 +62,11 @@ def lib():
     L = ctypes.CDLL(LIB_PATH)
     P, I, S = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
     L.mqa_topk_workspace_bytes.argtypes = [I, I, ctypes.POINTER(S)]
+    L.mqa_topk_workspace_bytes_ex.argtypes = [I, I, I, ctypes.POINTER(S)]
     common = [P, P, P, P, P, P, P, I, I]
     L.mqa_topk_prefill.argtypes = common + [I, P, S, P]
     L.mqa_topk_prefill_debug.argtypes = common + [I, P, S, P, ctypes.POINTER(DebugOptions)]
+    L.mqa_topk_prefill_ex.argtypes = common + [I, I, P, S, P, ctypes.POINTER(DebugOptions)]
     L.mqa_topk_prefill_noalloc.argtypes = common + [I, P]
     L.mqa_ue8m0_decode.argtypes = [P, P, I, P]
     L.mqa_logits_debug.argtypes = common + [P, S, P]
@@ -126,32 +129,35 @@ def _as(t, dtype, shape, name):
     return t
 
 
-def _inputs(q, k, key_scales, weights, starts, ends):
+def _inputs(q, k, key_scales, weights, starts, ends, heads=(HEADS,)):
     torch = _torch()
     rows, keys = int(q.shape[0]), int(k.shape[0])
-    q = _as_u8(q, (rows, HEADS, HEAD_DIM), "q")
+    h = int(q.shape[1]) if q.dim() == 3 and int(q.shape[1]) in heads else HEADS
+    q = _as_u8(q, (rows, h, HEAD_DIM), "q")
     k = _as_u8(k, (keys, HEAD_DIM), "k")
     key_scales = _as(key_scales, torch.float32, (keys,), "key_scales")
-    weights = _as(weights, torch.float32, (rows, HEADS), "weights")
+    weights = _as(weights, torch.float32, (rows, h), "weights")
     starts = _as(starts, torch.int32, (rows,), "starts")
     ends = _as(ends, torch.int32, (rows,), "ends")
     return q, k, key_scales, weights, starts, ends, rows, keys
 
 
 # ---------------------------------------------------------------- public API
-def workspace_bytes(rows: int, device: Optional[int] = None) -> int:
+def workspace_bytes(rows: int, device: Optional[int] = None, heads: int = HEADS) -> int:
     torch = _torch()
     dev = torch.cuda.current_device() if device is None else int(device)
     n = ctypes.c_size_t(0)
-    _check(lib().mqa_topk_workspace_bytes(dev, int(rows), ctypes.byref(n)), "mqa_topk_workspace_bytes")
+    _check(lib().mqa_topk_workspace_bytes_ex(dev, int(rows), int(heads), ctypes.byref(n)),
+           "mqa_topk_workspace_bytes_ex")
     return int(n.value)
 
 
-def alloc_workspace(rows: int, device=None):
-    """One fixed-size workspace for calls over up to `rows` rows (caller owns it)."""
+def alloc_workspace(rows: int, device=None, heads: int = HEADS):
+    """One fixed-size workspace for calls over up to `rows` rows of `heads`
+    index heads (caller owns it)."""
     torch = _torch()
     dev = torch.device("cuda", torch.cuda.current_device() if device is None else int(device))
-    return torch.empty(workspace_bytes(rows, dev.index), dtype=torch.uint8, device=dev)
+    return torch.empty(workspace_bytes(rows, dev.index, heads), dtype=torch.uint8, device=dev)
 
 
 def ue8m0_decode(scales, out=None, stream=None):
@@ -168,17 +174,23 @@ def ue8m0_decode(scales, out=None, stream=None):
 def mqa_topk_prefill(q, k, key_scales, weights, starts, ends, topk: int, workspace=None, out=None,
                      stream=None, debug: Optional[dict] = None):
     """Fused top-k prefill selection; returns out [rows, topk] int32 (relative
-    indices, unordered, -1 padded)."""
+    indices, unordered, -1 padded).  q is [rows, 32 or 64, 128] (index heads
+    taken from its shape), weights [rows, heads]."""
     torch = _torch()
-    q, k, key_scales, weights, starts, ends, rows, keys = _inputs(q, k, key_scales, weights, starts, ends)
+    q, k, key_scales, weights, starts, ends, rows, keys = _inputs(q, k, key_scales, weights, starts, ends,
+                                                                  heads=(32, 64))
+    heads = int(q.shape[1])
     if out is None:
         out = torch.empty((rows, int(topk)), dtype=torch.int32, device=q.device)
     out = _as(out, torch.int32, (rows, int(topk)), "out")
     if workspace is None:
-        workspace = alloc_workspace(rows, q.device.index)
+        workspace = alloc_workspace(rows, q.device.index, heads)
     args = [_ptr(q), _ptr(k), _ptr(key_scales), _ptr(weights), _ptr(starts), _ptr(ends), _ptr(out), rows, keys,
             int(topk), _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream)]
-    if debug:
+    if heads != HEADS:
+        opt = DebugOptions(**{f: int((debug or {}).get(f, 0)) for f, _ in DebugOptions._fields_})
+        _check(lib().mqa_topk_prefill_ex(*args[:10], heads, *args[10:], ctypes.byref(opt)), "mqa_topk_prefill_ex")
+    elif debug:
         opt = DebugOptions(**{f: int(debug.get(f, 0)) for f, _ in DebugOptions._fields_})
         _check(lib().mqa_topk_prefill_debug(*args, ctypes.byref(opt)), "mqa_topk_prefill_debug")
     else:

@@ -15,7 +15,10 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 OUT_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(OUT_DIR, "libmqatopk.so")
-SOURCES = ["mqa_fused.cu", "mqa_aux.cu", "mqatopk_api.cu"]
+# (source, object, extra flags): the fused kernel is compiled once per head
+# count (32 and 64 index heads per query row).
+SOURCES = [("mqa_fused.cu", "mqa_fused.o", []), ("mqa_fused.cu", "mqa_fused_h64.o", ["-DMQA_HEADS=64"]),
+           ("mqa_aux.cu", "mqa_aux.o", []), ("mqatopk_api.cu", "mqatopk_api.o", [])]
 HEADERS = ["mqa_internal.h", "ptx.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
@@ -41,12 +44,12 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
     os.makedirs(OUT_DIR, exist_ok=True)
     hdrs = [os.path.join(CSRC, h) for h in HEADERS] + [os.path.join(ROOT, "include", "mqatopk.h")]
     objs, jobs = [], []
-    for src in SOURCES:
+    for src, obj, defs in SOURCES:
         s = os.path.join(CSRC, src)
-        o = os.path.join(OUT_DIR, src.replace(".cu", ".o"))
+        o = os.path.join(OUT_DIR, obj)
         objs.append(o)
         if force or _stale(o, [s, *hdrs]):
-            jobs.append([nvcc(), *_flags(extra_flags), "-c", s, "-o", o])
+            jobs.append([nvcc(), *_flags(extra_flags), *defs, "-c", s, "-o", o])
     if jobs:
         with concurrent.futures.ThreadPoolExecutor(max_workers=len(jobs)) as ex:
             res = list(ex.map(lambda c: subprocess.run(c, capture_output=True, text=True), jobs))

@@ -32,7 +32,14 @@
 #include <climits>
 #include <mutex>
 
+#if MQA_HEADS == 64
+#define MQA_KNS h64
+#else
+#define MQA_KNS h32
+#endif
+
 namespace mqa {
+namespace MQA_KNS {
 
 constexpr uint32_t kIdesc = idesc_f8_e4m3_f32(kTileKeys, kCols);
 constexpr int kEpiThreads = kEpiWarps * 32;
@@ -166,26 +173,28 @@ __device__ __forceinline__ bool wait_counter(Smem &S, int *flag, int target, con
 }
 
 // ------------------------------------------------------------------ scoring
-// Each epilogue thread reads one row's accumulators with two 16x256b TMEM
-// loads (lanes 0-15 and 16-31 of its warp's quadrant): 4 keys (A = g, B = g+8,
-// C = g+16, D = g+24 with g = lane/4) x 8 heads (8i + 2c, 8i + 2c + 1 for
-// i < 4, c = lane%4).  relu(x) is formed as (x + |x|): a packed FP add whose
-// second operand carries an absolute-value modifier (FMA pipe); the 1/2 is
-// folded into the key scale.  x + |x| is exactly 2x or 0 and the halving is
-// exact.  The 4 threads of a key group then reduce-scatter their partial head
-// sums so that every thread owns the full sum of one key.  The summation
-// order is fixed and the fused and logits instantiations share this code, so
-// both produce bit-identical scores.
+// A row's kHeads accumulator columns are read in groups of 32: each epilogue
+// thread reads a group with two 16x256b TMEM loads (lanes 0-15 and 16-31 of
+// its warp's quadrant) and gets 4 keys (A = g, B = g+8, C = g+16, D = g+24
+// with g = lane/4) x 8 heads (8i + 2c, 8i + 2c + 1 for i < 4, c = lane%4) of
+// it.  relu(x) is formed as (x + |x|): a packed FP add whose second operand
+// carries an absolute-value modifier (FMA pipe); the 1/2 is folded into the
+// key scale.  x + |x| is exactly 2x or 0 and the halving is exact.  The 4
+// threads of a key group then reduce-scatter their partial head sums so that
+// every thread owns the full sum of one key.  The summation order is fixed
+// and the fused and logits instantiations share this code, so both produce
+// bit-identical scores.
 #ifndef MQA_RELU_ALU_CHUNKS
 #define MQA_RELU_ALU_CHUNKS 0
 #endif
-// Of a thread's 4 head-pair chunks per key, the first MQA_RELU_ALU_CHUNKS form
+// Of a thread's head-pair chunks per key, the first MQA_RELU_ALU_CHUNKS form
 // relu as max(x, 0) on the ALU pipe with pre-doubled weights (2w * max(x, 0));
 // the rest use x + |x| on the FMA pipe with w.  Both give 2 * w * relu(x)
 // exactly (one rounding of the same product), so the split only balances the
 // two pipes and leaves the scores bit-identical.
+constexpr int kHeadGroups = kHeads / 32;  // 32-column groups per row
 struct HeadW {
-  float2 w[4];  // weights of this thread's 8 heads of one row, as pairs (doubled for ALU chunks)
+  float2 w[4 * kHeadGroups];  // weights of this thread's heads of one row, as pairs (doubled for ALU chunks)
 };
 
 template <int kChunk>
@@ -195,20 +204,25 @@ __device__ __forceinline__ float2 relu2(uint32_t a, uint32_t b) {
   return __fadd2_rn(x, make_float2(fabsf(x.x), fabsf(x.y)));
 }
 
-// Full relu-weighted head sum of the key this thread owns (before scaling).
-__device__ __forceinline__ float row_head_sum(const uint32_t (&lo)[16], const uint32_t (&hi)[16], const HeadW &W,
-                                              int lane) {
-  float2 aA = make_float2(0.f, 0.f), aB = aA, aC = aA, aD = aA;
-#define MQA_HEAD_CHUNK(i)                                                    \
-  aA = __ffma2_rn(relu2<i>(lo[4 * i], lo[4 * i + 1]), W.w[i], aA);         \
-  aB = __ffma2_rn(relu2<i>(lo[4 * i + 2], lo[4 * i + 3]), W.w[i], aB);     \
-  aC = __ffma2_rn(relu2<i>(hi[4 * i], hi[4 * i + 1]), W.w[i], aC);         \
-  aD = __ffma2_rn(relu2<i>(hi[4 * i + 2], hi[4 * i + 3]), W.w[i], aD);
+// Accumulate head group G (columns 32G .. 32G + 31) of one row.
+template <int G>
+__device__ __forceinline__ void head_group(const uint32_t (&lo)[16], const uint32_t (&hi)[16], const HeadW &W,
+                                           float2 &aA, float2 &aB, float2 &aC, float2 &aD) {
+#define MQA_HEAD_CHUNK(i)                                                             \
+  aA = __ffma2_rn(relu2<4 * G + i>(lo[4 * i], lo[4 * i + 1]), W.w[4 * G + i], aA);     \
+  aB = __ffma2_rn(relu2<4 * G + i>(lo[4 * i + 2], lo[4 * i + 3]), W.w[4 * G + i], aB); \
+  aC = __ffma2_rn(relu2<4 * G + i>(hi[4 * i], hi[4 * i + 1]), W.w[4 * G + i], aC);     \
+  aD = __ffma2_rn(relu2<4 * G + i>(hi[4 * i + 2], hi[4 * i + 3]), W.w[4 * G + i], aD);
   MQA_HEAD_CHUNK(0)
   MQA_HEAD_CHUNK(1)
   MQA_HEAD_CHUNK(2)
   MQA_HEAD_CHUNK(3)
 #undef MQA_HEAD_CHUNK
+}
+
+// Full relu-weighted head sum of the key this thread owns (before scaling),
+// from the thread's partial sums of keys A..D.
+__device__ __forceinline__ float reduce_keys(float2 aA, float2 aB, float2 aC, float2 aD, int lane) {
   const float pA = aA.x + aA.y, pB = aB.x + aB.y, pC = aC.x + aC.y, pD = aD.x + aD.y;
   // round 1 (partner lane^1): even lanes keep keys A, B; odd lanes keep C, D
   const bool odd = lane & 1;
@@ -221,39 +235,36 @@ __device__ __forceinline__ float row_head_sum(const uint32_t (&lo)[16], const ui
   return (second ? k1 : k0) + __shfl_xor_sync(0xFFFFFFFFu, s, 2);
 }
 
-// Key (0..31 within the warp's quadrant) whose sum row_head_sum leaves in `lane`.
+// Key (0..31 within the warp's quadrant) whose sum reduce_keys leaves in `lane`.
 __device__ __forceinline__ int owned_key(int lane) { return (lane >> 2) + 8 * ((lane >> 1) & 1) + 16 * (lane & 1); }
 
 // Scaled head sums of this lane's key for the warp's kRowsPerWarp rows of one
 // tile, read from TMEM at `base` (the warp's quadrant, its first row).  Every
 // row is always loaded and summed (every TMEM address here is in the
 // allocation), so the code has no per-row branches; the caller masks rows
-// that do not take part.  Rows are loaded kLoadRows at a time; the TMEM buffer is released
-// (t_empty) once the last group is in registers.
-constexpr int kLoadRows = kRowsPerWarp >= 4 ? 2 : 1;
+// that do not take part.  A row's head groups are loaded together; the TMEM
+// buffer is released (t_empty) once the last row is in registers.
 __device__ __forceinline__ void score_rows(uint64_t *t_empty, uint32_t base, const HeadW (&W)[kRowsPerWarp],
-                                           float hsc, int lane,
-                                           float (&out)[kRowsPerWarp]) {
+                                           float hsc, int lane, float (&out)[kRowsPerWarp]) {
 #pragma unroll
-  for (int g = 0; g < kRowsPerWarp / kLoadRows; ++g) {
-    uint32_t lo[kLoadRows][16], hi[kLoadRows][16];
+  for (int rr = 0; rr < kRowsPerWarp; ++rr) {
+    uint32_t lo[kHeadGroups][16], hi[kHeadGroups][16];
 #pragma unroll
-    for (int j = 0; j < kLoadRows; ++j) {
-      const uint32_t col = (uint32_t)((g * kLoadRows + j) * kHeads);
-      tmem_ld_16x256b_x4(base + col, lo[j]);
-      tmem_ld_16x256b_x4(base + (16u << 16) + col, hi[j]);
+    for (int g = 0; g < kHeadGroups; ++g) {
+      const uint32_t col = (uint32_t)(rr * kHeads + 32 * g);
+      tmem_ld_16x256b_x4(base + col, lo[g]);
+      tmem_ld_16x256b_x4(base + (16u << 16) + col, hi[g]);
     }
     tmem_ld_wait();
-    if (g == kRowsPerWarp / kLoadRows - 1) {
+    if (rr == kRowsPerWarp - 1) {
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(t_empty);
     }
-#pragma unroll
-    for (int j = 0; j < kLoadRows; ++j) {
-      const int rr = g * kLoadRows + j;
-      out[rr] = row_head_sum(lo[j], hi[j], W[rr], lane) * hsc;
-    }
+    float2 aA = make_float2(0.f, 0.f), aB = aA, aC = aA, aD = aA;
+    head_group<0>(lo[0], hi[0], W[rr], aA, aB, aC, aD);
+    if constexpr (kHeadGroups > 1) head_group<1>(lo[1], hi[1], W[rr], aA, aB, aC, aD);
+    out[rr] = reduce_keys(aA, aB, aC, aD, lane) * hsc;
   }
 }
 
@@ -1013,7 +1024,7 @@ __device__ void producer(Smem &S, const CUtensorMap *q_map, const CUtensorMap *k
     ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
     if (!ok) return;
     int block = -1, mode = 0, chunk = 0, kchunk = -1, bs = 0;
-    uint32_t mask = 0xFFu;
+    uint32_t mask = (1u << kBlockRows) - 1u;
     if (lane == 0) {
       if (!kLogits) {
         const int head = *(volatile int *)&S.fifo_head;
@@ -1099,7 +1110,9 @@ __device__ void producer(Smem &S, const CUtensorMap *q_map, const CUtensorMap *k
       }
 #pragma unroll
       for (int r = 0; r < kBlockRows; ++r)
-        J.w[r][lane] = r < nrows ? __ldg(p.weights + (size_t)(r0 + r) * kHeads + lane) : 0.f;
+#pragma unroll
+        for (int h = lane; h < kHeads; h += 32)
+          J.w[r][h] = r < nrows ? __ldg(p.weights + (size_t)(r0 + r) * kHeads + h) : 0.f;
       // key range: the union of the taking-part rows' ranges
       const bool live = part && e > s;
       int lo = live ? s : INT_MAX, hi = live ? e : 0, len = live ? e - s : 0;
@@ -1337,7 +1350,7 @@ __device__ void epilogue(Smem &S, uint32_t tmem, const FusedParams &p, int warp,
       tau[rr] = kLogits ? NEG_INF : S.tau[r];
       cnt[rr] = 0;
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
+      for (int i = 0; i < 4 * kHeadGroups; ++i) {
         const float2 wv = *reinterpret_cast<const float2 *>(&J.w[r][8 * i + 2 * (lane & 3)]);
         W[rr].w[i] = i < MQA_RELU_ALU_CHUNKS ? make_float2(2.f * wv.x, 2.f * wv.y) : wv;
       }
@@ -1660,7 +1673,7 @@ __device__ void epilogue(Smem &S, uint32_t tmem, const FusedParams &p, int warp,
       // ew), and a row whose quadrant segment overflowed publishes a length
       // past the run's room.
       if (J.nchunks <= 8) {
-        if (ew == 0)
+        if (ew == 0 && lane < kBlockRows * kQuads)
           p.split_cnt[((size_t)J.bs * kBlockRows + (lane >> 2)) * 32 + J.chunk * kQuads + (lane & 3)] =
               S.segcnt[lane >> 2][lane & 3];
       } else if (gate_warp) {
@@ -1695,7 +1708,7 @@ __device__ void epilogue(Smem &S, uint32_t tmem, const FusedParams &p, int warp,
               Q.segcnt[i / nseg][i % nseg] = __ldcg(cnt_g + (i / nseg) * 32 + i % nseg);
           }
         } else {
-          Q.segcnt[lane >> 2][lane & 3] = S.segcnt[lane >> 2][lane & 3];
+          if (lane < kBlockRows * kQuads) Q.segcnt[lane >> 2][lane & 3] = S.segcnt[lane >> 2][lane & 3];
         }
         if (lane < kBlockRows) {
           Q.start[lane] = J.start[lane];
@@ -1934,6 +1947,31 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+static cudaError_t set_smem_attr(const void *fn) {
+  return cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)fused_smem_bytes());
+}
+
+cudaError_t launch_fused_topk(const CUtensorMap &q_map, const CUtensorMap &k_map, const CUtensorMap &s_map,
+                              const FusedParams &p, int ctas, cudaStream_t stream) {
+  static cudaError_t attr = set_smem_attr((const void *)mqa_fused_kernel<false>);
+  if (attr != cudaSuccess) return attr;
+  mqa_fused_kernel<false><<<ctas, kThreads, fused_smem_bytes(), stream>>>(q_map, k_map, s_map, p);
+  return cudaGetLastError();
+}
+
+#if MQA_HEADS == 32
+cudaError_t launch_logits(const CUtensorMap &q_map, const CUtensorMap &k_map, const CUtensorMap &s_map,
+                          const FusedParams &p, int ctas, cudaStream_t stream) {
+  static cudaError_t attr = set_smem_attr((const void *)mqa_fused_kernel<true>);
+  if (attr != cudaSuccess) return attr;
+  mqa_fused_kernel<true><<<ctas, kThreads, fused_smem_bytes(), stream>>>(q_map, k_map, s_map, p);
+  return cudaGetLastError();
+}
+#endif
+
+}  // namespace MQA_KNS
+
+#if MQA_HEADS == 32
 // ------------------------------------------------------------------ allocation-free scratch
 // Scratch for mqa_topk_prefill_noalloc: the 256-byte header plus the candidate
 // slabs of at most kStaticScratchCtas persistent CTAs, as a file-scope device
@@ -1959,25 +1997,6 @@ cudaError_t static_scratch_address(void **ptr) {
   *ptr = addr[dev];
   return cudaSuccess;
 }
-
-static cudaError_t set_smem_attr(const void *fn) {
-  return cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)fused_smem_bytes());
-}
-
-cudaError_t launch_fused_topk(const CUtensorMap &q_map, const CUtensorMap &k_map, const CUtensorMap &s_map,
-                              const FusedParams &p, int ctas, cudaStream_t stream) {
-  static cudaError_t attr = set_smem_attr((const void *)mqa_fused_kernel<false>);
-  if (attr != cudaSuccess) return attr;
-  mqa_fused_kernel<false><<<ctas, kThreads, fused_smem_bytes(), stream>>>(q_map, k_map, s_map, p);
-  return cudaGetLastError();
-}
-
-cudaError_t launch_logits(const CUtensorMap &q_map, const CUtensorMap &k_map, const CUtensorMap &s_map,
-                          const FusedParams &p, int ctas, cudaStream_t stream) {
-  static cudaError_t attr = set_smem_attr((const void *)mqa_fused_kernel<true>);
-  if (attr != cudaSuccess) return attr;
-  mqa_fused_kernel<true><<<ctas, kThreads, fused_smem_bytes(), stream>>>(q_map, k_map, s_map, p);
-  return cudaGetLastError();
-}
+#endif
 
 }  // namespace mqa

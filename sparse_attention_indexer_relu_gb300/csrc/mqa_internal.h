@@ -8,9 +8,16 @@
 
 namespace mqa {
 
-constexpr int kHeads = 32;      // index heads per query row
+// The fused kernel is compiled once per supported head count (MQA_HEADS 32
+// or 64); a 256-column accumulator tile holds 8 rows of 32 heads or 4 rows of
+// 64.  Host code is compiled for 32 and passes the block rows it needs.
+#ifndef MQA_HEADS
+#define MQA_HEADS 32
+#endif
+constexpr int kHeads = MQA_HEADS;  // index heads per query row
+static_assert(kHeads == 32 || kHeads == 64, "index heads: 32 or 64");
 constexpr int kDim = 128;       // head dimension (bytes per fp8 row)
-constexpr int kBlockRows = 8;   // query rows per block (one TMEM accumulator group)
+constexpr int kBlockRows = 256 / kHeads;  // query rows per block (one TMEM accumulator group)
 constexpr int kTileKeys = 128;  // keys per tile (UMMA M, one TMEM lane per key)
 constexpr int kCols = kBlockRows * kHeads;  // 256 accumulator columns per tile (UMMA N)
 constexpr int kKStages = 6;     // K-tile ring depth
@@ -19,7 +26,7 @@ constexpr int kQBytes = kCols * kDim;       // 32 KiB of q per block
 constexpr int kKTileBytes = kTileKeys * kDim;  // 16 KiB of k per tile
 
 #ifndef MQA_ROWS_PER_WARP
-#define MQA_ROWS_PER_WARP 2
+#define MQA_ROWS_PER_WARP (256 / MQA_HEADS / 4)
 #endif
 constexpr int kRowsPerWarp = MQA_ROWS_PER_WARP;  // rows of a block each epilogue warp scores
 constexpr int kQuadsC = 4;
@@ -94,16 +101,21 @@ struct FusedParams {
   long long timeout_ns;  // bound on every wait
 };
 
-// Launchers (defined next to their kernels).
+// Launchers (defined next to their kernels), per head count.
+namespace h32 {
 cudaError_t launch_fused_topk(const CUtensorMap &q_map, const CUtensorMap &k_map, const CUtensorMap &s_map,
                               const FusedParams &p, int ctas, cudaStream_t stream);
 cudaError_t launch_logits(const CUtensorMap &q_map, const CUtensorMap &k_map, const CUtensorMap &s_map,
                           const FusedParams &p, int ctas, cudaStream_t stream);
+}  // namespace h32
+namespace h64 {
+cudaError_t launch_fused_topk(const CUtensorMap &q_map, const CUtensorMap &k_map, const CUtensorMap &s_map,
+                              const FusedParams &p, int ctas, cudaStream_t stream);
+}  // namespace h64
 cudaError_t launch_ue8m0_decode(const uint8_t *scales, float *out, int keys, cudaStream_t stream);
 cudaError_t launch_dense_topk_rows(const float *logits, int rows, int keys, const int32_t *starts,
                                    const int32_t *ends, int32_t *out, int topk, int32_t *ws_status,
                                    cudaStream_t stream);
-size_t fused_smem_bytes();
 
 // Fused-op workspace layout: header, split-done counters, per-CTA slabs, split
 // slab, split counts (split_max == 0: header and slabs only).
@@ -119,12 +131,12 @@ __host__ __device__ inline long long split_row_capacity(int cap, int chunks) {
   const long long a = cap / (4 * chunks) + 64, b = cap / 8;
   return 4LL * chunks * (a > b ? a : b);
 }
-FusedLayout fused_layout(int ctas, int cap, int split_max);
+FusedLayout fused_layout(int ctas, int cap, int split_max, int block_rows);
 
 // Allocation-free variant: a static device scratch sized for this many CTAs.
 constexpr int kStaticScratchCtas = 8;
 constexpr size_t kStaticScratchBytes =
-    kWsHeaderBytes + (size_t)kStaticScratchCtas * kSlots * 2 * kBlockRows * kDefaultSlabCap * sizeof(uint32_t);
+    kWsHeaderBytes + (size_t)kStaticScratchCtas * kSlots * 2 * 8 * kDefaultSlabCap * sizeof(uint32_t);  // 8-row blocks
 // Device address of the static scratch on the current device (resolved on first use).
 cudaError_t static_scratch_address(void **ptr);
 

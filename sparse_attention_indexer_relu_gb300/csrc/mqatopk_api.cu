@@ -118,33 +118,36 @@ int check_common(const void *q, const void *k, const float *scales, const float 
 
 bool valid_topk(int topk) { return topk == 512 || topk == 1024 || topk == 2048; }
 
-size_t slab_bytes(int ctas, int cap) {
-  return (size_t)ctas * kSlots * 2 * kBlockRows * (size_t)cap * sizeof(uint32_t);
+// Rows per block: a 256-column accumulator tile holds 8 rows of 32 heads or 4 of 64.
+int block_rows(int heads) { return 256 / heads; }
+
+size_t slab_bytes(int ctas, int cap, int brows) {
+  return (size_t)ctas * kSlots * 2 * brows * (size_t)cap * sizeof(uint32_t);
 }
 
-int fused_ctas(const DeviceInfo &d, int rows) {
-  const int nb = (rows + kBlockRows - 1) / kBlockRows;
+int fused_ctas(const DeviceInfo &d, int rows, int brows) {
+  const int nb = (rows + brows - 1) / brows;
   return nb < d.sms ? nb : d.sms;
 }
 
 // With the key-range split, few-block calls also use idle SMs (one CTA per
 // key chunk), and up to two waves' worth of blocks can be split.
-int fused_ctas_split(const DeviceInfo &d, int rows) {
-  const long long nb = (rows + kBlockRows - 1) / kBlockRows;
+int fused_ctas_split(const DeviceInfo &d, int rows, int brows) {
+  const long long nb = (rows + brows - 1) / brows;
   return nb * kMaxChunks < d.sms ? (int)(nb * kMaxChunks) : d.sms;
 }
-int split_max_blocks(int ctas, int rows) {
-  const int nb = (rows + kBlockRows - 1) / kBlockRows;
+int split_max_blocks(int ctas, int rows, int brows) {
+  const int nb = (rows + brows - 1) / brows;
   return nb < 2 * ctas ? nb : 2 * ctas;
 }
 
 }  // namespace
 
-FusedLayout mqa::fused_layout(int ctas, int cap, int split_max) {
+FusedLayout mqa::fused_layout(int ctas, int cap, int split_max, int brows) {
   FusedLayout L;
   L.done_off = kWsHeaderBytes;
   L.slab_off = L.done_off + (((size_t)split_max * sizeof(int32_t) + 255) / 256) * 256;
-  L.split_off = L.slab_off + slab_bytes(ctas, cap);
+  L.split_off = L.slab_off + slab_bytes(ctas, cap, brows);
   long long rc = 0;
   if (split_max > 0) {
     // the largest split set the device plan may choose (see plan_split)
@@ -156,9 +159,9 @@ FusedLayout mqa::fused_layout(int ctas, int cap, int split_max) {
       rc = rc > cc ? rc : cc;
     }
   }
-  L.split_words = 2LL * kBlockRows * rc;
+  L.split_words = 2LL * brows * rc;
   L.cnt_off = L.split_off + (size_t)L.split_words * sizeof(uint32_t);
-  L.total = L.cnt_off + (size_t)split_max * kBlockRows * 32 * sizeof(int32_t);
+  L.total = L.cnt_off + (size_t)split_max * brows * 32 * sizeof(int32_t);
   L.reset_bytes = L.slab_off;
   return L;
 }
@@ -168,11 +171,12 @@ namespace {
 cudaStream_t as_stream(void *s) { return reinterpret_cast<cudaStream_t>(s); }
 
 int run_fused(const void *q, const void *k, const float *scales, const float *weights, const int32_t *starts,
-              const int32_t *ends, int32_t *out, int rows, int keys, int topk, void *workspace,
+              const int32_t *ends, int32_t *out, int rows, int keys, int topk, int heads, void *workspace,
               size_t workspace_bytes, void *stream, const mqa_topk_debug_options *opt) {
   int rc = check_common(q, k, scales, weights, starts, ends, out, rows, keys);
   if (rc != MQA_OK) return rc;
-  if (!valid_topk(topk)) return MQA_ERR_INVALID_ARGUMENT;
+  if (!valid_topk(topk) || (heads != 32 && heads != 64)) return MQA_ERR_INVALID_ARGUMENT;
+  const int brows = block_rows(heads);
   if (!workspace) return MQA_ERR_INVALID_ARGUMENT;
   if (!aligned(workspace, 256)) return MQA_ERR_MISALIGNED;
   int cap = kDefaultSlabCap;
@@ -190,21 +194,22 @@ int run_fused(const void *q, const void *k, const float *scales, const float *we
   if (rc != MQA_OK) return rc;
   // key-range split when the workspace holds its arrays (mqa_topk_workspace_bytes
   // sizes for it), else one CTA per block as far as SMs go
-  int ctas = fused_ctas_split(d, rows);
+  int ctas = fused_ctas_split(d, rows, brows);
   if (opt && opt->max_ctas && opt->max_ctas < ctas) ctas = opt->max_ctas;
-  int split_max = split_max_blocks(ctas, rows);
-  FusedLayout L = fused_layout(ctas, cap, split_max);
+  int split_max = split_max_blocks(ctas, rows, brows);
+  FusedLayout L = fused_layout(ctas, cap, split_max, brows);
   if (workspace_bytes < L.total) {
-    ctas = fused_ctas(d, rows);
+    ctas = fused_ctas(d, rows, brows);
     if (opt && opt->max_ctas && opt->max_ctas < ctas) ctas = opt->max_ctas;
     split_max = 0;
-    L = fused_layout(ctas, cap, 0);
+    L = fused_layout(ctas, cap, 0, brows);
     if (workspace_bytes < L.total) return MQA_ERR_WORKSPACE_TOO_SMALL;
   }
   rc = get_encoder();
   if (rc != MQA_OK) return rc;
   CUtensorMap qm, km, sm;
-  if (encode_rows128(&qm, q, (uint64_t)rows * kHeads, kCols) != MQA_OK ||
+  // q is [rows * heads, 128]: a block's 256 (row, head) rows per TMA box
+  if (encode_rows128(&qm, q, (uint64_t)rows * heads, kCols) != MQA_OK ||
       encode_rows128(&km, k, (uint64_t)keys, kTileKeys) != MQA_OK || encode_scales(&sm, scales, keys) != MQA_OK)
     return MQA_ERR_CUDA;
   FusedParams p;
@@ -227,7 +232,7 @@ int run_fused(const void *q, const void *k, const float *scales, const float *we
   p.rows = rows;
   p.keys = keys;
   p.topk = topk;
-  p.nblocks = (rows + kBlockRows - 1) / kBlockRows;
+  p.nblocks = (rows + brows - 1) / brows;
   p.cap = cap;
   p.gate_target = 3 * topk < cap / 2 ? 3 * topk : cap / 2;
   // gate every row that would otherwise bring more than twice the target
@@ -241,7 +246,9 @@ int run_fused(const void *q, const void *k, const float *scales, const float *we
     cudaGetLastError();
     return MQA_ERR_CUDA;
   }
-  if (launch_fused_topk(qm, km, sm, p, ctas, st) != cudaSuccess) return MQA_ERR_CUDA;
+  const cudaError_t le =
+      heads == 64 ? h64::launch_fused_topk(qm, km, sm, p, ctas, st) : h32::launch_fused_topk(qm, km, sm, p, ctas, st);
+  if (le != cudaSuccess) return MQA_ERR_CUDA;
   return MQA_OK;
 }
 
@@ -279,15 +286,15 @@ int run_logits_chunk(const DeviceInfo &d, const uint8_t *q, const void *k, const
     cudaGetLastError();
     return MQA_ERR_CUDA;
   }
-  return launch_logits(qm, km, sm, p, ctas, st) == cudaSuccess ? MQA_OK : MQA_ERR_CUDA;
+  return h32::launch_logits(qm, km, sm, p, ctas, st) == cudaSuccess ? MQA_OK : MQA_ERR_CUDA;
 }
 
 }  // namespace
 
 extern "C" {
 
-int mqa_topk_workspace_bytes(int device, int rows, size_t *bytes) {
-  if (!bytes || rows < 0) return MQA_ERR_INVALID_ARGUMENT;
+int mqa_topk_workspace_bytes_ex(int device, int rows, int heads, size_t *bytes) {
+  if (!bytes || rows < 0 || (heads != 32 && heads != 64)) return MQA_ERR_INVALID_ARGUMENT;
   DeviceInfo d;
   int rc = device_info(device, &d);
   if (rc != MQA_OK) return rc;
@@ -295,15 +302,20 @@ int mqa_topk_workspace_bytes(int device, int rows, size_t *bytes) {
     *bytes = kWsHeaderBytes;
     return MQA_OK;
   }
-  const int ctas = fused_ctas_split(d, rows);
-  *bytes = fused_layout(ctas, kDefaultSlabCap, split_max_blocks(ctas, rows)).total;
+  const int brows = block_rows(heads);
+  const int ctas = fused_ctas_split(d, rows, brows);
+  *bytes = fused_layout(ctas, kDefaultSlabCap, split_max_blocks(ctas, rows, brows), brows).total;
   return MQA_OK;
+}
+
+int mqa_topk_workspace_bytes(int device, int rows, size_t *bytes) {
+  return mqa_topk_workspace_bytes_ex(device, rows, 32, bytes);
 }
 
 int mqa_topk_prefill(const void *q, const void *k, const float *key_scales, const float *weights,
                      const int32_t *starts, const int32_t *ends, int32_t *out, int rows, int keys, int topk,
                      void *workspace, size_t workspace_bytes, void *stream) {
-  return run_fused(q, k, key_scales, weights, starts, ends, out, rows, keys, topk, workspace, workspace_bytes,
+  return run_fused(q, k, key_scales, weights, starts, ends, out, rows, keys, topk, 32, workspace, workspace_bytes,
                    stream, nullptr);
 }
 
@@ -311,8 +323,16 @@ int mqa_topk_prefill_debug(const void *q, const void *k, const float *key_scales
                            const int32_t *starts, const int32_t *ends, int32_t *out, int rows, int keys,
                            int topk, void *workspace, size_t workspace_bytes, void *stream,
                            const mqa_topk_debug_options *opt) {
-  return run_fused(q, k, key_scales, weights, starts, ends, out, rows, keys, topk, workspace, workspace_bytes,
+  return run_fused(q, k, key_scales, weights, starts, ends, out, rows, keys, topk, 32, workspace, workspace_bytes,
                    stream, opt);
+}
+
+int mqa_topk_prefill_ex(const void *q, const void *k, const float *key_scales, const float *weights,
+                        const int32_t *starts, const int32_t *ends, int32_t *out, int rows, int keys, int topk,
+                        int heads, void *workspace, size_t workspace_bytes, void *stream,
+                        const mqa_topk_debug_options *opt) {
+  return run_fused(q, k, key_scales, weights, starts, ends, out, rows, keys, topk, heads, workspace,
+                   workspace_bytes, stream, opt);
 }
 
 int mqa_topk_prefill_noalloc(const void *q, const void *k, const float *key_scales, const float *weights,
@@ -327,9 +347,9 @@ int mqa_topk_prefill_noalloc(const void *q, const void *k, const float *key_scal
   if (rc != MQA_OK) return rc;
   // The scratch need is set by the CTA count, which this entry caps; a call
   // whose need exceeded the static array would be rejected here.
-  int ctas = fused_ctas(d, rows);
+  int ctas = fused_ctas(d, rows, 8);
   if (ctas > kStaticScratchCtas) ctas = kStaticScratchCtas;
-  const size_t need = fused_layout(ctas, kDefaultSlabCap, 0).total;
+  const size_t need = fused_layout(ctas, kDefaultSlabCap, 0, 8).total;
   if (need > kStaticScratchBytes) return MQA_ERR_WORKSPACE_TOO_SMALL;
   void *scratch = nullptr;
   if (static_scratch_address(&scratch) != cudaSuccess) {
@@ -339,8 +359,8 @@ int mqa_topk_prefill_noalloc(const void *q, const void *k, const float *key_scal
   mqa_topk_debug_options opt;
   std::memset(&opt, 0, sizeof opt);
   opt.max_ctas = ctas;
-  return run_fused(q, k, key_scales, weights, starts, ends, out, rows, keys, topk, scratch, kStaticScratchBytes,
-                   stream, &opt);
+  return run_fused(q, k, key_scales, weights, starts, ends, out, rows, keys, topk, 32, scratch,
+                   kStaticScratchBytes, stream, &opt);
 }
 
 int mqa_ue8m0_decode(const uint8_t *scales, float *out, int keys, void *stream) {

@@ -200,6 +200,8 @@ CONFIGS = {
     "r16k_1m_k2048": lambda: make_single("r16k_1m_k2048", 16384, 1 << 20, 2048),
     "r16k_1m_k2048_adversarial": lambda: make_single("r16k_1m_k2048_adversarial", 16384, 1 << 20, 2048,
                                                      dup_frac=0.25, scaled_row_frac=0.01),
+    # 64 index heads per query row (DeepSeek-V3.2's indexer), prefill chunk
+    "h64_r2048_64k_k2048": lambda: make_single("h64_r2048_64k_k2048", 2048, 65536, 2048, heads=64),
     # Decode batches: each request verifies K + 1 = 8 query rows (speculative
     # K = 7) against its own context; row t of a request sees its context up to
     # N - 8 + t + 1 keys (the multi-request layout with 8 rows per request).

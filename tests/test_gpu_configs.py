@@ -43,6 +43,7 @@ CASES = [
     ("decode_b32_s8_64k_k2048", 48),
     ("decode_b4_s8_256k_k2048", 32),
     ("decode_b64_s8_mixed_k512", 64),
+    ("h64_r2048_64k_k2048", 40),
 ]
 
 
@@ -50,7 +51,7 @@ CASES = [
 def test_config_parity(mqa, name, nsample):
     p = synth.make(name)
     q, k, sc, w, s, e = to_device(p)
-    ws = mqa.alloc_workspace(p.rows)
+    ws = mqa.alloc_workspace(p.rows, heads=p.heads)
     out = mqa.mqa_topk_prefill(q, k, sc, w, s, e, p.topk, workspace=ws)
     status, stats = mqa.get_status(ws)
     got = out.cpu().numpy()

@@ -21,7 +21,7 @@ def mqa():
 def run_fused(mqa, p, debug=None, workspace=None):
     import torch
     q, k, sc, w, s, e = to_device(p)
-    ws = workspace if workspace is not None else mqa.alloc_workspace(p.rows)
+    ws = workspace if workspace is not None else mqa.alloc_workspace(p.rows, heads=p.heads)
     out = mqa.mqa_topk_prefill(q, k, sc, w, s, e, p.topk, workspace=ws, debug=debug)
     status, stats = mqa.get_status(ws)
     return out.cpu().numpy(), status, stats
@@ -182,6 +182,25 @@ def test_fused_key_split_overflow_rescans(mqa):
     got, status, stats = run_fused(mqa, p, debug={"force_gate": 2, "slab_capacity": 2560, "max_ctas": 4})
     assert status == 0, stats
     assert stats["split_blocks"] == 2 and stats["rows_rescanned"] > 0, stats
+    assert_parity(p, got)
+
+
+@pytest.mark.parametrize("seed,rows,keys,topk", [(40, 3, 700, 512), (41, 13, 5000, 1024), (42, 37, 20000, 2048)])
+def test_fused_64_heads_random_ranges(mqa, seed, rows, keys, topk):
+    """64 index heads per row (4-row blocks): arbitrary ranges, exact top-k."""
+    p = synth.random_small(seed, rows, keys, topk, heads=64)
+    got, status, stats = run_fused(mqa, p)
+    assert status == 0, stats
+    assert_parity(p, got)
+
+
+def test_fused_64_heads_gated_split(mqa):
+    """64 index heads, long causal rows: sampled gate, binned selection and
+    key chunks merged across CTAs."""
+    p = _causal(synth.random_small(43, 16, 60000, 2048, heads=64, empty_frac=0.0), 60000)
+    got, status, stats = run_fused(mqa, p)
+    assert status == 0, stats
+    assert stats["gated_rows"] == 16 and stats["split_blocks"] == 4, stats
     assert_parity(p, got)
 
 
