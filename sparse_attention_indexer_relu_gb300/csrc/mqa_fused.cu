@@ -224,12 +224,12 @@ __device__ __forceinline__ void head_group(const uint32_t (&lo)[16], const uint3
 // from the thread's partial sums of keys A..D.
 __device__ __forceinline__ float reduce_keys(float2 aA, float2 aB, float2 aC, float2 aD, int lane) {
   const float pA = aA.x + aA.y, pB = aB.x + aB.y, pC = aC.x + aC.y, pD = aD.x + aD.y;
-  // round 1 (partner lane^1): even lanes keep keys A, B; odd lanes keep C, D
+  // step 1 (partner lane^1): even lanes keep keys A, B; odd lanes keep C, D
   const bool odd = lane & 1;
   const float s0 = odd ? pA : pC, s1 = odd ? pB : pD;
   const float k0 = (odd ? pC : pA) + __shfl_xor_sync(0xFFFFFFFFu, s0, 1);
   const float k1 = (odd ? pD : pB) + __shfl_xor_sync(0xFFFFFFFFu, s1, 1);
-  // round 2 (partner lane^2): lanes with bit 1 clear keep the first key
+  // step 2 (partner lane^2): lanes with bit 1 clear keep the first key
   const bool second = lane & 2;
   const float s = second ? k0 : k1;
   return (second ? k1 : k0) + __shfl_xor_sync(0xFFFFFFFFu, s, 2);
