@@ -44,6 +44,9 @@ def load_library(path: str):
     lib.oracle_run.argtypes = [P, P, P, P, P, P, P, ctypes.c_int64, ctypes.c_int64,
                                ctypes.c_int, ctypes.c_int, ctypes.c_int, P, P, ctypes.c_int]
     lib.oracle_run.restype = ctypes.c_int
+    lib.oracle_run_blocks.argtypes = [P, P, P, P, P, P, P, ctypes.c_int64, ctypes.c_int64,
+                                      ctypes.c_int, ctypes.c_int, ctypes.c_int, P, ctypes.c_int]
+    lib.oracle_run_blocks.restype = ctypes.c_int
     return lib
 
 
@@ -117,6 +120,27 @@ def run(p, rows=None, want_topk=True, want_scores=False, topk=None, nthreads=Non
     if rc != 0:
         raise ValueError(f"oracle_run failed with status {rc}")
     return out, scores
+
+
+def run_blocks(p, btopk, rows=None, nthreads=None, lib=None):
+    """Top `btopk` blocks of 8 keys per listed row by their largest score:
+    [n, btopk] int32, block index relative to the row's first block
+    (floor(start / 8)), best first (ties by block index), -1 padded."""
+    q = _c(p.q, np.uint8)
+    k = _c(p.k, np.uint8)
+    g = _c(p.scales_ue8m0, np.uint8)
+    w = _c(p.weights, np.float32)
+    s = _c(p.starts, np.int32)
+    e = _c(p.ends, np.int32)
+    rows = np.arange(q.shape[0], dtype=np.int64) if rows is None else _c(rows, np.int64)
+    n = rows.shape[0]
+    out = np.empty((n, int(btopk)), np.int32)
+    rc = _load(lib).oracle_run_blocks(_ptr(q), _ptr(k), _ptr(g), _ptr(w), _ptr(s), _ptr(e), _ptr(rows), n,
+                                      k.shape[0], q.shape[1], q.shape[2], int(btopk), _ptr(out),
+                                      int(nthreads or default_threads()))
+    if rc != 0:
+        raise ValueError(f"oracle_run_blocks failed with status {rc}")
+    return out
 
 
 def topk(p, rows=None, nthreads=None, lib=None):

@@ -25,6 +25,12 @@
  *    request's Summary and Performance table define the target as the exact
  *    fp32 top-k up to ties at the boundary.  For determinism the oracle
  *    breaks ties by key index ascending (any tie choice is correct).
+ *  - Block selection (the two-level candidate selection of the pull request's
+ *    "Limitations of this PR -- TODOs": a source layer also writes, per row,
+ *    the top blocks of 8 keys ranked by their maximum score): block b holds
+ *    keys [8b, 8b + 8) of the key array; its score is the largest S over the
+ *    row's visible keys in it.  The output lists the chosen blocks as
+ *    b - floor(start / 8), ties by block index ascending, -1 padded.
  *
  * Arithmetic: every e4m3 value is an integer multiple of 2^-9 with magnitude
  * at most 448, so each q.k product is a multiple of 2^-18 below 2^18 and a
@@ -116,6 +122,19 @@ static int cmp_scored(const void *a, const void *b) {
     return (x->key > y->key) - (x->key < y->key);
 }
 
+/* order: larger block score first; equal scores by smaller block first */
+typedef struct {
+    double score;
+    int64_t block;
+} scored_block;
+
+static int cmp_block(const void *a, const void *b) {
+    const scored_block *x = (const scored_block *)a, *y = (const scored_block *)b;
+    if (x->score > y->score) return -1;
+    if (x->score < y->score) return 1;
+    return (x->block > y->block) - (x->block < y->block);
+}
+
 typedef struct {
     const uint8_t *q, *k, *scale_groups;
     const float *w;
@@ -125,6 +144,7 @@ typedef struct {
     int heads, dim, topk;
     int32_t *out;           /* [nlist, topk] */
     double *scores_out;     /* optional [nlist, keys] dense scores (-inf outside) */
+    int block_mode;         /* select blocks of 8 keys by their largest score */
     int64_t next;           /* shared work counter */
     pthread_mutex_t lock;
     int status;
@@ -171,7 +191,23 @@ static void *worker(void *arg) {
             if (buf) { buf[t].score = v; buf[t].key = j; }
             if (J->scores_out) J->scores_out[i * J->keys + j] = v;
         }
-        if (J->out) {
+        if (J->out && J->block_mode) {
+            /* blocks [s / 8, (e - 1) / 8]; buf holds keys s .. e - 1 in order */
+            int64_t b0 = s >> 3, nb = n > 0 ? ((e - 1) >> 3) - b0 + 1 : 0;
+            scored_block *blk = nb > 0 ? (scored_block *)malloc(sizeof(scored_block) * (size_t)nb) : NULL;
+            if (nb > 0 && !blk) { J->status = -1; break; }
+            for (int64_t b = 0; b < nb; ++b) { blk[b].score = -INFINITY; blk[b].block = b0 + b; }
+            for (int64_t t = 0; t < n; ++t) {
+                int64_t b = ((s + t) >> 3) - b0;
+                if (buf[t].score > blk[b].score) blk[b].score = buf[t].score;
+            }
+            if (nb > 0) qsort(blk, (size_t)nb, sizeof(scored_block), cmp_block);
+            int64_t c = nb < J->topk ? nb : J->topk;
+            int32_t *o = J->out + i * J->topk;
+            for (int64_t t = 0; t < c; ++t) o[t] = (int32_t)(blk[t].block - b0);
+            for (int64_t t = c; t < J->topk; ++t) o[t] = -1;
+            free(blk);
+        } else if (J->out) {
             if (n > 0) qsort(buf, (size_t)n, sizeof(scored_key), cmp_scored);
             int64_t c = n < J->topk ? n : J->topk;
             int32_t *o = J->out + i * J->topk;
@@ -209,10 +245,11 @@ static int run_jobs(job_t *J, int nthreads) {
  *  scores (nullable) [nlist, keys]: fp64 S(r, j), -inf outside [start, end).
  * A row whose range is empty or reversed sees no key.  A non-empty range that
  * leaves [0, keys) is rejected (-3).  Returns 0 on success. */
-int oracle_run(const uint8_t *q, const uint8_t *k, const uint8_t *scale_groups,
-               const float *w, const int32_t *starts, const int32_t *ends,
-               const int64_t *row_list, int64_t nlist, int64_t keys,
-               int heads, int dim, int topk, int32_t *out, double *scores, int nthreads) {
+static int run_mode(const uint8_t *q, const uint8_t *k, const uint8_t *scale_groups,
+                    const float *w, const int32_t *starts, const int32_t *ends,
+                    const int64_t *row_list, int64_t nlist, int64_t keys,
+                    int heads, int dim, int topk, int32_t *out, double *scores, int nthreads,
+                    int block_mode) {
     if (dim > 1024 || heads < 1 || dim < 1 || (out && topk < 1)) return -2;
     for (int64_t i = 0; i < nlist; ++i) {
         int64_t r = row_list[i];
@@ -223,6 +260,25 @@ int oracle_run(const uint8_t *q, const uint8_t *k, const uint8_t *scale_groups,
     J.q = q; J.k = k; J.scale_groups = scale_groups; J.w = w;
     J.starts = starts; J.ends = ends; J.row_list = row_list; J.nlist = nlist;
     J.keys = keys; J.heads = heads; J.dim = dim; J.topk = topk > 0 ? topk : 1;
-    J.out = out; J.scores_out = scores;
+    J.out = out; J.scores_out = scores; J.block_mode = block_mode;
     return run_jobs(&J, nthreads);
+}
+
+int oracle_run(const uint8_t *q, const uint8_t *k, const uint8_t *scale_groups,
+               const float *w, const int32_t *starts, const int32_t *ends,
+               const int64_t *row_list, int64_t nlist, int64_t keys,
+               int heads, int dim, int topk, int32_t *out, double *scores, int nthreads) {
+    return run_mode(q, k, scale_groups, w, starts, ends, row_list, nlist, keys, heads, dim, topk,
+                    out, scores, nthreads, 0);
+}
+
+/* Top `btopk` blocks of 8 keys per listed row by block score (see the header):
+ * out_blocks [nlist, btopk] receives b - floor(start / 8), -1 padded. */
+int oracle_run_blocks(const uint8_t *q, const uint8_t *k, const uint8_t *scale_groups,
+                      const float *w, const int32_t *starts, const int32_t *ends,
+                      const int64_t *row_list, int64_t nlist, int64_t keys,
+                      int heads, int dim, int btopk, int32_t *out_blocks, int nthreads) {
+    if (!out_blocks) return -2;
+    return run_mode(q, k, scale_groups, w, starts, ends, row_list, nlist, keys, heads, dim, btopk,
+                    out_blocks, NULL, nthreads, 1);
 }

@@ -33,6 +33,11 @@ MUTANTS = {
                   "else mag = ldexp(1.0 + (double)m / 8.0, (int)e - 8);"),
     "e4m3_subnormal": ("if (e == 0u) mag = ldexp((double)m, -9);", "if (e == 0u) mag = ldexp((double)m, -10);"),
     "e4m3_sign": ("return s ? -mag : mag;", "return mag;"),
+    "block_absolute_index": ("o[t] = (int32_t)(blk[t].block - b0);", "o[t] = (int32_t)(blk[t].block);"),
+    "block_last_not_max": ("if (buf[t].score > blk[b].score) blk[b].score = buf[t].score;",
+                           "blk[b].score = buf[t].score;"),
+    "block_order": ("if (x->score > y->score) return -1;\n    if (x->score < y->score) return 1;\n    return (x->block",
+                    "if (x->score > y->score) return 1;\n    if (x->score < y->score) return -1;\n    return (x->block"),
     "ue8m0_shift": ("uint32_t bits = ((uint32_t)J->scale_groups[4 * j]) << 23;",
                     "uint32_t bits = ((uint32_t)J->scale_groups[4 * j + 1] + 1) << 23;"),
 }

@@ -334,3 +334,86 @@ def test_fast_quantizer_matches_reference(lib=None):
     x = np.concatenate([rng.standard_normal(300000).astype(np.float32) * 3,
                         np.float32([1000.0, -700.0, 449.0, 2 ** -12, -2 ** -9])])
     assert np.array_equal(synth.quantize_e4m3fn_fast(x), synth.quantize_e4m3fn(x))
+
+
+# ----------------------------------------------------------------------------
+# block selection (two-level candidate selection): blocks of 8 keys ranked by
+# their largest score
+
+def check_blocks_against_scores(blk_row, scores_row, start, end, btopk, tol):
+    """blk_row must hold c = min(btopk, nb) distinct block indices relative to
+    floor(start / 8), then -1s, and every selected block's largest score must
+    be >= every unselected block's (up to tol)."""
+    b0 = start // 8
+    nb = ((end - 1) // 8 - b0 + 1) if end > start else 0
+    c = min(btopk, nb)
+    assert np.all(blk_row[c:] == -1)
+    sel = blk_row[:c]
+    assert np.all((sel >= 0) & (sel < nb)) and len(np.unique(sel)) == c
+    if c and c < nb:
+        bmax = np.full(nb, -np.inf)
+        for j in range(start, end):
+            b = j // 8 - b0
+            bmax[b] = max(bmax[b], scores_row[j])
+        mask = np.zeros(nb, bool)
+        mask[sel] = True
+        assert bmax[mask].min() >= bmax[~mask].max() - tol
+
+
+@pytest.mark.parametrize("seed", [7, 8])
+def test_blocks_match_numpy_formulation(seed, lib=None):
+    """Block maxima from the independent numpy scores rank the oracle's blocks."""
+    p = tiny_problem(seed, 12, 900, 64)
+    blk = oracle.run_blocks(p, 40, lib=lib)
+    sc = numpy_scores(p)
+    for r in range(p.rows):
+        tol = 1e-9 * (1 + np.abs(sc[r][np.isfinite(sc[r])]).max(initial=0))
+        check_blocks_against_scores(blk[r], sc[r], int(p.starts[r]), int(p.ends[r]), 40, tol)
+
+
+def test_blocks_reduce_to_key_topk_on_sparse_blocks(lib=None):
+    """Keys 8b+1 .. 8b+7 are zero vectors (score 0) and every other score is
+    positive, so block b's score is key 8b's: the block selection must equal
+    the key selection over the keys 8b alone (same scores, same tie rule)."""
+    p = tiny_problem(9, 6, 1600, 64, heads=8, dim=32)
+    p.q = (p.q & 0x7F).astype(np.uint8)              # non-negative q
+    p.k = (p.k & 0x7F).astype(np.uint8)              # non-negative k
+    p.weights = np.abs(p.weights).astype(np.float32) + np.float32(1e-3)
+    zero = np.arange(p.keys) % 8 != 0
+    p.k[zero] = 0
+    p.starts = (p.starts // 8 * 8).astype(np.int32)
+    p.ends = (p.ends // 8 * 8).astype(np.int32)
+    blk = oracle.run_blocks(p, 32, lib=lib)
+    sub = synth.Problem("sub", p.q, p.k[::8].copy(), p.scales_ue8m0[::8].copy(), p.weights,
+                        (p.starts // 8).astype(np.int32), (p.ends // 8).astype(np.int32), 32)
+    idx, _ = oracle.run(sub, lib=lib)
+    assert np.array_equal(blk, idx)
+
+
+def test_blocks_integer_bruteforce_tiny(lib=None):
+    """Exact block maxima from Python integers (codes decoded by hand, dots in
+    units of 2^-18, one head, unit weight, scale 1) on tiny rows."""
+    def dec(c):
+        s, e, m = (c >> 7) & 1, (c >> 3) & 15, c & 7
+        v = (m if e == 0 else (8 + m) << (e - 1))     # value * 2^9
+        return -v if s else v
+    rng = np.random.default_rng(4)
+    for trial in range(20):
+        keys = int(rng.integers(9, 60))
+        p = tiny_problem(200 + trial, 1, keys, 8, heads=1, dim=4)
+        p.weights[:] = 1.0
+        p.scales_ue8m0[:] = 127
+        s0 = int(rng.integers(0, keys - 1))
+        p.starts[:] = s0
+        p.ends[:] = int(rng.integers(s0 + 1, keys + 1))
+        st, en = int(p.starts[0]), int(p.ends[0])
+        qd = [dec(int(c)) for c in p.q[0, 0]]
+        score = {j: max(0, sum(a * dec(int(b)) for a, b in zip(qd, p.k[j]))) for j in range(st, en)}
+        b0 = st // 8
+        bmax = {}
+        for j, v in score.items():
+            bmax[j // 8 - b0] = max(bmax.get(j // 8 - b0, -1), v)
+        want = sorted(bmax, key=lambda b: (-bmax[b], b))[:5]
+        got = oracle.run_blocks(p, 5, lib=lib)[0]
+        assert got[:len(want)].tolist() == want
+        assert np.all(got[len(want):] == -1)
