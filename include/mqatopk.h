@@ -146,6 +146,21 @@ int mqa_topk_prefill_ex(const void *q, const void *k, const float *key_scales, c
                         int heads, void *workspace, size_t workspace_bytes, void *stream,
                         const mqa_topk_debug_options *opt);
 
+/* Block selection, the first half of the pages' two-level candidate selection
+ * (PR #60618, "Limitations of this PR -- TODOs": a candidate-source layer also
+ * writes, per row, the top 2,048 blocks of 8 keys ranked by their maximum
+ * score).  Block b holds keys [8b, 8b + 8) of k; its score is the largest
+ * s(r, j) over the row's visible keys in it.  out_blocks [rows, btopk] int32
+ * receives the btopk best blocks of each row as b - floor(starts[r] / 8),
+ * unordered, -1 padded when the row's range touches fewer blocks; ties at the
+ * btopk-th score are taken in any order.  btopk in {512, 1024, 2048}; 32
+ * heads; workspace as for mqa_topk_prefill (mqa_topk_workspace_bytes); opt
+ * (nullable) as for mqa_topk_prefill_debug.  Same errors as mqa_topk_prefill. */
+int mqa_block_topk_prefill(const void *q, const void *k, const float *key_scales, const float *weights,
+                           const int32_t *starts, const int32_t *ends, int32_t *out_blocks, int rows, int keys,
+                           int btopk, void *workspace, size_t workspace_bytes, void *stream,
+                           const mqa_topk_debug_options *opt);
+
 /* mqa_topk_prefill with test-only knobs (opt may be NULL). */
 int mqa_topk_prefill_debug(const void *q, const void *k, const float *key_scales, const float *weights,
                            const int32_t *starts, const int32_t *ends, int32_t *out, int rows, int keys,

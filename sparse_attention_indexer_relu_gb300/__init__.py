@@ -32,6 +32,7 @@ STAT_NAMES = ("status", "rows_rescanned", "compactions", "candidates", "gated_ro
               "kernel_us", "end_spread_us", "split_blocks")
 
 EXPORTS = ("mqa_topk_workspace_bytes", "mqa_topk_workspace_bytes_ex", "mqa_topk_prefill", "mqa_topk_prefill_ex",
+           "mqa_block_topk_prefill",
            "mqa_topk_prefill_debug", "mqa_topk_prefill_noalloc",
            "mqa_ue8m0_decode", "mqa_logits_debug", "mqa_topk_dense_baseline", "mqa_topk_get_status",
            "mqa_topk_strerror")
@@ -67,6 +68,7 @@ def lib():
     L.mqa_topk_prefill.argtypes = common + [I, P, S, P]
     L.mqa_topk_prefill_debug.argtypes = common + [I, P, S, P, ctypes.POINTER(DebugOptions)]
     L.mqa_topk_prefill_ex.argtypes = common + [I, I, P, S, P, ctypes.POINTER(DebugOptions)]
+    L.mqa_block_topk_prefill.argtypes = common + [I, P, S, P, ctypes.POINTER(DebugOptions)]
     L.mqa_topk_prefill_noalloc.argtypes = common + [I, P]
     L.mqa_ue8m0_decode.argtypes = [P, P, I, P]
     L.mqa_logits_debug.argtypes = common + [P, S, P]
@@ -195,6 +197,26 @@ def mqa_topk_prefill(q, k, key_scales, weights, starts, ends, topk: int, workspa
         _check(lib().mqa_topk_prefill_debug(*args, ctypes.byref(opt)), "mqa_topk_prefill_debug")
     else:
         _check(lib().mqa_topk_prefill(*args), "mqa_topk_prefill")
+    return out
+
+
+def mqa_block_topk_prefill(q, k, key_scales, weights, starts, ends, btopk: int, workspace=None, out=None,
+                           stream=None, debug: Optional[dict] = None):
+    """Block selection: each row's btopk best blocks of 8 keys by their largest
+    score, as block index - floor(start / 8); returns out [rows, btopk] int32
+    (unordered, -1 padded)."""
+    torch = _torch()
+    q, k, key_scales, weights, starts, ends, rows, keys = _inputs(q, k, key_scales, weights, starts, ends)
+    if out is None:
+        out = torch.empty((rows, int(btopk)), dtype=torch.int32, device=q.device)
+    out = _as(out, torch.int32, (rows, int(btopk)), "out")
+    if workspace is None:
+        workspace = alloc_workspace(rows, q.device.index)
+    opt = DebugOptions(**{f: int((debug or {}).get(f, 0)) for f, _ in DebugOptions._fields_})
+    _check(lib().mqa_block_topk_prefill(_ptr(q), _ptr(k), _ptr(key_scales), _ptr(weights), _ptr(starts), _ptr(ends),
+                                        _ptr(out), rows, keys, int(btopk), _ptr(workspace),
+                                        workspace.numel() * workspace.element_size(), _stream(stream),
+                                        ctypes.byref(opt)), "mqa_block_topk_prefill")
     return out
 
 

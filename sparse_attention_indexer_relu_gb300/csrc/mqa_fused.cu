@@ -32,7 +32,13 @@
 #include <climits>
 #include <mutex>
 
-#if MQA_HEADS == 64
+#ifndef MQA_BLOCKS
+#define MQA_BLOCKS 0
+#endif
+#if MQA_BLOCKS
+#define MQA_KNS h32b
+static_assert(MQA_HEADS == 32, "block selection is built for 32 heads");
+#elif MQA_HEADS == 64
 #define MQA_KNS h64
 #else
 #define MQA_KNS h32
@@ -42,6 +48,19 @@ namespace mqa {
 namespace MQA_KNS {
 
 constexpr uint32_t kIdesc = idesc_f8_e4m3_f32(kTileKeys, kCols);
+
+// Selection items: keys, or (block selection) blocks of 8 keys ranked by
+// their largest score.  A block b holds keys [8b, 8b + 8) of the key array.
+constexpr bool kBlocks = MQA_BLOCKS != 0;
+// Items a row with visible keys [s, e) selects from.
+__host__ __device__ __forceinline__ int row_items(int s, int e) {
+  if (e <= s) return 0;
+  return kBlocks ? ((e - 1) >> 3) - (s >> 3) + 1 : e - s;
+}
+// Output index of the item whose (first) key is `key`, in a row starting at `base`.
+__device__ __forceinline__ int32_t out_index(int key, int base) {
+  return kBlocks ? (key >> 3) - (base >> 3) : key - base;
+}
 constexpr int kEpiThreads = kEpiWarps * 32;
 constexpr int kEpiBarrier = 1;  // named barrier id for the epilogue warps
 constexpr int kGateBins = 288;  // 257 two-sided distance bins, padded to 9 per lane
@@ -468,7 +487,7 @@ __device__ MQA_SEL_FN int warp_emit(const RowSlab &R, uint32_t T, int take_eq, b
               R.keys[pos] = kk[j];
               R.idx[pos] = ii[j];
             } else {
-              out[pos] = ii[j] - base;
+              out[pos] = out_index(ii[j], base);
             }
           }
         }
@@ -658,7 +677,7 @@ __device__ MQA_SEL_FN int warp_emit_out(const RowSlab &R, uint32_t T, int take_e
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
         if (gt[j] || eq[j]) {
-          if (pos < limit) out[pos] = ii[j] - base;
+          if (pos < limit) out[pos] = out_index(ii[j], base);
           ++pos;
         }
       }
@@ -818,7 +837,7 @@ __device__ MQA_SEL_FN int warp_select_binned(const RowSlab &R, int k, float lo, 
 #pragma unroll
     for (int j = 0; j < 4 * kPass2Groups; ++j) {
       if ((up >> j) & 1u) {
-        if (po < k) out[po] = ii[j] - base;
+        if (po < k) out[po] = out_index(ii[j], base);
         ++po;
       }
       if ((in >> j) & 1u) {
@@ -909,7 +928,7 @@ __device__ MQA_SEL_FN int warp_select_binned(const RowSlab &R, int k, float lo, 
     const bool take = gt || (eq && eq_seen + __popc(eqm & ltm) < w);
     const uint32_t tm = __ballot_sync(0xFFFFFFFFu, take);
     const int pos = outc + __popc(tm & ltm);
-    if (take && pos < k) out[pos] = li[i] - base;
+    if (take && pos < k) out[pos] = out_index(li[i], base);
     outc += __popc(tm);
     eq_seen += __popc(eqm);
   }
@@ -928,10 +947,11 @@ __device__ void plan_split(Smem &S, const FusedParams &p, long long w_light) {
   const int cand = nb < ctas ? nb : (nb % ctas ? min(nb, nb % ctas + ctas) : 0);
   if (cand == 0 || cand > p.split_max) return;
   const long long L = w_light / kBlockRows;  // mean visible keys per row of the lightest block
+  const long long items = kBlocks ? L / 8 : L;  // and the items it selects from
   const long long nt = (L + kTileKeys - 1) / kTileKeys;
   if (nt < 8) return;  // too short to be worth a second sample pass
   float sfrac = 0.f;
-  if (L > p.gate_min) {
+  if (items > p.gate_min) {
     long long want = (32LL * L + (long long)p.gate_target * kTileKeys - 1) / ((long long)p.gate_target * kTileKeys);
     want = want < 4 ? 4 : (want > 64 ? 64 : want);
     sfrac = 2.f * (float)(want < nt ? want : nt) / (float)nt;
@@ -1115,7 +1135,7 @@ __device__ void producer(Smem &S, const CUtensorMap *q_map, const CUtensorMap *k
           J.w[r][h] = r < nrows ? __ldg(p.weights + (size_t)(r0 + r) * kHeads + h) : 0.f;
       // key range: the union of the taking-part rows' ranges
       const bool live = part && e > s;
-      int lo = live ? s : INT_MAX, hi = live ? e : 0, len = live ? e - s : 0;
+      int lo = live ? s : INT_MAX, hi = live ? e : 0, len = live ? row_items(s, e) : 0;
 #pragma unroll
       for (int off = 16; off > 0; off >>= 1) {
         lo = min(lo, __shfl_xor_sync(0xFFFFFFFFu, lo, off));
@@ -1320,7 +1340,7 @@ __device__ void epilogue(Smem &S, uint32_t tmem, const FusedParams &p, int warp,
       ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
       // per-row state for this scan: warp ew owns row ew
       if (gate_warp && lane == 0) {
-        const int n = J.end[ew] - J.start[ew];
+        const int n = row_items(J.start[ew], J.end[ew]);
         float t0 = NEG_INF;
         if (J.ns == 0 && J.mode == 0 && p.force_gate == 1 && n > 0) t0 = INFINITY;
         S.tau[ew] = t0;
@@ -1405,6 +1425,19 @@ __device__ void epilogue(Smem &S, uint32_t tmem, const FusedParams &p, int warp,
           sv[rr] = (act[rr] && key >= J.start[r] && key < J.end[r]) ? raw[rr] : NEG_INF;
         }
       }
+      if constexpr (kBlocks) {
+        // the 8 keys of a block sit in the lanes with the same lane % 4 (key
+        // offset lane / 4 within the block): the block's score is their
+        // largest, kept by the lane holding the block's first key (lane < 4)
+#pragma unroll
+        for (int rr = 0; rr < kRowsPerWarp; ++rr) {
+          float m = sv[rr];
+          m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 4));
+          m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 8));
+          m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 16));
+          sv[rr] = lane < 4 ? m : NEG_INF;
+        }
+      }
       ++tcount;
       return ok;
     };
@@ -1444,7 +1477,7 @@ __device__ void epilogue(Smem &S, uint32_t tmem, const FusedParams &p, int warp,
           // coarse bin of row ew that holds the target sample rank j
           if (gate_warp) {
           const int r = ew;
-          const int n = J.end[r] - J.start[r];
+          const int n = row_items(J.start[r], J.end[r]);
           const int m = S.msample[r];
           int on = 0, above = 0, jw = 0;
           uint32_t klo = 0, khi = 0;
@@ -1712,7 +1745,7 @@ __device__ void epilogue(Smem &S, uint32_t tmem, const FusedParams &p, int warp,
         }
         if (lane < kBlockRows) {
           Q.start[lane] = J.start[lane];
-          Q.n[lane] = J.end[lane] - J.start[lane];
+          Q.n[lane] = row_items(J.start[lane], J.end[lane]);
           Q.gated[lane] = S.tau[lane] > NEG_INF;
           Q.blo[lane] = S.tau[lane];
           Q.binv[lane] = S.binv[lane];
@@ -1959,7 +1992,7 @@ cudaError_t launch_fused_topk(const CUtensorMap &q_map, const CUtensorMap &k_map
   return cudaGetLastError();
 }
 
-#if MQA_HEADS == 32
+#if MQA_HEADS == 32 && !MQA_BLOCKS
 cudaError_t launch_logits(const CUtensorMap &q_map, const CUtensorMap &k_map, const CUtensorMap &s_map,
                           const FusedParams &p, int ctas, cudaStream_t stream) {
   static cudaError_t attr = set_smem_attr((const void *)mqa_fused_kernel<true>);
@@ -1971,7 +2004,7 @@ cudaError_t launch_logits(const CUtensorMap &q_map, const CUtensorMap &k_map, co
 
 }  // namespace MQA_KNS
 
-#if MQA_HEADS == 32
+#if MQA_HEADS == 32 && !MQA_BLOCKS
 // ------------------------------------------------------------------ allocation-free scratch
 // Scratch for mqa_topk_prefill_noalloc: the 256-byte header plus the candidate
 // slabs of at most kStaticScratchCtas persistent CTAs, as a file-scope device

@@ -112,6 +112,10 @@ namespace h64 {
 cudaError_t launch_fused_topk(const CUtensorMap &q_map, const CUtensorMap &k_map, const CUtensorMap &s_map,
                               const FusedParams &p, int ctas, cudaStream_t stream);
 }  // namespace h64
+namespace h32b {  // block selection: top blocks of 8 keys by their largest score
+cudaError_t launch_fused_topk(const CUtensorMap &q_map, const CUtensorMap &k_map, const CUtensorMap &s_map,
+                              const FusedParams &p, int ctas, cudaStream_t stream);
+}  // namespace h32b
 cudaError_t launch_ue8m0_decode(const uint8_t *scales, float *out, int keys, cudaStream_t stream);
 cudaError_t launch_dense_topk_rows(const float *logits, int rows, int keys, const int32_t *starts,
                                    const int32_t *ends, int32_t *out, int topk, int32_t *ws_status,

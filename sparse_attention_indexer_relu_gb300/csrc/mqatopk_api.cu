@@ -172,10 +172,10 @@ cudaStream_t as_stream(void *s) { return reinterpret_cast<cudaStream_t>(s); }
 
 int run_fused(const void *q, const void *k, const float *scales, const float *weights, const int32_t *starts,
               const int32_t *ends, int32_t *out, int rows, int keys, int topk, int heads, void *workspace,
-              size_t workspace_bytes, void *stream, const mqa_topk_debug_options *opt) {
+              size_t workspace_bytes, void *stream, const mqa_topk_debug_options *opt, bool blocks = false) {
   int rc = check_common(q, k, scales, weights, starts, ends, out, rows, keys);
   if (rc != MQA_OK) return rc;
-  if (!valid_topk(topk) || (heads != 32 && heads != 64)) return MQA_ERR_INVALID_ARGUMENT;
+  if (!valid_topk(topk) || (heads != 32 && heads != 64) || (blocks && heads != 32)) return MQA_ERR_INVALID_ARGUMENT;
   const int brows = block_rows(heads);
   if (!workspace) return MQA_ERR_INVALID_ARGUMENT;
   if (!aligned(workspace, 256)) return MQA_ERR_MISALIGNED;
@@ -246,8 +246,9 @@ int run_fused(const void *q, const void *k, const float *scales, const float *we
     cudaGetLastError();
     return MQA_ERR_CUDA;
   }
-  const cudaError_t le =
-      heads == 64 ? h64::launch_fused_topk(qm, km, sm, p, ctas, st) : h32::launch_fused_topk(qm, km, sm, p, ctas, st);
+  const cudaError_t le = blocks ? h32b::launch_fused_topk(qm, km, sm, p, ctas, st)
+                         : heads == 64 ? h64::launch_fused_topk(qm, km, sm, p, ctas, st)
+                                       : h32::launch_fused_topk(qm, km, sm, p, ctas, st);
   if (le != cudaSuccess) return MQA_ERR_CUDA;
   return MQA_OK;
 }
@@ -325,6 +326,14 @@ int mqa_topk_prefill_debug(const void *q, const void *k, const float *key_scales
                            const mqa_topk_debug_options *opt) {
   return run_fused(q, k, key_scales, weights, starts, ends, out, rows, keys, topk, 32, workspace, workspace_bytes,
                    stream, opt);
+}
+
+int mqa_block_topk_prefill(const void *q, const void *k, const float *key_scales, const float *weights,
+                           const int32_t *starts, const int32_t *ends, int32_t *out_blocks, int rows, int keys,
+                           int btopk, void *workspace, size_t workspace_bytes, void *stream,
+                           const mqa_topk_debug_options *opt) {
+  return run_fused(q, k, key_scales, weights, starts, ends, out_blocks, rows, keys, btopk, 32, workspace,
+                   workspace_bytes, stream, opt, true);
 }
 
 int mqa_topk_prefill_ex(const void *q, const void *k, const float *key_scales, const float *weights,

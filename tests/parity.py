@@ -68,3 +68,47 @@ def check_logits_rows(got, p, rows, scores):
             if err > tol:
                 bad.append((r, f"max err {err:.3g} > {tol:.3g}"))
     return bad
+
+
+def block_scores(scores_row, s, e):
+    """Block scores of a row: the largest oracle score over its visible keys in
+    each block of 8 keys, blocks floor(s/8) .. floor((e-1)/8)."""
+    if e <= s:
+        return np.zeros(0)
+    b0 = s // 8
+    nb = (e - 1) // 8 - b0 + 1
+    out = np.full(nb, -np.inf)
+    keys = np.arange(s, e)
+    np.maximum.at(out, keys // 8 - b0, scores_row[s:e])
+    return out
+
+
+def check_block_rows(got, p, rows, scores, btopk):
+    """got: [len(rows), btopk] block indices relative to floor(start/8) (GPU);
+    scores: oracle fp64 key scores.  Same rule as check_topk_rows, on blocks."""
+    bad = []
+    for i, r in enumerate(rows):
+        s, e = int(p.starts[r]), int(p.ends[r])
+        bs = block_scores(scores[i], s, e)
+        n = len(bs)
+        c = min(btopk, n)
+        g = got[i]
+        if not np.all(g[c:] == -1):
+            bad.append((r, "padding"))
+            continue
+        sel = g[:c]
+        if np.any(sel < 0) or np.any(sel >= n) or len(np.unique(sel)) != c:
+            bad.append((r, "indices"))
+            continue
+        if n <= btopk:
+            if set(sel.tolist()) != set(range(n)):
+                bad.append((r, "short row set"))
+            continue
+        tol = TOPK_TIE_TOL * np.max(np.abs(bs))
+        order = np.argsort(-bs, kind="stable")
+        kth = bs[order[c - 1]]
+        diff = set(order[:c].tolist()) ^ set(sel.tolist())
+        worst = max((abs(bs[j] - kth) for j in diff), default=0.0)
+        if worst > tol:
+            bad.append((r, f"tie rule: {len(diff)} blocks differ, worst |B-kth| = {worst:.3g} > {tol:.3g}"))
+    return bad

@@ -4,7 +4,7 @@ import pytest
 
 import oracle
 import synth
-from parity import check_logits_rows, check_topk_rows, to_device
+from parity import check_block_rows, check_logits_rows, check_topk_rows, to_device
 
 pytestmark = pytest.mark.gpu
 
@@ -202,6 +202,49 @@ def test_fused_64_heads_gated_split(mqa):
     assert status == 0, stats
     assert stats["gated_rows"] == 16 and stats["split_blocks"] == 4, stats
     assert_parity(p, got)
+
+
+def run_blocks(mqa, p, btopk, debug=None):
+    q, k, sc, w, s, e = to_device(p)
+    ws = mqa.alloc_workspace(p.rows)
+    out = mqa.mqa_block_topk_prefill(q, k, sc, w, s, e, btopk, workspace=ws, debug=debug)
+    status, stats = mqa.get_status(ws)
+    return out.cpu().numpy(), status, stats
+
+
+def assert_block_parity(p, got, btopk):
+    rows = np.arange(p.rows)
+    _, scores = oracle.run(p, rows=rows, want_topk=False, want_scores=True)
+    bad = check_block_rows(got, p, rows, scores, btopk)
+    assert not bad, bad[:10]
+
+
+@pytest.mark.parametrize("seed,rows,keys,btopk", [(50, 5, 900, 512), (51, 19, 9000, 512), (52, 33, 30000, 1024)])
+def test_block_selection_random_ranges(mqa, seed, rows, keys, btopk):
+    """Top blocks of 8 keys by their largest score, arbitrary ranges."""
+    p = synth.random_small(seed, rows, keys, 512)
+    got, status, stats = run_blocks(mqa, p, btopk)
+    assert status == 0, stats
+    assert_block_parity(p, got, btopk)
+
+
+def test_block_selection_gated_split(mqa):
+    """Long causal rows: the gate samples block scores, key chunks of a split
+    block are merged, the top 2048 blocks are exact up to ties."""
+    p = _causal(synth.random_small(53, 16, 200000, 2048, empty_frac=0.0), 200000)
+    got, status, stats = run_blocks(mqa, p, 2048)
+    assert status == 0, stats
+    assert stats["gated_rows"] == 16 and stats["rows_rescanned"] == 0, stats
+    assert_block_parity(p, got, 2048)
+
+
+def test_block_selection_forced_rescan(mqa):
+    """Gate forced to +inf: every row under-fills and is rescanned exactly."""
+    p = synth.random_small(54, 12, 40000, 512, empty_frac=0.0)
+    got, status, stats = run_blocks(mqa, p, 512, debug={"force_gate": 1})
+    assert status == 0, stats
+    assert stats["rows_rescanned"] > 0
+    assert_block_parity(p, got, 512)
 
 
 def test_fused_single_cta(mqa):
