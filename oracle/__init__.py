@@ -47,6 +47,9 @@ def load_library(path: str):
     lib.oracle_run_blocks.argtypes = [P, P, P, P, P, P, P, ctypes.c_int64, ctypes.c_int64,
                                       ctypes.c_int, ctypes.c_int, ctypes.c_int, P, ctypes.c_int]
     lib.oracle_run_blocks.restype = ctypes.c_int
+    lib.oracle_run_masked.argtypes = [P, P, P, P, P, P, P, ctypes.c_int64, ctypes.c_int64, ctypes.c_int, ctypes.c_int,
+                                      ctypes.c_int, P, ctypes.c_int64, P, P, ctypes.c_int]
+    lib.oracle_run_masked.restype = ctypes.c_int
     return lib
 
 
@@ -141,6 +144,31 @@ def run_blocks(p, btopk, rows=None, nthreads=None, lib=None):
     if rc != 0:
         raise ValueError(f"oracle_run_blocks failed with status {rc}")
     return out
+
+
+def run_masked(p, mask, rows=None, want_topk=True, want_scores=False, topk=None, nthreads=None, lib=None):
+    """Masked selection: mask [rows, words] uint32, bit (j / 8) % 32 of word
+    j / 256 allows key j for the row.  Returns (indices, scores) as `run`."""
+    q = _c(p.q, np.uint8)
+    k = _c(p.k, np.uint8)
+    g = _c(p.scales_ue8m0, np.uint8)
+    w = _c(p.weights, np.float32)
+    s = _c(p.starts, np.int32)
+    e = _c(p.ends, np.int32)
+    m = _c(mask, np.uint32)
+    rows = np.arange(q.shape[0], dtype=np.int64) if rows is None else _c(rows, np.int64)
+    topk = int(p.topk if topk is None else topk)
+    n = rows.shape[0]
+    out = np.empty((n, topk), np.int32) if want_topk else None
+    scores = np.empty((n, k.shape[0]), np.float64) if want_scores else None
+    rc = _load(lib).oracle_run_masked(_ptr(q), _ptr(k), _ptr(g), _ptr(w), _ptr(s), _ptr(e), _ptr(rows), n,
+                                      k.shape[0], q.shape[1], q.shape[2], topk, _ptr(m), m.shape[1],
+                                      _ptr(out) if out is not None else None,
+                                      _ptr(scores) if scores is not None else None,
+                                      int(nthreads or default_threads()))
+    if rc != 0:
+        raise ValueError(f"oracle_run_masked failed with status {rc}")
+    return out, scores
 
 
 def topk(p, rows=None, nthreads=None, lib=None):

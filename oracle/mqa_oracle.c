@@ -31,6 +31,11 @@
  *    keys [8b, 8b + 8) of the key array; its score is the largest S over the
  *    row's visible keys in it.  The output lists the chosen blocks as
  *    b - floor(start / 8), ties by block index ascending, -1 padded.
+ *  - Masked selection (the consumer layers of the same two-level selection
+ *    mask their scores to the source's blocks before their top-k): a key j of
+ *    row r is visible only if it lies in [start, end) and bit (j / 8) % 32 of
+ *    word j / 256 of row r's block mask is set; the selection is then the
+ *    one above over the visible keys.
  *
  * Arithmetic: every e4m3 value is an integer multiple of 2^-9 with magnitude
  * at most 448, so each q.k product is a multiple of 2^-18 below 2^18 and a
@@ -145,6 +150,8 @@ typedef struct {
     int32_t *out;           /* [nlist, topk] */
     double *scores_out;     /* optional [nlist, keys] dense scores (-inf outside) */
     int block_mode;         /* select blocks of 8 keys by their largest score */
+    const uint32_t *mask;   /* optional [rows, mask_words] block mask (masked selection) */
+    int64_t mask_words;
     int64_t next;           /* shared work counter */
     pthread_mutex_t lock;
     int status;
@@ -182,23 +189,29 @@ static void *worker(void *arg) {
             buf = (scored_key *)malloc(sizeof(scored_key) * (size_t)cap);
             if (!buf) { J->status = -1; free(qd); return NULL; }
         }
+        int64_t nv = 0; /* visible keys written to buf */
         for (int64_t t = 0; t < n; ++t) {
             int64_t j = s + t;
+            if (J->mask) {
+                const uint32_t word = J->mask[r * J->mask_words + (j >> 8)];
+                if (!((word >> ((j >> 3) & 31)) & 1u)) continue;
+            }
             uint32_t bits = ((uint32_t)J->scale_groups[4 * j]) << 23;
             float sc;
             memcpy(&sc, &bits, sizeof sc);
             double v = score_pair(qd, J->k, J->heads, J->dim, J->w + r * J->heads, (double)sc, j);
-            if (buf) { buf[t].score = v; buf[t].key = j; }
+            if (buf) { buf[nv].score = v; buf[nv].key = j; }
+            ++nv;
             if (J->scores_out) J->scores_out[i * J->keys + j] = v;
         }
         if (J->out && J->block_mode) {
-            /* blocks [s / 8, (e - 1) / 8]; buf holds keys s .. e - 1 in order */
+            /* blocks [s / 8, (e - 1) / 8]; buf holds the row's visible keys */
             int64_t b0 = s >> 3, nb = n > 0 ? ((e - 1) >> 3) - b0 + 1 : 0;
             scored_block *blk = nb > 0 ? (scored_block *)malloc(sizeof(scored_block) * (size_t)nb) : NULL;
             if (nb > 0 && !blk) { J->status = -1; break; }
             for (int64_t b = 0; b < nb; ++b) { blk[b].score = -INFINITY; blk[b].block = b0 + b; }
-            for (int64_t t = 0; t < n; ++t) {
-                int64_t b = ((s + t) >> 3) - b0;
+            for (int64_t t = 0; t < nv; ++t) {
+                int64_t b = (buf[t].key >> 3) - b0;
                 if (buf[t].score > blk[b].score) blk[b].score = buf[t].score;
             }
             if (nb > 0) qsort(blk, (size_t)nb, sizeof(scored_block), cmp_block);
@@ -208,8 +221,8 @@ static void *worker(void *arg) {
             for (int64_t t = c; t < J->topk; ++t) o[t] = -1;
             free(blk);
         } else if (J->out) {
-            if (n > 0) qsort(buf, (size_t)n, sizeof(scored_key), cmp_scored);
-            int64_t c = n < J->topk ? n : J->topk;
+            if (nv > 0) qsort(buf, (size_t)nv, sizeof(scored_key), cmp_scored);
+            int64_t c = nv < J->topk ? nv : J->topk;
             int32_t *o = J->out + i * J->topk;
             for (int64_t t = 0; t < c; ++t) o[t] = (int32_t)(buf[t].key - s);
             for (int64_t t = c; t < J->topk; ++t) o[t] = -1;
@@ -249,7 +262,7 @@ static int run_mode(const uint8_t *q, const uint8_t *k, const uint8_t *scale_gro
                     const float *w, const int32_t *starts, const int32_t *ends,
                     const int64_t *row_list, int64_t nlist, int64_t keys,
                     int heads, int dim, int topk, int32_t *out, double *scores, int nthreads,
-                    int block_mode) {
+                    int block_mode, const uint32_t *mask, int64_t mask_words) {
     if (dim > 1024 || heads < 1 || dim < 1 || (out && topk < 1)) return -2;
     for (int64_t i = 0; i < nlist; ++i) {
         int64_t r = row_list[i];
@@ -261,6 +274,7 @@ static int run_mode(const uint8_t *q, const uint8_t *k, const uint8_t *scale_gro
     J.starts = starts; J.ends = ends; J.row_list = row_list; J.nlist = nlist;
     J.keys = keys; J.heads = heads; J.dim = dim; J.topk = topk > 0 ? topk : 1;
     J.out = out; J.scores_out = scores; J.block_mode = block_mode;
+    J.mask = mask; J.mask_words = mask_words;
     return run_jobs(&J, nthreads);
 }
 
@@ -269,7 +283,20 @@ int oracle_run(const uint8_t *q, const uint8_t *k, const uint8_t *scale_groups,
                const int64_t *row_list, int64_t nlist, int64_t keys,
                int heads, int dim, int topk, int32_t *out, double *scores, int nthreads) {
     return run_mode(q, k, scale_groups, w, starts, ends, row_list, nlist, keys, heads, dim, topk,
-                    out, scores, nthreads, 0);
+                    out, scores, nthreads, 0, NULL, 0);
+}
+
+/* Masked selection (see the header): mask [rows, mask_words] indexed by the
+ * row's position in q, mask_words >= ceil(keys / 256).  out and scores as
+ * oracle_run, scores of masked keys are -inf. */
+int oracle_run_masked(const uint8_t *q, const uint8_t *k, const uint8_t *scale_groups,
+                      const float *w, const int32_t *starts, const int32_t *ends,
+                      const int64_t *row_list, int64_t nlist, int64_t keys,
+                      int heads, int dim, int topk, const uint32_t *mask, int64_t mask_words,
+                      int32_t *out, double *scores, int nthreads) {
+    if (!mask || mask_words * 256 < keys) return -2;
+    return run_mode(q, k, scale_groups, w, starts, ends, row_list, nlist, keys, heads, dim, topk,
+                    out, scores, nthreads, 0, mask, mask_words);
 }
 
 /* Top `btopk` blocks of 8 keys per listed row by block score (see the header):
@@ -280,5 +307,5 @@ int oracle_run_blocks(const uint8_t *q, const uint8_t *k, const uint8_t *scale_g
                       int heads, int dim, int btopk, int32_t *out_blocks, int nthreads) {
     if (!out_blocks) return -2;
     return run_mode(q, k, scale_groups, w, starts, ends, row_list, nlist, keys, heads, dim, btopk,
-                    out_blocks, NULL, nthreads, 1);
+                    out_blocks, NULL, nthreads, 1, NULL, 0);
 }

@@ -38,6 +38,8 @@ MUTANTS = {
                            "blk[b].score = buf[t].score;"),
     "block_order": ("if (x->score > y->score) return -1;\n    if (x->score < y->score) return 1;\n    return (x->block",
                     "if (x->score > y->score) return 1;\n    if (x->score < y->score) return -1;\n    return (x->block"),
+    "mask_bit_index": ("if (!((word >> ((j >> 3) & 31)) & 1u)) continue;", "if (!((word >> ((j >> 4) & 31)) & 1u)) continue;"),
+    "mask_ignored": ("            if (J->mask) {", "            if (0) {"),
     "ue8m0_shift": ("uint32_t bits = ((uint32_t)J->scale_groups[4 * j]) << 23;",
                     "uint32_t bits = ((uint32_t)J->scale_groups[4 * j + 1] + 1) << 23;"),
 }

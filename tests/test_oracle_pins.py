@@ -417,3 +417,73 @@ def test_blocks_integer_bruteforce_tiny(lib=None):
         got = oracle.run_blocks(p, 5, lib=lib)[0]
         assert got[:len(want)].tolist() == want
         assert np.all(got[len(want):] == -1)
+
+
+# ----------------------------------------------------------------------------
+# masked selection (the consumer half of the two-level selection)
+
+def random_block_mask(rng, rows, keys, frac):
+    words = (keys + 255) // 256
+    bits = rng.random((rows, words * 32)) < frac
+    return np.packbits(bits.reshape(rows, words, 32)[:, :, ::-1], axis=-1).view(">u4").reshape(rows, words) \
+        .astype(np.uint32)
+
+
+def allowed_keys(mask_row, keys):
+    j = np.arange(keys)
+    return ((mask_row[j >> 8] >> ((j >> 3) & 31)) & 1).astype(bool)
+
+
+def test_masked_full_mask_is_unmasked(lib=None):
+    p = tiny_problem(60, 9, 2000, 64)
+    full = np.full((p.rows, (p.keys + 255) // 256), 0xFFFFFFFF, np.uint32)
+    a, _ = oracle.run_masked(p, full, lib=lib)
+    b, _ = oracle.run(p, lib=lib)
+    assert np.array_equal(a, b)
+
+
+@pytest.mark.parametrize("frac", [0.1, 0.6])
+def test_masked_matches_numpy_formulation(frac, lib=None):
+    """Allowed keys from an independent bit decode, scores from the numpy
+    formulation: the masked selection is the top-k over the allowed keys."""
+    rng = np.random.default_rng(61)
+    p = tiny_problem(61, 10, 2500, 48)
+    mask = random_block_mask(rng, p.rows, p.keys, frac)
+    idx, _ = oracle.run_masked(p, mask, lib=lib)
+    sc = numpy_scores(p)
+    for r in range(p.rows):
+        s, e = int(p.starts[r]), int(p.ends[r])
+        allow = allowed_keys(mask[r], p.keys)
+        vis = np.full(p.keys, -np.inf)
+        vis[allow] = sc[r][allow]
+        keep = np.nonzero(allow[s:e])[0]            # visible relative indices
+        c = min(48, len(keep))
+        sel = idx[r][:c]
+        assert np.all(idx[r][c:] == -1)
+        assert set(sel.tolist()) <= set(keep.tolist()) and len(np.unique(sel)) == c
+        if 0 < c < len(keep):
+            rest = np.setdiff1d(keep, sel)
+            assert vis[s + sel].min() >= vis[s + rest].max() - 1e-9 * (1 + np.abs(sc[r][np.isfinite(sc[r])]).max())
+
+
+def test_masked_integer_bruteforce_tiny(lib=None):
+    def dec(c):
+        s, e, m = (c >> 7) & 1, (c >> 3) & 15, c & 7
+        v = (m if e == 0 else (8 + m) << (e - 1))
+        return -v if s else v
+    rng = np.random.default_rng(62)
+    for trial in range(20):
+        keys = int(rng.integers(20, 120))
+        p = tiny_problem(300 + trial, 1, keys, 6, heads=1, dim=4)
+        p.weights[:] = 1.0
+        p.scales_ue8m0[:] = 127
+        p.starts[:] = 0
+        p.ends[:] = keys
+        mask = random_block_mask(rng, 1, keys, 0.5)
+        allow = allowed_keys(mask[0], keys)
+        qd = [dec(int(c)) for c in p.q[0, 0]]
+        score = {j: max(0, sum(a * dec(int(b)) for a, b in zip(qd, p.k[j]))) for j in range(keys) if allow[j]}
+        want = sorted(score, key=lambda j: (-score[j], j))[:6]
+        got, _ = oracle.run_masked(p, mask, topk=6, lib=lib)
+        assert got[0][:len(want)].tolist() == want
+        assert np.all(got[0][len(want):] == -1)
