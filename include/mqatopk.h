@@ -161,6 +161,30 @@ int mqa_block_topk_prefill(const void *q, const void *k, const float *key_scales
                            int btopk, void *workspace, size_t workspace_bytes, void *stream,
                            const mqa_topk_debug_options *opt);
 
+/* Masked selection, the consumer half of the two-level candidate selection
+ * (PR #60618, "Limitations of this PR -- TODOs": consumer layers mask their
+ * scores to the source layer's blocks before their top-k).  As
+ * mqa_topk_prefill, but key j of row r is visible only if it lies in
+ * [starts[r], ends[r]) and bit (j / 8) % 32 of word j / 256 of mask row r is
+ * set.
+ *  mask       [rows, mask_words] uint32, 16-byte aligned; mask_words a multiple
+ *             of 4 and >= ceil(keys / 256)
+ *  row_items  [rows] int32: the number of visible keys of each row (it sizes
+ *             the row's sampled gate); mqa_block_mask writes it
+ * 32 heads; workspace as for mqa_topk_prefill. */
+int mqa_topk_prefill_masked(const void *q, const void *k, const float *key_scales, const float *weights,
+                            const int32_t *starts, const int32_t *ends, const uint32_t *mask, int mask_words,
+                            const int32_t *row_items, int32_t *out, int rows, int keys, int topk, void *workspace,
+                            size_t workspace_bytes, void *stream, const mqa_topk_debug_options *opt);
+
+/* Build the block mask of mqa_topk_prefill_masked from per-row block lists
+ * (block_lists [rows, list_len] int32, entries relative to floor(starts[r] /
+ * 8) as mqa_block_topk_prefill writes them, -1 or out-of-range entries
+ * ignored), and count each row's visible keys into row_items [rows].  One
+ * launch on `stream`; mask and row_items are overwritten. */
+int mqa_block_mask(const int32_t *block_lists, const int32_t *starts, const int32_t *ends, int rows, int list_len,
+                   int keys, uint32_t *mask, int mask_words, int32_t *row_items, void *stream);
+
 /* mqa_topk_prefill with test-only knobs (opt may be NULL). */
 int mqa_topk_prefill_debug(const void *q, const void *k, const float *key_scales, const float *weights,
                            const int32_t *starts, const int32_t *ends, int32_t *out, int rows, int keys,

@@ -32,7 +32,7 @@ STAT_NAMES = ("status", "rows_rescanned", "compactions", "candidates", "gated_ro
               "kernel_us", "end_spread_us", "split_blocks")
 
 EXPORTS = ("mqa_topk_workspace_bytes", "mqa_topk_workspace_bytes_ex", "mqa_topk_prefill", "mqa_topk_prefill_ex",
-           "mqa_block_topk_prefill",
+           "mqa_block_topk_prefill", "mqa_topk_prefill_masked", "mqa_block_mask",
            "mqa_topk_prefill_debug", "mqa_topk_prefill_noalloc",
            "mqa_ue8m0_decode", "mqa_logits_debug", "mqa_topk_dense_baseline", "mqa_topk_get_status",
            "mqa_topk_strerror")
@@ -69,6 +69,8 @@ def lib():
     L.mqa_topk_prefill_debug.argtypes = common + [I, P, S, P, ctypes.POINTER(DebugOptions)]
     L.mqa_topk_prefill_ex.argtypes = common + [I, I, P, S, P, ctypes.POINTER(DebugOptions)]
     L.mqa_block_topk_prefill.argtypes = common + [I, P, S, P, ctypes.POINTER(DebugOptions)]
+    L.mqa_topk_prefill_masked.argtypes = [P, P, P, P, P, P, P, I, P, P, I, I, I, P, S, P, ctypes.POINTER(DebugOptions)]
+    L.mqa_block_mask.argtypes = [P, P, P, I, I, I, P, I, P, P]
     L.mqa_topk_prefill_noalloc.argtypes = common + [I, P]
     L.mqa_ue8m0_decode.argtypes = [P, P, I, P]
     L.mqa_logits_debug.argtypes = common + [P, S, P]
@@ -217,6 +219,40 @@ def mqa_block_topk_prefill(q, k, key_scales, weights, starts, ends, btopk: int, 
                                         _ptr(out), rows, keys, int(btopk), _ptr(workspace),
                                         workspace.numel() * workspace.element_size(), _stream(stream),
                                         ctypes.byref(opt)), "mqa_block_topk_prefill")
+    return out
+
+
+def block_mask(block_lists, starts, ends, keys: int, mask_words: Optional[int] = None, stream=None):
+    """Per-row block mask (and visible-key counts) from block lists [rows, L]
+    int32 relative to floor(start / 8): returns (mask [rows, words] uint32,
+    row_items [rows] int32)."""
+    torch = _torch()
+    rows, L = int(block_lists.shape[0]), int(block_lists.shape[1])
+    words = mask_words or ((int(keys) + 1023) // 1024) * 4
+    lists = _as(block_lists, torch.int32, (rows, L), "block_lists")
+    mask = torch.empty((rows, words), dtype=torch.int32, device=lists.device)
+    items = torch.empty(rows, dtype=torch.int32, device=lists.device)
+    _check(lib().mqa_block_mask(_ptr(lists), _ptr(starts), _ptr(ends), rows, L, int(keys), _ptr(mask), words,
+                                _ptr(items), _stream(stream)), "mqa_block_mask")
+    return mask, items
+
+
+def mqa_topk_prefill_masked(q, k, key_scales, weights, starts, ends, mask, row_items, topk: int, workspace=None,
+                            out=None, stream=None, debug: Optional[dict] = None):
+    """Top-k over the keys each row's block mask allows (see block_mask)."""
+    torch = _torch()
+    q, k, key_scales, weights, starts, ends, rows, keys = _inputs(q, k, key_scales, weights, starts, ends)
+    if out is None:
+        out = torch.empty((rows, int(topk)), dtype=torch.int32, device=q.device)
+    out = _as(out, torch.int32, (rows, int(topk)), "out")
+    if workspace is None:
+        workspace = alloc_workspace(rows, q.device.index)
+    opt = DebugOptions(**{f: int((debug or {}).get(f, 0)) for f, _ in DebugOptions._fields_})
+    _check(lib().mqa_topk_prefill_masked(_ptr(q), _ptr(k), _ptr(key_scales), _ptr(weights), _ptr(starts),
+                                         _ptr(ends), _ptr(mask), int(mask.shape[1]), _ptr(row_items), _ptr(out),
+                                         rows, keys, int(topk), _ptr(workspace),
+                                         workspace.numel() * workspace.element_size(), _stream(stream),
+                                         ctypes.byref(opt)), "mqa_topk_prefill_masked")
     return out
 
 

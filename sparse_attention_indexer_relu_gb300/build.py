@@ -16,10 +16,11 @@ CSRC = os.path.join(HERE, "csrc")
 OUT_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(OUT_DIR, "libmqatopk.so")
 # (source, object, extra flags): the fused kernel is compiled once per head
-# count (32 and 64 index heads per query row), and once more for block
-# selection (top blocks of 8 keys).
+# count (32 and 64 index heads per query row), and once each for block
+# selection (top blocks of 8 keys) and masked selection.
 SOURCES = [("mqa_fused.cu", "mqa_fused.o", []), ("mqa_fused.cu", "mqa_fused_h64.o", ["-DMQA_HEADS=64"]),
            ("mqa_fused.cu", "mqa_fused_blocks.o", ["-DMQA_BLOCKS=1"]),
+           ("mqa_fused.cu", "mqa_fused_masked.o", ["-DMQA_MASKED=1"]),
            ("mqa_aux.cu", "mqa_aux.o", []), ("mqatopk_api.cu", "mqatopk_api.o", [])]
 HEADERS = ["mqa_internal.h", "ptx.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

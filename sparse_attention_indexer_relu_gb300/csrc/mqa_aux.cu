@@ -149,4 +149,50 @@ cudaError_t launch_dense_topk_rows(const float *logits, int rows, int keys, cons
   return cudaGetLastError();
 }
 
+// ------------------------------------------------------------------ block masks
+// Masked selection takes, per row, a bit mask over the blocks of 8 keys of the
+// key array (bit b % 32 of word b / 32 allows keys [8b, 8b + 8)).  This kernel
+// builds it from the candidate-source layer's block lists (block indices
+// relative to floor(start / 8), -1 for none; the consumer layers of the
+// two-level selection mask their scores to those blocks: vLLM pull request
+// #60618, "Limitations of this PR -- TODOs") and counts each row's allowed
+// keys inside [start, end), which sizes the row's gate.  One CTA per row.
+__global__ void __launch_bounds__(256) block_mask_kernel(const int32_t *__restrict__ lists,
+                                                         const int32_t *__restrict__ starts,
+                                                         const int32_t *__restrict__ ends, int list_len, int keys,
+                                                         uint32_t *__restrict__ mask, int mask_words,
+                                                         int32_t *__restrict__ row_items) {
+  __shared__ int partial[8];
+  const int r = blockIdx.x;
+  uint32_t *m = mask + (size_t)r * mask_words;
+  for (int w = threadIdx.x; w < mask_words; w += blockDim.x) m[w] = 0u;
+  __syncthreads();
+  const int s = max(__ldg(starts + r), 0), e = max(s, min(__ldg(ends + r), keys));
+  const int b0 = s >> 3, blast = e > s ? (e - 1) >> 3 : b0 - 1;
+  int cnt = 0;
+  for (int i = threadIdx.x; i < list_len; i += blockDim.x) {
+    const int rel = __ldg(lists + (size_t)r * list_len + i);
+    if (rel < 0 || rel > blast - b0) continue;
+    const int b = b0 + rel;
+    const uint32_t bit = 1u << (b & 31);
+    if (!(atomicOr(&m[b >> 5], bit) & bit)) cnt += min(e, 8 * b + 8) - max(s, 8 * b);  // first setter counts
+  }
+  cnt = __reduce_add_sync(0xFFFFFFFFu, cnt);
+  if ((threadIdx.x & 31) == 0) partial[threadIdx.x >> 5] = cnt;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int t = 0;
+    for (int i = 0; i < (int)(blockDim.x >> 5); ++i) t += partial[i];
+    row_items[r] = t;
+  }
+}
+
+cudaError_t launch_block_mask(const int32_t *lists, const int32_t *starts, const int32_t *ends, int rows,
+                              int list_len, int keys, uint32_t *mask, int mask_words, int32_t *row_items,
+                              cudaStream_t stream) {
+  if (rows <= 0) return cudaSuccess;
+  block_mask_kernel<<<rows, 256, 0, stream>>>(lists, starts, ends, list_len, keys, mask, mask_words, row_items);
+  return cudaGetLastError();
+}
+
 }  // namespace mqa

@@ -35,9 +35,15 @@
 #ifndef MQA_BLOCKS
 #define MQA_BLOCKS 0
 #endif
+#ifndef MQA_MASKED
+#define MQA_MASKED 0
+#endif
 #if MQA_BLOCKS
 #define MQA_KNS h32b
-static_assert(MQA_HEADS == 32, "block selection is built for 32 heads");
+static_assert(MQA_HEADS == 32 && !MQA_MASKED, "block selection is built for 32 heads");
+#elif MQA_MASKED
+#define MQA_KNS h32m
+static_assert(MQA_HEADS == 32, "masked selection is built for 32 heads");
 #elif MQA_HEADS == 64
 #define MQA_KNS h64
 #else
@@ -52,6 +58,9 @@ constexpr uint32_t kIdesc = idesc_f8_e4m3_f32(kTileKeys, kCols);
 // Selection items: keys, or (block selection) blocks of 8 keys ranked by
 // their largest score.  A block b holds keys [8b, 8b + 8) of the key array.
 constexpr bool kBlocks = MQA_BLOCKS != 0;
+// Masked selection: a key is visible only if its block of 8 is set in the
+// row's block mask (bit (j / 8) % 32 of word j / 256).
+constexpr bool kMasked = MQA_MASKED != 0;
 // Items a row with visible keys [s, e) selects from.
 __host__ __device__ __forceinline__ int row_items(int s, int e) {
   if (e <= s) return 0;
@@ -79,6 +88,7 @@ struct JobInfo {
   int bs;         // split block index (its arrays in the split workspace)
   int s_lo_t, s_nt;  // tiles [s_lo_t, s_lo_t + s_nt) the sample plan spans (the whole block)
   int start[kBlockRows], end[kBlockRows];
+  int items[kBlockRows];  // items each row selects from (keys, blocks, or allowed keys)
   alignas(16) float w[kBlockRows][kHeads];
 };
 
@@ -99,6 +109,7 @@ struct Smem {
   alignas(1024) uint8_t kring[kKStages][kKTileBytes];
   alignas(1024) uint8_t q[2][kQBytes];
   alignas(128) float sring[kSStages][kTileKeys];  // key scales of the tiles in flight
+  alignas(16) uint32_t mring[kSStages][kBlockRows][4];  // block-mask words of the tiles in flight (masked)
   JobInfo job[2];
   SelSlot sel[2];
   float tau[kBlockRows];
@@ -1022,6 +1033,7 @@ __device__ __forceinline__ int sample_tile(const JobInfo &J, int u) {
 // ------------------------------------------------------------------ producer (warp 0)
 template <bool kLogits>
 __device__ void producer(Smem &S, const CUtensorMap *q_map, const CUtensorMap *k_map, const CUtensorMap *s_map,
+                         const CUtensorMap *m_map,
                          const FusedParams &p, int lane) {
   const uint64_t pol_k = policy_evict_last(), pol_q = policy_evict_first();
   // claim order: whole blocks, then nsplit blocks as nchunks consecutive key chunks each
@@ -1135,7 +1147,10 @@ __device__ void producer(Smem &S, const CUtensorMap *q_map, const CUtensorMap *k
           J.w[r][h] = r < nrows ? __ldg(p.weights + (size_t)(r0 + r) * kHeads + h) : 0.f;
       // key range: the union of the taking-part rows' ranges
       const bool live = part && e > s;
-      int lo = live ? s : INT_MAX, hi = live ? e : 0, len = live ? row_items(s, e) : 0;
+      int items = row_items(s, e);
+      if (kMasked && lane < kBlockRows && lane < nrows) items = max(0, min(items, __ldg(p.row_items + r0 + lane)));
+      if (lane < kBlockRows) J.items[lane] = items;
+      int lo = live ? s : INT_MAX, hi = live ? e : 0, len = live ? items : 0;
 #pragma unroll
       for (int off = 16; off > 0; off >>= 1) {
         lo = min(lo, __shfl_xor_sync(0xFFFFFFFFu, lo, off));
@@ -1204,8 +1219,16 @@ __device__ void producer(Smem &S, const CUtensorMap *q_map, const CUtensorMap *k
         tma_load_2d(&S.kring[stage][0], k_map, &S.k_full[stage], 0, tile * kTileKeys, pol_k);
         // the tile's key scales (zero past the last key), released by the epilogue
         if (!wait_bar(S, &S.sc_empty[sst], ((kcount / kSStages) & 1) ^ 1, p, kBackoffIdle)) break;
-        mbar_arrive_expect_tx(&S.sc_full[sst], kTileKeys * sizeof(float));
-        tma_load_1d(&S.sring[sst][0], s_map, &S.sc_full[sst], tile * kTileKeys, pol_k);
+        if constexpr (kMasked) {
+          // the tile's 16 blocks are half of mask word tile / 2; the box is the
+          // 16-byte-aligned group of 4 words holding it, for the block's rows
+          mbar_arrive_expect_tx(&S.sc_full[sst], kTileKeys * sizeof(float) + sizeof(S.mring[0]));
+          tma_load_1d(&S.sring[sst][0], s_map, &S.sc_full[sst], tile * kTileKeys, pol_k);
+          tma_load_2d(&S.mring[sst][0][0], m_map, &S.sc_full[sst], (tile >> 1) & ~3, Jc.block * kBlockRows, pol_k);
+        } else {
+          mbar_arrive_expect_tx(&S.sc_full[sst], kTileKeys * sizeof(float));
+          tma_load_1d(&S.sring[sst][0], s_map, &S.sc_full[sst], tile * kTileKeys, pol_k);
+        }
         ++kcount;
       }
     }
@@ -1340,7 +1363,7 @@ __device__ void epilogue(Smem &S, uint32_t tmem, const FusedParams &p, int warp,
       ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
       // per-row state for this scan: warp ew owns row ew
       if (gate_warp && lane == 0) {
-        const int n = row_items(J.start[ew], J.end[ew]);
+        const int n = J.items[ew];
         float t0 = NEG_INF;
         if (J.ns == 0 && J.mode == 0 && p.force_gate == 1 && n > 0) t0 = INFINITY;
         S.tau[ew] = t0;
@@ -1413,6 +1436,11 @@ __device__ void epilogue(Smem &S, uint32_t tmem, const FusedParams &p, int warp,
       const uint32_t base = tmem + lane_addr + (uint32_t)(buf * kCols + rbase * kHeads);
       float raw[kRowsPerWarp];
       score_rows(&S.t_empty[buf], base, W, hsc, lane, raw);
+      uint32_t mw[kRowsPerWarp];
+      if constexpr (kMasked) {
+#pragma unroll
+        for (int rr = 0; rr < kRowsPerWarp; ++rr) mw[rr] = S.mring[sst][rbase + rr][(tile >> 1) & 3];
+      }
       if (lane == 0) mbar_arrive(&S.sc_empty[sst]);
       if (tile >= f_lo && tile < f_hi) {
         // the tile lies inside every row's range: no per-key mask
@@ -1424,6 +1452,13 @@ __device__ void epilogue(Smem &S, uint32_t tmem, const FusedParams &p, int warp,
           const int r = rbase + rr;
           sv[rr] = (act[rr] && key >= J.start[r] && key < J.end[r]) ? raw[rr] : NEG_INF;
         }
+      }
+      if constexpr (kMasked) {
+        // keys of blocks the row's mask leaves out are not visible
+        const int bit = ((tile & 1) << 4) + (kown >> 3);
+#pragma unroll
+        for (int rr = 0; rr < kRowsPerWarp; ++rr)
+          if (!((mw[rr] >> bit) & 1u)) sv[rr] = NEG_INF;
       }
       if constexpr (kBlocks) {
         // the 8 keys of a block sit in the lanes with the same lane % 4 (key
@@ -1477,7 +1512,7 @@ __device__ void epilogue(Smem &S, uint32_t tmem, const FusedParams &p, int warp,
           // coarse bin of row ew that holds the target sample rank j
           if (gate_warp) {
           const int r = ew;
-          const int n = row_items(J.start[r], J.end[r]);
+          const int n = J.items[r];
           const int m = S.msample[r];
           int on = 0, above = 0, jw = 0;
           uint32_t klo = 0, khi = 0;
@@ -1745,7 +1780,7 @@ __device__ void epilogue(Smem &S, uint32_t tmem, const FusedParams &p, int warp,
         }
         if (lane < kBlockRows) {
           Q.start[lane] = J.start[lane];
-          Q.n[lane] = row_items(J.start[lane], J.end[lane]);
+          Q.n[lane] = J.items[lane];
           Q.gated[lane] = S.tau[lane] > NEG_INF;
           Q.blo[lane] = S.tau[lane];
           Q.binv[lane] = S.binv[lane];
@@ -1904,7 +1939,8 @@ __device__ void selection(Smem &S, const FusedParams &p, int warp, int lane) {
 template <bool kLogits>
 __global__ void __launch_bounds__(kThreads, 1)
     mqa_fused_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant__ CUtensorMap k_map,
-                     const __grid_constant__ CUtensorMap s_map, const FusedParams p) {
+                     const __grid_constant__ CUtensorMap s_map, const __grid_constant__ CUtensorMap m_map,
+                     const FusedParams p) {
   extern __shared__ uint8_t smem_raw[];
   Smem &S = get_smem(smem_raw);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -1945,6 +1981,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_prefetch_desc(&q_map);
     tma_prefetch_desc(&k_map);
     tma_prefetch_desc(&s_map);
+    if (kMasked) tma_prefetch_desc(&m_map);
   }
   if (warp == 1) {
     tmem_alloc(&S.tmem_base, 2 * kCols);
@@ -1959,7 +1996,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = S.tmem_base;
 
   if (warp == 0) {
-    producer<kLogits>(S, &q_map, &k_map, &s_map, p, lane);
+    producer<kLogits>(S, &q_map, &k_map, &s_map, &m_map, p, lane);
   } else if (warp == 1) {
     if (lane == 0) mma_issuer(S, tmem, p);
   } else if (warp >= kEpiWarp0) {
@@ -1985,26 +2022,28 @@ static cudaError_t set_smem_attr(const void *fn) {
 }
 
 cudaError_t launch_fused_topk(const CUtensorMap &q_map, const CUtensorMap &k_map, const CUtensorMap &s_map,
-                              const FusedParams &p, int ctas, cudaStream_t stream) {
+                              const FusedParams &p, int ctas, cudaStream_t stream, const CUtensorMap *m_map) {
   static cudaError_t attr = set_smem_attr((const void *)mqa_fused_kernel<false>);
   if (attr != cudaSuccess) return attr;
-  mqa_fused_kernel<false><<<ctas, kThreads, fused_smem_bytes(), stream>>>(q_map, k_map, s_map, p);
+  // the block-mask map is read only by the masked build; the others get a placeholder
+  const CUtensorMap &mm = m_map ? *m_map : s_map;
+  mqa_fused_kernel<false><<<ctas, kThreads, fused_smem_bytes(), stream>>>(q_map, k_map, s_map, mm, p);
   return cudaGetLastError();
 }
 
-#if MQA_HEADS == 32 && !MQA_BLOCKS
+#if MQA_HEADS == 32 && !MQA_BLOCKS && !MQA_MASKED
 cudaError_t launch_logits(const CUtensorMap &q_map, const CUtensorMap &k_map, const CUtensorMap &s_map,
                           const FusedParams &p, int ctas, cudaStream_t stream) {
   static cudaError_t attr = set_smem_attr((const void *)mqa_fused_kernel<true>);
   if (attr != cudaSuccess) return attr;
-  mqa_fused_kernel<true><<<ctas, kThreads, fused_smem_bytes(), stream>>>(q_map, k_map, s_map, p);
+  mqa_fused_kernel<true><<<ctas, kThreads, fused_smem_bytes(), stream>>>(q_map, k_map, s_map, s_map, p);
   return cudaGetLastError();
 }
 #endif
 
 }  // namespace MQA_KNS
 
-#if MQA_HEADS == 32 && !MQA_BLOCKS
+#if MQA_HEADS == 32 && !MQA_BLOCKS && !MQA_MASKED
 // ------------------------------------------------------------------ allocation-free scratch
 // Scratch for mqa_topk_prefill_noalloc: the 256-byte header plus the candidate
 // slabs of at most kStaticScratchCtas persistent CTAs, as a file-scope device

@@ -87,6 +87,7 @@ struct FusedParams {
   int32_t *split_done;   // per split block: chunks finished (zeroed with the header)
   int split_max;         // split blocks the arrays above hold
   long long split_words; // uint32 words of split_slab
+  const int32_t *row_items;  // masked selection: allowed keys per row
   int rows;              // rows of this call
   int row0;              // first global row (logits mode: chunk offset)
   int keys;
@@ -104,18 +105,25 @@ struct FusedParams {
 // Launchers (defined next to their kernels), per head count.
 namespace h32 {
 cudaError_t launch_fused_topk(const CUtensorMap &q_map, const CUtensorMap &k_map, const CUtensorMap &s_map,
-                              const FusedParams &p, int ctas, cudaStream_t stream);
+                              const FusedParams &p, int ctas, cudaStream_t stream, const CUtensorMap *m_map = nullptr);
 cudaError_t launch_logits(const CUtensorMap &q_map, const CUtensorMap &k_map, const CUtensorMap &s_map,
                           const FusedParams &p, int ctas, cudaStream_t stream);
 }  // namespace h32
 namespace h64 {
 cudaError_t launch_fused_topk(const CUtensorMap &q_map, const CUtensorMap &k_map, const CUtensorMap &s_map,
-                              const FusedParams &p, int ctas, cudaStream_t stream);
+                              const FusedParams &p, int ctas, cudaStream_t stream, const CUtensorMap *m_map = nullptr);
 }  // namespace h64
 namespace h32b {  // block selection: top blocks of 8 keys by their largest score
 cudaError_t launch_fused_topk(const CUtensorMap &q_map, const CUtensorMap &k_map, const CUtensorMap &s_map,
-                              const FusedParams &p, int ctas, cudaStream_t stream);
+                              const FusedParams &p, int ctas, cudaStream_t stream, const CUtensorMap *m_map = nullptr);
 }  // namespace h32b
+namespace h32m {  // masked selection: keys restricted to a per-row block mask
+cudaError_t launch_fused_topk(const CUtensorMap &q_map, const CUtensorMap &k_map, const CUtensorMap &s_map,
+                              const FusedParams &p, int ctas, cudaStream_t stream, const CUtensorMap *m_map = nullptr);
+}  // namespace h32m
+cudaError_t launch_block_mask(const int32_t *lists, const int32_t *starts, const int32_t *ends, int rows,
+                              int list_len, int keys, uint32_t *mask, int mask_words, int32_t *row_items,
+                              cudaStream_t stream);
 cudaError_t launch_ue8m0_decode(const uint8_t *scales, float *out, int keys, cudaStream_t stream);
 cudaError_t launch_dense_topk_rows(const float *logits, int rows, int keys, const int32_t *starts,
                                    const int32_t *ends, int32_t *out, int topk, int32_t *ws_status,

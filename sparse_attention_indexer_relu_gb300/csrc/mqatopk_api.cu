@@ -104,6 +104,19 @@ int encode_scales(CUtensorMap *map, const float *base, uint64_t n) {
   return r == CUDA_SUCCESS ? MQA_OK : MQA_ERR_CUDA;
 }
 
+// 2-D uint32 block mask [rows, words], read in boxes of 4 words x 8 rows
+// (out-of-range words read as 0, i.e. no key allowed).
+int encode_mask(CUtensorMap *map, const uint32_t *base, uint64_t rows, uint64_t words) {
+  const cuuint64_t dims[2] = {(cuuint64_t)words, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)(words * sizeof(uint32_t))};
+  const cuuint32_t box[2] = {4, (cuuint32_t)kBlockRows};
+  const cuuint32_t estr[2] = {1, 1};
+  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<uint32_t *>(base), dims, strides, box,
+                        estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                        CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? MQA_OK : MQA_ERR_CUDA;
+}
+
 inline bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 int check_common(const void *q, const void *k, const float *scales, const float *weights, const int32_t *starts,
@@ -172,10 +185,15 @@ cudaStream_t as_stream(void *s) { return reinterpret_cast<cudaStream_t>(s); }
 
 int run_fused(const void *q, const void *k, const float *scales, const float *weights, const int32_t *starts,
               const int32_t *ends, int32_t *out, int rows, int keys, int topk, int heads, void *workspace,
-              size_t workspace_bytes, void *stream, const mqa_topk_debug_options *opt, bool blocks = false) {
+              size_t workspace_bytes, void *stream, const mqa_topk_debug_options *opt, bool blocks = false,
+              const uint32_t *mask = nullptr, int mask_words = 0, const int32_t *row_items = nullptr) {
   int rc = check_common(q, k, scales, weights, starts, ends, out, rows, keys);
   if (rc != MQA_OK) return rc;
   if (!valid_topk(topk) || (heads != 32 && heads != 64) || (blocks && heads != 32)) return MQA_ERR_INVALID_ARGUMENT;
+  if (mask && (heads != 32 || blocks || !row_items || mask_words % 4 != 0 ||
+               (long long)mask_words * 256 < (long long)keys))
+    return MQA_ERR_INVALID_ARGUMENT;
+  if (mask && (!aligned(mask, 16) || !aligned(row_items, 4))) return MQA_ERR_MISALIGNED;
   const int brows = block_rows(heads);
   if (!workspace) return MQA_ERR_INVALID_ARGUMENT;
   if (!aligned(workspace, 256)) return MQA_ERR_MISALIGNED;
@@ -207,7 +225,8 @@ int run_fused(const void *q, const void *k, const float *scales, const float *we
   }
   rc = get_encoder();
   if (rc != MQA_OK) return rc;
-  CUtensorMap qm, km, sm;
+  CUtensorMap qm, km, sm, mm;
+  if (mask && encode_mask(&mm, mask, (uint64_t)rows, (uint64_t)mask_words) != MQA_OK) return MQA_ERR_CUDA;
   // q is [rows * heads, 128]: a block's 256 (row, head) rows per TMA box
   if (encode_rows128(&qm, q, (uint64_t)rows * heads, kCols) != MQA_OK ||
       encode_rows128(&km, k, (uint64_t)keys, kTileKeys) != MQA_OK || encode_scales(&sm, scales, keys) != MQA_OK)
@@ -233,6 +252,7 @@ int run_fused(const void *q, const void *k, const float *scales, const float *we
   p.keys = keys;
   p.topk = topk;
   p.nblocks = (rows + brows - 1) / brows;
+  p.row_items = row_items;
   p.cap = cap;
   p.gate_target = 3 * topk < cap / 2 ? 3 * topk : cap / 2;
   // gate every row that would otherwise bring more than twice the target
@@ -246,7 +266,8 @@ int run_fused(const void *q, const void *k, const float *scales, const float *we
     cudaGetLastError();
     return MQA_ERR_CUDA;
   }
-  const cudaError_t le = blocks ? h32b::launch_fused_topk(qm, km, sm, p, ctas, st)
+  const cudaError_t le = mask     ? h32m::launch_fused_topk(qm, km, sm, p, ctas, st, &mm)
+                         : blocks ? h32b::launch_fused_topk(qm, km, sm, p, ctas, st)
                          : heads == 64 ? h64::launch_fused_topk(qm, km, sm, p, ctas, st)
                                        : h32::launch_fused_topk(qm, km, sm, p, ctas, st);
   if (le != cudaSuccess) return MQA_ERR_CUDA;
@@ -326,6 +347,32 @@ int mqa_topk_prefill_debug(const void *q, const void *k, const float *key_scales
                            const mqa_topk_debug_options *opt) {
   return run_fused(q, k, key_scales, weights, starts, ends, out, rows, keys, topk, 32, workspace, workspace_bytes,
                    stream, opt);
+}
+
+int mqa_block_mask(const int32_t *block_lists, const int32_t *starts, const int32_t *ends, int rows, int list_len,
+                   int keys, uint32_t *mask, int mask_words, int32_t *row_items, void *stream) {
+  if (rows < 0 || list_len < 0 || keys < 1 || keys > MQA_MAX_KEYS || mask_words % 4 != 0 ||
+      (long long)mask_words * 256 < (long long)keys)
+    return MQA_ERR_INVALID_ARGUMENT;
+  if (rows == 0) return MQA_OK;
+  if (!starts || !ends || !mask || !row_items || (list_len > 0 && !block_lists)) return MQA_ERR_INVALID_ARGUMENT;
+  if (!aligned(mask, 16)) return MQA_ERR_MISALIGNED;
+  DeviceInfo d;
+  int rc = current_device_info(&d);
+  if (rc != MQA_OK) return rc;
+  return launch_block_mask(block_lists, starts, ends, rows, list_len, keys, mask, mask_words, row_items,
+                           as_stream(stream)) == cudaSuccess
+             ? MQA_OK
+             : MQA_ERR_CUDA;
+}
+
+int mqa_topk_prefill_masked(const void *q, const void *k, const float *key_scales, const float *weights,
+                            const int32_t *starts, const int32_t *ends, const uint32_t *mask, int mask_words,
+                            const int32_t *row_items, int32_t *out, int rows, int keys, int topk, void *workspace,
+                            size_t workspace_bytes, void *stream, const mqa_topk_debug_options *opt) {
+  if (!mask) return MQA_ERR_INVALID_ARGUMENT;
+  return run_fused(q, k, key_scales, weights, starts, ends, out, rows, keys, topk, 32, workspace, workspace_bytes,
+                   stream, opt, false, mask, mask_words, row_items);
 }
 
 int mqa_block_topk_prefill(const void *q, const void *k, const float *key_scales, const float *weights,

@@ -112,3 +112,56 @@ def check_block_rows(got, p, rows, scores, btopk):
         if worst > tol:
             bad.append((r, f"tie rule: {len(diff)} blocks differ, worst |B-kth| = {worst:.3g} > {tol:.3g}"))
     return bad
+
+
+def numpy_block_mask(lists, starts, ends, keys, words):
+    """Block mask and visible-key counts built on the CPU from block lists
+    relative to floor(start / 8) (-1 / out-of-range entries ignored)."""
+    rows = lists.shape[0]
+    mask = np.zeros((rows, words), np.uint32)
+    items = np.zeros(rows, np.int32)
+    for r in range(rows):
+        s = max(int(starts[r]), 0)
+        e = max(s, min(int(ends[r]), keys))
+        b0, blast = s // 8, ((e - 1) // 8 if e > s else s // 8 - 1)
+        seen = set()
+        for rel in lists[r]:
+            rel = int(rel)
+            if rel < 0 or rel > blast - b0:
+                continue
+            b = b0 + rel
+            if b in seen:
+                continue
+            seen.add(b)
+            mask[r, b // 32] |= np.uint32(1 << (b % 32))
+            items[r] += min(e, 8 * b + 8) - max(s, 8 * b)
+    return mask, items
+
+
+def check_masked_rows(got, p, rows, scores):
+    """Masked selection: visible keys are those with a finite oracle score."""
+    bad = []
+    for i, r in enumerate(rows):
+        s, e = int(p.starts[r]), int(p.ends[r])
+        vis = scores[i, s:e] if e > s else np.zeros(0)
+        keep = np.nonzero(np.isfinite(vis))[0]
+        c = min(p.topk, len(keep))
+        g = got[i]
+        if not np.all(g[c:] == -1):
+            bad.append((r, "padding"))
+            continue
+        sel = g[:c]
+        if not set(sel.tolist()) <= set(keep.tolist()) or len(np.unique(sel)) != c:
+            bad.append((r, "indices"))
+            continue
+        if len(keep) <= p.topk:
+            continue
+        v = vis[keep]
+        tol = TOPK_TIE_TOL * np.max(np.abs(v))
+        order = keep[np.argsort(-v, kind="stable")]
+        kth = vis[order[c - 1]]
+        diff = set(order[:c].tolist()) ^ set(sel.tolist())
+        worst = max((abs(vis[j] - kth) for j in diff), default=0.0)
+        if worst > tol:
+            bad.append((r, f"tie rule: {len(diff)} keys differ, worst |S-kth| = {worst:.3g} > {tol:.3g}"))
+    return bad

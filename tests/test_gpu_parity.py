@@ -4,7 +4,8 @@ import pytest
 
 import oracle
 import synth
-from parity import check_block_rows, check_logits_rows, check_topk_rows, to_device
+from parity import (check_block_rows, check_logits_rows, check_masked_rows, check_topk_rows, numpy_block_mask,
+                    to_device)
 
 pytestmark = pytest.mark.gpu
 
@@ -245,6 +246,68 @@ def test_block_selection_forced_rescan(mqa):
     assert status == 0, stats
     assert stats["rows_rescanned"] > 0
     assert_block_parity(p, got, 512)
+
+
+def run_masked(mqa, p, mask, items, debug=None):
+    import torch
+    q, k, sc, w, s, e = to_device(p)
+    ws = mqa.alloc_workspace(p.rows)
+    m = torch.from_numpy(mask.view(np.int32)).cuda()
+    it = torch.from_numpy(items).cuda()
+    out = mqa.mqa_topk_prefill_masked(q, k, sc, w, s, e, m, it, p.topk, workspace=ws, debug=debug)
+    status, stats = mqa.get_status(ws)
+    return out.cpu().numpy(), status, stats
+
+
+def assert_masked_parity(p, got, mask):
+    rows = np.arange(p.rows)
+    _, scores = oracle.run_masked(p, mask, rows=rows, want_topk=False, want_scores=True)
+    bad = check_masked_rows(got, p, rows, scores)
+    assert not bad, bad[:10]
+
+
+def test_block_mask_kernel_bit_exact(mqa):
+    """The list-to-mask kernel equals the CPU construction, counts included."""
+    import torch
+    rng = np.random.default_rng(70)
+    rows, keys, L = 40, 70000, 300
+    starts = rng.integers(0, keys, rows).astype(np.int32)
+    ends = np.minimum(keys, starts + rng.integers(0, 30000, rows)).astype(np.int32)
+    lists = rng.integers(-1, 4000, (rows, L)).astype(np.int32)
+    words = ((keys + 1023) // 1024) * 4
+    want_m, want_i = numpy_block_mask(lists, starts, ends, keys, words)
+    t = lambda a: torch.from_numpy(a).cuda()
+    m, it = mqa.block_mask(t(lists), t(starts), t(ends), keys, words)
+    assert np.array_equal(m.cpu().numpy().view(np.uint32), want_m)
+    assert np.array_equal(it.cpu().numpy(), want_i)
+
+
+@pytest.mark.parametrize("seed,rows,keys,topk,frac", [(71, 9, 3000, 512, 0.5), (72, 24, 40000, 512, 0.3),
+                                                      (73, 17, 90000, 1024, 0.05)])
+def test_masked_selection_random_masks(mqa, seed, rows, keys, topk, frac):
+    """Top-k over the keys of each row's allowed blocks (random masks)."""
+    p = synth.random_small(seed, rows, keys, topk)
+    rng = np.random.default_rng(seed)
+    picks = rng.integers(0, keys // 8 + 1, (rows, 4096))  # relative block indices, many past the range
+    lists = np.where(rng.random((rows, 4096)) < frac, picks, -1).astype(np.int32)
+    words = ((keys + 1023) // 1024) * 4
+    mask, items = numpy_block_mask(lists, p.starts, p.ends, keys, words)
+    got, status, stats = run_masked(mqa, p, mask, items)
+    assert status == 0, stats
+    assert_masked_parity(p, got, mask)
+
+
+def test_two_level_source_then_consumer(mqa):
+    """The two-level chain on long causal rows: the oracle's top 2048 blocks of
+    8 keys (source) restrict the consumer's top-512."""
+    p = _causal(synth.random_small(74, 16, 200000, 512, empty_frac=0.0), 200000)
+    lists = oracle.run_blocks(p, 2048)
+    words = ((p.keys + 1023) // 1024) * 4
+    mask, items = numpy_block_mask(lists, p.starts, p.ends, p.keys, words)
+    got, status, stats = run_masked(mqa, p, mask, items)
+    assert status == 0, stats
+    assert stats["gated_rows"] == 16, stats
+    assert_masked_parity(p, got, mask)
 
 
 def test_fused_single_cta(mqa):
