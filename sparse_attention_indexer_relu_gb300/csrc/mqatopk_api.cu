@@ -255,6 +255,10 @@ int run_fused(const void *q, const void *k, const float *scales, const float *we
   p.row_items = row_items;
   p.cap = cap;
   p.gate_target = 3 * topk < cap / 2 ? 3 * topk : cap / 2;
+  // Masked rows see few of their range's keys, so a sample of the range holds
+  // few gate-passing keys: a larger target keeps about 32 of them in the
+  // sample (at most 64 tiles) and the gate's under-fill risk negligible.
+  if (mask && p.gate_target < 4096) p.gate_target = 4096 < cap / 2 ? 4096 : cap / 2;
   // gate every row that would otherwise bring more than twice the target
   // candidates to the selection (and every row the slab cannot hold)
   p.gate_min = 2 * p.gate_target;
