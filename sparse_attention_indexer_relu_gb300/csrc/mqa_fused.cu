@@ -164,7 +164,7 @@ __device__ __noinline__ void raise_timeout(Smem &S, const FusedParams &p) {
 }
 
 #ifndef MQA_BACKOFF_SCALE
-#define MQA_BACKOFF_SCALE 1
+#define MQA_BACKOFF_SCALE 4
 #endif
 // Sleep between polls of a waiting role, so that warps which wait for long
 // stretches (producer, selection, MMA issuer) leave issue slots to the
@@ -215,13 +215,17 @@ __device__ __forceinline__ bool wait_counter(Smem &S, int *flag, int target, con
 // and the fused and logits instantiations share this code, so both produce
 // bit-identical scores.
 #ifndef MQA_RELU_ALU_CHUNKS
-#define MQA_RELU_ALU_CHUNKS 0
+#define MQA_RELU_ALU_CHUNKS 1
 #endif
 // Of a thread's head-pair chunks per key, the first MQA_RELU_ALU_CHUNKS form
 // relu as max(x, 0) on the ALU pipe with pre-doubled weights (2w * max(x, 0));
 // the rest use x + |x| on the FMA pipe with w.  Both give 2 * w * relu(x)
 // exactly (one rounding of the same product), so the split only balances the
-// two pipes and leaves the scores bit-identical.
+// two pipes and leaves the scores bit-identical.  A packed FFMA2 or FADD2
+// holds the FMA pipe for two cycles, so the relu add and the weighted
+// accumulate keep that pipe saturated through the head sum; moving one chunk
+// of four to the ALU pipe was the fastest split measured (none, a quarter,
+// three eighths and a half were compared).
 constexpr int kHeadGroups = kHeads / 32;  // 32-column groups per row
 struct HeadW {
   float2 w[4 * kHeadGroups];  // weights of this thread's heads of one row, as pairs (doubled for ALU chunks)
