@@ -297,14 +297,38 @@ def main():
 KERNEL_SOURCES = ("mqa_fused.cu", "ptx.cuh", "mqa_internal.h")
 
 
+def _strip_comments(src):
+    """C/C++ source text without comments and blank space (string literals
+    kept), so that edits to comments alone leave the digest unchanged."""
+    out, i, n = [], 0, len(src)
+    while i < n:
+        c = src[i]
+        if c == '"':
+            j = i + 1
+            while j < n and src[j] != '"':
+                j += 2 if src[j] == "\\" else 1
+            out.append(src[i:j + 1])
+            i = j + 1
+        elif src.startswith("//", i):
+            j = src.find("\n", i)
+            i = n if j < 0 else j
+        elif src.startswith("/*", i):
+            j = src.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+        else:
+            out.append(c)
+            i += 1
+    return " ".join("".join(out).split())
+
+
 def kernel_source_digest():
-    """sha256 over the fused kernel's source files, to tie a DRAM capture to
-    the exact kernel it was taken on."""
+    """sha256 over the fused kernel's source files (comments and spacing
+    removed), to tie a DRAM capture to the kernel code it was taken on."""
     import hashlib
     h = hashlib.sha256()
     for f in KERNEL_SOURCES:
-        with open(os.path.join(ROOT, "sparse_attention_indexer_relu_gb300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(ROOT, "sparse_attention_indexer_relu_gb300", "csrc", f), encoding="utf-8") as fh:
+            h.update(_strip_comments(fh.read()).encode())
     return h.hexdigest()
 
 

@@ -10,19 +10,26 @@
 // logits matrix never reaches HBM.  A second instantiation of the same
 // pipeline writes the logits instead (debug entry and dense baseline).
 //
-// CTA layout (384 threads):
-//   warp 0      producer: claims row blocks heaviest first, loads q (TMA) and
-//               per-row ranges/weights, streams 128-key K tiles (TMA) through a
-//               6-stage ring.
+// CTA layout (640 threads with 32 index heads):
+//   warp 0      producer: claims row blocks heaviest first (or key chunks of
+//               the last blocks), loads q (TMA) and per-row ranges/weights,
+//               streams 128-key K tiles (TMA) through a 6-stage ring and the
+//               tiles' key scales through an 8-stage ring.
 //   warp 1      MMA issuer: per K tile, 4 x tcgen05.mma kind::f8f6f4
 //               (M = 128 keys, N = 8 rows x 32 heads, K = 32) into one of two
 //               256-column TMEM accumulators.
-//   warps 2-3   selection: per finished block, exact radix top-k over each
-//               row's candidates, output write or rescan request.
-//   warps 4-11  epilogue: TMEM -> registers (one key per thread), relu-weighted
-//               head sum, key scale, range mask; sampled gate; candidate
-//               emission to per-(row, quadrant) slab segments; exact
-//               compaction on rescans.
+//   warps 2-3   selection: per finished block, each row's top-k from its
+//               candidates (score-binned count and gather, exact radix over
+//               the threshold bin), output write or rescan request.
+//   warps 4-19  epilogue: warp w reads TMEM lane quadrant w % 4 (32 keys) for
+//               2 of the block's rows (16x256b loads: 4 keys x 8 heads per
+//               thread), relu-weighted head sum, 4-lane reduce-scatter, key
+//               scale, range mask; sampled gate; candidate emission to
+//               per-(row, quadrant) slab segments; exact compaction on
+//               rescans; selection help once the producer has no block left.
+// The same source is compiled for 64 index heads (4-row blocks), for block
+// selection (the top blocks of 8 keys) and for masked selection (keys limited
+// to a per-row block mask).
 // Every wait is bounded by a time limit; on expiry the kernel records
 // MQA_DEV_WAIT_TIMEOUT in the workspace status word and unwinds.
 #include "mqa_internal.h"
@@ -1335,13 +1342,13 @@ constexpr int kHelperScratchBytes = 1024 + 8 * kSelList;
 static_assert(kEpiWarps * kHelperScratchBytes <= (int)(sizeof(Smem::kring) + sizeof(Smem::q)),
               "helper scratch exceeds the K ring and q buffers");
 
-// ------------------------------------------------------------------ epilogue (warps 4-11)
+// ------------------------------------------------------------------ epilogue (warps 4 and up)
 template <bool kLogits>
 __device__ void epilogue(Smem &S, uint32_t tmem, const FusedParams &p, int warp, int lane) {
-  const int ew = warp - kEpiWarp0;  // 0..7
+  const int ew = warp - kEpiWarp0;  // 0 .. kEpiWarps - 1
   const int quad = warp & 3;        // TMEM lane quadrant this warp may access
   const int rbase = kRowsPerWarp * (ew >> 2);  // this warp's rows: rbase .. rbase + kRowsPerWarp - 1
-  const bool gate_warp = ew < kBlockRows;        // warps 0..7 also own row ew's gate / compaction
+  const bool gate_warp = ew < kBlockRows;        // the first kBlockRows warps also own row ew's gate / compaction
   const uint32_t lane_addr = (uint32_t)(quad * 32) << 16;
   const float NEG_INF = -INFINITY;
   const int cap = p.cap, seg = p.cap / kQuads;

@@ -233,6 +233,46 @@ def random_small(seed: int, rows: int, keys: int, topk: int, heads=HEADS, dim=HE
                    ends.astype(np.int32), topk)
 
 
+MAX_KEYS = 1 << 24  # the largest key count the library accepts
+
+
+def max_keys(seed: int = 90, rows: int = 16, used: int = 400_000, topk: int = 2048) -> Problem:
+    """A chunk at the largest key count (2^24 keys: K is 2 GiB).  Row 0 sees
+    the last `used` keys (long enough to be gated), row 1 the first 5000,
+    rows 2-4 end at the last key with 1, k - 1 and k + 1 keys, and the rest
+    have random ranges inside the last `used` keys.  Only keys that some row
+    sees are drawn; the others hold code 0."""
+    rng = np.random.default_rng(seed)
+    keys, lo, head = MAX_KEYS, MAX_KEYS - used, 8192
+    q = quantize_e4m3fn_fast(rng.standard_normal((rows, HEADS, HEAD_DIM), dtype=np.float32))
+    w = (rng.standard_normal((rows, HEADS), dtype=np.float32) / np.float32(math.sqrt(HEADS))).astype(np.float32)
+    k = np.zeros((keys, HEAD_DIM), np.uint8)
+    k[lo:] = quantize_e4m3fn_fast(rng.standard_normal((used, HEAD_DIM), dtype=np.float32))
+    k[:head] = quantize_e4m3fn_fast(rng.standard_normal((head, HEAD_DIM), dtype=np.float32))
+    exps = np.full(keys, 127, np.uint8)
+    exps[lo:] = rng.integers(120, 128, size=used).astype(np.uint8)
+    exps[:head] = rng.integers(120, 128, size=head).astype(np.uint8)
+    starts = np.empty(rows, np.int64)
+    ends = np.empty(rows, np.int64)
+    fixed = [(lo, keys), (0, 5000), (keys - 1, keys), (keys - (topk - 1), keys), (keys - (topk + 1), keys)]
+    for i in range(rows):
+        if i < len(fixed):
+            starts[i], ends[i] = fixed[i]
+        else:
+            a, b = np.sort(rng.integers(lo, keys + 1, size=2))
+            starts[i], ends[i] = a, b
+    return Problem(f"max_keys_{seed}", q, k, ue8m0_bytes(exps), w, starts.astype(np.int32), ends.astype(np.int32),
+                   topk)
+
+
+def window(p: Problem, r: int) -> Problem:
+    """Row r of p alone, with K cut to the row's range (indices relative to
+    the range start are unchanged)."""
+    s, e = int(p.starts[r]), int(p.ends[r])
+    return Problem(f"{p.name}_row{r}", p.q[r:r + 1], p.k[s:e], p.scales_ue8m0[s:e], p.weights[r:r + 1],
+                   np.zeros(1, np.int32), np.array([e - s], np.int32), p.topk)
+
+
 def sample_rows(p: Problem, count: int, seed: int = 1234) -> np.ndarray:
     """Deterministic row sample for checks and CPU timing on big chunks: evenly
     spaced rows, the first and last row, every specially treated row (capped),

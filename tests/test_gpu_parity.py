@@ -339,6 +339,21 @@ def test_bounded_wait_reports_timeout(mqa):
     assert_parity(p, got)
 
 
+def test_fused_max_keys(mqa):
+    """2^24 keys, the largest key count the library accepts (K is 2 GiB):
+    ranges that end at the last key, one gated 400K-key range, one at key 0.
+    Each row is checked against the oracle on its own key window."""
+    p = synth.max_keys()
+    got, status, stats = run_fused(mqa, p)
+    assert status == 0, stats
+    assert stats["gated_rows"] >= 1, stats
+    for r in range(p.rows):
+        sub = synth.window(p, r)
+        _, scores = oracle.run(sub, want_topk=False, want_scores=True)
+        bad = check_topk_rows(got[r:r + 1], sub, np.array([0]), scores)
+        assert not bad, (r, bad[:5])
+
+
 def test_out_of_range_rows_clamped(mqa):
     p = synth.random_small(26, 8, 3000, 512)
     p.starts[0], p.ends[0] = -5, 700
