@@ -99,11 +99,11 @@ typedef struct mqa_topk_debug_options {
  * sections "Memory" and the workspace list of `get_fused_mqa_topk_workspaces`
  * on the API page):
  *  - a 256-byte header (claim counter, status, counters);
- *  - one persistent CTA per SM (at most 8 per 8-row block), two slabs of
+ *  - one persistent CTA per SM (at most 32 per block of rows), two slabs of
  *    8 rows x 16384 candidate records (8 B each) per CTA;
  *  - the key-range split arrays: for up to min(blocks, 2 x CTAs) blocks whose
  *    key range several CTAs scan as chunks, a slab of 8 rows x (16384 + 512)
- *    records (more per block at 4 or 8 chunks, for fewer blocks), the
+ *    records (more per block at 4 or more chunks, for fewer blocks), the
  *    per-chunk segment counts and a finished-chunk counter per block.
  * A workspace below this size but at least the header plus the per-CTA slabs
  * of min(blocks, SMs) CTAs still works: the call then splits no block. 
