@@ -193,6 +193,8 @@ def main():
                     help="topk: the fused key top-k (the headline line); blocks: the top 2048 blocks of 8 keys; "
                          "masked: the top 512 keys inside each row's top 2048 blocks (both stages of the "
                          "two-level selection, timed on their own; no e2e, dense or CPU legs)")
+    ap.add_argument("--graph", action="store_true",
+                    help="capture one step into a CUDA graph after the warm-up and time its replays")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-dense", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
@@ -246,6 +248,15 @@ def main():
     status, stats = mqa.get_status(wsb)
     if status != 0:
         raise RuntimeError(f"device status {status} {stats}")
+    if args.graph:
+        # one memset node and one kernel node per step; inputs are read at replay time
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            step()
+        graph.replay()
+        torch.cuda.synchronize()
+        step = graph.replay
+        stream = torch.cuda.current_stream()
 
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     with ClockSampler(torch.cuda.current_device()) as clk:
@@ -284,7 +295,7 @@ def main():
                    "rows": p.rows, "keys": p.keys,
                    "topk": {"topk": p.topk, "blocks": 2048, "masked": 512}[args.mode], "pairs": pairs,
                    "heads": p.heads, "head_dim": 128, "parallelism": f"replicas x{ws}",
-                   "l2": l2_note(p)},
+                   "l2": l2_note(p), "cuda_graph": bool(args.graph)},
         "rows_per_s": rows_per_s,
         "gpu_launches": args.steps,
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
@@ -402,42 +413,67 @@ def time_dense(mqa, torch, q, k, scales, w, s, e, p, pairs, reps=2):
 
 
 def time_e2e(mqa, torch, dev, p, pairs, args, ws):
-    """Same metric through the public API from pinned host buffers: H2D of the
-    step's inputs, UE8M0 decode, fused call, D2H of the selected indices."""
+    """Same metric through the public API from pinned host buffers: every step
+    copies its inputs host->device, decodes the UE8M0 scales, runs the fused
+    call and copies the selected indices device->host.  Steps are pipelined as
+    a serving loop would run them: two device buffer sets, the next step's
+    input copies on a copy stream while the current step computes, and the
+    result copy on a third stream."""
     pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()
-    hq, hk, hg, hw, hs, he = (pin(p.q), pin(p.k), pin(p.scales_ue8m0), pin(p.weights), pin(p.starts),
-                              pin(p.ends))
-    hout = torch.empty((p.rows, p.topk), dtype=torch.int32).pin_memory()
-    dq, dk, dg, dw, ds, de = (torch.empty_like(x, device=dev) for x in (hq, hk, hg, hw, hs, he))
-    sc = torch.empty(p.keys, dtype=torch.float32, device=dev)
-    dout = torch.empty((p.rows, p.topk), dtype=torch.int32, device=dev)
+    host = [pin(p.q), pin(p.k), pin(p.scales_ue8m0), pin(p.weights), pin(p.starts), pin(p.ends)]
+    hout = [torch.empty((p.rows, p.topk), dtype=torch.int32).pin_memory() for _ in range(2)]
+    sets = []
+    for _ in range(2):
+        d = [torch.empty_like(x, device=dev) for x in host]
+        sets.append({"in": d, "sc": torch.empty(p.keys, dtype=torch.float32, device=dev),
+                     "out": torch.empty((p.rows, p.topk), dtype=torch.int32, device=dev),
+                     "ready": torch.cuda.Event(), "done": torch.cuda.Event(), "free": torch.cuda.Event()})
     wsb = mqa.alloc_workspace(p.rows, heads=p.heads)
-    h2d = sum(x.numel() * x.element_size() for x in (hq, hk, hg, hw, hs, he))
-    d2h = hout.numel() * hout.element_size()
+    h2d = sum(x.numel() * x.element_size() for x in host)
+    d2h = hout[0].numel() * hout[0].element_size()
+    comp = torch.cuda.current_stream()
+    up, down = torch.cuda.Stream(), torch.cuda.Stream()
+    for b in sets:
+        b["free"].record(comp)
 
-    def step():
-        for d, h in ((dq, hq), (dk, hk), (dg, hg), (dw, hw), (ds, hs), (de, he)):
-            d.copy_(h, non_blocking=True)
-        mqa.ue8m0_decode(dg, out=sc)
-        mqa.mqa_topk_prefill(dq, dk, sc, dw, ds, de, p.topk, workspace=wsb, out=dout)
-        hout.copy_(dout, non_blocking=True)
+    def step(i):
+        b = sets[i % 2]
+        with torch.cuda.stream(up):
+            up.wait_event(b["free"])  # the previous use of this set has been computed and read back
+            for d, h in zip(b["in"], host):
+                d.copy_(h, non_blocking=True)
+            b["ready"].record(up)
+        comp.wait_event(b["ready"])
+        dq, dk, dg, dw, ds, de = b["in"]
+        mqa.ue8m0_decode(dg, out=b["sc"])
+        mqa.mqa_topk_prefill(dq, dk, b["sc"], dw, ds, de, p.topk, workspace=wsb, out=b["out"])
+        b["done"].record(comp)
+        with torch.cuda.stream(down):
+            down.wait_event(b["done"])
+            hout[i % 2].copy_(b["out"], non_blocking=True)
+            b["free"].record(down)
+        return b["free"]
 
-    for _ in range(args.warmup):
-        step()
+    for i in range(args.warmup):
+        step(i)
     torch.cuda.synchronize()
     steps = max(3, args.steps // 2)
     barrier(ws)
-    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    a.record()
-    for _ in range(steps):
-        step()
-    b.record()
+    a, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(comp)
+    up.wait_event(a)  # no copy of the timed steps starts before the start event
+    last = None
+    for i in range(steps):
+        last = step(i)
+    comp.wait_event(last)  # the last result is back on the host side
+    e.record(comp)
     torch.cuda.synchronize()
     barrier(ws)
-    ms = max_over_ranks(a.elapsed_time(b), ws, dev)
+    ms = max_over_ranks(a.elapsed_time(e), ws, dev)
     value = sum_over_ranks(float(pairs) * steps, ws, dev) / (ms / 1e3)
     return {"value": value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-            "ms_per_step": ms / steps, "steps": steps, "gpu_launches_per_step": 2}
+            "ms_per_step": ms / steps, "steps": steps, "gpu_launches_per_step": 2,
+            "pipelining": "2 buffer sets; input copies, compute and result copies on 3 streams"}
 
 
 def run_reference(args, ws, rank):

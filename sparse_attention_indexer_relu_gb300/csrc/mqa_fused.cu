@@ -154,6 +154,7 @@ struct Smem {
 };
 
 size_t fused_smem_bytes() { return sizeof(Smem) + 1024; }
+constexpr int kAttrDevices = 64;  // device ordinals the launchers track
 static_assert(sizeof(Smem) + 1024 <= 232448, "shared memory above the 227 KB opt-in limit");
 
 __device__ __forceinline__ Smem &get_smem(uint8_t *raw) {
@@ -2028,13 +2029,25 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-static cudaError_t set_smem_attr(const void *fn) {
-  return cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)fused_smem_bytes());
+// The shared-memory opt-in is a per-device function attribute: set it once on
+// each device a launch runs on (done[] is the calling kernel's own record).
+static cudaError_t set_smem_attr(const void *fn, bool (&done)[kAttrDevices]) {
+  static std::mutex mu;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return cudaGetLastError();
+  if (dev < 0 || dev >= kAttrDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lk(mu);
+  if (done[dev]) return cudaSuccess;
+  const cudaError_t e =
+      cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)fused_smem_bytes());
+  if (e == cudaSuccess) done[dev] = true;
+  return e;
 }
 
 cudaError_t launch_fused_topk(const CUtensorMap &q_map, const CUtensorMap &k_map, const CUtensorMap &s_map,
                               const FusedParams &p, int ctas, cudaStream_t stream, const CUtensorMap *m_map) {
-  static cudaError_t attr = set_smem_attr((const void *)mqa_fused_kernel<false>);
+  static bool attr_done[kAttrDevices] = {};
+  const cudaError_t attr = set_smem_attr((const void *)mqa_fused_kernel<false>, attr_done);
   if (attr != cudaSuccess) return attr;
   // the block-mask map is read only by the masked build; the others get a placeholder
   const CUtensorMap &mm = m_map ? *m_map : s_map;
@@ -2045,7 +2058,8 @@ cudaError_t launch_fused_topk(const CUtensorMap &q_map, const CUtensorMap &k_map
 #if MQA_HEADS == 32 && !MQA_BLOCKS && !MQA_MASKED
 cudaError_t launch_logits(const CUtensorMap &q_map, const CUtensorMap &k_map, const CUtensorMap &s_map,
                           const FusedParams &p, int ctas, cudaStream_t stream) {
-  static cudaError_t attr = set_smem_attr((const void *)mqa_fused_kernel<true>);
+  static bool attr_done[kAttrDevices] = {};
+  const cudaError_t attr = set_smem_attr((const void *)mqa_fused_kernel<true>, attr_done);
   if (attr != cudaSuccess) return attr;
   mqa_fused_kernel<true><<<ctas, kThreads, fused_smem_bytes(), stream>>>(q_map, k_map, s_map, s_map, p);
   return cudaGetLastError();

@@ -354,6 +354,40 @@ def test_fused_max_keys(mqa):
         assert not bad, (r, bad[:5])
 
 
+def test_fused_cuda_graph_replay(mqa):
+    """The fused call captured into a CUDA graph (one memset node and one
+    kernel node on the caller's workspace) and replayed: every replay gives
+    the exact top-k, also after the inputs change in place."""
+    import torch
+    p = synth.random_small(28, 40, 30000, 1024, empty_frac=0.05)
+    q, k, sc, w, s, e = to_device(p)
+    ws = mqa.alloc_workspace(p.rows)
+    out = torch.empty((p.rows, p.topk), dtype=torch.int32, device="cuda")
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        mqa.mqa_topk_prefill(q, k, sc, w, s, e, p.topk, workspace=ws, out=out)  # first use outside capture
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        mqa.mqa_topk_prefill(q, k, sc, w, s, e, p.topk, workspace=ws, out=out)
+    for _ in range(3):
+        out.fill_(7)
+        g.replay()
+        torch.cuda.synchronize()
+        status, stats = mqa.get_status(ws)
+        assert status == 0, stats
+        assert_parity(p, out.cpu().numpy())
+    # new weights in place: the replay reads the current inputs
+    p2 = synth.random_small(29, 40, 30000, 1024, empty_frac=0.05)
+    p2.q, p2.k, p2.scales_ue8m0, p2.starts, p2.ends = p.q, p.k, p.scales_ue8m0, p.starts, p.ends
+    w.copy_(torch.from_numpy(p2.weights).cuda())
+    g.replay()
+    torch.cuda.synchronize()
+    assert_parity(p2, out.cpu().numpy())
+
+
 def test_out_of_range_rows_clamped(mqa):
     p = synth.random_small(26, 8, 3000, 512)
     p.starts[0], p.ends[0] = -5, 700
