@@ -124,7 +124,11 @@ int mqa_topk_workspace_bytes(int device, int rows, size_t *bytes);
  *             stream but not by calls that overlap in time.
  * The result is exact up to ties at the k-th score: a sampled per-row gate
  * filters candidates, and any row the gate cannot serve (too many or too few
- * candidates) is rescanned exactly. */
+ * candidates) is rescanned exactly.
+ * The call only enqueues work on `stream` (a memset of the workspace header
+ * and one kernel launch), so it may be captured into a CUDA graph once a call
+ * outside the capture has run on the device; replays read the buffers'
+ * current contents. */
 int mqa_topk_prefill(const void *q, const void *k, const float *key_scales, const float *weights,
                      const int32_t *starts, const int32_t *ends, int32_t *out, int rows, int keys, int topk,
                      void *workspace, size_t workspace_bytes, void *stream);
