@@ -50,6 +50,12 @@ def load_library(path: str):
     lib.oracle_run_masked.argtypes = [P, P, P, P, P, P, P, ctypes.c_int64, ctypes.c_int64, ctypes.c_int, ctypes.c_int,
                                       ctypes.c_int, P, ctypes.c_int64, P, P, ctypes.c_int]
     lib.oracle_run_masked.restype = ctypes.c_int
+    lib.oracle_e4m3_encode.argtypes = [ctypes.c_double]
+    lib.oracle_e4m3_encode.restype = ctypes.c_uint8
+    lib.oracle_fold_prep.argtypes = [P, P, ctypes.c_int64, ctypes.c_int, ctypes.c_int, ctypes.c_int, P, P, P, P]
+    lib.oracle_fold_score.argtypes = [P, P, P, P, P, P, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int64,
+                                      ctypes.c_int64]
+    lib.oracle_fold_score.restype = ctypes.c_double
     return lib
 
 
@@ -98,6 +104,43 @@ def head_dots(q: np.ndarray, k: np.ndarray, row: int, key: int, lib=None) -> np.
     out = np.empty(heads, np.float64)
     _load(lib).oracle_head_dots(_ptr(q), _ptr(k), heads, dim, row, key, _ptr(out))
     return out
+
+
+FOLD_TERMS = 4
+
+
+def e4m3_encode(x: float, lib=None) -> int:
+    """e4m3fn code nearest to x (|x| <= 448), ties to even."""
+    return int(_load(lib).oracle_e4m3_encode(ctypes.c_double(float(x))))
+
+
+def fold_prep(q, w, terms=FOLD_TERMS, lib=None):
+    """The folded query v = sum_h w_h q_h (fp32, fused multiply-add per head in
+    head order) written as `terms` e4m3 vectors with power-of-two scales.
+    Returns (codes [rows, terms, dim] uint8, exps [rows, terms] int32,
+    v [rows, dim] float32, beta [rows] float64: 2-norm of the last residual)."""
+    q = _c(q, np.uint8)
+    w = _c(w, np.float32)
+    rows, heads, dim = q.shape
+    codes = np.empty((rows, terms, dim), np.uint8)
+    exps = np.empty((rows, terms), np.int32)
+    v = np.empty((rows, dim), np.float32)
+    beta = np.empty(rows, np.float64)
+    _load(lib).oracle_fold_prep(_ptr(q), _ptr(w), rows, heads, dim, terms, _ptr(codes), _ptr(exps), _ptr(v),
+                                _ptr(beta))
+    return codes, exps, v, beta
+
+
+def fold_score(p, codes, exps, row, key, lib=None):
+    """scale_j * (sum_t 2^e_t E(u_t) . E(k_j) + sum_h w_h |s_h|) / 2 in fp64."""
+    q = _c(p.q, np.uint8)
+    k = _c(p.k, np.uint8)
+    g = _c(p.scales_ue8m0, np.uint8)
+    w = _c(p.weights, np.float32)
+    c = _c(codes, np.uint8)
+    e = _c(exps, np.int32)
+    return float(_load(lib).oracle_fold_score(_ptr(q), _ptr(k), _ptr(g), _ptr(w), _ptr(c), _ptr(e), q.shape[1],
+                                              q.shape[2], c.shape[1], int(row), int(key)))
 
 
 def run(p, rows=None, want_topk=True, want_scores=False, topk=None, nthreads=None, lib=None):

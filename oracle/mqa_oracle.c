@@ -309,3 +309,101 @@ int oracle_run_blocks(const uint8_t *q, const uint8_t *k, const uint8_t *scale_g
     return run_mode(q, k, scale_groups, w, starts, ends, row_list, nlist, keys, heads, dim, btopk,
                     out_blocks, NULL, nthreads, 1, NULL, 0);
 }
+
+
+/* ---- the fold --------------------------------------------------------------
+ * vLLM pull request #60618, "What this PR does", Scoring bullet: since
+ * relu(s) = (s + |s|) / 2, the weighted sum of the heads' linear halves is one
+ * query (the heads folded with their weights) times the key, which can run on
+ * the tensor core, leaving only the |s| terms to the math warps:
+ *     sum_h w_h relu(s_h) = ( v . k + sum_h w_h |s_h| ) / 2,  v = sum_h w_h q_h.
+ * The pages give no format for v on the tensor core.  Reading: v is formed in
+ * fp32 with one fused multiply-add per head, heads in order (the e4m3 codes
+ * below are decided in that precision, the kernel's), and written as `terms`
+ * e4m3 vectors with power-of-two scales: term t has exponent e_t, the
+ * smallest integer with max_d |r_t[d]| * 2^-e_t <= 448 (0 when r_t is zero),
+ * codes u_t[d] = e4m3 round-to-nearest-even of r_t[d] * 2^-e_t, and
+ * r_{t+1} = r_t - 2^e_t * E(u_t) (exact in fp32).  beta is the 2-norm of the
+ * last residual: |v . k - sum_t 2^e_t E(u_t) . k| <= beta * |k|_2. */
+
+/* e4m3fn code nearest to x (|x| <= 448), ties to the even code, by search over
+ * the table; the sign of a zero result follows x. */
+uint8_t oracle_e4m3_encode(double x) {
+    pthread_once(&g_table_once, build_table);
+    const int neg = signbit(x) ? 1 : 0;
+    const double a = fabs(x);
+    unsigned best = 0;
+    double bd = INFINITY;
+    for (unsigned c = 0; c < 0x7F; ++c) { /* non-negative finite codes 0x00..0x7E */
+        const double d = fabs(g_e4m3[c] - a);
+        if (d < bd || (d == bd && (c & 1u) == 0u)) {
+            bd = d;
+            best = c;
+        }
+    }
+    return (uint8_t)(best | (neg ? 0x80u : 0u));
+}
+
+/* smallest integer e with m * 2^-e <= 448, for m > 0 */
+static int fold_exponent(double m) {
+    int ex;
+    const double f = frexp(m, &ex); /* m = f * 2^ex, f in [0.5, 1) */
+    return ex - 9 + (f > 0.875 ? 1 : 0);
+}
+
+void oracle_fold_prep(const uint8_t *q, const float *w, int64_t rows, int heads, int dim, int terms,
+                      uint8_t *codes, int32_t *exps, float *v_out, double *beta) {
+    pthread_once(&g_table_once, build_table);
+    float *r = (float *)malloc(sizeof(float) * (size_t)dim);
+    for (int64_t row = 0; row < rows; ++row) {
+        for (int d = 0; d < dim; ++d) {
+            float acc = 0.0f;
+            for (int h = 0; h < heads; ++h)
+                acc = fmaf(w[row * heads + h], (float)g_e4m3[q[(row * heads + h) * (int64_t)dim + d]], acc);
+            r[d] = acc;
+            if (v_out) v_out[row * dim + d] = acc;
+        }
+        for (int t = 0; t < terms; ++t) {
+            float m = 0.0f;
+            for (int d = 0; d < dim; ++d) m = fmaxf(m, fabsf(r[d]));
+            const int e = m > 0.0f ? fold_exponent((double)m) : 0;
+            exps[row * terms + t] = e;
+            uint8_t *u = codes + (row * terms + t) * (int64_t)dim;
+            for (int d = 0; d < dim; ++d) {
+                u[d] = oracle_e4m3_encode(ldexp((double)r[d], -e));
+                r[d] = r[d] - (float)ldexp(g_e4m3[u[d]], e);
+            }
+        }
+        double s = 0.0;
+        for (int d = 0; d < dim; ++d) s += (double)r[d] * (double)r[d];
+        beta[row] = sqrt(s);
+    }
+    free(r);
+}
+
+/* Score of one pair through the fold (what a folded kernel computes, in fp64):
+ * scale_j * ( sum_t 2^e_t E(u_t) . E(k_j) + sum_h w_h |s_h| ) / 2. */
+double oracle_fold_score(const uint8_t *q, const uint8_t *k, const uint8_t *scale_groups, const float *w,
+                         const uint8_t *codes, const int32_t *exps, int heads, int dim, int terms,
+                         int64_t row, int64_t key) {
+    pthread_once(&g_table_once, build_table);
+    const uint8_t *kr = k + key * (int64_t)dim;
+    double lin = 0.0;
+    for (int t = 0; t < terms; ++t) {
+        const uint8_t *u = codes + (row * terms + t) * (int64_t)dim;
+        double acc = 0.0;
+        for (int d = 0; d < dim; ++d) acc += g_e4m3[u[d]] * g_e4m3[kr[d]];
+        lin += ldexp(acc, exps[row * terms + t]);
+    }
+    double ab = 0.0;
+    for (int h = 0; h < heads; ++h) {
+        const uint8_t *qr = q + (row * heads + h) * (int64_t)dim;
+        double acc = 0.0;
+        for (int d = 0; d < dim; ++d) acc += g_e4m3[qr[d]] * g_e4m3[kr[d]];
+        ab += (double)w[row * heads + h] * fabs(acc);
+    }
+    uint32_t bits = ((uint32_t)scale_groups[4 * key]) << 23;
+    float sc;
+    memcpy(&sc, &bits, sizeof sc);
+    return (double)sc * 0.5 * (lin + ab);
+}

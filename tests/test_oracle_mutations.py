@@ -40,6 +40,11 @@ MUTANTS = {
                     "if (x->score > y->score) return 1;\n    if (x->score < y->score) return -1;\n    return (x->block"),
     "mask_bit_index": ("if (!((word >> ((j >> 3) & 31)) & 1u)) continue;", "if (!((word >> ((j >> 4) & 31)) & 1u)) continue;"),
     "mask_ignored": ("            if (J->mask) {", "            if (0) {"),
+    "fold_exponent_low": ("    return ex - 9 + (f > 0.875 ? 1 : 0);", "    return ex - 10 + (f > 0.875 ? 1 : 0);"),
+    "fold_ties_odd": ("if (d < bd || (d == bd && (c & 1u) == 0u)) {", "if (d < bd || (d == bd && (c & 1u) == 1u)) {"),
+    "fold_weight_index": ("acc = fmaf(w[row * heads + h], (float)g_e4m3[q[(row * heads + h) * (int64_t)dim + d]], acc);",
+                          "acc = fmaf(w[row * heads + (heads - 1 - h)], (float)g_e4m3[q[(row * heads + h) * (int64_t)dim + d]], acc);"),
+    "fold_residual_sign": ("r[d] = r[d] - (float)ldexp(g_e4m3[u[d]], e);", "r[d] = r[d] + (float)ldexp(g_e4m3[u[d]], e);"),
     "ue8m0_shift": ("uint32_t bits = ((uint32_t)J->scale_groups[4 * j]) << 23;",
                     "uint32_t bits = ((uint32_t)J->scale_groups[4 * j + 1] + 1) << 23;"),
 }

@@ -487,3 +487,86 @@ def test_masked_integer_bruteforce_tiny(lib=None):
         got, _ = oracle.run_masked(p, mask, topk=6, lib=lib)
         assert got[0][:len(want)].tolist() == want
         assert np.all(got[0][len(want):] == -1)
+
+
+# ---------------------------------------------------------------- the fold (relu(s) = (s + |s|) / 2)
+def _e4m3_values(lib=None):
+    return oracle.e4m3_table(lib=lib)
+
+
+def test_e4m3_encode_is_torch_round_to_nearest_even(lib=None):
+    """The oracle's encoder (search over the table) against torch's float8_e4m3fn
+    cast, an independent RNE implementation, on random values, every halfway
+    point between adjacent codes, subnormals and signed zeros."""
+    tab = _e4m3_values(lib)
+    pos = np.sort(tab[:0x7F])
+    halves = (pos[:-1] + pos[1:]) / 2
+    rng = np.random.default_rng(90)
+    xs = np.concatenate([rng.uniform(-448, 448, 3000), rng.uniform(-2, 2, 2000), rng.uniform(-0.02, 0.02, 1000),
+                         halves, -halves, pos, -pos, [0.0, -0.0, 448.0, -448.0]]).astype(np.float32)
+    want = torch.from_numpy(xs).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    got = np.array([oracle.e4m3_encode(float(x), lib=lib) for x in xs], np.uint8)
+    assert np.array_equal(got, want)
+
+
+def test_fold_query_is_the_weighted_head_sum(lib=None):
+    """v = sum_h w_h E(q_h) formed in fp32: within fp32 rounding of the exact fp64 sum."""
+    p = synth.random_small(91, 12, 100, 512)
+    _, _, v, _ = oracle.fold_prep(p.q, p.weights, lib=lib)
+    tab = _e4m3_values(lib)
+    qd = tab[p.q.astype(np.int64)]                       # [rows, heads, dim]
+    exact = np.einsum("rh,rhd->rd", p.weights.astype(np.float64), qd)
+    bound = 32 * 2.0 ** -24 * np.einsum("rh,rhd->rd", np.abs(p.weights.astype(np.float64)), np.abs(qd))
+    assert np.all(np.abs(v.astype(np.float64) - exact) <= bound + 1e-30)
+
+
+def test_fold_terms_reconstruct_and_are_minimal(lib=None):
+    """sum_t 2^e_t E(u_t) plus the residual rebuilds v exactly; every term's
+    exponent is the smallest that keeps its scaled residual within 448; beta is
+    the residual's 2-norm; with 4 terms the residual is below 2^-16 of v."""
+    tab = _e4m3_values(lib)
+    for seed in (92, 93):
+        p = synth.random_small(seed, 16, 100, 512)
+        p.weights[3] *= 1e6
+        p.weights[5] *= 1e-6
+        codes, exps, v, beta = oracle.fold_prep(p.q, p.weights, lib=lib)
+        for r in range(p.rows):
+            res = v[r].astype(np.float64)
+            for t in range(codes.shape[1]):
+                m = np.abs(res).max()
+                e = int(exps[r, t])
+                if m > 0:
+                    assert m * 2.0 ** -e <= 448 < m * 2.0 ** -(e - 1)
+                term = tab[codes[r, t].astype(np.int64)]
+                assert np.all(np.isfinite(term)) and np.abs(term).max() <= 448
+                res = res - np.ldexp(term, e)
+            assert math.isclose(np.linalg.norm(res), beta[r], rel_tol=1e-12, abs_tol=1e-300)
+            assert beta[r] <= 2.0 ** -16 * np.linalg.norm(v[r].astype(np.float64)) + 1e-300
+
+
+def test_fold_score_identity_and_error_bound(lib=None):
+    """The fold's score equals the definition's up to the residual: the
+    identity scale * (v_exact . k + sum_h w_h |s_h|) / 2 = S holds in fp64, and
+    |S_fold - S| <= scale * beta * |k|_2 / 2 plus the fp32 rounding of v."""
+    p = synth.random_small(94, 6, 400, 512, empty_frac=0.0)
+    p.starts[:] = 0
+    p.ends[:] = p.keys
+    codes, exps, v, beta = oracle.fold_prep(p.q, p.weights, lib=lib)
+    _, scores = oracle.run(p, want_topk=False, want_scores=True, lib=lib)
+    tab = _e4m3_values(lib)
+    qd = tab[p.q.astype(np.int64)]
+    kd = tab[p.k.astype(np.int64)]
+    scale = oracle.ue8m0_decode(p.scales_ue8m0, lib=lib).astype(np.float64)
+    w64 = p.weights.astype(np.float64)
+    v_exact = np.einsum("rh,rhd->rd", w64, qd)
+    s_heads = np.einsum("rhd,jd->rjh", qd, kd)
+    ident = scale[None, :] * 0.5 * (v_exact @ kd.T + np.einsum("rh,rjh->rj", w64, np.abs(s_heads)))
+    assert np.allclose(ident, scores, rtol=1e-12, atol=1e-12 * np.abs(scores).max())
+    rng = np.random.default_rng(95)
+    knorm = np.linalg.norm(kd, axis=1)
+    vround = np.linalg.norm(v.astype(np.float64) - v_exact, axis=1)
+    for _ in range(60):
+        r, j = int(rng.integers(p.rows)), int(rng.integers(p.keys))
+        f = oracle.fold_score(p, codes, exps, r, j, lib=lib)
+        bound = scale[j] * 0.5 * (beta[r] + vround[r]) * knorm[j] * (1 + 1e-9) + 1e-12 * abs(scores[r, j])
+        assert abs(f - scores[r, j]) <= bound, (r, j)
