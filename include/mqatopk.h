@@ -225,6 +225,27 @@ int mqa_topk_prefill_noalloc(const void *q, const void *k, const float *key_scal
  * 1 <= e <= 254).  keys >= 0. */
 int mqa_ue8m0_decode(const uint8_t *scales, float *out, int keys, void *stream);
 
+/* Fold preparation (vLLM pull request #60618, "What this PR does", Scoring
+ * bullet: since relu(s) = (s + |s|) / 2, the heads' weighted linear halves
+ * sum to one folded query v = sum_h w_h q_h times the key).  Per row:
+ *  - v[d] in fp32, one fused multiply-add per head in head order;
+ *  - MQA_FOLD_TERMS e4m3 terms with power-of-two scales: term t has exponent
+ *    e_t, the smallest integer with max_d |r_t[d]| * 2^-e_t <= 448 (0 for a
+ *    zero residual), codes u_t = e4m3 round-to-nearest-even of r_t * 2^-e_t,
+ *    and r_{t+1} = r_t - 2^e_t E(u_t) (r_0 = v);
+ *  - beta = |r_T|_2, so |v . k - sum_t 2^e_t E(u_t) . k| <= beta |k|_2.
+ *  q       [rows, 32, 128] uint8 e4m3fn codes, 16-byte aligned
+ *  weights [rows, 32] fp32
+ *  codes   [rows, MQA_FOLD_TERMS, 128] uint8 (written), 16-byte aligned
+ *  exps    [rows, MQA_FOLD_TERMS] int32 (written)
+ *  beta    [rows] fp32 (written)
+ * rows >= 0 (0 is a no-op).  The fused kernels do not read these yet (the
+ * fold columns need more accumulator columns than the two 256-column buffers
+ * leave); the entry gives callers and later kernels the folded query. */
+#define MQA_FOLD_TERMS 4
+int mqa_fold_prep(const void *q, const float *weights, uint8_t *codes, int32_t *exps, float *beta, int rows,
+                  void *stream);
+
 /* Debug: the scores themselves.  logits is [rows, keys] fp32, row-major;
  * s(r, j) for keys in [starts[r], ends[r]) and -inf elsewhere.  Same inputs
  * and limits as mqa_topk_prefill (topk unused); computed by the same tensor-

@@ -34,7 +34,7 @@ STAT_NAMES = ("status", "rows_rescanned", "compactions", "candidates", "gated_ro
 EXPORTS = ("mqa_topk_workspace_bytes", "mqa_topk_workspace_bytes_ex", "mqa_topk_prefill", "mqa_topk_prefill_ex",
            "mqa_block_topk_prefill", "mqa_topk_prefill_masked", "mqa_block_mask",
            "mqa_topk_prefill_debug", "mqa_topk_prefill_noalloc",
-           "mqa_ue8m0_decode", "mqa_logits_debug", "mqa_topk_dense_baseline", "mqa_topk_get_status",
+           "mqa_ue8m0_decode", "mqa_fold_prep", "mqa_logits_debug", "mqa_topk_dense_baseline", "mqa_topk_get_status",
            "mqa_topk_strerror")
 
 
@@ -73,6 +73,7 @@ def lib():
     L.mqa_block_mask.argtypes = [P, P, P, I, I, I, P, I, P, P]
     L.mqa_topk_prefill_noalloc.argtypes = common + [I, P]
     L.mqa_ue8m0_decode.argtypes = [P, P, I, P]
+    L.mqa_fold_prep.argtypes = [P, P, P, P, P, I, P]
     L.mqa_logits_debug.argtypes = common + [P, S, P]
     L.mqa_topk_dense_baseline.argtypes = common + [I, P, S, P, S, P]
     L.mqa_topk_get_status.argtypes = [P, ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_int32), P]
@@ -173,6 +174,25 @@ def ue8m0_decode(scales, out=None, stream=None):
         out = torch.empty(keys, dtype=torch.float32, device=scales.device)
     _check(lib().mqa_ue8m0_decode(_ptr(scales), _ptr(out), keys, _stream(stream)), "mqa_ue8m0_decode")
     return out
+
+
+FOLD_TERMS = 4
+
+
+def fold_prep(q, weights, stream=None):
+    """Folded query of each row as FOLD_TERMS e4m3 terms with power-of-two
+    scales: returns (codes [rows, FOLD_TERMS, 128] uint8, exps [rows,
+    FOLD_TERMS] int32, beta [rows] float32, the residual's 2-norm)."""
+    torch = _torch()
+    rows = int(q.shape[0])
+    q = _as_u8(q, (rows, HEADS, 128), "q")
+    weights = _as(weights, torch.float32, (rows, HEADS), "weights")
+    codes = torch.empty((rows, FOLD_TERMS, 128), dtype=torch.uint8, device=q.device)
+    exps = torch.empty((rows, FOLD_TERMS), dtype=torch.int32, device=q.device)
+    beta = torch.empty(rows, dtype=torch.float32, device=q.device)
+    _check(lib().mqa_fold_prep(_ptr(q), _ptr(weights), _ptr(codes), _ptr(exps), _ptr(beta), rows, _stream(stream)),
+           "mqa_fold_prep")
+    return codes, exps, beta
 
 
 def mqa_topk_prefill(q, k, key_scales, weights, starts, ends, topk: int, workspace=None, out=None,

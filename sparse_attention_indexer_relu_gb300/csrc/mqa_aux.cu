@@ -1,6 +1,11 @@
-// Auxiliary kernels: UE8M0 key-scale decode and the dense baseline's per-row
-// top-k over materialised logits.
+// Auxiliary kernels: UE8M0 key-scale decode, the dense baseline's per-row
+// top-k over materialised logits, the block mask of the two-level selection
+// and the fold preparation.
+#include "mqa_fold.h"
 #include "mqa_internal.h"
+
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
 #include "ptx.cuh"
 
 namespace mqa {
@@ -192,6 +197,74 @@ cudaError_t launch_block_mask(const int32_t *lists, const int32_t *starts, const
                               cudaStream_t stream) {
   if (rows <= 0) return cudaSuccess;
   block_mask_kernel<<<rows, 256, 0, stream>>>(lists, starts, ends, list_len, keys, mask, mask_words, row_items);
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------- the fold
+// Folded query of each row and its split into e4m3 terms (vLLM pull request
+// #60618, "What this PR does", Scoring bullet: relu(s) = (s + |s|) / 2, so the
+// weighted sum of the heads' linear halves is one query, v = sum_h w_h q_h,
+// times the key).  One warp per row, lane l owns dimensions 4l .. 4l + 3:
+//  - v[d] is formed in fp32 with one fused multiply-add per head, heads in
+//    order;
+//  - term t: e_t is the smallest integer with max_d |r_t[d]| * 2^-e_t <= 448
+//    (0 for a zero residual), u_t[d] = e4m3 round-to-nearest-even of
+//    r_t[d] * 2^-e_t, r_{t+1} = r_t - 2^e_t E(u_t) (exact in fp32);
+//  - beta = the 2-norm of the last residual, which bounds the linear half's
+//    error by beta * |k|_2 for any key k.
+__device__ __forceinline__ float e4m3_value(uint32_t code) {
+  const __half_raw h = __nv_cvt_fp8_to_halfraw((__nv_fp8_storage_t)code, __NV_E4M3);
+  return __half2float(__half(h));
+}
+
+__global__ void __launch_bounds__(256) fold_prep_kernel(const uint8_t *__restrict__ q, const float *__restrict__ w,
+                                                        uint8_t *__restrict__ codes, int32_t *__restrict__ exps,
+                                                        float *__restrict__ beta, int rows) {
+  const int lane = threadIdx.x & 31;
+  const int r = blockIdx.x * 8 + (threadIdx.x >> 5);
+  if (r >= rows) return;
+  const uint8_t *qr = q + (size_t)r * kFoldHeads * kDim;
+  const float *wr = w + (size_t)r * kFoldHeads;
+  float v[4] = {0.f, 0.f, 0.f, 0.f};
+  for (int h = 0; h < kFoldHeads; ++h) {
+    const float wh = wr[h];
+    const uint32_t c4 = *reinterpret_cast<const uint32_t *>(qr + h * kDim + 4 * lane);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) v[i] = fmaf(wh, e4m3_value((c4 >> (8 * i)) & 0xFFu), v[i]);
+  }
+  for (int t = 0; t < kFoldTerms; ++t) {
+    float m = 0.f;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) m = fmaxf(m, fabsf(v[i]));
+    m = __uint_as_float(__reduce_max_sync(0xFFFFFFFFu, __float_as_uint(m)));  // non-negative: bits order as values
+    int e = 0;
+    if (m > 0.f) {
+      int ex;
+      const float fm = frexpf(m, &ex);
+      e = ex - 9 + (fm > 0.875f ? 1 : 0);
+    }
+    uint32_t packed = 0;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint32_t c = __nv_cvt_float_to_fp8(ldexpf(v[i], -e), __NV_SATFINITE, __NV_E4M3);
+      v[i] = v[i] - ldexpf(e4m3_value(c), e);
+      packed |= c << (8 * i);
+    }
+    *reinterpret_cast<uint32_t *>(codes + ((size_t)r * kFoldTerms + t) * kDim + 4 * lane) = packed;
+    if (lane == 0) exps[(size_t)r * kFoldTerms + t] = e;
+  }
+  float ss = 0.f;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) ss = fmaf(v[i], v[i], ss);
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xFFFFFFFFu, ss, off);
+  if (lane == 0) beta[r] = sqrtf(ss);
+}
+
+cudaError_t launch_fold_prep(const uint8_t *q, const float *w, uint8_t *codes, int32_t *exps, float *beta, int rows,
+                             cudaStream_t stream) {
+  if (rows <= 0) return cudaSuccess;
+  fold_prep_kernel<<<(rows + 7) / 8, 256, 0, stream>>>(q, w, codes, exps, beta, rows);
   return cudaGetLastError();
 }
 

@@ -1,6 +1,7 @@
 // C ABI of the library (include/mqatopk.h): argument checks, workspace sizing,
 // TMA descriptor encoding and launches.  Host code only.
 #include "../../include/mqatopk.h"
+#include "mqa_fold.h"
 #include "mqa_internal.h"
 
 #include <cuda.h>
@@ -432,6 +433,23 @@ int mqa_ue8m0_decode(const uint8_t *scales, float *out, int keys, void *stream) 
   int rc = current_device_info(&d);
   if (rc != MQA_OK) return rc;
   return launch_ue8m0_decode(scales, out, keys, as_stream(stream)) == cudaSuccess ? MQA_OK : MQA_ERR_CUDA;
+}
+
+int mqa_fold_prep(const void *q, const float *weights, uint8_t *codes, int32_t *exps, float *beta, int rows,
+                  void *stream) {
+  static_assert(MQA_FOLD_TERMS == kFoldTerms, "fold term count");
+  if (rows < 0) return MQA_ERR_INVALID_ARGUMENT;
+  if (rows == 0) return MQA_OK;
+  if (!q || !weights || !codes || !exps || !beta) return MQA_ERR_INVALID_ARGUMENT;
+  if (!aligned(q, 16) || !aligned(codes, 16) || !aligned(weights, 4) || !aligned(exps, 4) || !aligned(beta, 4))
+    return MQA_ERR_MISALIGNED;
+  DeviceInfo d;
+  int rc = current_device_info(&d);
+  if (rc != MQA_OK) return rc;
+  return launch_fold_prep(reinterpret_cast<const uint8_t *>(q), weights, codes, exps, beta, rows,
+                          as_stream(stream)) == cudaSuccess
+             ? MQA_OK
+             : MQA_ERR_CUDA;
 }
 
 int mqa_logits_debug(const void *q, const void *k, const float *key_scales, const float *weights,

@@ -114,3 +114,12 @@ def test_workspace_query_without_device():
         pytest.skip("device present")
     n = ctypes.c_size_t(0)
     assert mqa.lib().mqa_topk_workspace_bytes(0, 16, ctypes.byref(n)) in (5, 6)
+
+
+def test_fold_prep_rejects_bad_arguments():
+    L = mqa.lib()
+    assert L.mqa_fold_prep(P(0x1000), P(0x2000), P(0x3000), P(0x4000), P(0x5000), -1, None) == 1
+    assert L.mqa_fold_prep(P(0x1000), P(0x2000), P(0x3000), P(0x4000), P(0x5000), 0, None) == 0
+    assert L.mqa_fold_prep(None, P(0x2000), P(0x3000), P(0x4000), P(0x5000), 4, None) == 1
+    assert L.mqa_fold_prep(P(0x1001), P(0x2000), P(0x3000), P(0x4000), P(0x5000), 4, None) == 2
+    assert L.mqa_fold_prep(P(0x1000), P(0x2000), P(0x3008), P(0x4000), P(0x5000), 4, None) == 2

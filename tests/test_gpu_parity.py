@@ -388,6 +388,28 @@ def test_fused_cuda_graph_replay(mqa):
     assert_parity(p2, out.cpu().numpy())
 
 
+@pytest.mark.parametrize("name", ["random", "r2048_32k_k512"])
+def test_fold_prep_bit_exact(mqa, name):
+    """Folded query terms: codes and exponents bit for bit against the oracle
+    (both decide them in fp32), the residual norm to fp32 rounding; rows with
+    weights scaled by 1e6 and 1e-6 and an all-zero row included."""
+    import torch
+    if name == "random":
+        p = synth.random_small(96, 37, 10, 512)
+        p.weights[3] *= 1e6
+        p.weights[4] *= 1e-6
+        p.weights[5] = 0.0
+    else:
+        p = synth.make(name)
+    q = torch.from_numpy(p.q).cuda()
+    w = torch.from_numpy(p.weights).cuda()
+    codes, exps, beta = mqa.fold_prep(q, w)
+    oc, oe, _, ob = oracle.fold_prep(p.q, p.weights)
+    assert np.array_equal(codes.cpu().numpy(), oc)
+    assert np.array_equal(exps.cpu().numpy(), oe)
+    assert np.allclose(beta.cpu().numpy().astype(np.float64), ob, rtol=1e-5, atol=0.0)
+
+
 def test_out_of_range_rows_clamped(mqa):
     p = synth.random_small(26, 8, 3000, 512)
     p.starts[0], p.ends[0] = -5, 700
