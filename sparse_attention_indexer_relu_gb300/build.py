@@ -17,12 +17,14 @@ OUT_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(OUT_DIR, "libmqatopk.so")
 # (source, object, extra flags): the fused kernel is compiled once per head
 # count (32 and 64 index heads per query row), and once each for block
-# selection (top blocks of 8 keys) and masked selection.  The block and masked
+# selection (top blocks of 8 keys), masked selection, and the key selection
+# whose parked epilogue warps select rows in pairs (few-block calls).  The block and masked
 # compilations form every relu on the FMA pipe: for them that measured faster
 # (1.2% and 3.2% at 1M keys) than the default quarter on the ALU pipe.
 SOURCES = [("mqa_fused.cu", "mqa_fused.o", []), ("mqa_fused.cu", "mqa_fused_h64.o", ["-DMQA_HEADS=64"]),
            ("mqa_fused.cu", "mqa_fused_blocks.o", ["-DMQA_BLOCKS=1", "-DMQA_RELU_ALU_CHUNKS=0"]),
            ("mqa_fused.cu", "mqa_fused_masked.o", ["-DMQA_MASKED=1", "-DMQA_RELU_ALU_CHUNKS=0"]),
+           ("mqa_fused.cu", "mqa_fused_pairs.o", ["-DMQA_PAIR_HELPERS=1"]),
            ("mqa_aux.cu", "mqa_aux.o", []), ("mqatopk_api.cu", "mqatopk_api.o", [])]
 HEADERS = ["mqa_internal.h", "ptx.cuh", "mqa_fold.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

@@ -45,7 +45,13 @@
 #ifndef MQA_MASKED
 #define MQA_MASKED 0
 #endif
-#if MQA_BLOCKS
+#ifndef MQA_PAIR_HELPERS
+#define MQA_PAIR_HELPERS 0
+#endif
+#if MQA_PAIR_HELPERS
+#define MQA_KNS h32p
+static_assert(MQA_HEADS == 32 && !MQA_BLOCKS && !MQA_MASKED, "the pair-helper build is the 32-head key selection");
+#elif MQA_BLOCKS
 #define MQA_KNS h32b
 static_assert(MQA_HEADS == 32 && !MQA_MASKED, "block selection is built for 32 heads");
 #elif MQA_MASKED
@@ -151,6 +157,11 @@ struct Smem {
   int selnext[2];    // rows claimed over all uses of the selection slot
   uint32_t selfail[2];
   int prod_parked;   // the producer has issued its last job and waits for every job to retire
+#if MQA_PAIR_HELPERS
+  int pair_cnt[kEpiWarps / 2];  // arrivals at the two-warp syncs of each helper pair (monotonic)
+  int pair_row[kEpiWarps / 2];  // the row the pair's leader claimed
+  int helping[2];               // 1 + the slot use the parked helper pairs select (selection warps then stop claiming)
+#endif
 };
 
 size_t fused_smem_bytes() { return sizeof(Smem) + 1024; }
@@ -1338,6 +1349,10 @@ __device__ __noinline__ int pack_chunk_row(uint32_t *keys_r, int32_t *idx_r, con
 // warps (defined with the selection below).
 __device__ void work_slot_rows(Smem &S, const FusedParams &p, int slot, int use, int *hist, uint32_t *lk,
                                int32_t *li, int lane);
+#if MQA_PAIR_HELPERS
+__device__ void work_slot_rows_pair(Smem &S, const FusedParams &p, int slot, int use, int m, int member, int *hist,
+                                    uint32_t *lk, int32_t *li, int lane);
+#endif
 // Scratch of one helping epilogue warp: a 256-bin histogram and the list.
 constexpr int kHelperScratchBytes = 1024 + 8 * kSelList;
 static_assert(kEpiWarps * kHelperScratchBytes <= (int)(sizeof(Smem::kring) + sizeof(Smem::q)),
@@ -1817,10 +1832,19 @@ __device__ void epilogue(Smem &S, uint32_t tmem, const FusedParams &p, int warp,
       const bool parked =
           bar_or(kEpiBarrier, kEpiThreads, ew == 0 && lane == 0 && *(volatile int *)&S.prod_parked != 0);
       if (parked) {
+#if MQA_PAIR_HELPERS
+        // warps (2i, 2i + 1) select each row together, in the leader's scratch
+        if (ew == 0 && lane == 0) *(volatile int *)&S.helping[slot] = (job_iter >> 1) + 1;
+        uint8_t *scr = &S.kring[0][0] + (size_t)(ew & ~1) * kHelperScratchBytes;
+        work_slot_rows_pair(S, p, slot, job_iter >> 1, ew >> 1, ew & 1, reinterpret_cast<int *>(scr),
+                            reinterpret_cast<uint32_t *>(scr + 1024),
+                            reinterpret_cast<int32_t *>(scr + 1024 + 4 * kSelList), lane);
+#else
         uint8_t *scr = &S.kring[0][0] + (size_t)ew * kHelperScratchBytes;
         work_slot_rows(S, p, slot, job_iter >> 1, reinterpret_cast<int *>(scr),
                        reinterpret_cast<uint32_t *>(scr + 1024), reinterpret_cast<int32_t *>(scr + 1024 + 4 * kSelList),
                        lane);
+#endif
       }
     }
     __syncwarp();
@@ -1828,6 +1852,246 @@ __device__ void epilogue(Smem &S, uint32_t tmem, const FusedParams &p, int warp,
     ++job_iter;
   }
 }
+
+#if MQA_PAIR_HELPERS
+// ------------------------------------------------------------------ two-warp row selection
+// A pair of warps selects one row together: both count half of the row's
+// pieces into one histogram, both gather half of them (output and list slots
+// reserved with shared atomics, so the order is free), and the leader finishes
+// the list.  The two warps meet at bounded syncs on a shared counter.
+__device__ bool pair_sync(Smem &S, int m, const FusedParams &p, int lane) {
+  __threadfence_block();
+  __syncwarp();
+  bool ok = true;
+  if (lane == 0) {
+    const int v = atomicAdd(&S.pair_cnt[m], 1);
+    ok = wait_counter(S, &S.pair_cnt[m], (v / 2 + 1) * 2, p);
+    __threadfence_block();
+  }
+  return __shfl_sync(0xFFFFFFFFu, ok, 0) != 0;
+}
+
+// score_hist over the pieces of this member's batches (hist already zeroed)
+__device__ void score_hist_half(const RowSlab &R, float lo, float inv, int *hist, int lane, int member) {
+  const PieceMap pm = piece_map(R, lane);
+#pragma unroll 1
+  for (int t0 = member * kHistDepth; t0 < pm.total; t0 += 2 * kHistDepth) {
+    int at[kHistDepth], lim[kHistDepth];
+    uint4 kk[kHistDepth];
+#pragma unroll
+    for (int j = 0; j < kHistDepth; ++j) piece_at(R, pm, t0 + j, at[j], lim[j]);
+#pragma unroll
+    for (int j = 0; j < kHistDepth; ++j)
+      kk[j] = 4 * lane < lim[j] ? __ldcg(reinterpret_cast<const uint4 *>(R.keys + at[j] + 4 * lane))
+                                : make_uint4(0, 0, 0, 0);
+#pragma unroll
+    for (int j = 0; j < kHistDepth; ++j) {
+      const int e = 4 * lane;
+      if (e < lim[j]) atomicAdd(&hist[score_bin(key2f(kk[j].x), lo, inv)], 1);
+      if (e + 1 < lim[j]) atomicAdd(&hist[score_bin(key2f(kk[j].y), lo, inv)], 1);
+      if (e + 2 < lim[j]) atomicAdd(&hist[score_bin(key2f(kk[j].z), lo, inv)], 1);
+      if (e + 3 < lim[j]) atomicAdd(&hist[score_bin(key2f(kk[j].w), lo, inv)], 1);
+    }
+  }
+}
+
+constexpr int kPairOut = 200, kPairList = 201;  // shared output / list counters in the leader's histogram
+
+// Returns the leader's written count, 0 for the other member, or -1 (both)
+// when the threshold bin does not fit the list.
+__device__ int pair_select_binned(Smem &S, const FusedParams &p, int m, int member, const RowSlab &R, int k,
+                                  float lo, float inv, int *hist, uint32_t *lk, int32_t *li, int32_t *out, int base,
+                                  int lane) {
+  if (member == 0) {
+    for (int b = lane; b < kScoreBins; b += 32) hist[b] = 0;
+    if (lane == 0) {
+      hist[kPairOut] = 0;
+      hist[kPairList] = 0;
+    }
+  }
+  if (!pair_sync(S, m, p, lane)) return -2;
+  score_hist_half(R, lo, inv, hist, lane, member);
+  if (!pair_sync(S, m, p, lane)) return -2;
+  int c[kBinsPerLane], tot = 0;
+#pragma unroll
+  for (int j = 0; j < kBinsPerLane; ++j) {
+    c[j] = hist[kScoreBins - 1 - kBinsPerLane * lane - j];
+    tot += c[j];
+  }
+  int incl = tot;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int v = __shfl_up_sync(0xFFFFFFFFu, incl, off);
+    if (lane >= off) incl += v;
+  }
+  const int excl = incl - tot;
+  const uint32_t bm = __ballot_sync(0xFFFFFFFFu, excl < k && k <= incl);
+  const int src = bm ? __ffs(bm) - 1 : 31;
+  int B = 0, above = 0, nB = 0;
+  if (lane == src) {
+    int run = excl;
+#pragma unroll
+    for (int j = 0; j < kBinsPerLane; ++j) {
+      if (run + c[j] >= k) {
+        B = kScoreBins - 1 - kBinsPerLane * lane - j;
+        above = run;
+        nB = c[j];
+        break;
+      }
+      run += c[j];
+    }
+  }
+  B = __shfl_sync(0xFFFFFFFFu, B, src);
+  above = __shfl_sync(0xFFFFFFFFu, above, src);
+  nB = __shfl_sync(0xFFFFFFFFu, nB, src);
+  if (nB > kSelList || nB <= 0) return -1;
+  const uint32_t lo_key = f2key(lo);
+  const uint64_t kb_lo = first_key_of_bin(B, lo_key, lo, inv);
+  const uint64_t kb_hi = B == kScoreBins - 1 ? (uint64_t)kKeyPosInf + 1 : first_key_of_bin(B + 1, lo_key, lo, inv);
+  const PieceMap pm = piece_map(R, lane);
+#pragma unroll 1
+  for (int t0 = member * kPass2Groups; t0 < pm.total; t0 += 2 * kPass2Groups) {
+    int at[kPass2Groups], lim[kPass2Groups];
+    uint32_t kk[4 * kPass2Groups];
+    int32_t ii[4 * kPass2Groups];
+#pragma unroll
+    for (int gi = 0; gi < kPass2Groups; ++gi) piece_at(R, pm, t0 + gi, at[gi], lim[gi]);
+#pragma unroll
+    for (int gi = 0; gi < kPass2Groups; ++gi) {
+      uint4 kv = make_uint4(0, 0, 0, 0);
+      int4 iv = make_int4(0, 0, 0, 0);
+      if (4 * lane < lim[gi]) {
+        kv = __ldcg(reinterpret_cast<const uint4 *>(R.keys + at[gi] + 4 * lane));
+        iv = __ldcg(reinterpret_cast<const int4 *>(R.idx + at[gi] + 4 * lane));
+      }
+      kk[4 * gi] = kv.x; kk[4 * gi + 1] = kv.y; kk[4 * gi + 2] = kv.z; kk[4 * gi + 3] = kv.w;
+      ii[4 * gi] = iv.x; ii[4 * gi + 1] = iv.y; ii[4 * gi + 2] = iv.z; ii[4 * gi + 3] = iv.w;
+    }
+    uint32_t up = 0, in = 0;
+#pragma unroll
+    for (int j = 0; j < 4 * kPass2Groups; ++j) {
+      const bool v = 4 * lane + (j & 3) < lim[j >> 2];
+      if (v && kk[j] >= kb_hi) up |= 1u << j;
+      if (v && kk[j] >= kb_lo && kk[j] < kb_hi) in |= 1u << j;
+    }
+    const int packed = __popc(up) + (__popc(in) << 16);
+    int pincl = packed;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int v = __shfl_up_sync(0xFFFFFFFFu, pincl, off);
+      if (lane >= off) pincl += v;
+    }
+    const int pexcl = pincl - packed;
+    const int ptot = __shfl_sync(0xFFFFFFFFu, pincl, 31);
+    int ro = 0, rl = 0;
+    if (lane == 0) {
+      if (ptot & 0xFFFF) ro = atomicAdd(&hist[kPairOut], ptot & 0xFFFF);
+      if (ptot >> 16) rl = atomicAdd(&hist[kPairList], ptot >> 16);
+    }
+    ro = __shfl_sync(0xFFFFFFFFu, ro, 0);
+    rl = __shfl_sync(0xFFFFFFFFu, rl, 0);
+    int po = ro + (pexcl & 0xFFFF), pl = rl + (pexcl >> 16);
+#pragma unroll
+    for (int j = 0; j < 4 * kPass2Groups; ++j) {
+      if ((up >> j) & 1u) {
+        if (po < k) out[po] = out_index(ii[j], base);
+        ++po;
+      }
+      if ((in >> j) & 1u) {
+        if (pl < kSelList) {
+          lk[pl] = kk[j];
+          li[pl] = ii[j];
+        }
+        ++pl;
+      }
+    }
+  }
+  if (!pair_sync(S, m, p, lane)) return -2;
+  if (member != 0) return 0;
+  int outc = hist[kPairOut];
+  const int lc = min(hist[kPairList], kSelList);
+  __syncwarp();
+  // exact threshold among the list: the want-th largest key (as warp_select_binned)
+  const int want = k - above;
+  uint32_t kl = 0xFFFFFFFFu, kh = 0u;
+  for (int i = lane; i < lc; i += 32) {
+    kl = min(kl, lk[i]);
+    kh = max(kh, lk[i]);
+  }
+  kl = __reduce_min_sync(0xFFFFFFFFu, kl);
+  kh = __reduce_max_sync(0xFFFFFFFFu, kh);
+  const uint32_t diff = kl ^ kh;
+  int hb = diff ? 32 - __clz(diff) : 0;
+  uint32_t prefix = hb >= 32 ? 0u : (kh & ~((1u << hb) - 1u));
+  int w = want;
+#pragma unroll 1
+  while (hb > 0) {
+    const int bits = hb >= 8 ? 8 : hb;
+    const int shift = hb - bits;
+    const uint32_t dmask = (1u << bits) - 1u;
+    const uint32_t hi_mask = hb >= 32 ? 0u : (0xFFFFFFFFu << hb);
+    for (int b = lane; b < 256; b += 32) hist[b] = 0;
+    __syncwarp();
+    for (int i = lane; i < lc; i += 32) {
+      const uint32_t v = lk[i];
+      if ((v & hi_mask) == prefix) atomicAdd(&hist[(v >> shift) & dmask], 1);
+    }
+    __syncwarp();
+    int cc[8], t8 = 0;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      cc[j] = hist[255 - 8 * lane - j];
+      t8 += cc[j];
+    }
+    int in8 = t8;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int v = __shfl_up_sync(0xFFFFFFFFu, in8, off);
+      if (lane >= off) in8 += v;
+    }
+    const int ex8 = in8 - t8;
+    const uint32_t bm8 = __ballot_sync(0xFFFFFFFFu, ex8 < w && w <= in8);
+    const int s8 = bm8 ? __ffs(bm8) - 1 : 31;
+    int bin = 0, ab = 0;
+    if (lane == s8) {
+      int run = ex8;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        if (run + cc[j] >= w) {
+          bin = 255 - 8 * lane - j;
+          ab = run;
+          break;
+        }
+        run += cc[j];
+      }
+    }
+    bin = __shfl_sync(0xFFFFFFFFu, bin, s8);
+    ab = __shfl_sync(0xFFFFFFFFu, ab, s8);
+    w -= ab;
+    prefix |= (uint32_t)bin << shift;
+    hb = shift;
+    __syncwarp();
+  }
+  const uint32_t T = prefix;
+  int eq_seen = 0;
+  const uint32_t ltm = lanemask_lt();
+  for (int i0 = 0; i0 < lc; i0 += 32) {
+    const int i = i0 + lane;
+    const bool v = i < lc;
+    const uint32_t key = v ? lk[i] : 0u;
+    const bool gt = v && key > T, eq = v && key == T;
+    const uint32_t eqm = __ballot_sync(0xFFFFFFFFu, eq);
+    const bool take = gt || (eq && eq_seen + __popc(eqm & ltm) < w);
+    const uint32_t tm = __ballot_sync(0xFFFFFFFFu, take);
+    const int pos = outc + __popc(tm & ltm);
+    if (take && pos < k) out[pos] = out_index(li[i], base);
+    outc += __popc(tm);
+    eq_seen += __popc(eqm);
+  }
+  return outc < k ? outc : k;
+}
+
+#endif
 
 // ------------------------------------------------------------------ per-row selection work
 // Row r of the block in selection slot `slot`: its top-k indices go to out,
@@ -1893,7 +2157,12 @@ __device__ void work_slot_rows(Smem &S, const FusedParams &p, int slot, int use,
   const int base = use * kBlockRows;
   for (;;) {
     int r = -1;
-    if (lane == 0) {
+#if MQA_PAIR_HELPERS
+    const bool claim = lane == 0 && *(volatile int *)&S.helping[slot] != use + 1;
+#else
+    const bool claim = lane == 0;
+#endif
+    if (claim) {
       int v = *(volatile int *)&S.selnext[slot];
       while (v < base + kBlockRows) {
         const int w = atomicCAS(&S.selnext[slot], v, v + 1);
@@ -1932,6 +2201,122 @@ __device__ void work_slot_rows(Smem &S, const FusedParams &p, int slot, int use,
 }
 
 // ------------------------------------------------------------------ selection (warps 2-3)
+#if MQA_PAIR_HELPERS
+// Row r selected by pair m (member 0 leads); returns true when the row must
+// be rescanned.  Both members pass the same syncs on every path.
+__device__ bool select_row_pair(Smem &S, const FusedParams &p, int slot, int r, int m, int member, int *hist,
+                                uint32_t *lk, int32_t *li, int lane, bool &ok) {
+  const SelSlot &Q = S.sel[slot];
+  bool fail = false;
+  if (r < Q.nrows && ((Q.mask >> r) & 1u)) {
+    const int cap = p.cap, topk = p.topk, n = Q.n[r];
+    const int rcap = Q.split ? Q.nseg * Q.seglen : cap;
+    uint32_t *slab_keys = Q.split ? p.split_slab + (size_t)Q.bs * 2 * kBlockRows * rcap
+                                  : p.slab + ((size_t)(blockIdx.x * kSlots + slot) * 2 * kBlockRows) * (size_t)cap;
+    int32_t *slab_idx = reinterpret_cast<int32_t *>(slab_keys + (size_t)kBlockRows * rcap);
+    RowSlab R;
+    R.keys = slab_keys + (size_t)r * rcap;
+    R.idx = slab_idx + (size_t)r * rcap;
+    R.seg = Q.seglen;
+    R.nseg = Q.nseg;
+    R.c = &Q.segcnt[r][0];
+    bool over = false;
+    for (int q = 0; q < R.nseg; ++q) over = over || R.c[q] > R.seg;
+    const int cnt = R.total();
+    if (Q.mode == 0) {
+      const bool under = Q.gated[r] && cnt < min(topk, n);
+      if (member == 0 && lane == 0) {
+        if (Q.gated[r]) atomicAdd(p.ws + kWsGatedRows, 1);
+        atomicAdd(p.ws + kWsCandidates, cnt);
+        if (over) atomicAdd(p.ws + kWsOverflowRows, 1);
+        if (under) atomicAdd(p.ws + kWsUnderfillRows, 1);
+      }
+      fail = over || under;
+    } else if (member == 0 && lane == 0) {
+      atomicAdd(p.ws + kWsRowsRescanned, 1);
+    }
+    if (!fail) {
+      int32_t *out = p.out + (size_t)(Q.block * kBlockRows + r) * topk;
+      int wrote = -1;
+      if (cnt > topk && Q.binned[r]) {
+        wrote = pair_select_binned(S, p, m, member, R, topk, Q.blo[r], Q.binv[r], hist, lk, li, out, Q.start[r],
+                                   lane);
+        if (wrote == -2) {
+          ok = false;
+          return false;
+        }
+      }
+      if (member == 0) {
+        if (cnt <= topk) {
+          wrote = warp_emit_out(R, 0u, 0, true, out, Q.start[r], topk, lane);
+        } else if (wrote < 0) {
+          if (Q.binned[r] && lane == 0) atomicAdd(p.ws + kWsSelFallback, 1);
+          int take_eq = 0;
+          const uint32_t T = warp_select_range(R, topk, hist, lane, &take_eq);
+          wrote = warp_emit_out(R, T, take_eq, false, out, Q.start[r], topk, lane);
+        }
+        for (int i = wrote + lane; i < topk; i += 32) out[i] = -1;
+      }
+    }
+  }
+  ok = pair_sync(S, m, p, lane);
+  return fail;
+}
+
+// The rows of the block in selection slot `slot`, claimed by pair m's leader
+// and selected by the pair; the pair's leader counts them done (as work_slot_rows).
+__device__ void work_slot_rows_pair(Smem &S, const FusedParams &p, int slot, int use, int m, int member, int *hist,
+                                    uint32_t *lk, int32_t *li, int lane) {
+  const int base = use * kBlockRows;
+  for (;;) {
+    if (member == 0 && lane == 0) {
+      int r = -1;
+      int v = *(volatile int *)&S.selnext[slot];
+      while (v < base + kBlockRows) {
+        const int w = atomicCAS(&S.selnext[slot], v, v + 1);
+        if (w == v) {
+          r = v - base;
+          break;
+        }
+        v = w;
+      }
+      *(volatile int *)&S.pair_row[m] = r;
+    }
+    if (!pair_sync(S, m, p, lane)) return;
+    const int r = *(volatile int *)&S.pair_row[m];
+    if (r < 0) {
+      // both have read the end marker before the leader may overwrite it
+      pair_sync(S, m, p, lane);
+      return;
+    }
+    bool ok = true;
+    const bool fail = select_row_pair(S, p, slot, r, m, member, hist, lk, li, lane, ok);
+    if (!ok) return;
+    if (member == 0 && lane == 0) {
+      if (fail) atomicOr(&S.selfail[slot], 1u << r);
+      __threadfence_block();
+      const int done = atomicAdd(&S.seldone[slot], 1);
+      if (done == base + kBlockRows - 1) {
+        const SelSlot &Q = S.sel[slot];
+        const uint32_t fm = atomicExch(&S.selfail[slot], 0u);
+        if (fm) {
+          const int tail = S.fifo_tail;
+          S.fifo_block[tail & 7] = Q.block;
+          S.fifo_mask[tail & 7] = fm;
+          __threadfence_block();
+          *(volatile int *)&S.fifo_tail = tail + 1;
+        }
+        __threadfence_block();
+        if (Q.nrows > 0) atomicAdd(p.ws + kWsBlocksDone, 1);
+        atomicAdd(&S.retired, 1);
+        mbar_arrive(&S.s_empty[slot]);
+      }
+    }
+  }
+}
+
+#endif
+
 __device__ void selection(Smem &S, const FusedParams &p, int warp, int lane) {
   const int sw = warp - kSelWarp0;
   int job_iter = 0;
@@ -1987,6 +2372,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     S.nsplit = 0;
     S.nchunks = 1;
     S.prod_parked = 0;
+#if MQA_PAIR_HELPERS
+    S.helping[0] = 0;
+    S.helping[1] = 0;
+    for (int i = 0; i < kEpiWarps / 2; ++i) {
+      S.pair_cnt[i] = 0;
+      S.pair_row[i] = -1;
+    }
+#endif
     fence_mbar_init();
   }
   if (warp == 0 && lane == 0) {
@@ -2055,7 +2448,7 @@ cudaError_t launch_fused_topk(const CUtensorMap &q_map, const CUtensorMap &k_map
   return cudaGetLastError();
 }
 
-#if MQA_HEADS == 32 && !MQA_BLOCKS && !MQA_MASKED
+#if MQA_HEADS == 32 && !MQA_BLOCKS && !MQA_MASKED && !MQA_PAIR_HELPERS
 cudaError_t launch_logits(const CUtensorMap &q_map, const CUtensorMap &k_map, const CUtensorMap &s_map,
                           const FusedParams &p, int ctas, cudaStream_t stream) {
   static bool attr_done[kAttrDevices] = {};
@@ -2068,7 +2461,7 @@ cudaError_t launch_logits(const CUtensorMap &q_map, const CUtensorMap &k_map, co
 
 }  // namespace MQA_KNS
 
-#if MQA_HEADS == 32 && !MQA_BLOCKS && !MQA_MASKED
+#if MQA_HEADS == 32 && !MQA_BLOCKS && !MQA_MASKED && !MQA_PAIR_HELPERS
 // ------------------------------------------------------------------ allocation-free scratch
 // Scratch for mqa_topk_prefill_noalloc: the 256-byte header plus the candidate
 // slabs of at most kStaticScratchCtas persistent CTAs, as a file-scope device

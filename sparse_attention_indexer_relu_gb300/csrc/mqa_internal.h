@@ -117,6 +117,10 @@ namespace h32b {  // block selection: top blocks of 8 keys by their largest scor
 cudaError_t launch_fused_topk(const CUtensorMap &q_map, const CUtensorMap &k_map, const CUtensorMap &s_map,
                               const FusedParams &p, int ctas, cudaStream_t stream, const CUtensorMap *m_map = nullptr);
 }  // namespace h32b
+namespace h32p {  // key selection whose parked epilogue warps select rows in pairs (few-block calls)
+cudaError_t launch_fused_topk(const CUtensorMap &q_map, const CUtensorMap &k_map, const CUtensorMap &s_map,
+                              const FusedParams &p, int ctas, cudaStream_t stream, const CUtensorMap *m_map = nullptr);
+}  // namespace h32p
 namespace h32m {  // masked selection: keys restricted to a per-row block mask
 cudaError_t launch_fused_topk(const CUtensorMap &q_map, const CUtensorMap &k_map, const CUtensorMap &s_map,
                               const FusedParams &p, int ctas, cudaStream_t stream, const CUtensorMap *m_map = nullptr);

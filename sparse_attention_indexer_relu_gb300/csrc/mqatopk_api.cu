@@ -271,9 +271,15 @@ int run_fused(const void *q, const void *k, const float *scales, const float *we
     cudaGetLastError();
     return MQA_ERR_CUDA;
   }
+  // Calls with few blocks per CTA (decode batches, small chunks) end in the
+  // selection of the last blocks' rows: they run the compilation whose parked
+  // epilogue warps select each row in pairs.  It is a separate kernel because
+  // the extra code slows the long scans of the other build by a few percent.
+  const bool few_blocks = (long long)p.nblocks * 4 <= ctas;
   const cudaError_t le = mask     ? h32m::launch_fused_topk(qm, km, sm, p, ctas, st, &mm)
                          : blocks ? h32b::launch_fused_topk(qm, km, sm, p, ctas, st)
                          : heads == 64 ? h64::launch_fused_topk(qm, km, sm, p, ctas, st)
+                         : few_blocks  ? h32p::launch_fused_topk(qm, km, sm, p, ctas, st)
                                        : h32::launch_fused_topk(qm, km, sm, p, ctas, st);
   if (le != cudaSuccess) return MQA_ERR_CUDA;
   return MQA_OK;
