@@ -28,8 +28,9 @@
 //               per-(row, quadrant) slab segments; exact compaction on
 //               rescans; selection help once the producer has no block left.
 // The same source is compiled for 64 index heads (4-row blocks), for block
-// selection (the top blocks of 8 keys) and for masked selection (keys limited
-// to a per-row block mask).
+// selection (the top blocks of 8 keys), for masked selection (keys limited to
+// a per-row block mask) and, for calls with few blocks, with the parked
+// epilogue warps selecting each row in pairs.
 // Every wait is bounded by a time limit; on expiry the kernel records
 // MQA_DEV_WAIT_TIMEOUT in the workspace status word and unwinds.
 #include "mqa_internal.h"
