@@ -76,7 +76,16 @@ extern "C" {
 #define MQA_STAT_END_SPREAD_US 11 /* first to last CTA end, microseconds (tail) */
 #define MQA_STAT_SPLIT_BLOCKS 12  /* blocks whose key range several CTAs scanned
                                      (key chunks merged by the last to finish) */
-#define MQA_STATS_COUNT 13
+#define MQA_STAT_UNSAFE_ROWS 13   /* rows whose weights the fold could not serve
+                                     within its error bound: rescanned exactly
+                                     with the direct head sum */
+#define MQA_STAT_FOLD_BOUND_PPM 14 /* largest fold error bound over the rows the
+                                      fold served, in millionths of the error a
+                                      row allows (2^-16 of its largest |score|);
+                                      above 1000000 a row is unsafe */
+#define MQA_STAT_PAIR_ROWS 15     /* rows selected by a pair of parked epilogue
+                                     warps (few-block calls) */
+#define MQA_STATS_COUNT 16
 
 /* Test-only knobs for mqa_topk_prefill_debug.  Zero-initialise for defaults. */
 typedef struct mqa_topk_debug_options {
@@ -91,6 +100,11 @@ typedef struct mqa_topk_debug_options {
                           kernel unwinds and MQA_DEV_WAIT_TIMEOUT is recorded */
   int wait_timeout_ms; /* bound on every device-side wait; 0 = default (4000) */
   int max_ctas;        /* persistent CTAs; 0 = one per SM */
+  int force_unsafe;    /* 1: every row that the fold would serve is classified
+                          unsafe (rescanned exactly with the direct head sum) */
+  int head_sum;        /* 32-head key selection only: 0 or 2 the direct head
+                          sum (8-row blocks); 1 the relu fold on the tensor
+                          core (6-row blocks) */
 } mqa_topk_debug_options;
 
 /* Bytes of workspace one mqa_topk_prefill call over `rows` rows needs on
@@ -214,10 +228,17 @@ int mqa_topk_prefill_debug(const void *q, const void *k, const float *key_scales
  *  - Every call shares the one array and resets its header on `stream`.
  *    Calls that overlap on the GPU (other streams, other host threads) race
  *    on the scratch and give wrong results: serialise them.
- *  - Device status and counters: not exposed (the scratch is internal). */
+ *  - Device status and counters: mqa_topk_noalloc_get_status. */
 int mqa_topk_prefill_noalloc(const void *q, const void *k, const float *key_scales, const float *weights,
                              const int32_t *starts, const int32_t *ends, int32_t *out, int rows, int keys,
                              int topk, void *stream);
+
+/* Status word and counters of the last mqa_topk_prefill_noalloc call on the
+ * current device, as mqa_topk_get_status reads them from a workspace (the
+ * pages have no counterpart).  A status with MQA_DEV_WAIT_TIMEOUT means that
+ * call's output is undefined.  Synchronises `stream`; status (host) receives
+ * the MQA_DEV_* bits, stats (host, nullable) MQA_STATS_COUNT counters. */
+int mqa_topk_noalloc_get_status(int32_t *status, int32_t *stats, void *stream);
 
 /* UE8M0 -> fp32 key-scale decode (API page, `fused_mqa_topk_key_scales`
  * docstring): scales is [keys, 4] uint8 whose first byte per key is the
@@ -239,9 +260,13 @@ int mqa_ue8m0_decode(const uint8_t *scales, float *out, int keys, void *stream);
  *  codes   [rows, MQA_FOLD_TERMS, 128] uint8 (written), 16-byte aligned
  *  exps    [rows, MQA_FOLD_TERMS] int32 (written)
  *  beta    [rows] fp32 (written)
- * rows >= 0 (0 is a no-op).  The fused kernels do not read these yet (the
- * fold columns need more accumulator columns than the two 256-column buffers
- * leave); the entry gives callers and later kernels the folded query. */
+ * rows >= 0 (0 is a no-op).  The fold compilation of the fused kernel
+ * (mqa_topk_prefill_debug / _ex with head_sum = 1) computes the same terms in
+ * its per-call preparation and runs them as extra accumulator columns; it
+ * classifies a row as unsafe, and rescans it exactly with the direct head
+ * sum, when beta times the largest key_scale * |k|_2 over the keys could move
+ * a score by more than 2^-16 of the row's largest |score| (MQA_STAT_UNSAFE_ROWS,
+ * MQA_STAT_FOLD_BOUND_PPM). */
 #define MQA_FOLD_TERMS 4
 int mqa_fold_prep(const void *q, const float *weights, uint8_t *codes, int32_t *exps, float *beta, int rows,
                   void *stream);

@@ -29,11 +29,11 @@ MQA_OK = 0
 STATUS_BITS = {1: "range_clamped", 2: "wait_timeout", 4: "internal"}
 STAT_NAMES = ("status", "rows_rescanned", "compactions", "candidates", "gated_rows", "blocks_done",
               "sample_tiles", "overflow_rows", "underfill_rows", "select_fallback",
-              "kernel_us", "end_spread_us", "split_blocks")
+              "kernel_us", "end_spread_us", "split_blocks", "unsafe_rows", "fold_bound_ppm", "pair_rows")
 
 EXPORTS = ("mqa_topk_workspace_bytes", "mqa_topk_workspace_bytes_ex", "mqa_topk_prefill", "mqa_topk_prefill_ex",
            "mqa_block_topk_prefill", "mqa_topk_prefill_masked", "mqa_block_mask",
-           "mqa_topk_prefill_debug", "mqa_topk_prefill_noalloc",
+           "mqa_topk_prefill_debug", "mqa_topk_prefill_noalloc", "mqa_topk_noalloc_get_status",
            "mqa_ue8m0_decode", "mqa_fold_prep", "mqa_logits_debug", "mqa_topk_dense_baseline", "mqa_topk_get_status",
            "mqa_topk_strerror")
 
@@ -46,7 +46,8 @@ class MQAError(RuntimeError):
 
 class DebugOptions(ctypes.Structure):
     _fields_ = [("force_gate", ctypes.c_int), ("slab_capacity", ctypes.c_int), ("stall", ctypes.c_int),
-                ("wait_timeout_ms", ctypes.c_int), ("max_ctas", ctypes.c_int)]
+                ("wait_timeout_ms", ctypes.c_int), ("max_ctas", ctypes.c_int), ("force_unsafe", ctypes.c_int),
+                ("head_sum", ctypes.c_int)]
 
 
 _lib = None
@@ -72,6 +73,7 @@ def lib():
     L.mqa_topk_prefill_masked.argtypes = [P, P, P, P, P, P, P, I, P, P, I, I, I, P, S, P, ctypes.POINTER(DebugOptions)]
     L.mqa_block_mask.argtypes = [P, P, P, I, I, I, P, I, P, P]
     L.mqa_topk_prefill_noalloc.argtypes = common + [I, P]
+    L.mqa_topk_noalloc_get_status.argtypes = [ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_int32), P]
     L.mqa_ue8m0_decode.argtypes = [P, P, I, P]
     L.mqa_fold_prep.argtypes = [P, P, P, P, P, I, P]
     L.mqa_logits_debug.argtypes = common + [P, S, P]
@@ -290,6 +292,15 @@ def mqa_topk_prefill_noalloc(q, k, key_scales, weights, starts, ends, topk: int,
                                           _ptr(ends), _ptr(out), rows, keys, int(topk), _stream(stream)),
            "mqa_topk_prefill_noalloc")
     return out
+
+
+def noalloc_get_status(stream=None):
+    """(status bits, {counter name: value}) of the last mqa_topk_prefill_noalloc
+    call on the current device (synchronises)."""
+    st = ctypes.c_int32(0)
+    stats = (ctypes.c_int32 * len(STAT_NAMES))()
+    _check(lib().mqa_topk_noalloc_get_status(ctypes.byref(st), stats, _stream(stream)), "mqa_topk_noalloc_get_status")
+    return int(st.value), dict(zip(STAT_NAMES, [int(v) for v in stats]))
 
 
 def mqa_logits_debug(q, k, key_scales, weights, starts, ends, logits=None, workspace=None, stream=None):

@@ -15,13 +15,17 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 OUT_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(OUT_DIR, "libmqatopk.so")
-# (source, object, extra flags): the fused kernel is compiled once per head
-# count (32 and 64 index heads per query row), and once each for block
-# selection (top blocks of 8 keys), masked selection, and the key selection
-# whose parked epilogue warps select rows in pairs (few-block calls).  The block and masked
+# (source, object, extra flags): the fused kernel is compiled for 32-head key
+# selection with the direct head sum (8-row blocks), for 32-head key selection
+# with the relu fold on the tensor core (6-row blocks), for 64 index heads per
+# query row, and once each for block selection (top blocks of 8 keys), masked
+# selection, and the 8-row key selection whose parked epilogue warps select
+# rows in pairs (few-block calls; it also holds the logits instantiation and
+# the allocation-free scratch).  The block and masked
 # compilations form every relu on the FMA pipe: for them that measured faster
 # (1.2% and 3.2% at 1M keys) than the default quarter on the ALU pipe.
-SOURCES = [("mqa_fused.cu", "mqa_fused.o", []), ("mqa_fused.cu", "mqa_fused_h64.o", ["-DMQA_HEADS=64"]),
+SOURCES = [("mqa_fused.cu", "mqa_fused.o", []), ("mqa_fused.cu", "mqa_fused_fold.o", ["-DMQA_FOLD=1"]),
+           ("mqa_fused.cu", "mqa_fused_h64.o", ["-DMQA_HEADS=64"]),
            ("mqa_fused.cu", "mqa_fused_blocks.o", ["-DMQA_BLOCKS=1", "-DMQA_RELU_ALU_CHUNKS=0"]),
            ("mqa_fused.cu", "mqa_fused_masked.o", ["-DMQA_MASKED=1", "-DMQA_RELU_ALU_CHUNKS=0"]),
            ("mqa_fused.cu", "mqa_fused_pairs.o", ["-DMQA_PAIR_HELPERS=1"]),

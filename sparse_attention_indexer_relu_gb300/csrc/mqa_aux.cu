@@ -217,12 +217,10 @@ __device__ __forceinline__ float e4m3_value(uint32_t code) {
   return __half2float(__half(h));
 }
 
-__global__ void __launch_bounds__(256) fold_prep_kernel(const uint8_t *__restrict__ q, const float *__restrict__ w,
-                                                        uint8_t *__restrict__ codes, int32_t *__restrict__ exps,
-                                                        float *__restrict__ beta, int rows) {
-  const int lane = threadIdx.x & 31;
-  const int r = blockIdx.x * 8 + (threadIdx.x >> 5);
-  if (r >= rows) return;
+// One warp folds row r (lane l owns dimensions 4l .. 4l + 3).
+__device__ __forceinline__ void fold_row(const uint8_t *__restrict__ q, const float *__restrict__ w,
+                                         uint8_t *__restrict__ codes, int32_t *__restrict__ exps,
+                                         float *__restrict__ beta, int r, int lane) {
   const uint8_t *qr = q + (size_t)r * kFoldHeads * kDim;
   const float *wr = w + (size_t)r * kFoldHeads;
   float v[4] = {0.f, 0.f, 0.f, 0.f};
@@ -261,10 +259,75 @@ __global__ void __launch_bounds__(256) fold_prep_kernel(const uint8_t *__restric
   if (lane == 0) beta[r] = sqrtf(ss);
 }
 
+__global__ void __launch_bounds__(256) fold_prep_kernel(const uint8_t *__restrict__ q, const float *__restrict__ w,
+                                                        uint8_t *__restrict__ codes, int32_t *__restrict__ exps,
+                                                        float *__restrict__ beta, int rows) {
+  const int r = blockIdx.x * 8 + (threadIdx.x >> 5);
+  if (r < rows) fold_row(q, w, codes, exps, beta, r, threadIdx.x & 31);
+}
+
 cudaError_t launch_fold_prep(const uint8_t *q, const float *w, uint8_t *codes, int32_t *exps, float *beta, int rows,
                              cudaStream_t stream) {
   if (rows <= 0) return cudaSuccess;
   fold_prep_kernel<<<(rows + 7) / 8, 256, 0, stream>>>(q, w, codes, exps, beta, rows);
+  return cudaGetLastError();
+}
+
+// Per-call preparation for the fold compilation of the fused kernel.  CTAs
+// below row_ctas fold 8 rows each (as fold_prep_kernel); the others bound the
+// keys: key_scale_j * |k_j|_2 for every key (one thread per key; squares of
+// e4m3 values are exact in fp32, the sum and square root round, so the result
+// is scaled up by 2^-15 to stay an upper bound), maximised into *key_norm with
+// an unsigned atomic max on the fp32 bits (non-negative values order as their
+// bits, and every NaN lies above +inf; a NaN code or an infinite scale gives a
+// NaN or inf that every row's bound test rejects).
+__global__ void __launch_bounds__(256) fold_call_prep_kernel(const uint8_t *__restrict__ q,
+                                                             const float *__restrict__ w,
+                                                             const uint8_t *__restrict__ k,
+                                                             const float *__restrict__ scales,
+                                                             uint8_t *__restrict__ codes, int32_t *__restrict__ exps,
+                                                             float *__restrict__ beta, int rows, int keys,
+                                                             int row_ctas, int32_t *key_norm) {
+  const int lane = threadIdx.x & 31;
+  if ((int)blockIdx.x < row_ctas) {
+    const int r = blockIdx.x * 8 + (threadIdx.x >> 5);
+    if (r < rows) fold_row(q, w, codes, exps, beta, r, lane);
+    return;
+  }
+  float best = 0.f;
+  const int stride = (gridDim.x - row_ctas) * blockDim.x;
+  for (int j = (blockIdx.x - row_ctas) * blockDim.x + threadIdx.x; j < keys; j += stride) {
+    const uint4 *kr = reinterpret_cast<const uint4 *>(k + (size_t)j * kDim);
+    float2 acc = make_float2(0.f, 0.f);
+#pragma unroll
+    for (int c = 0; c < kDim / 16; ++c) {
+      const uint4 u = __ldcs(kr + c);
+      const uint32_t wv[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const __half2_raw lo = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(wv[i] & 0xFFFFu), __NV_E4M3);
+        const __half2_raw hi = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(wv[i] >> 16), __NV_E4M3);
+        const float2 a = __half22float2(__half2(lo)), b = __half22float2(__half2(hi));
+        acc = __ffma2_rn(a, a, acc);
+        acc = __ffma2_rn(b, b, acc);
+      }
+    }
+    const float n = sqrtf((acc.x + acc.y) * 1.0000153f) * 1.0000153f * __ldg(scales + j);
+    best = (n > best || n != n) ? n : best;
+  }
+  best = __uint_as_float(__reduce_max_sync(0xFFFFFFFFu, __float_as_uint(best)));
+  if (lane == 0 && best != 0.f) atomicMax(reinterpret_cast<unsigned *>(key_norm), __float_as_uint(best));
+}
+
+cudaError_t launch_fold_call_prep(const uint8_t *q, const float *w, const uint8_t *k, const float *scales,
+                                  uint8_t *codes, int32_t *exps, float *beta, int rows, int keys,
+                                  int32_t *key_norm, cudaStream_t stream) {
+  if (rows <= 0 || keys <= 0) return cudaSuccess;
+  const int row_ctas = (rows + 7) / 8;
+  int key_ctas = (keys + 255) / 256;
+  key_ctas = key_ctas > 1216 ? 1216 : key_ctas;  // 8 per SM of a 152-SM part, grid-stride beyond
+  fold_call_prep_kernel<<<row_ctas + key_ctas, 256, 0, stream>>>(q, w, k, scales, codes, exps, beta, rows, keys,
+                                                                 row_ctas, key_norm);
   return cudaGetLastError();
 }
 

@@ -49,7 +49,11 @@
 #ifndef MQA_PAIR_HELPERS
 #define MQA_PAIR_HELPERS 0
 #endif
-#if MQA_PAIR_HELPERS
+#if MQA_FOLD
+#define MQA_KNS h32f
+static_assert(MQA_HEADS == 32 && !MQA_BLOCKS && !MQA_MASKED && !MQA_PAIR_HELPERS,
+              "the fold build is the 32-head key selection");
+#elif MQA_PAIR_HELPERS
 #define MQA_KNS h32p
 static_assert(MQA_HEADS == 32 && !MQA_BLOCKS && !MQA_MASKED, "the pair-helper build is the 32-head key selection");
 #elif MQA_BLOCKS
@@ -68,6 +72,8 @@ namespace mqa {
 namespace MQA_KNS {
 
 constexpr uint32_t kIdesc = idesc_f8_e4m3_f32(kTileKeys, kCols);
+constexpr uint32_t kTmemAllocCols = 512;  // a power of two holding every accumulator buffer
+
 
 // Selection items: keys, or (block selection) blocks of 8 keys ranked by
 // their largest score.  A block b holds keys [8b, 8b + 8) of the key array.
@@ -104,6 +110,8 @@ struct JobInfo {
   int start[kBlockRows], end[kBlockRows];
   int items[kBlockRows];  // items each row selects from (keys, blocks, or allowed keys)
   alignas(16) float w[kBlockRows][kHeads];
+  alignas(16) float fm[kBlockRows][kFoldRowTerms];  // fold: 2^e_t of the row's folded-query terms
+  float beta[kBlockRows];                           // fold: 2-norm of the row's fold residual
 };
 
 struct SelSlot {  // what the selection warps need from a finished scan
@@ -114,6 +122,9 @@ struct SelSlot {  // what the selection warps need from a finished scan
   int gated[kBlockRows];
   float blo[kBlockRows], binv[kBlockRows];  // score-bin origin (the gate) and bins per unit score
   int binned[kBlockRows];                    // mode-0 gated row: selected through score bins
+  int unsafe[kBlockRows];                    // fold: the gate found the row's fold error bound too large
+  int check[kBlockRows];                     // fold: classify the row in selection (no sampled score)
+  float beta[kBlockRows];                    // fold: 2-norm of the row's fold residual
   int split;    // candidates are in the split slab of block bs, nseg segments of seglen per row
   int bs, nseg, seglen;
   int segcnt[kBlockRows][32];  // records per (row, segment): 4 quadrant segments, or one run per key chunk
@@ -140,11 +151,12 @@ struct Smem {
   uint32_t sel_lk[kSelWarps][kSelList];  // keys of the threshold bin's members
   int32_t sel_li[kSelWarps][kSelList];   // and their key indices
   uint32_t smax[kBlockRows];             // largest sample order key per row (current scan)
+  uint32_t smin[kBlockRows];             // fold: smallest sample order key per row (current scan)
   float binv[kBlockRows];                // score bins per unit score (current scan)
   uint16_t order[kMaxSortBlocks];
   uint64_t k_full[kKStages], k_empty[kKStages];
   uint64_t sc_full[kSStages], sc_empty[kSStages];
-  uint64_t t_full[2], t_empty[2];
+  uint64_t t_full[kTmemBufs], t_empty[kTmemBufs];
   uint64_t j_full[2], j_empty[2];
   uint64_t s_full[2], s_empty[2];
   uint64_t drain, stall_bar;
@@ -158,6 +170,9 @@ struct Smem {
   int selnext[2];    // rows claimed over all uses of the selection slot
   uint32_t selfail[2];
   int prod_parked;   // the producer has issued its last job and waits for every job to retire
+  float key_norm;    // fold: largest key_scale * |k|_2 over the keys (this call)
+  int unsafe[kBlockRows];  // fold: rows of the current scan whose fold error bound is too large
+  int classified[kBlockRows];  // fold: rows of the current scan classified at the gate
 #if MQA_PAIR_HELPERS
   int pair_cnt[kEpiWarps / 2];  // arrivals at the two-warp syncs of each helper pair (monotonic)
   int pair_row[kEpiWarps / 2];  // the row the pair's leader claimed
@@ -321,6 +336,92 @@ __device__ __forceinline__ void score_rows(uint64_t *t_empty, uint32_t base, con
     out[rr] = reduce_keys(aA, aB, aC, aD, lane) * hsc;
   }
 }
+
+#if MQA_FOLD
+// ------------------------------------------------------------------ scoring with the fold
+// relu(s) = (s + |s|) / 2, so sum_h w_h relu(s_h) = (v . k + sum_h w_h |s_h|) / 2
+// with the folded query v = sum_h w_h q_h (vLLM pull request #60618, "What
+// this PR does", Scoring bullet).  The tensor core computes v . k from v's
+// four e4m3 terms: u_t . k in the row's four fold columns, v . k = sum_t
+// 2^e_t u_t . k up to the residual (at most beta |k|_2).  So the head sum is one
+// packed FMA with an absolute-value operand per head pair:
+//     s(r, j) = (scale_j / 2) * (sum_h w_h |s_h| + sum_t 2^e_t u_t . k_j).
+// The direct form (exact rescans) forms 2 relu(s) = s + |s| per head and
+// leaves the fold columns out:  s(r, j) = (scale_j / 2) * sum_h w_h 2 relu(s_h).
+//
+// Thread layout (16x256b loads, as the other compilations): per row, thread
+// t holds keys A..D (t/4, +8, +16, +24) x heads 8i + 2c, 8i + 2c + 1 (c = t %
+// 4), the 4 lanes of a key group then reduce-scatter.  The fold columns of the
+// warp's two rows (rbase even: 8 adjacent columns) arrive with one 16x256b.x1
+// load per half of the lanes: lane c holds terms 2(c % 2), 2(c % 2) + 1 of row
+// rbase + c / 2 for keys A..D, so it adds 2^e-scaled terms into that row's
+// partial sums (the other row's multipliers are zero) before the exchange.
+// Both rows are loaded before one wait and the accumulator buffer is released
+// before any arithmetic.
+static_assert(!kFold || kRowsPerWarp == 2, "the fold layout pairs a warp's rows");
+static_assert(!kFold || kFoldCols == kFoldBoxRows, "fold columns match the fold-term TMA box");
+
+struct FoldM {
+  float2 m[2];  // per row of the warp: (2^e, 2^e') of this lane's two terms, or zeros
+};
+
+__device__ __forceinline__ void tmem_ld_16x256b_x1(uint32_t taddr, uint32_t (&v)[4]) {
+  asm volatile("tcgen05.ld.sync.aligned.16x256b.x1.b32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3])
+               : "r"(taddr)
+               : "memory");
+}
+
+template <bool kDirect>
+__device__ __forceinline__ void score_rows_fold(uint64_t *t_empty, uint32_t base, uint32_t fold_addr,
+                                                const HeadW (&W)[kRowsPerWarp], const FoldM &M, float hsc, int lane,
+                                                float (&out)[kRowsPerWarp]) {
+  uint32_t lo[kRowsPerWarp][16], hi[kRowsPerWarp][16], flo[4], fhi[4];
+#pragma unroll
+  for (int rr = 0; rr < kRowsPerWarp; ++rr) {
+    tmem_ld_16x256b_x4(base + (uint32_t)(rr * kHeads), lo[rr]);
+    tmem_ld_16x256b_x4(base + (16u << 16) + (uint32_t)(rr * kHeads), hi[rr]);
+  }
+  if (!kDirect) {
+    tmem_ld_16x256b_x1(fold_addr, flo);
+    tmem_ld_16x256b_x1(fold_addr + (16u << 16), fhi);
+  }
+  tmem_ld_wait();
+  tc_fence_before();
+  __syncwarp();
+  if (lane == 0) mbar_arrive(t_empty);
+#pragma unroll
+  for (int rr = 0; rr < kRowsPerWarp; ++rr) {
+    float2 aA = make_float2(0.f, 0.f), aB = aA, aC = aA, aD = aA;
+    if (!kDirect) {
+      // this lane's fold terms of keys A, B (low lanes) and C, D (high lanes)
+      aA = __fmul2_rn(make_float2(__uint_as_float(flo[0]), __uint_as_float(flo[1])), M.m[rr]);
+      aB = __fmul2_rn(make_float2(__uint_as_float(flo[2]), __uint_as_float(flo[3])), M.m[rr]);
+      aC = __fmul2_rn(make_float2(__uint_as_float(fhi[0]), __uint_as_float(fhi[1])), M.m[rr]);
+      aD = __fmul2_rn(make_float2(__uint_as_float(fhi[2]), __uint_as_float(fhi[3])), M.m[rr]);
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float2 xA = make_float2(__uint_as_float(lo[rr][4 * i]), __uint_as_float(lo[rr][4 * i + 1]));
+      const float2 xB = make_float2(__uint_as_float(lo[rr][4 * i + 2]), __uint_as_float(lo[rr][4 * i + 3]));
+      const float2 xC = make_float2(__uint_as_float(hi[rr][4 * i]), __uint_as_float(hi[rr][4 * i + 1]));
+      const float2 xD = make_float2(__uint_as_float(hi[rr][4 * i + 2]), __uint_as_float(hi[rr][4 * i + 3]));
+      if (kDirect) {
+        aA = __ffma2_rn(__fadd2_rn(xA, make_float2(fabsf(xA.x), fabsf(xA.y))), W[rr].w[i], aA);
+        aB = __ffma2_rn(__fadd2_rn(xB, make_float2(fabsf(xB.x), fabsf(xB.y))), W[rr].w[i], aB);
+        aC = __ffma2_rn(__fadd2_rn(xC, make_float2(fabsf(xC.x), fabsf(xC.y))), W[rr].w[i], aC);
+        aD = __ffma2_rn(__fadd2_rn(xD, make_float2(fabsf(xD.x), fabsf(xD.y))), W[rr].w[i], aD);
+      } else {
+        aA = __ffma2_rn(make_float2(fabsf(xA.x), fabsf(xA.y)), W[rr].w[i], aA);
+        aB = __ffma2_rn(make_float2(fabsf(xB.x), fabsf(xB.y)), W[rr].w[i], aB);
+        aC = __ffma2_rn(make_float2(fabsf(xC.x), fabsf(xC.y)), W[rr].w[i], aC);
+        aD = __ffma2_rn(make_float2(fabsf(xD.x), fabsf(xD.y)), W[rr].w[i], aD);
+      }
+    }
+    out[rr] = reduce_keys(aA, aB, aC, aD, lane) * hsc;
+  }
+}
+#endif
 
 // ------------------------------------------------------------------ sample gate bins
 // Distance d (in order-key units) below the row's reference maximum, binned on
@@ -576,9 +677,8 @@ __device__ void warp_key_range(const RowSlab &R, int lane, uint32_t *kmin, uint3
 // two, so 8-bit radix digits start at the highest bit where they differ
 // (usually three levels; no pile-up of all keys in one bin).  Eight 16-byte
 // loads per lane are in flight per batch.
-__device__ MQA_SEL_FN uint32_t warp_select_range(const RowSlab &R, int k, int *hist, int lane, int *take_eq) {
-  uint32_t kmin, kmax;
-  warp_key_range(R, lane, &kmin, &kmax);
+__device__ MQA_SEL_FN uint32_t warp_select_range(const RowSlab &R, int k, int *hist, int lane, int *take_eq,
+                                                  uint32_t kmin, uint32_t kmax) {
   const uint32_t diff = kmin ^ kmax;
   int hi = diff ? 32 - __clz(diff) : 0;  // bits [0, hi) vary among the candidates
   uint32_t prefix = hi >= 32 ? 0u : (kmax & ~((1u << hi) - 1u));
@@ -648,6 +748,11 @@ __device__ MQA_SEL_FN uint32_t warp_select_range(const RowSlab &R, int k, int *h
   }
   *take_eq = want;
   return prefix;
+}
+__device__ __forceinline__ uint32_t warp_select_range(const RowSlab &R, int k, int *hist, int lane, int *take_eq) {
+  uint32_t kmin, kmax;
+  warp_key_range(R, lane, &kmin, &kmax);
+  return warp_select_range(R, k, hist, lane, take_eq, kmin, kmax);
 }
 
 // Write the row's top-k indices (idx - base) to out: every key > T plus
@@ -1057,7 +1162,7 @@ __device__ __forceinline__ int sample_tile(const JobInfo &J, int u) {
 // ------------------------------------------------------------------ producer (warp 0)
 template <bool kLogits>
 __device__ void producer(Smem &S, const CUtensorMap *q_map, const CUtensorMap *k_map, const CUtensorMap *s_map,
-                         const CUtensorMap *m_map,
+                         const CUtensorMap *x_map,
                          const FusedParams &p, int lane) {
   const uint64_t pol_k = policy_evict_last(), pol_q = policy_evict_first();
   // claim order: whole blocks, then nsplit blocks as nchunks consecutive key chunks each
@@ -1169,6 +1274,14 @@ __device__ void producer(Smem &S, const CUtensorMap *q_map, const CUtensorMap *k
 #pragma unroll
         for (int h = lane; h < kHeads; h += 32)
           J.w[r][h] = r < nrows ? __ldg(p.weights + (size_t)(r0 + r) * kHeads + h) : 0.f;
+      if constexpr (kFold) {
+        // the folded query's term scales 2^e_t (exact) and residual norm
+        if (lane < kBlockRows * kFoldRowTerms) {
+          const int r = lane / kFoldRowTerms, t = lane % kFoldRowTerms;
+          J.fm[r][t] = r < nrows ? ldexpf(1.f, __ldg(p.fold_exps + (size_t)(r0 + r) * kFoldRowTerms + t)) : 0.f;
+        }
+        if (lane < kBlockRows) J.beta[lane] = lane < nrows ? __ldg(p.fold_beta + r0 + lane) : 0.f;
+      }
       // key range: the union of the taking-part rows' ranges
       const bool live = part && e > s;
       int items = row_items(s, e);
@@ -1227,7 +1340,10 @@ __device__ void producer(Smem &S, const CUtensorMap *q_map, const CUtensorMap *k
     __syncwarp();
     if (lane == 0 && block >= 0 && ntiles > 0) {
       mbar_arrive_expect_tx(&S.j_full[slot], kQBytes);
-      tma_load_2d(&S.q[slot][0], q_map, &S.j_full[slot], 0, block * kCols, pol_q);
+      tma_load_2d(&S.q[slot][0], q_map, &S.j_full[slot], 0, block * kHeadCols, pol_q);
+      // fold: the block's folded-query terms follow its q rows (B operand rows kHeadCols..kCols-1)
+      if (kFold)
+        tma_load_2d(&S.q[slot][kHeadCols * kDim], x_map, &S.j_full[slot], 0, block * kBlockRows * kFoldRowTerms, pol_q);
     } else {
       mbar_arrive(&S.j_full[slot]);
     }
@@ -1248,7 +1364,7 @@ __device__ void producer(Smem &S, const CUtensorMap *q_map, const CUtensorMap *k
           // 16-byte-aligned group of 4 words holding it, for the block's rows
           mbar_arrive_expect_tx(&S.sc_full[sst], kTileKeys * sizeof(float) + sizeof(S.mring[0]));
           tma_load_1d(&S.sring[sst][0], s_map, &S.sc_full[sst], tile * kTileKeys, pol_k);
-          tma_load_2d(&S.mring[sst][0][0], m_map, &S.sc_full[sst], (tile >> 1) & ~3, Jc.block * kBlockRows, pol_k);
+          tma_load_2d(&S.mring[sst][0][0], x_map, &S.sc_full[sst], (tile >> 1) & ~3, Jc.block * kBlockRows, pol_k);
         } else {
           mbar_arrive_expect_tx(&S.sc_full[sst], kTileKeys * sizeof(float));
           tma_load_1d(&S.sring[sst][0], s_map, &S.sc_full[sst], tile * kTileKeys, pol_k);
@@ -1264,33 +1380,41 @@ __device__ void producer(Smem &S, const CUtensorMap *q_map, const CUtensorMap *k
 
 // ------------------------------------------------------------------ MMA issuer (warp 1, lane 0)
 __device__ void mma_issuer(Smem &S, uint32_t tmem, const FusedParams &p) {
-  int job_iter = 0, kcount = 0, tcount = 0;
+  int job_iter = 0;
+  int stage = 0, kphase = 0;  // K ring slot and the parity its full barrier completes with
+  int buf = 0, tphase = 0;    // accumulator buffer and the parity of its current use
+  // Descriptors of the first K slot; a slot (and a 32-byte K step) moves the
+  // start address field (bits 0-13, in 16-byte units) without carrying out of
+  // it, since every shared address is below 2^18.
+  const uint64_t a_desc0 = sw128_kmajor_desc(smem_u32(&S.kring[0][0]));
   for (;;) {
     const int slot = job_iter & 1;
     if (!wait_bar(S, &S.j_full[slot], (job_iter >> 1) & 1, p, kBackoffMma)) break;
     const JobInfo &J = S.job[slot];
     if (J.block < 0) break;
     const int ntiles = 2 * J.ns + J.nt;
-    const uint32_t b_base = smem_u32(&S.q[slot][0]);
+    const uint64_t b_desc = sw128_kmajor_desc(smem_u32(&S.q[slot][0]));
     bool ok = true;
     for (int u = 0; u < ntiles && ok; ++u) {
-      const int stage = kcount % kKStages;
-      const int buf = tcount & 1;
-      ok = wait_bar(S, &S.k_full[stage], (kcount / kKStages) & 1, p, kBackoffMma) &&
-           wait_bar(S, &S.t_empty[buf], ((tcount >> 1) & 1) ^ 1, p, kBackoffMma);
+      ok = wait_bar(S, &S.k_full[stage], kphase, p, kBackoffMma) &&
+           wait_bar(S, &S.t_empty[buf], tphase ^ 1, p, kBackoffMma);
       if (!ok) break;
       tc_fence_after();
-      const uint32_t a_base = smem_u32(&S.kring[stage][0]);
-      const uint32_t d = tmem + (uint32_t)(buf * kCols);
+      const uint64_t a_desc = a_desc0 + (uint64_t)(stage * (kKTileBytes >> 4));
+      const uint32_t d = tmem + (uint32_t)(buf * kTmemStride);
 #pragma unroll
-      for (int kk = 0; kk < kDim / 32; ++kk) {
-        umma_f8(d, sw128_kmajor_desc(a_base + 32 * kk), sw128_kmajor_desc(b_base + 32 * kk), kIdesc,
-                kk > 0 ? 1u : 0u);
-      }
+      for (int kk = 0; kk < kDim / 32; ++kk)
+        umma_f8(d, a_desc + (uint64_t)(2 * kk), b_desc + (uint64_t)(2 * kk), kIdesc, kk > 0 ? 1u : 0u);
       umma_commit(&S.k_empty[stage]);
       umma_commit(&S.t_full[buf]);
-      ++kcount;
-      ++tcount;
+      if (++stage == kKStages) {
+        stage = 0;
+        kphase ^= 1;
+      }
+      if (++buf == kTmemBufs) {
+        buf = 0;
+        tphase ^= 1;
+      }
     }
     if (!ok) break;
     umma_commit(&S.j_empty[slot]);
@@ -1359,6 +1483,29 @@ constexpr int kHelperScratchBytes = 1024 + 8 * kSelList;
 static_assert(kEpiWarps * kHelperScratchBytes <= (int)(sizeof(Smem::kring) + sizeof(Smem::q)),
               "helper scratch exceeds the K ring and q buffers");
 
+#if MQA_FOLD
+// Classification of a row for the fold ("weights unsafe to scale", vLLM pull
+// request #60618, "What this PR does", Exact rescan bullet).  The fold's error
+// on any of the row's scores is at most (scale_j / 2) beta |k_j|_2 <=
+// beta * key_norm / 2 (Cauchy-Schwarz on the folded query's residual).  The
+// row is safe when that bound stays below 2^-16 of the row's largest |score|,
+// of which `seen` (some computed |score| of the row) less the bound is a lower
+// bound.  Non-finite weights or scales make the bound NaN or inf: unsafe.
+// Lane 0 records the bound in millionths of the allowed error (the largest
+// over rows) and, when `count`, counts unsafe rows.  Warp-uniform result.
+__device__ bool fold_safe(const FusedParams &p, float key_norm, float beta, float seen, bool count, int lane) {
+  const float bound = 0.5f * beta * key_norm;
+  const bool safe = p.force_unsafe == 0 && bound * 65537.f <= seen;
+  if (lane == 0) {
+    const float rel = bound * 65537.f / seen;
+    const int ppm = rel < 2000.f ? (int)ceilf(rel * 1e6f) : INT_MAX;  // inf and NaN: INT_MAX
+    atomicMax(p.ws + kWsFoldBound, ppm);
+    if (!safe && count) atomicAdd(p.ws + kWsUnsafeRows, 1);
+  }
+  return safe;
+}
+#endif
+
 // ------------------------------------------------------------------ epilogue (warps 4 and up)
 template <bool kLogits>
 __device__ void epilogue(Smem &S, uint32_t tmem, const FusedParams &p, int warp, int lane) {
@@ -1399,7 +1546,10 @@ __device__ void epilogue(Smem &S, uint32_t tmem, const FusedParams &p, int warp,
         S.ref_frozen[ew] = 0;
         S.msample[ew] = 0;
         S.smax[ew] = 0;
+        S.smin[ew] = 0xFFFFFFFFu;
         S.binv[ew] = 0.f;
+        S.unsafe[ew] = 0;
+        S.classified[ew] = 0;
       }
       if (gate_warp)
         for (int b = lane; b < kGateBins; b += 32) S.hist[ew][b] = 0;
@@ -1412,6 +1562,17 @@ __device__ void epilogue(Smem &S, uint32_t tmem, const FusedParams &p, int warp,
     bool act[kRowsPerWarp];
     float tau[kRowsPerWarp];
     HeadW W[kRowsPerWarp];
+#if MQA_FOLD
+    // the scales 2^e of this lane's two fold terms, for the row they belong to
+    FoldM FM;
+    {
+      const int c = lane & 3;
+#pragma unroll
+      for (int rr = 0; rr < kRowsPerWarp; ++rr)
+        FM.m[rr] = (c >> 1) == rr ? *reinterpret_cast<const float2 *>(&J.fm[rbase + rr][2 * (c & 1)])
+                                  : make_float2(0.f, 0.f);
+    }
+#endif
 #pragma unroll
     for (int rr = 0; rr < kRowsPerWarp; ++rr) {
       const int r = rbase + rr;
@@ -1423,7 +1584,7 @@ __device__ void epilogue(Smem &S, uint32_t tmem, const FusedParams &p, int warp,
 #pragma unroll
       for (int i = 0; i < 4 * kHeadGroups; ++i) {
         const float2 wv = *reinterpret_cast<const float2 *>(&J.w[r][8 * i + 2 * (lane & 3)]);
-        W[rr].w[i] = i < MQA_RELU_ALU_CHUNKS ? make_float2(2.f * wv.x, 2.f * wv.y) : wv;
+        W[rr].w[i] = !kFold && i < MQA_RELU_ALU_CHUNKS ? make_float2(2.f * wv.x, 2.f * wv.y) : wv;
       }
     }
     const int ns = J.ns, ns2 = 2 * J.ns, ntiles = 2 * J.ns + J.nt, mode = J.mode;
@@ -1450,20 +1611,31 @@ __device__ void epilogue(Smem &S, uint32_t tmem, const FusedParams &p, int warp,
       seg_idx = reinterpret_cast<int32_t *>(base + (size_t)kBlockRows * rcap) + off;
     }
     bool bail = false;
-    const int kown = quad * 32 + owned_key(lane);  // key of this thread within a tile
+    // key of this thread within a tile
+    const int kown = quad * 32 + owned_key(lane);
     // One tile: wait for its accumulators and scales, score this lane's key for
-    // the warp's 4 rows (masked to each row's range), release TMEM and scales.
+    // the warp's rows (masked to each row's range), release TMEM and scales.
     auto score_tile = [&](int tile, float (&sv)[kRowsPerWarp]) -> bool {
-      const int buf = tcount & 1, sst = tcount % kSStages;
+      const int buf = tcount % kTmemBufs, sst = tcount % kSStages;
       const int key = tile * kTileKeys + kown;
-      bool ok = wait_bar(S, &S.t_full[buf], (tcount >> 1) & 1, p);
+      bool ok = wait_bar(S, &S.t_full[buf], (tcount / kTmemBufs) & 1, p);
       ok = wait_bar(S, &S.sc_full[sst], (tcount / kSStages) & 1, p) && ok;
       ok = __all_sync(0xFFFFFFFFu, ok);
       tc_fence_after();
       const float hsc = 0.5f * S.sring[sst][kown];
-      const uint32_t base = tmem + lane_addr + (uint32_t)(buf * kCols + rbase * kHeads);
       float raw[kRowsPerWarp];
+#if MQA_FOLD
+      {
+        const uint32_t tb = tmem + lane_addr + (uint32_t)(buf * kTmemStride);
+        const uint32_t hb = tb + (uint32_t)(rbase * kHeads), fb = tb + (uint32_t)(kHeadCols + rbase * kFoldRowTerms);
+        // exact rescans score directly; every other scan through the fold
+        if (mode == 1) score_rows_fold<true>(&S.t_empty[buf], hb, fb, W, FM, hsc, lane, raw);
+        else score_rows_fold<false>(&S.t_empty[buf], hb, fb, W, FM, hsc, lane, raw);
+      }
+#else
+      const uint32_t base = tmem + lane_addr + (uint32_t)(buf * kCols + rbase * kHeads);
       score_rows(&S.t_empty[buf], base, W, hsc, lane, raw);
+#endif
       uint32_t mw[kRowsPerWarp];
       if constexpr (kMasked) {
 #pragma unroll
@@ -1614,6 +1786,10 @@ __device__ void epilogue(Smem &S, uint32_t tmem, const FusedParams &p, int warp,
           if (act[rr]) {
             const uint32_t m = __reduce_max_sync(0xFFFFFFFFu, sv[rr] > NEG_INF ? f2key(sv[rr]) : 0u);
             if (lane == 0 && m) atomicMax(&S.smax[r], m);
+            if constexpr (kFold) {
+              const uint32_t n = __reduce_min_sync(0xFFFFFFFFu, sv[rr] > NEG_INF ? f2key(sv[rr]) : 0xFFFFFFFFu);
+              if (lane == 0 && n != 0xFFFFFFFFu) atomicMin(&S.smin[r], n);
+            }
           }
           if (act[rr] && S.g_on[r] && sv[rr] > NEG_INF) {
             const uint32_t kv = f2key(sv[rr]), klo = S.g_klo[r], khi = S.g_khi[r];
@@ -1663,6 +1839,21 @@ __device__ void epilogue(Smem &S, uint32_t tmem, const FusedParams &p, int warp,
               t = (uint64_t)khi >= drop ? key2f(khi - (uint32_t)drop) : NEG_INF;
             }
           }
+#if MQA_FOLD
+          // A row that needs the fold (more visible keys than top-k) is
+          // classified from its samples' largest |score|; an unsafe row emits
+          // nothing, so it under-fills and is rescanned with the direct sum.
+          if (((J.mask >> r) & 1u) && J.mode == 0 && J.items[r] > p.topk && S.smax[r] != 0) {
+            // the largest |score| among the samples: at the top or the bottom
+            const float seen = fmaxf(fabsf(key2f(S.smax[r])), fabsf(key2f(S.smin[r])));
+            const bool safe = fold_safe(p, S.key_norm, J.beta[r], seen, J.chunk <= 0, lane);
+            if (!safe) t = INFINITY;
+            if (lane == 0) {
+              S.unsafe[r] = !safe;
+              S.classified[r] = 1;
+            }
+          }
+#endif
           if (lane == 0) {
             S.tau[r] = t;
             // linear score bins from the gate to the largest sample score
@@ -1813,6 +2004,10 @@ __device__ void epilogue(Smem &S, uint32_t tmem, const FusedParams &p, int warp,
           Q.blo[lane] = S.tau[lane];
           Q.binv[lane] = S.binv[lane];
           Q.binned[lane] = J.mode == 0 && S.tau[lane] > NEG_INF;
+          Q.unsafe[lane] = kFold && J.mode == 0 && S.unsafe[lane];
+          // rows the gate did not classify that may still need the fold's scores
+          Q.check[lane] = kFold && J.mode == 0 && !S.classified[lane] && J.items[lane] > p.topk;
+          Q.beta[lane] = kFold ? J.beta[lane] : 0.f;
         }
         if (lane == 0) {
           Q.block = J.block;
@@ -2118,14 +2313,16 @@ __device__ bool select_row(Smem &S, const FusedParams &p, int slot, int r, int *
   for (int q = 0; q < R.nseg; ++q) over = over || R.c[q] > R.seg;
   const int cnt = R.total();
   if (Q.mode == 0) {
-    const bool under = Q.gated[r] && cnt < min(topk, n);
+    // a row the fold classified unsafe emitted nothing and is rescanned
+    const bool unsafe = kFold && Q.unsafe[r] != 0;
+    const bool under = !unsafe && Q.gated[r] && cnt < min(topk, n);
     if (lane == 0) {
-      if (Q.gated[r]) atomicAdd(p.ws + kWsGatedRows, 1);
+      if (Q.gated[r] && !unsafe) atomicAdd(p.ws + kWsGatedRows, 1);
       atomicAdd(p.ws + kWsCandidates, cnt);
       if (over) atomicAdd(p.ws + kWsOverflowRows, 1);
       if (under) atomicAdd(p.ws + kWsUnderfillRows, 1);
     }
-    if (over || under) return true;
+    if (over || under || unsafe) return true;
   } else if (lane == 0) {
     atomicAdd(p.ws + kWsRowsRescanned, 1);
   }
@@ -2139,7 +2336,17 @@ __device__ bool select_row(Smem &S, const FusedParams &p, int slot, int r, int *
     if (wrote < 0) {
       if (Q.binned[r] && lane == 0) atomicAdd(p.ws + kWsSelFallback, 1);
       int take_eq = 0;
+#if MQA_FOLD
+      uint32_t kmin, kmax;
+      warp_key_range(R, lane, &kmin, &kmax);
+      // a row the gate did not classify: its candidates are all its visible
+      // keys, so the largest of their |scores| is the row's
+      if (Q.check[r] && !fold_safe(p, S.key_norm, Q.beta[r], fmaxf(fabsf(key2f(kmin)), fabsf(key2f(kmax))), true, lane))
+        return true;
+      const uint32_t T = warp_select_range(R, topk, hist, lane, &take_eq, kmin, kmax);
+#else
       const uint32_t T = warp_select_range(R, topk, hist, lane, &take_eq);
+#endif
       wrote = warp_emit_out(R, T, take_eq, false, out, Q.start[r], topk, lane);
     }
   }
@@ -2294,6 +2501,7 @@ __device__ void work_slot_rows_pair(Smem &S, const FusedParams &p, int slot, int
     const bool fail = select_row_pair(S, p, slot, r, m, member, hist, lk, li, lane, ok);
     if (!ok) return;
     if (member == 0 && lane == 0) {
+      if (r < S.sel[slot].nrows && ((S.sel[slot].mask >> r) & 1u)) atomicAdd(p.ws + kWsPairRows, 1);
       if (fail) atomicOr(&S.selfail[slot], 1u << r);
       __threadfence_block();
       const int done = atomicAdd(&S.seldone[slot], 1);
@@ -2337,7 +2545,7 @@ __device__ void selection(Smem &S, const FusedParams &p, int warp, int lane) {
 template <bool kLogits>
 __global__ void __launch_bounds__(kThreads, 1)
     mqa_fused_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant__ CUtensorMap k_map,
-                     const __grid_constant__ CUtensorMap s_map, const __grid_constant__ CUtensorMap m_map,
+                     const __grid_constant__ CUtensorMap s_map, const __grid_constant__ CUtensorMap x_map,
                      const FusedParams p) {
   extern __shared__ uint8_t smem_raw[];
   Smem &S = get_smem(smem_raw);
@@ -2353,9 +2561,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&S.sc_full[i], 1);
       mbar_init(&S.sc_empty[i], kEpiWarps);
     }
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < kTmemBufs; ++i) {
       mbar_init(&S.t_full[i], 1);
       mbar_init(&S.t_empty[i], kEpiWarps);
+    }
+    for (int i = 0; i < 2; ++i) {
       mbar_init(&S.j_full[i], 32);
       mbar_init(&S.j_empty[i], 1 + kEpiWarps);
       mbar_init(&S.s_full[i], 1);
@@ -2373,6 +2583,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     S.nsplit = 0;
     S.nchunks = 1;
     S.prod_parked = 0;
+    // fold: the per-call preparation wrote the keys' largest scale * |k|_2
+    S.key_norm = kFold && !kLogits ? __int_as_float(__ldcg(p.ws + kWsKeyNorm)) : 0.f;
 #if MQA_PAIR_HELPERS
     S.helping[0] = 0;
     S.helping[1] = 0;
@@ -2387,10 +2599,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_prefetch_desc(&q_map);
     tma_prefetch_desc(&k_map);
     tma_prefetch_desc(&s_map);
-    if (kMasked) tma_prefetch_desc(&m_map);
+    if (kMasked || kFold) tma_prefetch_desc(&x_map);
   }
   if (warp == 1) {
-    tmem_alloc(&S.tmem_base, 2 * kCols);
+    tmem_alloc(&S.tmem_base, kTmemAllocCols);
     tmem_relinquish();
   }
   if (!kLogits) build_order(S, p);
@@ -2402,7 +2614,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = S.tmem_base;
 
   if (warp == 0) {
-    producer<kLogits>(S, &q_map, &k_map, &s_map, &m_map, p, lane);
+    producer<kLogits>(S, &q_map, &k_map, &s_map, &x_map, p, lane);
   } else if (warp == 1) {
     if (lane == 0) mma_issuer(S, tmem, p);
   } else if (warp >= kEpiWarp0) {
@@ -2419,7 +2631,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 1) {
     __syncwarp();
     tc_fence_after();
-    tmem_dealloc(tmem, 2 * kCols);
+    tmem_dealloc(tmem, kTmemAllocCols);
   }
 }
 
@@ -2439,17 +2651,18 @@ static cudaError_t set_smem_attr(const void *fn, bool (&done)[kAttrDevices]) {
 }
 
 cudaError_t launch_fused_topk(const CUtensorMap &q_map, const CUtensorMap &k_map, const CUtensorMap &s_map,
-                              const FusedParams &p, int ctas, cudaStream_t stream, const CUtensorMap *m_map) {
+                              const FusedParams &p, int ctas, cudaStream_t stream, const CUtensorMap *x_map) {
   static bool attr_done[kAttrDevices] = {};
+  if ((kMasked || kFold) && !x_map) return cudaErrorInvalidValue;
   const cudaError_t attr = set_smem_attr((const void *)mqa_fused_kernel<false>, attr_done);
   if (attr != cudaSuccess) return attr;
-  // the block-mask map is read only by the masked build; the others get a placeholder
-  const CUtensorMap &mm = m_map ? *m_map : s_map;
-  mqa_fused_kernel<false><<<ctas, kThreads, fused_smem_bytes(), stream>>>(q_map, k_map, s_map, mm, p);
+  // the extra map is read only by the masked and fold builds; the others get a placeholder
+  const CUtensorMap &xm = x_map ? *x_map : s_map;
+  mqa_fused_kernel<false><<<ctas, kThreads, fused_smem_bytes(), stream>>>(q_map, k_map, s_map, xm, p);
   return cudaGetLastError();
 }
 
-#if MQA_HEADS == 32 && !MQA_BLOCKS && !MQA_MASKED && !MQA_PAIR_HELPERS
+#if MQA_PAIR_HELPERS
 cudaError_t launch_logits(const CUtensorMap &q_map, const CUtensorMap &k_map, const CUtensorMap &s_map,
                           const FusedParams &p, int ctas, cudaStream_t stream) {
   static bool attr_done[kAttrDevices] = {};
@@ -2462,7 +2675,7 @@ cudaError_t launch_logits(const CUtensorMap &q_map, const CUtensorMap &k_map, co
 
 }  // namespace MQA_KNS
 
-#if MQA_HEADS == 32 && !MQA_BLOCKS && !MQA_MASKED && !MQA_PAIR_HELPERS
+#if MQA_PAIR_HELPERS
 // ------------------------------------------------------------------ allocation-free scratch
 // Scratch for mqa_topk_prefill_noalloc: the 256-byte header plus the candidate
 // slabs of at most kStaticScratchCtas persistent CTAs, as a file-scope device

@@ -157,7 +157,7 @@ int split_max_blocks(int ctas, int rows, int brows) {
 
 }  // namespace
 
-FusedLayout mqa::fused_layout(int ctas, int cap, int split_max, int brows) {
+FusedLayout mqa::fused_layout(int ctas, int cap, int split_max, int brows, int fold_rows) {
   FusedLayout L;
   L.done_off = kWsHeaderBytes;
   L.slab_off = L.done_off + (((size_t)split_max * sizeof(int32_t) + 255) / 256) * 256;
@@ -175,7 +175,13 @@ FusedLayout mqa::fused_layout(int ctas, int cap, int split_max, int brows) {
   }
   L.split_words = 2LL * brows * rc;
   L.cnt_off = L.split_off + (size_t)L.split_words * sizeof(uint32_t);
-  L.total = L.cnt_off + (size_t)split_max * brows * 32 * sizeof(int32_t);
+  const size_t cnt_end = L.cnt_off + (size_t)split_max * brows * 32 * sizeof(int32_t);
+  // fold: each row's folded-query terms [rows, 4, 128] (TMA source, 1024-byte
+  // aligned), their exponents [rows, 4] and residual norms [rows]
+  L.fold_codes_off = (cnt_end + 1023) / 1024 * 1024;
+  L.fold_exps_off = L.fold_codes_off + (size_t)fold_rows * kFoldRowTerms * kDim;
+  L.fold_beta_off = L.fold_exps_off + ((size_t)fold_rows * kFoldRowTerms * sizeof(int32_t) + 15) / 16 * 16;
+  L.total = fold_rows > 0 ? L.fold_beta_off + (size_t)fold_rows * sizeof(float) : cnt_end;
   L.reset_bytes = L.slab_off;
   return L;
 }
@@ -184,10 +190,60 @@ namespace {
 
 cudaStream_t as_stream(void *s) { return reinterpret_cast<cudaStream_t>(s); }
 
+// Which compilation of the fused kernel serves a call, and its block shape.
+enum class Build { kDirect, kFold, kPairs, kHeads64, kBlocks, kMasked };
+
+struct Plan {
+  Build build;
+  int brows;     // rows per block
+  int ctas;      // persistent CTAs
+  int split_max; // blocks the split arrays hold (0: no key-range split)
+  FusedLayout L;
+};
+
+// The compilation a call runs on: block selection, masked selection and 64
+// heads have their own.  32-head key selection runs the direct head sum with
+// 8-row blocks; calls with few blocks per CTA (decode batches, small chunks,
+// the allocation-free entry) run its compilation whose parked epilogue warps
+// select rows in pairs.  The fold compilation (6-row blocks) runs when the
+// caller asks for it (debug option head_sum = 1).
+Build pick_build(const DeviceInfo &d, int rows, int heads, bool blocks, bool masked, bool noalloc, int head_sum = 0) {
+  if (masked) return Build::kMasked;
+  if (blocks) return Build::kBlocks;
+  if (heads == 64) return Build::kHeads64;
+  if (noalloc) return Build::kPairs;
+  if (head_sum == 1) return Build::kFold;
+  const int nb8 = (rows + 7) / 8;
+  const int ctas8 = fused_ctas_split(d, rows, 8);
+  return (long long)nb8 * 4 <= ctas8 ? Build::kPairs : Build::kDirect;
+}
+
+int build_rows(Build b) {
+  switch (b) {
+    case Build::kFold: return kFoldBlockRows;
+    case Build::kHeads64: return block_rows(64);
+    default: return block_rows(32);
+  }
+}
+
+// Split plan and workspace layout of a call; max_ctas (0: none) caps the CTAs.
+Plan plan_call(const DeviceInfo &d, Build b, int rows, int cap, int max_ctas, bool allow_split) {
+  Plan P;
+  P.build = b;
+  P.brows = build_rows(b);
+  const int fold_rows = b == Build::kFold ? rows : 0;
+  P.ctas = allow_split ? fused_ctas_split(d, rows, P.brows) : fused_ctas(d, rows, P.brows);
+  if (max_ctas && max_ctas < P.ctas) P.ctas = max_ctas;
+  P.split_max = allow_split ? split_max_blocks(P.ctas, rows, P.brows) : 0;
+  P.L = fused_layout(P.ctas, cap, P.split_max, P.brows, fold_rows);
+  return P;
+}
+
 int run_fused(const void *q, const void *k, const float *scales, const float *weights, const int32_t *starts,
               const int32_t *ends, int32_t *out, int rows, int keys, int topk, int heads, void *workspace,
               size_t workspace_bytes, void *stream, const mqa_topk_debug_options *opt, bool blocks = false,
-              const uint32_t *mask = nullptr, int mask_words = 0, const int32_t *row_items = nullptr) {
+              const uint32_t *mask = nullptr, int mask_words = 0, const int32_t *row_items = nullptr,
+              bool noalloc = false) {
   int rc = check_common(q, k, scales, weights, starts, ends, out, rows, keys);
   if (rc != MQA_OK) return rc;
   if (!valid_topk(topk) || (heads != 32 && heads != 64) || (blocks && heads != 32)) return MQA_ERR_INVALID_ARGUMENT;
@@ -195,7 +251,6 @@ int run_fused(const void *q, const void *k, const float *scales, const float *we
                (long long)mask_words * 256 < (long long)keys))
     return MQA_ERR_INVALID_ARGUMENT;
   if (mask && (!aligned(mask, 16) || !aligned(row_items, 4))) return MQA_ERR_MISALIGNED;
-  const int brows = block_rows(heads);
   if (!workspace) return MQA_ERR_INVALID_ARGUMENT;
   if (!aligned(workspace, 256)) return MQA_ERR_MISALIGNED;
   int cap = kDefaultSlabCap;
@@ -205,31 +260,36 @@ int run_fused(const void *q, const void *k, const float *scales, const float *we
     if (cap % (kQuads * 32) != 0 || cap / kQuads < topk + 64 || cap > kDefaultSlabCap)
       return MQA_ERR_INVALID_ARGUMENT;
   }
-  if (opt && (opt->force_gate < 0 || opt->force_gate > 2 || opt->wait_timeout_ms < 0 || opt->max_ctas < 0))
+  if (opt && (opt->force_gate < 0 || opt->force_gate > 2 || opt->wait_timeout_ms < 0 || opt->max_ctas < 0 ||
+              opt->force_unsafe < 0 || opt->force_unsafe > 1 || opt->head_sum < 0 || opt->head_sum > 2))
     return MQA_ERR_INVALID_ARGUMENT;
   if (rows == 0) return MQA_OK;
   DeviceInfo d;
   rc = current_device_info(&d);
   if (rc != MQA_OK) return rc;
+  const int max_ctas = opt ? opt->max_ctas : 0;
+  const Build b = pick_build(d, rows, heads, blocks, mask != nullptr, noalloc, opt ? opt->head_sum : 0);
   // key-range split when the workspace holds its arrays (mqa_topk_workspace_bytes
   // sizes for it), else one CTA per block as far as SMs go
-  int ctas = fused_ctas_split(d, rows, brows);
-  if (opt && opt->max_ctas && opt->max_ctas < ctas) ctas = opt->max_ctas;
-  int split_max = split_max_blocks(ctas, rows, brows);
-  FusedLayout L = fused_layout(ctas, cap, split_max, brows);
-  if (workspace_bytes < L.total) {
-    ctas = fused_ctas(d, rows, brows);
-    if (opt && opt->max_ctas && opt->max_ctas < ctas) ctas = opt->max_ctas;
-    split_max = 0;
-    L = fused_layout(ctas, cap, 0, brows);
-    if (workspace_bytes < L.total) return MQA_ERR_WORKSPACE_TOO_SMALL;
+  Plan P = plan_call(d, b, rows, cap, max_ctas, true);
+  if (workspace_bytes < P.L.total) {
+    P = plan_call(d, b, rows, cap, max_ctas, false);
+    if (workspace_bytes < P.L.total) return MQA_ERR_WORKSPACE_TOO_SMALL;
   }
+  const FusedLayout &L = P.L;
+  const int brows = P.brows;
   rc = get_encoder();
   if (rc != MQA_OK) return rc;
-  CUtensorMap qm, km, sm, mm;
-  if (mask && encode_mask(&mm, mask, (uint64_t)rows, (uint64_t)mask_words) != MQA_OK) return MQA_ERR_CUDA;
-  // q is [rows * heads, 128]: a block's 256 (row, head) rows per TMA box
-  if (encode_rows128(&qm, q, (uint64_t)rows * heads, kCols) != MQA_OK ||
+  uint8_t *wsb = reinterpret_cast<uint8_t *>(workspace);
+  CUtensorMap qm, km, sm, xm;
+  if (mask && encode_mask(&xm, mask, (uint64_t)rows, (uint64_t)mask_words) != MQA_OK) return MQA_ERR_CUDA;
+  // the fold compilation's B operand rows: the block's folded-query terms after its q rows
+  if (b == Build::kFold &&
+      encode_rows128(&xm, wsb + L.fold_codes_off, (uint64_t)rows * kFoldRowTerms, kFoldBoxRows) !=
+          MQA_OK)
+    return MQA_ERR_CUDA;
+  // q is [rows * heads, 128]: a block's (row, head) rows per TMA box
+  if (encode_rows128(&qm, q, (uint64_t)rows * heads, (uint32_t)(brows * heads)) != MQA_OK ||
       encode_rows128(&km, k, (uint64_t)keys, kTileKeys) != MQA_OK || encode_scales(&sm, scales, keys) != MQA_OK)
     return MQA_ERR_CUDA;
   FusedParams p;
@@ -240,14 +300,17 @@ int run_fused(const void *q, const void *k, const float *scales, const float *we
   p.ends = ends;
   p.out = out;
   p.ws = reinterpret_cast<int32_t *>(workspace);
-  uint8_t *wsb = reinterpret_cast<uint8_t *>(workspace);
   p.slab = reinterpret_cast<uint32_t *>(wsb + L.slab_off);
-  p.split_max = split_max;
-  if (split_max > 0) {
+  p.split_max = P.split_max;
+  if (P.split_max > 0) {
     p.split_done = reinterpret_cast<int32_t *>(wsb + L.done_off);
     p.split_slab = reinterpret_cast<uint32_t *>(wsb + L.split_off);
     p.split_cnt = reinterpret_cast<int32_t *>(wsb + L.cnt_off);
     p.split_words = L.split_words;
+  }
+  if (b == Build::kFold) {
+    p.fold_exps = reinterpret_cast<const int32_t *>(wsb + L.fold_exps_off);
+    p.fold_beta = reinterpret_cast<const float *>(wsb + L.fold_beta_off);
   }
   p.rows = rows;
   p.keys = keys;
@@ -264,6 +327,7 @@ int run_fused(const void *q, const void *k, const float *scales, const float *we
   // candidates to the selection (and every row the slab cannot hold)
   p.gate_min = 2 * p.gate_target;
   p.force_gate = opt ? opt->force_gate : 0;
+  p.force_unsafe = opt ? opt->force_unsafe : 0;
   p.stall = opt ? opt->stall : 0;
   p.timeout_ns = (long long)((opt && opt->wait_timeout_ms) ? opt->wait_timeout_ms : 4000) * 1000000LL;
   cudaStream_t st = as_stream(stream);
@@ -271,16 +335,21 @@ int run_fused(const void *q, const void *k, const float *scales, const float *we
     cudaGetLastError();
     return MQA_ERR_CUDA;
   }
-  // Calls with few blocks per CTA (decode batches, small chunks) end in the
-  // selection of the last blocks' rows: they run the compilation whose parked
-  // epilogue warps select each row in pairs.  It is a separate kernel because
-  // the extra code slows the long scans of the other build by a few percent.
-  const bool few_blocks = (long long)p.nblocks * 4 <= ctas;
-  const cudaError_t le = mask     ? h32m::launch_fused_topk(qm, km, sm, p, ctas, st, &mm)
-                         : blocks ? h32b::launch_fused_topk(qm, km, sm, p, ctas, st)
-                         : heads == 64 ? h64::launch_fused_topk(qm, km, sm, p, ctas, st)
-                         : few_blocks  ? h32p::launch_fused_topk(qm, km, sm, p, ctas, st)
-                                       : h32::launch_fused_topk(qm, km, sm, p, ctas, st);
+  if (b == Build::kFold &&
+      launch_fold_call_prep(reinterpret_cast<const uint8_t *>(q), weights, reinterpret_cast<const uint8_t *>(k), scales,
+                            wsb + L.fold_codes_off, reinterpret_cast<int32_t *>(wsb + L.fold_exps_off),
+                            reinterpret_cast<float *>(wsb + L.fold_beta_off), rows, keys, p.ws + kWsKeyNorm,
+                            st) != cudaSuccess)
+    return MQA_ERR_CUDA;
+  cudaError_t le = cudaSuccess;
+  switch (b) {
+    case Build::kMasked: le = h32m::launch_fused_topk(qm, km, sm, p, P.ctas, st, &xm); break;
+    case Build::kBlocks: le = h32b::launch_fused_topk(qm, km, sm, p, P.ctas, st); break;
+    case Build::kHeads64: le = h64::launch_fused_topk(qm, km, sm, p, P.ctas, st); break;
+    case Build::kPairs: le = h32p::launch_fused_topk(qm, km, sm, p, P.ctas, st); break;
+    case Build::kFold: le = h32f::launch_fused_topk(qm, km, sm, p, P.ctas, st, &xm); break;
+    case Build::kDirect: le = h32::launch_fused_topk(qm, km, sm, p, P.ctas, st); break;
+  }
   if (le != cudaSuccess) return MQA_ERR_CUDA;
   return MQA_OK;
 }
@@ -319,7 +388,7 @@ int run_logits_chunk(const DeviceInfo &d, const uint8_t *q, const void *k, const
     cudaGetLastError();
     return MQA_ERR_CUDA;
   }
-  return h32::launch_logits(qm, km, sm, p, ctas, st) == cudaSuccess ? MQA_OK : MQA_ERR_CUDA;
+  return h32p::launch_logits(qm, km, sm, p, ctas, st) == cudaSuccess ? MQA_OK : MQA_ERR_CUDA;
 }
 
 }  // namespace
@@ -335,9 +404,8 @@ int mqa_topk_workspace_bytes_ex(int device, int rows, int heads, size_t *bytes) 
     *bytes = kWsHeaderBytes;
     return MQA_OK;
   }
-  const int brows = block_rows(heads);
-  const int ctas = fused_ctas_split(d, rows, brows);
-  *bytes = fused_layout(ctas, kDefaultSlabCap, split_max_blocks(ctas, rows, brows), brows).total;
+  const Build b = pick_build(d, rows, heads, false, false, false);
+  *bytes = plan_call(d, b, rows, kDefaultSlabCap, 0, true).L.total;
   return MQA_OK;
 }
 
@@ -412,12 +480,21 @@ int mqa_topk_prefill_noalloc(const void *q, const void *k, const float *key_scal
   DeviceInfo d;
   rc = current_device_info(&d);
   if (rc != MQA_OK) return rc;
-  // The scratch need is set by the CTA count, which this entry caps; a call
-  // whose need exceeded the static array would be rejected here.
-  int ctas = fused_ctas(d, rows, 8);
-  if (ctas > kStaticScratchCtas) ctas = kStaticScratchCtas;
-  const size_t need = fused_layout(ctas, kDefaultSlabCap, 0, 8).total;
-  if (need > kStaticScratchBytes) return MQA_ERR_WORKSPACE_TOO_SMALL;
+  // The scratch need is set by the CTA count, which this entry caps: the most
+  // CTAs (at most kStaticScratchCtas) whose layout with the key-range split
+  // fits the array, else the unsplit layout of up to kStaticScratchCtas CTAs
+  // (which always fits).  The call runs the direct head sum (8-row blocks),
+  // whose scratch does not grow with rows or keys.
+  int ctas = 0;
+  for (int c = kStaticScratchCtas; c >= 1 && !ctas; --c) {
+    const Plan P = plan_call(d, Build::kPairs, rows, kDefaultSlabCap, c, true);
+    if (P.split_max > 0 && P.L.total <= kStaticScratchBytes) ctas = P.ctas;
+  }
+  if (!ctas) {
+    const Plan P = plan_call(d, Build::kPairs, rows, kDefaultSlabCap, kStaticScratchCtas, false);
+    if (P.L.total > kStaticScratchBytes) return MQA_ERR_WORKSPACE_TOO_SMALL;
+    ctas = P.ctas;
+  }
   void *scratch = nullptr;
   if (static_scratch_address(&scratch) != cudaSuccess) {
     cudaGetLastError();
@@ -427,7 +504,20 @@ int mqa_topk_prefill_noalloc(const void *q, const void *k, const float *key_scal
   std::memset(&opt, 0, sizeof opt);
   opt.max_ctas = ctas;
   return run_fused(q, k, key_scales, weights, starts, ends, out, rows, keys, topk, 32, scratch,
-                   kStaticScratchBytes, stream, &opt);
+                   kStaticScratchBytes, stream, &opt, false, nullptr, 0, nullptr, true);
+}
+
+int mqa_topk_noalloc_get_status(int32_t *status, int32_t *stats, void *stream) {
+  if (!status) return MQA_ERR_INVALID_ARGUMENT;
+  DeviceInfo d;
+  int rc = current_device_info(&d);
+  if (rc != MQA_OK) return rc;
+  void *scratch = nullptr;
+  if (static_scratch_address(&scratch) != cudaSuccess) {
+    cudaGetLastError();
+    return MQA_ERR_CUDA;
+  }
+  return mqa_topk_get_status(scratch, status, stats, stream);
 }
 
 int mqa_ue8m0_decode(const uint8_t *scales, float *out, int keys, void *stream) {
@@ -534,6 +624,9 @@ int mqa_topk_get_status(const void *workspace, int32_t *status, int32_t *stats, 
     stats[MQA_STAT_UNDERFILL_ROWS] = h[kWsUnderfillRows];
     stats[MQA_STAT_SELECT_FALLBACK] = h[kWsSelFallback];
     stats[MQA_STAT_SPLIT_BLOCKS] = h[kWsSplitBlocks];
+    stats[MQA_STAT_UNSAFE_ROWS] = h[kWsUnsafeRows];
+    stats[MQA_STAT_FOLD_BOUND_PPM] = h[kWsFoldBound];
+    stats[MQA_STAT_PAIR_ROWS] = h[kWsPairRows];
     uint64_t t_start_inv, t_end_inv, t_end;
     memcpy(&t_start_inv, h + kWsTStartMinInv, 8);
     memcpy(&t_end_inv, h + kWsTEndMinInv, 8);
