@@ -161,6 +161,9 @@ def test_fused_key_split_few_blocks(mqa):
     assert status == 0, stats
     assert stats["split_blocks"] == 3, stats
     assert stats["gated_rows"] == 24 and stats["rows_rescanned"] == 0, stats
+    # few blocks per CTA: the compilation whose parked epilogue warps select
+    # rows in pairs took part in the selection
+    assert stats["pair_rows"] > 0, stats
     assert_parity(p, got)
 
 
