@@ -238,6 +238,8 @@ def main():
             mqa.mqa_block_topk_prefill(q, k, scales, w, s, e, 2048, workspace=wsb, out=blk)
             bmask, items = mqa.block_mask(blk, s, e, p.keys)
             out = torch.empty((p.rows, 512), dtype=torch.int32, device=dev)
+            # the consumer scores only the keys its mask allows
+            pairs = int(items.to(torch.int64).sum().item())
 
             def step():
                 mqa.mqa_topk_prefill_masked(q, k, scales, w, s, e, bmask, items, 512, workspace=wsb, out=out)
@@ -283,6 +285,7 @@ def main():
 
     # roofline of the fused kernel (tensor-bound: 8192 flop per scored pair)
     k_ms = statistics.mean(kernel_ms)
+    k_ms_median = statistics.median(kernel_ms)
     achieved = pairs * plan.FLOP_PER_PAIR / (k_ms / 1e3) / 1e12
     peak, peak_src = fp8_peak_tflops()
     traffic = load_traffic(args.workload) if args.mode == "topk" else None
@@ -294,9 +297,11 @@ def main():
         "config": {"workload": args.workload if args.mode == "topk" else f"{args.workload} {args.mode}",
                    "rows": p.rows, "keys": p.keys,
                    "topk": {"topk": p.topk, "blocks": 2048, "masked": 512}[args.mode], "pairs": pairs,
+                   "visible_pairs": p.pairs(),
                    "heads": p.heads, "head_dim": 128, "parallelism": f"replicas x{ws}",
                    "l2": l2_note(p), "cuda_graph": bool(args.graph)},
         "rows_per_s": rows_per_s,
+        "step_ms_median": k_ms_median,
         "gpu_launches": args.steps,
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                      "frac": achieved / peak, "traffic": traffic,

@@ -85,7 +85,10 @@ extern "C" {
                                       above 1000000 a row is unsafe */
 #define MQA_STAT_PAIR_ROWS 15     /* rows selected by a pair of parked epilogue
                                      warps (few-block calls) */
-#define MQA_STATS_COUNT 16
+#define MQA_STAT_SKIPPED_TILES 16 /* masked selection: 128-key tiles left
+                                     unscored because no row of the block
+                                     allows a key in them */
+#define MQA_STATS_COUNT 17
 
 /* Test-only knobs for mqa_topk_prefill_debug.  Zero-initialise for defaults. */
 typedef struct mqa_topk_debug_options {

@@ -29,7 +29,8 @@ MQA_OK = 0
 STATUS_BITS = {1: "range_clamped", 2: "wait_timeout", 4: "internal"}
 STAT_NAMES = ("status", "rows_rescanned", "compactions", "candidates", "gated_rows", "blocks_done",
               "sample_tiles", "overflow_rows", "underfill_rows", "select_fallback",
-              "kernel_us", "end_spread_us", "split_blocks", "unsafe_rows", "fold_bound_ppm", "pair_rows")
+              "kernel_us", "end_spread_us", "split_blocks", "unsafe_rows", "fold_bound_ppm", "pair_rows",
+              "skipped_tiles")
 
 EXPORTS = ("mqa_topk_workspace_bytes", "mqa_topk_workspace_bytes_ex", "mqa_topk_prefill", "mqa_topk_prefill_ex",
            "mqa_block_topk_prefill", "mqa_topk_prefill_masked", "mqa_block_mask",

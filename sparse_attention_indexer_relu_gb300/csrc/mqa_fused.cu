@@ -81,6 +81,7 @@ constexpr bool kBlocks = MQA_BLOCKS != 0;
 // Masked selection: a key is visible only if its block of 8 is set in the
 // row's block mask (bit (j / 8) % 32 of word j / 256).
 constexpr bool kMasked = MQA_MASKED != 0;
+constexpr int kSkipTiles = 8192;  // masked selection: longest tile range the skip bitmap covers
 // Items a row with visible keys [s, e) selects from.
 __host__ __device__ __forceinline__ int row_items(int s, int e) {
   if (e <= s) return 0;
@@ -112,6 +113,13 @@ struct JobInfo {
   alignas(16) float w[kBlockRows][kHeads];
   alignas(16) float fm[kBlockRows][kFoldRowTerms];  // fold: 2^e_t of the row's folded-query terms
   float beta[kBlockRows];                           // fold: 2-norm of the row's fold residual
+#if MQA_MASKED
+  // Masked selection: main tile i takes part when bit (i + toff) of tbytes is
+  // set (some taking-part row has an allowed block in it); every tile takes
+  // part when skip == 0 (ranges longer than the bitmap).
+  int skip, toff;
+  uint8_t tbytes[kSkipTiles / 8 + 8];
+#endif
 };
 
 struct SelSlot {  // what the selection warps need from a finished scan
@@ -1154,6 +1162,20 @@ __device__ void build_order(Smem &S, const FusedParams &p) {
   __syncthreads();
 }
 
+// Masked selection: does main tile i of the job hold an allowed key of some
+// taking-part row?  (Always true in the other compilations.)
+__device__ __forceinline__ bool tile_on(const JobInfo &J, int i) {
+#if MQA_MASKED
+  if (!J.skip) return true;
+  const int b = i + J.toff;
+  return (J.tbytes[b >> 3] >> (b & 7)) & 1u;
+#else
+  (void)J;
+  (void)i;
+  return true;
+#endif
+}
+
 __device__ __forceinline__ int sample_tile(const JobInfo &J, int u) {
   // (2u + 1) * nt < 2^31 for nt <= 2^17 tiles and u < 64
   return J.s_lo_t + (int)((unsigned)((2 * u + 1) * J.s_nt) / (unsigned)(2 * J.ns));
@@ -1333,6 +1355,43 @@ __device__ void producer(Smem &S, const CUtensorMap *q_map, const CUtensorMap *k
         J.s_lo_t = s_lo_t;
         J.s_nt = s_nt;
       }
+#if MQA_MASKED
+      {
+        // Which main tiles hold an allowed block of a taking-part row: lane
+        // l covers 8-tile groups l, l + 32, ... from base (lo_t rounded down
+        // to 8), one 16-byte load of 4 mask words (8 tiles) per row and group.
+        const int base = lo_t & ~7, ngroups = (lo_t + nt - base + 7) >> 3;
+        const bool skip = !kLogits && nt > 0 && nt <= kSkipTiles;
+        int skipped = 0;
+        if (skip) {
+          for (int g = lane; g < ngroups; g += 32) {
+            uint32_t on = 0, in = 0;
+#pragma unroll
+            for (int r = 0; r < kBlockRows; ++r) {
+              if (!((pm >> r) & 1u)) continue;
+              const uint4 w4 = __ldg(reinterpret_cast<const uint4 *>(p.mask + (size_t)(r0 + r) * p.mask_words +
+                                                                     (base >> 1) + 4 * g));
+              const uint32_t wv[4] = {w4.x, w4.y, w4.z, w4.w};
+#pragma unroll
+              for (int k = 0; k < 8; ++k)
+                if ((wv[k >> 1] >> (16 * (k & 1))) & 0xFFFFu) on |= 1u << k;
+            }
+            const int t0 = base + 8 * g;
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+              if (t0 + k >= lo_t && t0 + k < lo_t + nt) in |= 1u << k;
+            J.tbytes[g] = (uint8_t)(on & in);
+            skipped += __popc(in) - __popc(on & in);
+          }
+        }
+        skipped = __reduce_add_sync(0xFFFFFFFFu, skipped);
+        if (lane == 0) {
+          J.skip = skip;
+          J.toff = lo_t - base;
+          if (skipped) atomicAdd(p.ws + kWsSkippedTiles, skipped);
+        }
+      }
+#endif
       ntiles = 2 * ns + nt;
     } else if (lane == 0) {
       J.block = -1;
@@ -1351,6 +1410,7 @@ __device__ void producer(Smem &S, const CUtensorMap *q_map, const CUtensorMap *k
     if (lane == 0) {
       const JobInfo &Jc = S.job[slot];
       for (int u = 0; u < ntiles; ++u) {
+        if (u >= 2 * Jc.ns && !tile_on(Jc, u - 2 * Jc.ns)) continue;
         const int tile = u < 2 * Jc.ns ? sample_tile(Jc, u < Jc.ns ? u : u - Jc.ns) : Jc.lo_t + (u - 2 * Jc.ns);
         const int stage = kcount % kKStages;
         const int sst = kcount % kSStages;
@@ -1396,6 +1456,7 @@ __device__ void mma_issuer(Smem &S, uint32_t tmem, const FusedParams &p) {
     const uint64_t b_desc = sw128_kmajor_desc(smem_u32(&S.q[slot][0]));
     bool ok = true;
     for (int u = 0; u < ntiles && ok; ++u) {
+      if (u >= 2 * J.ns && !tile_on(J, u - 2 * J.ns)) continue;
       ok = wait_bar(S, &S.k_full[stage], kphase, p, kBackoffMma) &&
            wait_bar(S, &S.t_empty[buf], tphase ^ 1, p, kBackoffMma);
       if (!ok) break;
@@ -1870,6 +1931,7 @@ __device__ void epilogue(Smem &S, uint32_t tmem, const FusedParams &p, int warp,
     }
     // ---- main tiles
     for (int u = ns2; u < ntiles && !bail; ++u) {
+      if (!tile_on(J, u - ns2)) continue;
       const int tile = J.lo_t + (u - ns2);
       const int key = tile * kTileKeys + kown;
       float sv[kRowsPerWarp];

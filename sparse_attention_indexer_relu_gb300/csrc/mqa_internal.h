@@ -89,6 +89,7 @@ enum WsWord : int {
   kWsUnsafeRows = 19,    // fold: rows whose fold error bound was too large (rescanned exactly)
   kWsFoldBound = 20,     // fold: largest error bound over classified rows, ppm of the allowed error
   kWsPairRows = 21,      // rows selected by a pair of parked epilogue warps
+  kWsSkippedTiles = 22,  // masked selection: tiles left out (no allowed key in any of the block's rows)
   kWsWords = 64
 };
 constexpr size_t kWsHeaderBytes = 256;
@@ -114,6 +115,8 @@ struct FusedParams {
   int split_max;         // split blocks the arrays above hold
   long long split_words; // uint32 words of split_slab
   const int32_t *row_items;  // masked selection: allowed keys per row
+  const uint32_t *mask;      // masked selection: [rows, mask_words] block-mask words
+  int mask_words;
   const int32_t *fold_exps;  // fold: [rows, 4] power-of-two exponents of the folded query's terms
   const float *fold_beta;    // fold: [rows] 2-norm of the folded query's residual
   int rows;              // rows of this call

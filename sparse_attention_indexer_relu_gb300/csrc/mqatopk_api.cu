@@ -317,6 +317,8 @@ int run_fused(const void *q, const void *k, const float *scales, const float *we
   p.topk = topk;
   p.nblocks = (rows + brows - 1) / brows;
   p.row_items = row_items;
+  p.mask = mask;
+  p.mask_words = mask_words;
   p.cap = cap;
   p.gate_target = 3 * topk < cap / 2 ? 3 * topk : cap / 2;
   // Masked rows see few of their range's keys, so a sample of the range holds
@@ -627,6 +629,7 @@ int mqa_topk_get_status(const void *workspace, int32_t *status, int32_t *stats, 
     stats[MQA_STAT_UNSAFE_ROWS] = h[kWsUnsafeRows];
     stats[MQA_STAT_FOLD_BOUND_PPM] = h[kWsFoldBound];
     stats[MQA_STAT_PAIR_ROWS] = h[kWsPairRows];
+    stats[MQA_STAT_SKIPPED_TILES] = h[kWsSkippedTiles];
     uint64_t t_start_inv, t_end_inv, t_end;
     memcpy(&t_start_inv, h + kWsTStartMinInv, 8);
     memcpy(&t_end_inv, h + kWsTEndMinInv, 8);

@@ -300,6 +300,49 @@ def test_masked_selection_random_masks(mqa, seed, rows, keys, topk, frac):
     assert_masked_parity(p, got, mask)
 
 
+def _expected_skipped_tiles(p, mask, block_rows=8):
+    """Main tiles of each row block's key range (the union of its rows'
+    ranges) in which no row of the block allows a key."""
+    total = 0
+    for b0 in range(0, p.rows, block_rows):
+        rr = [r for r in range(b0, min(p.rows, b0 + block_rows)) if p.ends[r] > p.starts[r]]
+        if not rr:
+            continue
+        lo = min(int(p.starts[r]) for r in rr)
+        hi = max(int(p.ends[r]) for r in rr)
+        for t in range(lo // 128, (hi + 127) // 128):
+            half = (mask[b0:b0 + block_rows, t // 2] >> np.uint32(16 * (t % 2))) & np.uint32(0xFFFF)
+            total += int(not half.any())
+    return total
+
+
+def test_masked_skips_tiles_without_allowed_keys(mqa):
+    """Each row allows blocks in one narrow window of a long range: the tiles
+    no row of a block allows are left out (counted exactly when no row is
+    rescanned) and the result still equals the oracle's."""
+    rng = np.random.default_rng(75)
+    p = synth.random_small(75, 24, 200000, 512, empty_frac=0.0)
+    keys = p.keys
+    lists = np.full((p.rows, 1024), -1, np.int32)
+    for r in range(p.rows):
+        nb = (int(p.ends[r]) - 1) // 8 - int(p.starts[r]) // 8 + 1
+        win = min(nb, 2000)
+        w0 = int(rng.integers(0, nb - win + 1))
+        pick = w0 + rng.choice(win, size=min(700, win), replace=False)
+        lists[r, :len(pick)] = pick
+    words = ((keys + 1023) // 1024) * 4
+    mask, items = numpy_block_mask(lists, p.starts, p.ends, keys, words)
+    got, status, stats = run_masked(mqa, p, mask, items)
+    assert status == 0, stats
+    want = _expected_skipped_tiles(p, mask)
+    assert want > 0
+    if stats["rows_rescanned"] == 0:
+        assert stats["skipped_tiles"] == want, (stats, want)
+    else:
+        assert stats["skipped_tiles"] >= want, (stats, want)
+    assert_masked_parity(p, got, mask)
+
+
 def test_two_level_source_then_consumer(mqa):
     """The two-level chain on long causal rows: the oracle's top 2048 blocks of
     8 keys (source) restrict the consumer's top-512."""
