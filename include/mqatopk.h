@@ -108,6 +108,9 @@ typedef struct mqa_topk_debug_options {
   int head_sum;        /* 32-head key selection only: 0 or 2 the direct head
                           sum (8-row blocks); 1 the relu fold on the tensor
                           core (6-row blocks) */
+  int masked_scan;     /* masked selection only: 0 gathers each row's allowed
+                          blocks and scores only them; 1 scans every tile of
+                          each 8-row block's key range and masks the scores */
 } mqa_topk_debug_options;
 
 /* Bytes of workspace one mqa_topk_prefill call over `rows` rows needs on
@@ -191,8 +194,17 @@ int mqa_block_topk_prefill(const void *q, const void *k, const float *key_scales
  *  mask       [rows, mask_words] uint32, 16-byte aligned; mask_words a multiple
  *             of 4 and >= ceil(keys / 256)
  *  row_items  [rows] int32: the number of visible keys of each row (it sizes
- *             the row's sampled gate); mqa_block_mask writes it
- * 32 heads; workspace as for mqa_topk_prefill. */
+ *             the row's sampled gate in the scan of opt->masked_scan = 1;
+ *             the default path reads the mask alone); mqa_block_mask writes it
+ * By default each row's allowed blocks are gathered from k and only their
+ * keys are scored (the page's remark that scoring only the candidate blocks
+ * speeds the consumers up): the workspace needs only the 256-byte header,
+ * the cost follows the allowed keys, and the statistics count rows finished
+ * (MQA_STAT_BLOCKS_DONE) and visible keys scored (MQA_STAT_CANDIDATES).  With
+ * opt->masked_scan = 1 the fused scan of mqa_topk_prefill runs instead over
+ * every tile of each 8-row block's range (tiles no row of the block allows
+ * are left out, MQA_STAT_SKIPPED_TILES) with the full workspace.
+ * 32 heads; workspace as for mqa_topk_prefill (header only by default). */
 int mqa_topk_prefill_masked(const void *q, const void *k, const float *key_scales, const float *weights,
                             const int32_t *starts, const int32_t *ends, const uint32_t *mask, int mask_words,
                             const int32_t *row_items, int32_t *out, int rows, int keys, int topk, void *workspace,

@@ -48,7 +48,7 @@ class MQAError(RuntimeError):
 class DebugOptions(ctypes.Structure):
     _fields_ = [("force_gate", ctypes.c_int), ("slab_capacity", ctypes.c_int), ("stall", ctypes.c_int),
                 ("wait_timeout_ms", ctypes.c_int), ("max_ctas", ctypes.c_int), ("force_unsafe", ctypes.c_int),
-                ("head_sum", ctypes.c_int)]
+                ("head_sum", ctypes.c_int), ("masked_scan", ctypes.c_int)]
 
 
 _lib = None

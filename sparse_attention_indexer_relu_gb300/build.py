@@ -29,7 +29,8 @@ SOURCES = [("mqa_fused.cu", "mqa_fused.o", []), ("mqa_fused.cu", "mqa_fused_fold
            ("mqa_fused.cu", "mqa_fused_blocks.o", ["-DMQA_BLOCKS=1", "-DMQA_RELU_ALU_CHUNKS=0"]),
            ("mqa_fused.cu", "mqa_fused_masked.o", ["-DMQA_MASKED=1", "-DMQA_RELU_ALU_CHUNKS=0"]),
            ("mqa_fused.cu", "mqa_fused_pairs.o", ["-DMQA_PAIR_HELPERS=1"]),
-           ("mqa_aux.cu", "mqa_aux.o", []), ("mqatopk_api.cu", "mqatopk_api.o", [])]
+           ("mqa_gather.cu", "mqa_gather.o", []), ("mqa_aux.cu", "mqa_aux.o", []),
+           ("mqatopk_api.cu", "mqatopk_api.o", [])]
 HEADERS = ["mqa_internal.h", "ptx.cuh", "mqa_fold.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

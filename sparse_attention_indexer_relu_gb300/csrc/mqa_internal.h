@@ -164,6 +164,25 @@ namespace h32m {  // masked selection: keys restricted to a per-row block mask
 cudaError_t launch_fused_topk(const CUtensorMap &q_map, const CUtensorMap &k_map, const CUtensorMap &s_map,
                               const FusedParams &p, int ctas, cudaStream_t stream, const CUtensorMap *x_map = nullptr);
 }  // namespace h32m
+// Masked selection that gathers each row's allowed blocks and scores only
+// them (32 heads): one persistent CTA per SM, rows claimed through the
+// header's claim word.  q_map: q as [rows * 32, 128] in boxes of 32 rows.
+struct GatherParams {
+  const uint8_t *k;       // [keys, 128] e4m3 codes, 16-byte aligned
+  const float *scales;    // [keys] fp32
+  const float *weights;   // [rows, 32]
+  const int32_t *starts;  // [rows]
+  const int32_t *ends;    // [rows]
+  const uint32_t *mask;   // [rows, mask_words] block-mask words
+  int mask_words;
+  int32_t *out;           // [rows, topk]
+  int32_t *ws;            // workspace header (int32 words)
+  int rows, keys, topk;
+  int stall;              // debug: wait on a barrier nobody arrives on
+  long long timeout_ns;   // bound on every wait
+};
+size_t gather_smem_bytes();
+cudaError_t launch_gather_masked(const CUtensorMap &q_map, const GatherParams &p, int ctas, cudaStream_t stream);
 cudaError_t launch_block_mask(const int32_t *lists, const int32_t *starts, const int32_t *ends, int rows,
                               int list_len, int keys, uint32_t *mask, int mask_words, int32_t *row_items,
                               cudaStream_t stream);

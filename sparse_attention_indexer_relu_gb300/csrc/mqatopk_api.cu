@@ -239,6 +239,43 @@ Plan plan_call(const DeviceInfo &d, Build b, int rows, int cap, int max_ctas, bo
   return P;
 }
 
+// Masked selection through the gathering kernel: the workspace header only.
+int run_gather(const DeviceInfo &d, const void *q, const void *k, const float *scales, const float *weights,
+               const int32_t *starts, const int32_t *ends, const uint32_t *mask, int mask_words, int32_t *out,
+               int rows, int keys, int topk, void *workspace, size_t workspace_bytes, void *stream,
+               const mqa_topk_debug_options *opt) {
+  if (workspace_bytes < kWsHeaderBytes) return MQA_ERR_WORKSPACE_TOO_SMALL;
+  int rc = get_encoder();
+  if (rc != MQA_OK) return rc;
+  CUtensorMap qm;
+  // one query row's 32 heads per box
+  if (encode_rows128(&qm, q, (uint64_t)rows * 32, 32) != MQA_OK) return MQA_ERR_CUDA;
+  GatherParams p;
+  std::memset(&p, 0, sizeof p);
+  p.k = reinterpret_cast<const uint8_t *>(k);
+  p.scales = scales;
+  p.weights = weights;
+  p.starts = starts;
+  p.ends = ends;
+  p.mask = mask;
+  p.mask_words = mask_words;
+  p.out = out;
+  p.ws = reinterpret_cast<int32_t *>(workspace);
+  p.rows = rows;
+  p.keys = keys;
+  p.topk = topk;
+  p.stall = opt ? opt->stall : 0;
+  p.timeout_ns = (long long)((opt && opt->wait_timeout_ms) ? opt->wait_timeout_ms : 4000) * 1000000LL;
+  int ctas = rows < d.sms ? rows : d.sms;
+  if (opt && opt->max_ctas && opt->max_ctas < ctas) ctas = opt->max_ctas;
+  cudaStream_t st = as_stream(stream);
+  if (cudaMemsetAsync(workspace, 0, kWsHeaderBytes, st) != cudaSuccess) {
+    cudaGetLastError();
+    return MQA_ERR_CUDA;
+  }
+  return launch_gather_masked(qm, p, ctas, st) == cudaSuccess ? MQA_OK : MQA_ERR_CUDA;
+}
+
 int run_fused(const void *q, const void *k, const float *scales, const float *weights, const int32_t *starts,
               const int32_t *ends, int32_t *out, int rows, int keys, int topk, int heads, void *workspace,
               size_t workspace_bytes, void *stream, const mqa_topk_debug_options *opt, bool blocks = false,
@@ -261,13 +298,19 @@ int run_fused(const void *q, const void *k, const float *scales, const float *we
       return MQA_ERR_INVALID_ARGUMENT;
   }
   if (opt && (opt->force_gate < 0 || opt->force_gate > 2 || opt->wait_timeout_ms < 0 || opt->max_ctas < 0 ||
-              opt->force_unsafe < 0 || opt->force_unsafe > 1 || opt->head_sum < 0 || opt->head_sum > 2))
+              opt->force_unsafe < 0 || opt->force_unsafe > 1 || opt->head_sum < 0 || opt->head_sum > 2 ||
+              opt->masked_scan < 0 || opt->masked_scan > 1))
     return MQA_ERR_INVALID_ARGUMENT;
   if (rows == 0) return MQA_OK;
   DeviceInfo d;
   rc = current_device_info(&d);
   if (rc != MQA_OK) return rc;
   const int max_ctas = opt ? opt->max_ctas : 0;
+  // masked selection scores only the allowed blocks unless the caller asks
+  // for the scan of every tile in each row block's range
+  if (mask && !(opt && opt->masked_scan))
+    return run_gather(d, q, k, scales, weights, starts, ends, mask, mask_words, out, rows, keys, topk, workspace,
+                      workspace_bytes, stream, opt);
   const Build b = pick_build(d, rows, heads, blocks, mask != nullptr, noalloc, opt ? opt->head_sum : 0);
   // key-range split when the workspace holds its arrays (mqa_topk_workspace_bytes
   // sizes for it), else one CTA per block as far as SMs go

@@ -285,19 +285,84 @@ def test_block_mask_kernel_bit_exact(mqa):
     assert np.array_equal(it.cpu().numpy(), want_i)
 
 
+@pytest.mark.parametrize("scan", [0, 1], ids=["gather", "scan"])
 @pytest.mark.parametrize("seed,rows,keys,topk,frac", [(71, 9, 3000, 512, 0.5), (72, 24, 40000, 512, 0.3),
-                                                      (73, 17, 90000, 1024, 0.05)])
-def test_masked_selection_random_masks(mqa, seed, rows, keys, topk, frac):
-    """Top-k over the keys of each row's allowed blocks (random masks)."""
+                                                      (73, 17, 90000, 1024, 0.05), (76, 13, 120000, 2048, 0.6)])
+def test_masked_selection_random_masks(mqa, seed, rows, keys, topk, frac, scan):
+    """Top-k over the keys of each row's allowed blocks (random masks), by
+    the gathering kernel (rows of up to ~2,400 allowed blocks: up to three
+    1,024-block jobs and a running top-k) and by the masked scan."""
     p = synth.random_small(seed, rows, keys, topk)
     rng = np.random.default_rng(seed)
     picks = rng.integers(0, keys // 8 + 1, (rows, 4096))  # relative block indices, many past the range
     lists = np.where(rng.random((rows, 4096)) < frac, picks, -1).astype(np.int32)
     words = ((keys + 1023) // 1024) * 4
     mask, items = numpy_block_mask(lists, p.starts, p.ends, keys, words)
+    got, status, stats = run_masked(mqa, p, mask, items, debug={"masked_scan": scan})
+    assert status == 0, stats
+    if scan == 0:
+        assert stats["blocks_done"] == rows and stats["candidates"] == int(items.sum()), stats
+    assert_masked_parity(p, got, mask)
+
+
+def _full_mask(p):
+    words = ((p.keys + 1023) // 1024) * 4
+    mask = np.full((p.rows, words), 0xFFFFFFFF, np.uint32)
+    items = np.maximum(p.ends - p.starts, 0).astype(np.int32)
+    return mask, items
+
+
+def test_masked_gather_full_mask_equals_unmasked(mqa):
+    """A mask that allows every block: the gathering kernel's selection is the
+    unmasked top-k (rows of up to 6,250 blocks, seven jobs each)."""
+    p = synth.random_small(77, 20, 50000, 512)
+    mask, items = _full_mask(p)
     got, status, stats = run_masked(mqa, p, mask, items)
     assert status == 0, stats
+    assert stats["candidates"] == int(items.sum()), stats
+    assert_parity(p, got)
+
+
+def test_masked_gather_job_boundaries(mqa):
+    """Rows whose allowed blocks number exactly 1,024 (one full job), 1,025
+    (a second job of one block), 2,048, one, none, and blocks cut by the range
+    at both ends; one CTA serves every row, reusing both job slots."""
+    rng = np.random.default_rng(78)
+    keys, rows = 60000, 8
+    p = synth.random_small(78, rows, keys, 512, empty_frac=0.0)
+    starts = np.array([3, 1001, 5, 17, 0, 999, 100, 50003], np.int32)
+    ends = np.array([59997, 41005, 30000, 59999, 60000, 999, 9000, 50013], np.int32)
+    p = synth.Problem(p.name, p.q, p.k, p.scales_ue8m0, p.weights, starts, ends, 512)
+    words = ((keys + 1023) // 1024) * 4
+    mask = np.zeros((rows, words), np.uint32)
+
+    def allow(r, blocks):
+        for b in blocks:
+            mask[r, b // 32] |= np.uint32(1 << (b % 32))
+    for r, nb in ((0, 1024), (1, 1025), (2, 2048), (4, 3000)):
+        lo, hi = int(starts[r]) // 8, (int(ends[r]) - 1) // 8
+        allow(r, rng.choice(np.arange(lo, hi + 1), size=nb, replace=False))
+    allow(3, [17 // 8])                          # one block, cut by the start
+    allow(6, [100 // 8, (9000 - 1) // 8, 500])   # both end blocks cut by the range
+    allow(7, [50003 // 8, 50012 // 8])           # a 10-key row
+    mask[5, :] = 0xFFFFFFFF                      # an empty range
+    _, items = _full_mask(p)
+    got, status, stats = run_masked(mqa, p, mask, items, debug={"max_ctas": 1})
+    assert status == 0, stats
+    assert stats["blocks_done"] == rows, stats
     assert_masked_parity(p, got, mask)
+
+
+def test_masked_gather_timeout_then_recovers(mqa):
+    """A stalled gathering kernel ends at the time limit with the timeout bit;
+    the next call on the same context is correct."""
+    p = synth.random_small(79, 12, 20000, 512)
+    mask, items = _full_mask(p)
+    _, status, _ = run_masked(mqa, p, mask, items, debug={"stall": 1, "wait_timeout_ms": 200})
+    assert status & 2
+    got, status, stats = run_masked(mqa, p, mask, items)
+    assert status == 0, stats
+    assert_parity(p, got)
 
 
 def _expected_skipped_tiles(p, mask, block_rows=8):
@@ -317,9 +382,9 @@ def _expected_skipped_tiles(p, mask, block_rows=8):
 
 
 def test_masked_skips_tiles_without_allowed_keys(mqa):
-    """Each row allows blocks in one narrow window of a long range: the tiles
-    no row of a block allows are left out (counted exactly when no row is
-    rescanned) and the result still equals the oracle's."""
+    """The masked scan: each row allows blocks in one narrow window of a long
+    range; the tiles no row of a block allows are left out (counted exactly
+    when no row is rescanned) and the result still equals the oracle's."""
     rng = np.random.default_rng(75)
     p = synth.random_small(75, 24, 200000, 512, empty_frac=0.0)
     keys = p.keys
@@ -332,7 +397,7 @@ def test_masked_skips_tiles_without_allowed_keys(mqa):
         lists[r, :len(pick)] = pick
     words = ((keys + 1023) // 1024) * 4
     mask, items = numpy_block_mask(lists, p.starts, p.ends, keys, words)
-    got, status, stats = run_masked(mqa, p, mask, items)
+    got, status, stats = run_masked(mqa, p, mask, items, debug={"masked_scan": 1})
     assert status == 0, stats
     want = _expected_skipped_tiles(p, mask)
     assert want > 0
@@ -351,6 +416,10 @@ def test_two_level_source_then_consumer(mqa):
     words = ((p.keys + 1023) // 1024) * 4
     mask, items = numpy_block_mask(lists, p.starts, p.ends, p.keys, words)
     got, status, stats = run_masked(mqa, p, mask, items)
+    assert status == 0, stats
+    assert stats["blocks_done"] == 16 and stats["candidates"] == int(items.sum()), stats
+    assert_masked_parity(p, got, mask)
+    got, status, stats = run_masked(mqa, p, mask, items, debug={"masked_scan": 1})
     assert status == 0, stats
     assert stats["gated_rows"] == 16, stats
     assert_masked_parity(p, got, mask)
