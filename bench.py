@@ -193,8 +193,9 @@ def main():
                     help="topk: the fused key top-k (the headline line); blocks: the top 2048 blocks of 8 keys; "
                          "masked: the top 512 keys inside each row's top 2048 blocks (both stages of the "
                          "two-level selection, timed on their own; no e2e, dense or CPU legs)")
-    ap.add_argument("--graph", action="store_true",
-                    help="capture one step into a CUDA graph after the warm-up and time its replays")
+    ap.add_argument("--no-graph", dest="graph", action="store_false",
+                    help="time plain launches instead of replays of one step captured into a CUDA graph "
+                         "after the warm-up (the default; per-step times also give the median)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-dense", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
@@ -288,6 +289,13 @@ def main():
     k_ms_median = statistics.median(kernel_ms)
     achieved = pairs * plan.FLOP_PER_PAIR / (k_ms / 1e3) / 1e12
     peak, peak_src = fp8_peak_tflops()
+    # the tensor pipe's own FP8 ceiling on this GPU (back-to-back MMA tiles of
+    # the kernel's shape, no loads), measured live
+    try:
+        pipe = mqa.fp8_mma_probe()
+    except Exception as ex:  # noqa: BLE001 -- reported, not fatal
+        pipe = None
+        print(f"fp8 probe failed: {ex}", file=sys.stderr)
     traffic = load_traffic(args.workload) if args.mode == "topk" else None
 
     result = {
@@ -306,7 +314,9 @@ def main():
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                      "frac": achieved / peak, "traffic": traffic,
                      "peak_source": f"{peak_src} bf16 x {FP8_OVER_BF16:g} (nominal fp8:bf16)",
-                     "kernel_ms": k_ms, "flop_per_pair": plan.FLOP_PER_PAIR},
+                     "kernel_ms": k_ms, "flop_per_pair": plan.FLOP_PER_PAIR,
+                     "fp8_pipe_ceiling_tflops": pipe,
+                     "frac_of_pipe_ceiling": (achieved / pipe) if pipe else None},
         "clocks": clk.summary(),
         "stats": stats,
     }

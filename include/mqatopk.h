@@ -301,6 +301,16 @@ int mqa_logits_debug(const void *q, const void *k, const float *key_scales, cons
  * "Motivation"), then select each row's top-k from them.  Same inputs and
  * output convention as mqa_topk_prefill; `workspace` is a 256-byte header as
  * for mqa_logits_debug.  logits_budget_bytes must hold at least one row. */
+/* Measurement helper with no counterpart in the method: one CTA per SM issues
+ * tiles_per_sm back-to-back 128 x 256 x 128 FP8 MMA tiles (e4m3 inputs, fp32
+ * accumulation in TMEM, the fused kernel's tile shape) from fixed shared-memory
+ * operands, no loads and no epilogue.  The FLOPs it does are sms * tiles_per_sm
+ * * 2 * 128 * 256 * 128; timing the launch on `stream` gives the tensor pipe's
+ * FP8 ceiling at the clocks the GPU holds.  status (device, int32, zeroed by
+ * the caller) receives MQA_DEV_WAIT_TIMEOUT if the final wait ran out.
+ * tiles_per_sm in [1, 2^26]. */
+int mqa_fp8_mma_probe(long long tiles_per_sm, int32_t *status, void *stream);
+
 int mqa_topk_dense_baseline(const void *q, const void *k, const float *key_scales, const float *weights,
                             const int32_t *starts, const int32_t *ends, int32_t *out, int rows, int keys,
                             int topk, void *logits_ws, size_t logits_budget_bytes, void *workspace,

@@ -36,7 +36,7 @@ EXPORTS = ("mqa_topk_workspace_bytes", "mqa_topk_workspace_bytes_ex", "mqa_topk_
            "mqa_block_topk_prefill", "mqa_topk_prefill_masked", "mqa_block_mask",
            "mqa_topk_prefill_debug", "mqa_topk_prefill_noalloc", "mqa_topk_noalloc_get_status",
            "mqa_ue8m0_decode", "mqa_fold_prep", "mqa_logits_debug", "mqa_topk_dense_baseline", "mqa_topk_get_status",
-           "mqa_topk_strerror")
+           "mqa_fp8_mma_probe", "mqa_topk_strerror")
 
 
 class MQAError(RuntimeError):
@@ -76,6 +76,7 @@ def lib():
     L.mqa_topk_prefill_noalloc.argtypes = common + [I, P]
     L.mqa_topk_noalloc_get_status.argtypes = [ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_int32), P]
     L.mqa_ue8m0_decode.argtypes = [P, P, I, P]
+    L.mqa_fp8_mma_probe.argtypes = [ctypes.c_longlong, P, P]
     L.mqa_fold_prep.argtypes = [P, P, P, P, P, I, P]
     L.mqa_logits_debug.argtypes = common + [P, S, P]
     L.mqa_topk_dense_baseline.argtypes = common + [I, P, S, P, S, P]
@@ -177,6 +178,26 @@ def ue8m0_decode(scales, out=None, stream=None):
         out = torch.empty(keys, dtype=torch.float32, device=scales.device)
     _check(lib().mqa_ue8m0_decode(_ptr(scales), _ptr(out), keys, _stream(stream)), "mqa_ue8m0_decode")
     return out
+
+
+def fp8_mma_probe(tiles_per_sm: int = 40000, device=None):
+    """The tensor pipe's FP8 MMA ceiling in TFLOP/s: one timed launch of
+    mqa_fp8_mma_probe (back-to-back 128 x 256 x 128 tiles on every SM) after
+    a short warm-up launch."""
+    torch = _torch()
+    dev = torch.device("cuda", torch.cuda.current_device() if device is None else device)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    _check(lib().mqa_fp8_mma_probe(1000, _ptr(status), _stream(stream)), "mqa_fp8_mma_probe")
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    _check(lib().mqa_fp8_mma_probe(int(tiles_per_sm), _ptr(status), _stream(stream)), "mqa_fp8_mma_probe")
+    b.record(stream)
+    b.synchronize()
+    if int(status.item()) != 0:
+        raise RuntimeError(f"fp8 probe status {int(status.item())}")
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    return sms * tiles_per_sm * 2.0 * 128 * 256 * 128 / (a.elapsed_time(b) * 1e-3) / 1e12
 
 
 FOLD_TERMS = 4

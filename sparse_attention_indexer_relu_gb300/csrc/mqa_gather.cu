@@ -14,19 +14,21 @@
 // (exact, any order, then -1) is chosen in shared memory.
 //
 // Roles of one persistent CTA (one per SM, 20 warps):
-//  - warps 0-5 gather the job's K blocks into a 6-stage ring of tiles with
+//  - warps 0-9 gather the job's K blocks into a 6-stage ring of tiles with
 //    16-byte asynchronous copies (the copies a warp keeps in flight are
-//    bounded: the 16,384-row, 128K-key masked top-512 took 14.2 ms with two
-//    loader warps, 10.9 ms with four and 9.7 ms with six);
-//  - warp 6 issues the MMAs into 16 TMEM accumulators of 32 columns;
-//  - warp 7 claims rows, turns a row's block-mask words into lists of at
+//    bounded, so the gather rate grows with the loader warps: the 16,384-row,
+//    128K-key masked top-512 on random block lists took 14.2 ms with two
+//    loader warps, 10.9 ms with four, 9.7 ms with six and 8.1 ms with ten);
+//  - warp 10 issues the MMAs into 16 TMEM accumulators of 32 columns;
+//  - warp 11 claims rows, turns a row's block-mask words into lists of at
 //    most 1,024 blocks (a "job"; a row with more allowed blocks is several
 //    jobs) and loads the row's q;
-//  - warps 8-15 (two sets of four, one warp per TMEM lane quadrant; the sets
-//    take alternate tiles) form each key's score and store its order key in
-//    the job's score buffer;
-//  - warps 16-19 select: a radix select over the job's scores plus the row's
-//    running top-k from its earlier jobs.
+//  - warps 12-15 (one warp per TMEM lane quadrant) form each key's score and
+//    store its order key in the job's score buffer, with the job's key count
+//    and order-key range;
+//  - warps 16-19 select: a value-bin histogram over that range, one pass that
+//    emits the keys of the bins above the one holding the k-th largest and
+//    copies that bin out, and a radix select over the copy.
 // Two job slots let a job's selection overlap the next job's scoring.
 #include <mutex>
 
@@ -41,7 +43,7 @@ constexpr int kBlk = 8;                      // keys per block
 constexpr int kTileBlocks = kTileKeys / kBlk;  // 16 blocks per 128-key tile
 constexpr int kStages = 6;                   // K ring depth
 #ifndef MQA_GATHER_LOADER_WARPS
-#define MQA_GATHER_LOADER_WARPS 6
+#define MQA_GATHER_LOADER_WARPS 10
 #endif
 constexpr int kLoaderWarps = MQA_GATHER_LOADER_WARPS;  // warps 0 .. kLoaderWarps - 1
 static_assert(kLoaderWarps % 2 == 0, "two loader warps per block of 8 keys");
@@ -56,7 +58,7 @@ constexpr int kList = 1024;                  // selection: threshold-bin keys co
 #define MQA_GATHER_EPI_SETS 1
 #endif
 #ifndef MQA_GATHER_SEL_WARPS
-#define MQA_GATHER_SEL_WARPS 8
+#define MQA_GATHER_SEL_WARPS 4
 #endif
 constexpr int kEpiSets = MQA_GATHER_EPI_SETS;
 constexpr int kMmaWarp = kLoaderWarps;
@@ -918,4 +920,71 @@ cudaError_t launch_gather_masked(const CUtensorMap &q_map, const GatherParams &p
   return cudaGetLastError();
 }
 
+}  // namespace mqa
+
+// ------------------------------------------------------------------ tensor-pipe probe
+// A measurement helper, not part of the method: every CTA (one per SM) issues
+// back-to-back 128 x 256 x 128 FP8 MMA tiles (four K = 32 steps, e4m3 inputs,
+// fp32 accumulation, the fused kernel's shape) from fixed shared-memory
+// operands into two TMEM accumulators.  Timing it gives the tensor pipe's
+// FP8 issue ceiling on this GPU at the clocks it holds.
+namespace mqa {
+namespace probe {
+__global__ void __launch_bounds__(128, 1) fp8_mma_probe(long long tiles, int32_t *status) {
+  extern __shared__ uint8_t raw[];
+  __shared__ uint32_t tbase;
+  __shared__ __align__(8) uint64_t bar;
+  uint8_t *A = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(raw) + 1023) & ~uintptr_t(1023));
+  uint8_t *B = A + 128 * kDim;
+  const int warp = threadIdx.x >> 5;
+  for (int i = threadIdx.x; i < (128 + 256) * kDim; i += blockDim.x) A[i] = (uint8_t)(0x30 + (i & 7));
+  if (warp == 0) {
+    tmem_alloc(&tbase, 512);
+    tmem_relinquish();
+  }
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+  }
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (threadIdx.x == 0) {
+    constexpr uint32_t idesc = idesc_f8_e4m3_f32(128, 256);
+    const uint64_t ad = sw128_kmajor_desc(smem_u32(A)), bd = sw128_kmajor_desc(smem_u32(B));
+    for (long long t = 0; t < tiles; ++t) {
+      const uint32_t d = tbase + (uint32_t)((t & 1) * 256);
+#pragma unroll
+      for (int kk = 0; kk < kDim / 32; ++kk)
+        umma_f8(d, ad + (uint64_t)(2 * kk), bd + (uint64_t)(2 * kk), idesc, kk > 0 ? 1u : 0u);
+    }
+    umma_commit(&bar);
+    // bounded: about 2 s of polling at most
+    const uint64_t t0 = globaltimer_ns();
+    bool done = false;
+    while (!(done = mbar_try_wait(&bar, 0)) && globaltimer_ns() - t0 < 2000000000ull) {
+    }
+    if (!done) atomicOr(status, kDevWaitTimeout);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tbase, 512);
+  }
+}
+}  // namespace probe
+
+cudaError_t launch_fp8_mma_probe(long long tiles, int32_t *status, cudaStream_t stream) {
+  int dev = 0, sms = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  const int smem = (128 + 256) * kDim + 1024;
+  e = cudaFuncSetAttribute((const void *)probe::fp8_mma_probe, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  probe::fp8_mma_probe<<<sms, 128, smem, stream>>>(tiles, status);
+  return cudaGetLastError();
+}
 }  // namespace mqa

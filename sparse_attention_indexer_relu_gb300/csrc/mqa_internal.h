@@ -183,6 +183,9 @@ struct GatherParams {
 };
 size_t gather_smem_bytes();
 cudaError_t launch_gather_masked(const CUtensorMap &q_map, const GatherParams &p, int ctas, cudaStream_t stream);
+// FP8 tensor-pipe probe: one CTA per SM issuing `tiles` back-to-back
+// 128 x 256 x 128 MMA tiles; a wait past its bound sets *status bits.
+cudaError_t launch_fp8_mma_probe(long long tiles, int32_t *status, cudaStream_t stream);
 cudaError_t launch_block_mask(const int32_t *lists, const int32_t *starts, const int32_t *ends, int rows,
                               int list_len, int keys, uint32_t *mask, int mask_words, int32_t *row_items,
                               cudaStream_t stream);

@@ -697,4 +697,12 @@ const char *mqa_topk_strerror(int code) {
   }
 }
 
+int mqa_fp8_mma_probe(long long tiles_per_sm, int32_t *status, void *stream) {
+  if (tiles_per_sm < 1 || tiles_per_sm > (1LL << 26) || !status) return MQA_ERR_INVALID_ARGUMENT;
+  DeviceInfo d;
+  const int rc = current_device_info(&d);
+  if (rc != MQA_OK) return rc;
+  return launch_fp8_mma_probe(tiles_per_sm, status, as_stream(stream)) == cudaSuccess ? MQA_OK : MQA_ERR_CUDA;
+}
+
 }  // extern "C"
