@@ -79,6 +79,7 @@ static_assert(kBufs % kEpiSets == 0, "a TMEM buffer always goes to the same epil
 
 struct Job {
   int row;          // -1: no more work
+  int lb;           // the job's block list: blist[lb]
   int start, end;   // the row's key range (clamped)
   int nblocks;      // blocks in this job's list
   int first, last;  // the row's first / last job
@@ -89,7 +90,7 @@ struct Smem {
   alignas(1024) uint8_t kring[kStages][kTileKeys * kDim];
   alignas(1024) uint8_t q[2][kQRowBytes];
   uint32_t sbuf[2][kSegKeys];     // order keys of a job's gathered keys (0: not a visible key)
-  int32_t blist[2][kSegBlocks];   // the job's blocks (global block index), ascending
+  int32_t blist[3][kSegBlocks];   // job j's blocks (global block index, ascending) in list j % 3
   uint32_t ckey[2][kMaxTopk];     // the row's running top-k over its earlier jobs (ping-pong)
   int32_t cidx[2][kMaxTopk];
   int whist[kHistCopies][256];   // selection histograms
@@ -266,6 +267,13 @@ __device__ void builder(Smem &S, const CUtensorMap *q_map, const GatherParams &p
     bool first = true;
     for (;;) {
       const int slot = it & 1;
+      // The list of job `it` goes to blist[it % 3], last used by job it - 3,
+      // whose selection ended before job it - 1 was published; so it is built
+      // before the wait for job it - 2's slot, while that job is selected.
+      const int lb = it % 3;
+      int n = 0;
+      if (!done) n = build_list(mrow, &wpos, wend, blo, bhi, S.blist[lb], lane);
+      const bool last = wpos >= wend;
       bool ok = true;
       if (lane == 0) ok = wait_bar(S, &S.j_empty[slot], ((it >> 1) & 1) ^ 1, p, 256);
       if (!__shfl_sync(0xFFFFFFFFu, ok, 0)) {
@@ -282,11 +290,10 @@ __device__ void builder(Smem &S, const CUtensorMap *q_map, const GatherParams &p
         }
         return;
       }
-      const int n = build_list(mrow, &wpos, wend, blo, bhi, S.blist[slot], lane);
-      const bool last = wpos >= wend;
       J.w[lane] = wl;
       if (lane == 0) {
         J.row = row;
+        J.lb = lb;
         J.start = s;
         J.end = e;
         J.nblocks = n;
@@ -312,13 +319,14 @@ __device__ void builder(Smem &S, const CUtensorMap *q_map, const GatherParams &p
   }
 }
 
-// ------------------------------------------------------------------ warps 0 and 3: K gathers
+// ------------------------------------------------------------------ warps 0-9: K gathers
 // The blocks of a tile are copied with 16-byte asynchronous copies into the
 // 128-byte-swizzled K-major layout the MMA reads (16-byte chunk c of tile row
 // r at r * 128 + ((c ^ r % 8) * 16)).  Loader thread lt copies chunk lt % 8
-// of row lt / 8 of every block of the tile, so each warp instruction reads
-// 512 contiguous bytes of k.  Each loader thread's copies of a tile arrive on
-// the tile's k_full barrier when they land (64 arrivals complete it); the MMA
+// of row (lt / 8) % 8 of blocks lt / 64, lt / 64 + kLoaderWarps / 2, ... of
+// the tile, so each warp instruction reads 512 contiguous bytes of k.  Each
+// loader thread's copies of a tile arrive on the tile's k_full barrier when
+// they land (one arrival per loader thread completes it); the MMA
 // issuer fences the copies into the tensor core's proxy after its wait, so
 // the loaders never stall on their own copies.  Keys past the last key are
 // not copied (their rows are never read back).
@@ -348,7 +356,7 @@ __device__ void k_loader(Smem &S, const GatherParams &p, int lane, int lt) {
     const Job &J = S.job[slot];
     if (J.row < 0) break;
     const int n = J.nblocks, ntiles = (n + kTileBlocks - 1) / kTileBlocks;
-    const int32_t *list = S.blist[slot];
+    const int32_t *list = S.blist[J.lb];
     for (int u = 0; u < ntiles; ++u) {
       const int stage = kc % kStages;
       if (lane == 0) ok = wait_bar(S, &S.k_empty[stage], ((kc / kStages) & 1) ^ 1, p, 64);
@@ -424,7 +432,7 @@ __device__ void epilogue(Smem &S, uint32_t tmem, const GatherParams &p, int warp
     float2 w2[kN / 2];
 #pragma unroll
     for (int h = 0; h < kN / 2; ++h) w2[h] = make_float2(J.w[2 * h], J.w[2 * h + 1]);
-    const int32_t *list = S.blist[slot];
+    const int32_t *list = S.blist[J.lb];
     uint32_t *sb = S.sbuf[slot];
     // this set's tiles of the job: u0, u0 + 2, ...; the key and scale of the
     // next one are fetched while the current one is scored
@@ -669,8 +677,10 @@ __device__ void list_threshold(Smem &S, int n, int tid, int lane) {
 //    select over the copy settles the threshold among them;
 //  - a bin with more entries (or a degenerate range) runs the radix select
 //    over every entry instead.
+// Keys below `floor` (the running top-k's smallest key when it is full: no
+// such key can be selected) are left out of the histogram and the copy.
 __device__ int select_job(Smem &S, const Entries &E, const int32_t *ci, const int32_t *list, int total, uint32_t kmin,
-                          uint32_t kmax, int topk, const Sink &K, int tid, int lane, uint32_t *tmin) {
+                          uint32_t kmax, uint32_t floor, int topk, const Sink &K, int tid, int lane, uint32_t *tmin) {
   const int tot = E.size();
   if (total <= topk) {
     emit_threshold(S, E, ci, list, 0u, 0, 0, 0, true, K, tid, lane);
@@ -687,7 +697,7 @@ __device__ int select_job(Smem &S, const Entries &E, const int32_t *ci, const in
 #pragma unroll 4
     for (int i = tid; i < tot; i += kSelThreads) {
       const uint32_t key = E.at(i);
-      if (key != 0u) atomicAdd(&S.whist[wid][score_bin(key, smin, inv)], 1);
+      if (key != 0u && key >= floor) atomicAdd(&S.whist[wid][score_bin(key, smin, inv)], 1);
     }
     sel_sync();
     if (tid < 32) {
@@ -738,7 +748,7 @@ __device__ int select_job(Smem &S, const Entries &E, const int32_t *ci, const in
     for (int i0 = 0; i0 < tot; i0 += kSelThreads) {
       const int i = i0 + tid;
       const uint32_t key = i < tot ? E.at(i) : 0u;
-      const int b = key != 0u ? score_bin(key, smin, inv) : -1;
+      const int b = key != 0u && key >= floor ? score_bin(key, smin, inv) : -1;
       const bool gt = b > bstar, in = b == bstar;
       const uint32_t mg = __ballot_sync(0xFFFFFFFFu, gt), mi = __ballot_sync(0xFFFFFFFFu, in);
       if (gt || in) {
@@ -804,6 +814,9 @@ __device__ void selection(Smem &S, const GatherParams &p, int warp, int lane) {
       kmin = min(kmin, clo);
       kmax = max(kmax, chi);
     }
+    // a full running top-k bounds every key that can still be selected
+    const uint32_t floor = cn == topk ? clo : 0u;
+    kmin = max(kmin, floor);
     if (tid == 0) {
       S.cnt_gt = 0;
       S.cnt_eq = 0;
@@ -813,7 +826,7 @@ __device__ void selection(Smem &S, const GatherParams &p, int warp, int lane) {
     const int cout = cin ^ 1;
     const Sink K{p.out + (size_t)J.row * topk, S.ckey[cout], S.cidx[cout], J.start, last};
     uint32_t tmin;
-    const int c = select_job(S, E, S.cidx[cin], S.blist[slot], total, kmin, kmax, topk, K, tid, lane, &tmin);
+    const int c = select_job(S, E, S.cidx[cin], S.blist[J.lb], total, kmin, kmax, floor, topk, K, tid, lane, &tmin);
     if (last)
       for (int i = c + tid; i < topk; i += kSelThreads) K.orow[i] = -1;
     if (tid == 0) {
