@@ -694,10 +694,14 @@ __device__ int select_job(Smem &S, const Entries &E, const int32_t *ci, const in
   if (binned) {
     for (int b = tid; b < kHistCopies * 256; b += kSelThreads) (&S.whist[0][0])[b] = 0;
     sel_sync();
-#pragma unroll 4
-    for (int i = tid; i < tot; i += kSelThreads) {
-      const uint32_t key = E.at(i);
-      if (key != 0u && key >= floor) atomicAdd(&S.whist[wid][score_bin(key, smin, inv)], 1);
+    // four entries per thread and step, loaded before any is counted
+    for (int i0 = tid; i0 < tot; i0 += 4 * kSelThreads) {
+      uint32_t kk[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) kk[u] = i0 + u * kSelThreads < tot ? E.at(i0 + u * kSelThreads) : 0u;
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        if (kk[u] != 0u && kk[u] >= floor) atomicAdd(&S.whist[wid][score_bin(kk[u], smin, inv)], 1);
     }
     sel_sync();
     if (tid < 32) {
@@ -745,24 +749,36 @@ __device__ int select_job(Smem &S, const Entries &E, const int32_t *ci, const in
       g0 += S.wabove[w];
       l0 += S.win[w];
     }
-    for (int i0 = 0; i0 < tot; i0 += kSelThreads) {
-      const int i = i0 + tid;
-      const uint32_t key = i < tot ? E.at(i) : 0u;
-      const int b = key != 0u && key >= floor ? score_bin(key, smin, inv) : -1;
-      const bool gt = b > bstar, in = b == bstar;
-      const uint32_t mg = __ballot_sync(0xFFFFFFFFu, gt), mi = __ballot_sync(0xFFFFFFFFu, in);
-      if (gt || in) {
-        const int idx = i < E.cn ? ci[i] : list[(i - E.cn) >> 3] * kBlk + ((i - E.cn) & 7);
-        if (gt) {
-          K.put(g0 + __popc(mg & ltm), key, idx);
-        } else {
-          const int l = l0 + __popc(mi & ltm);
-          S.lkey[l] = key;
-          S.lidx[l] = idx;
-        }
+    // four entries per thread and step (the same entries per warp as the
+    // histogram pass), all loaded and binned before any is written
+    for (int i00 = 0; i00 < tot; i00 += 4 * kSelThreads) {
+      uint32_t kk[4];
+      int bb[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int i = i00 + u * kSelThreads + tid;
+        kk[u] = i < tot ? E.at(i) : 0u;
       }
-      g0 += __popc(mg);
-      l0 += __popc(mi);
+#pragma unroll
+      for (int u = 0; u < 4; ++u) bb[u] = kk[u] != 0u && kk[u] >= floor ? score_bin(kk[u], smin, inv) : -1;
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int i = i00 + u * kSelThreads + tid;
+        const bool gt = bb[u] > bstar, in = bb[u] == bstar;
+        const uint32_t mg = __ballot_sync(0xFFFFFFFFu, gt), mi = __ballot_sync(0xFFFFFFFFu, in);
+        if (gt || in) {
+          const int idx = i < E.cn ? ci[i] : list[(i - E.cn) >> 3] * kBlk + ((i - E.cn) & 7);
+          if (gt) {
+            K.put(g0 + __popc(mg & ltm), kk[u], idx);
+          } else {
+            const int l = l0 + __popc(mi & ltm);
+            S.lkey[l] = kk[u];
+            S.lidx[l] = idx;
+          }
+        }
+        g0 += __popc(mg);
+        l0 += __popc(mi);
+      }
     }
     sel_sync();
     list_threshold(S, n, tid, lane);
