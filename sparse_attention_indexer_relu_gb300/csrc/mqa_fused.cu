@@ -2129,8 +2129,12 @@ __device__ bool pair_sync(Smem &S, int m, const FusedParams &p, int lane) {
   return __shfl_sync(0xFFFFFFFFu, ok, 0) != 0;
 }
 
-// score_hist over the pieces of this member's batches (hist already zeroed)
-__device__ void score_hist_half(const RowSlab &R, float lo, float inv, int *hist, int lane, int member) {
+// score_hist over the pieces of this member's batches, into this member's
+// four histogram copies (one per lane % 4: candidates crowd into the bins
+// just above the gate), already zeroed
+constexpr int kPairHistCopies = 8;  // 2 members x 4 lane groups
+__device__ void score_hist_half(const RowSlab &R, float lo, float inv, int *hcopies, int lane, int member) {
+  int *hist = hcopies + (member * 4 + (lane & 3)) * kScoreBins;
   const PieceMap pm = piece_map(R, lane);
 #pragma unroll 1
   for (int t0 = member * kHistDepth; t0 < pm.total; t0 += 2 * kHistDepth) {
@@ -2160,20 +2164,25 @@ constexpr int kPairOut = 200, kPairList = 201;  // shared output / list counters
 __device__ int pair_select_binned(Smem &S, const FusedParams &p, int m, int member, const RowSlab &R, int k,
                                   float lo, float inv, int *hist, uint32_t *lk, int32_t *li, int32_t *out, int base,
                                   int lane) {
-  if (member == 0) {
-    for (int b = lane; b < kScoreBins; b += 32) hist[b] = 0;
-    if (lane == 0) {
-      hist[kPairOut] = 0;
-      hist[kPairList] = 0;
-    }
+  // the histogram copies follow the pair's list in its scratch (the second
+  // member's share of the scratch is otherwise unused)
+  int *hcopies = reinterpret_cast<int *>(li + kSelList);
+  for (int b = lane; b < 4 * kScoreBins; b += 32) hcopies[member * 4 * kScoreBins + b] = 0;
+  if (member == 0 && lane == 0) {
+    hist[kPairOut] = 0;
+    hist[kPairList] = 0;
   }
   if (!pair_sync(S, m, p, lane)) return -2;
-  score_hist_half(R, lo, inv, hist, lane, member);
+  score_hist_half(R, lo, inv, hcopies, lane, member);
   if (!pair_sync(S, m, p, lane)) return -2;
   int c[kBinsPerLane], tot = 0;
 #pragma unroll
   for (int j = 0; j < kBinsPerLane; ++j) {
-    c[j] = hist[kScoreBins - 1 - kBinsPerLane * lane - j];
+    const int b = kScoreBins - 1 - kBinsPerLane * lane - j;
+    int v = 0;
+#pragma unroll
+    for (int cp = 0; cp < kPairHistCopies; ++cp) v += hcopies[cp * kScoreBins + b];
+    c[j] = v;
     tot += c[j];
   }
   int incl = tot;
@@ -2203,9 +2212,6 @@ __device__ int pair_select_binned(Smem &S, const FusedParams &p, int m, int memb
   above = __shfl_sync(0xFFFFFFFFu, above, src);
   nB = __shfl_sync(0xFFFFFFFFu, nB, src);
   if (nB > kSelList || nB <= 0) return -1;
-  const uint32_t lo_key = f2key(lo);
-  const uint64_t kb_lo = first_key_of_bin(B, lo_key, lo, inv);
-  const uint64_t kb_hi = B == kScoreBins - 1 ? (uint64_t)kKeyPosInf + 1 : first_key_of_bin(B + 1, lo_key, lo, inv);
   const PieceMap pm = piece_map(R, lane);
 #pragma unroll 1
   for (int t0 = member * kPass2Groups; t0 < pm.total; t0 += 2 * kPass2Groups) {
@@ -2225,12 +2231,14 @@ __device__ int pair_select_binned(Smem &S, const FusedParams &p, int m, int memb
       kk[4 * gi] = kv.x; kk[4 * gi + 1] = kv.y; kk[4 * gi + 2] = kv.z; kk[4 * gi + 3] = kv.w;
       ii[4 * gi] = iv.x; ii[4 * gi + 1] = iv.y; ii[4 * gi + 2] = iv.z; ii[4 * gi + 3] = iv.w;
     }
+    // the bin compared directly (the same monotone function as the count pass)
     uint32_t up = 0, in = 0;
 #pragma unroll
     for (int j = 0; j < 4 * kPass2Groups; ++j) {
       const bool v = 4 * lane + (j & 3) < lim[j >> 2];
-      if (v && kk[j] >= kb_hi) up |= 1u << j;
-      if (v && kk[j] >= kb_lo && kk[j] < kb_hi) in |= 1u << j;
+      const int bj = score_bin(key2f(kk[j]), lo, inv);
+      if (v && bj > B) up |= 1u << j;
+      if (v && bj == B) in |= 1u << j;
     }
     const int packed = __popc(up) + (__popc(in) << 16);
     int pincl = packed;
