@@ -121,10 +121,12 @@ typedef struct mqa_topk_debug_options {
  *  - a 256-byte header (claim counter, status, counters);
  *  - one persistent CTA per SM (at most 32 per block of rows), two slabs of
  *    8 rows x 16384 candidate records (8 B each) per CTA;
- *  - the key-range split arrays: for up to min(blocks, 2 x CTAs) blocks whose
- *    key range several CTAs scan as chunks, a slab of 8 rows x (16384 + 512)
+ *  - the key-range split arrays: for the blocks whose key range several CTAs
+ *    scan as chunks (every block when there are fewer blocks than CTAs, else
+ *    the last partial wave of blocks), a slab of 8 rows x (16384 + 512)
  *    records (more per block at 4 or more chunks, for fewer blocks), the
  *    per-chunk segment counts and a finished-chunk counter per block.
+ * 398.5 MB for 16,384 rows on 152 SMs.
  * A workspace below this size but at least the header plus the per-CTA slabs
  * of min(blocks, SMs) CTAs still works: the call then splits no block. 
  * Returns MQA_ERR_NO_DEVICE / MQA_ERR_CUDA when the device cannot be queried. */

@@ -1086,13 +1086,14 @@ __device__ MQA_SEL_FN int warp_select_binned(const RowSlab &R, int k, float lo, 
 // ------------------------------------------------------------------ heaviest-first order
 // Key-range split plan (every CTA computes the same one).  The last blocks of
 // the claim order are cut into `nchunks` key chunks when that shortens the
-// final rounds: with few blocks all of them (idle SMs take the chunks), else
-// the blocks of the last partial wave plus one full wave before it.  Costs
+// final rounds: with fewer blocks than CTAs all of them (idle SMs take the
+// chunks), else the blocks of the last partial wave (splitting one full wave
+// before it as well measured no faster and doubled the split's workspace).  Costs
 // are counted in units of the lightest block's scan; each chunk also scores
 // the block's whole sample again (fraction sfrac of a block).
 __device__ void plan_split(Smem &S, const FusedParams &p, long long w_light) {
   const int nb = p.nblocks, ctas = gridDim.x;
-  const int cand = nb < ctas ? nb : (nb % ctas ? min(nb, nb % ctas + ctas) : 0);
+  const int cand = nb < ctas ? nb : nb % ctas;
   if (cand == 0 || cand > p.split_max) return;
   const long long L = w_light / kBlockRows;  // mean visible keys per row of the lightest block
   const long long items = kBlocks ? L / 8 : L;  // and the items it selects from

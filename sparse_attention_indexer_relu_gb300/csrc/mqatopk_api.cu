@@ -152,7 +152,7 @@ int fused_ctas_split(const DeviceInfo &d, int rows, int brows) {
 }
 int split_max_blocks(int ctas, int rows, int brows) {
   const int nb = (rows + brows - 1) / brows;
-  return nb < 2 * ctas ? nb : 2 * ctas;
+  return nb < ctas ? nb : nb % ctas;
 }
 
 }  // namespace
