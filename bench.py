@@ -287,7 +287,8 @@ def main():
     # roofline of the fused kernel (tensor-bound: 8192 flop per scored pair)
     k_ms = statistics.mean(kernel_ms)
     k_ms_median = statistics.median(kernel_ms)
-    achieved = pairs * plan.FLOP_PER_PAIR / (k_ms / 1e3) / 1e12
+    fpp = plan.flop_per_pair(p.heads)
+    achieved = pairs * fpp / (k_ms / 1e3) / 1e12
     peak, peak_src = fp8_peak_tflops()
     # the tensor pipe's own FP8 ceiling on this GPU (back-to-back MMA tiles of
     # the kernel's shape, no loads), measured live
@@ -314,7 +315,7 @@ def main():
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                      "frac": achieved / peak, "traffic": traffic,
                      "peak_source": f"{peak_src} bf16 x {FP8_OVER_BF16:g} (nominal fp8:bf16)",
-                     "kernel_ms": k_ms, "flop_per_pair": plan.FLOP_PER_PAIR,
+                     "kernel_ms": k_ms, "flop_per_pair": fpp,
                      "fp8_pipe_ceiling_tflops": pipe,
                      "frac_of_pipe_ceiling": (achieved / pipe) if pipe else None},
         "clocks": clk.summary(),

@@ -9,7 +9,13 @@ ceil(rows / rows_per_call) call pairs.
 """
 from __future__ import annotations
 
-FLOP_PER_PAIR = 2 * 32 * 128  # one multiply-add per head and dimension
+FLOP_PER_PAIR = 2 * 32 * 128  # one multiply-add per head and dimension (32 heads)
+
+
+def flop_per_pair(heads: int = 32) -> int:
+    """Tensor FLOPs per scored (row, key) pair: one multiply-add per head and
+    dimension (head_dim 128)."""
+    return 2 * heads * 128
 LOGIT_BYTES = 4
 
 
