@@ -303,6 +303,31 @@ int mqa_logits_debug(const void *q, const void *k, const float *key_scales, cons
  * "Motivation"), then select each row's top-k from them.  Same inputs and
  * output convention as mqa_topk_prefill; `workspace` is a 256-byte header as
  * for mqa_logits_debug.  logits_budget_bytes must hold at least one row. */
+/* Device staging bytes for mqa_topk_prefill_host with these sizes on `device`:
+ * the inputs, the decoded scales, the output and the fused op's workspace. */
+int mqa_topk_host_staging_bytes(int device, int rows, int keys, int topk, size_t *bytes);
+
+/* The fused op from host buffers (32 heads): copies q, k, the UE8M0 scale
+ * bytes ([keys, 4]), weights, starts and ends host -> device into `staging`
+ * (device, 256-byte aligned, mqa_topk_host_staging_bytes long), decodes the
+ * scales, runs mqa_topk_prefill and copies the indices device -> host into
+ * out_host [rows, topk].  Host buffers as the device-buffer entry lays them
+ * out.  Everything is enqueued on `stream` with one plain asynchronous copy
+ * per buffer: with pinned host memory the copies overlap other streams'
+ * work, and out_host holds the result once the stream has reached this
+ * point (the call itself does not synchronise).  The status word and
+ * counters of the call: mqa_topk_host_get_status.  The pages have no
+ * host-buffer entry: it is the end-to-end form of mqa_topk_prefill. */
+int mqa_topk_prefill_host(const void *q_host, const void *k_host, const uint8_t *scales_ue8m0_host,
+                          const float *weights_host, const int32_t *starts_host, const int32_t *ends_host,
+                          int32_t *out_host, int rows, int keys, int topk, void *staging, size_t staging_bytes,
+                          void *stream);
+
+/* mqa_topk_get_status for the workspace inside a staging buffer of
+ * mqa_topk_prefill_host (the same rows, keys and topk). */
+int mqa_topk_host_get_status(const void *staging, int rows, int keys, int topk, int32_t *status, int32_t *stats,
+                             void *stream);
+
 /* Measurement helper with no counterpart in the method: one CTA per SM issues
  * tiles_per_sm back-to-back 128 x 256 x 128 FP8 MMA tiles (e4m3 inputs, fp32
  * accumulation in TMEM, the fused kernel's tile shape) from fixed shared-memory

@@ -36,7 +36,8 @@ EXPORTS = ("mqa_topk_workspace_bytes", "mqa_topk_workspace_bytes_ex", "mqa_topk_
            "mqa_block_topk_prefill", "mqa_topk_prefill_masked", "mqa_block_mask",
            "mqa_topk_prefill_debug", "mqa_topk_prefill_noalloc", "mqa_topk_noalloc_get_status",
            "mqa_ue8m0_decode", "mqa_fold_prep", "mqa_logits_debug", "mqa_topk_dense_baseline", "mqa_topk_get_status",
-           "mqa_fp8_mma_probe", "mqa_topk_strerror")
+           "mqa_fp8_mma_probe", "mqa_topk_host_staging_bytes", "mqa_topk_prefill_host", "mqa_topk_host_get_status",
+           "mqa_topk_strerror")
 
 
 class MQAError(RuntimeError):
@@ -77,6 +78,9 @@ def lib():
     L.mqa_topk_noalloc_get_status.argtypes = [ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_int32), P]
     L.mqa_ue8m0_decode.argtypes = [P, P, I, P]
     L.mqa_fp8_mma_probe.argtypes = [ctypes.c_longlong, P, P]
+    L.mqa_topk_host_staging_bytes.argtypes = [I, I, I, I, ctypes.POINTER(S)]
+    L.mqa_topk_prefill_host.argtypes = [P, P, P, P, P, P, P, I, I, I, P, S, P]
+    L.mqa_topk_host_get_status.argtypes = [P, I, I, I, ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_int32), P]
     L.mqa_fold_prep.argtypes = [P, P, P, P, P, I, P]
     L.mqa_logits_debug.argtypes = common + [P, S, P]
     L.mqa_topk_dense_baseline.argtypes = common + [I, P, S, P, S, P]
@@ -360,6 +364,44 @@ def mqa_topk_dense_baseline(q, k, key_scales, weights, starts, ends, topk: int,
                                          _ptr(workspace), workspace.numel(), _stream(stream)),
            "mqa_topk_dense_baseline")
     return out
+
+
+def alloc_host_staging(rows: int, keys: int, topk: int, device=None):
+    """Device staging for mqa_topk_prefill_host (inputs, scales, output and
+    workspace; caller owns it)."""
+    torch = _torch()
+    dev = torch.device("cuda", torch.cuda.current_device() if device is None else int(device))
+    n = ctypes.c_size_t()
+    _check(lib().mqa_topk_host_staging_bytes(dev.index, int(rows), int(keys), int(topk), ctypes.byref(n)),
+           "mqa_topk_host_staging_bytes")
+    return torch.empty(n.value, dtype=torch.uint8, device=dev)
+
+
+def mqa_topk_prefill_host(q, k, scales_ue8m0, weights, starts, ends, topk: int, staging, out, stream=None):
+    """The fused op from host tensors (pinned for asynchronous copies): every
+    copy, the scale decode and the kernel are enqueued by the C entry on
+    `stream`; `out` (host int32 [rows, topk]) is valid once the stream has
+    reached this point."""
+    torch = _torch()
+    rows, keys = int(q.shape[0]), int(k.shape[0])
+    for t, name in ((q, "q"), (k, "k"), (scales_ue8m0, "scales_ue8m0"), (weights, "weights"), (starts, "starts"),
+                    (ends, "ends"), (out, "out")):
+        if t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name}: a contiguous host tensor is expected")
+    _check(lib().mqa_topk_prefill_host(_ptr(q), _ptr(k), _ptr(scales_ue8m0), _ptr(weights), _ptr(starts),
+                                       _ptr(ends), _ptr(out), rows, keys, int(topk), _ptr(staging),
+                                       staging.numel() * staging.element_size(), _stream(stream)),
+           "mqa_topk_prefill_host")
+    return out
+
+
+def host_get_status(staging, rows: int, keys: int, topk: int, stream=None):
+    """get_status for the workspace inside a mqa_topk_prefill_host staging buffer."""
+    st = ctypes.c_int32(0)
+    stats = (ctypes.c_int32 * len(STAT_NAMES))()
+    _check(lib().mqa_topk_host_get_status(_ptr(staging), int(rows), int(keys), int(topk), ctypes.byref(st), stats,
+                                          _stream(stream)), "mqa_topk_host_get_status")
+    return int(st.value), dict(zip(STAT_NAMES, [int(v) for v in stats]))
 
 
 def get_status(workspace, stream=None):

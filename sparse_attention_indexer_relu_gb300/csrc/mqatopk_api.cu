@@ -697,6 +697,98 @@ const char *mqa_topk_strerror(int code) {
   }
 }
 
+// Device staging of mqa_topk_prefill_host: q, k, the UE8M0 bytes, the decoded
+// scales, weights, starts, ends, out, then the fused op's workspace, each
+// 256-byte aligned.
+namespace {
+struct HostStaging {
+  size_t q, k, g, sc, w, s, e, out, ws, total;
+};
+inline size_t up256(size_t x) { return (x + 255) / 256 * 256; }
+HostStaging host_staging(int rows, int keys, int topk, size_t ws_bytes) {
+  HostStaging H;
+  H.q = 0;
+  H.k = H.q + up256((size_t)rows * 32 * kDim);
+  H.g = H.k + up256((size_t)keys * kDim);
+  H.sc = H.g + up256((size_t)keys * 4);
+  H.w = H.sc + up256((size_t)keys * sizeof(float));
+  H.s = H.w + up256((size_t)rows * 32 * sizeof(float));
+  H.e = H.s + up256((size_t)rows * sizeof(int32_t));
+  H.out = H.e + up256((size_t)rows * sizeof(int32_t));
+  H.ws = H.out + up256((size_t)rows * topk * sizeof(int32_t));
+  H.total = H.ws + up256(ws_bytes);
+  return H;
+}
+}  // namespace
+
+int mqa_topk_host_staging_bytes(int device, int rows, int keys, int topk, size_t *bytes) {
+  if (!bytes || rows < 0 || keys < 1 || keys > MQA_MAX_KEYS || !valid_topk(topk)) return MQA_ERR_INVALID_ARGUMENT;
+  size_t ws = 0;
+  const int rc = mqa_topk_workspace_bytes(device, rows, &ws);
+  if (rc != MQA_OK) return rc;
+  *bytes = host_staging(rows, keys, topk, ws).total;
+  return MQA_OK;
+}
+
+int mqa_topk_prefill_host(const void *q_host, const void *k_host, const uint8_t *scales_ue8m0_host,
+                          const float *weights_host, const int32_t *starts_host, const int32_t *ends_host,
+                          int32_t *out_host, int rows, int keys, int topk, void *staging, size_t staging_bytes,
+                          void *stream) {
+  if (rows < 0 || keys < 1 || keys > MQA_MAX_KEYS || !valid_topk(topk)) return MQA_ERR_INVALID_ARGUMENT;
+  if (rows == 0) return MQA_OK;
+  if (!q_host || !k_host || !scales_ue8m0_host || !weights_host || !starts_host || !ends_host || !out_host ||
+      !staging)
+    return MQA_ERR_INVALID_ARGUMENT;
+  if (!aligned(staging, 256)) return MQA_ERR_MISALIGNED;
+  DeviceInfo d;
+  int rc = current_device_info(&d);
+  if (rc != MQA_OK) return rc;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return MQA_ERR_CUDA;
+  size_t ws_bytes = 0;
+  rc = mqa_topk_workspace_bytes(dev, rows, &ws_bytes);
+  if (rc != MQA_OK) return rc;
+  const HostStaging H = host_staging(rows, keys, topk, ws_bytes);
+  if (staging_bytes < H.total) return MQA_ERR_WORKSPACE_TOO_SMALL;
+  uint8_t *b = reinterpret_cast<uint8_t *>(staging);
+  cudaStream_t st = as_stream(stream);
+  // one plain asynchronous copy per input (pinned host buffers overlap with
+  // other streams' work; pageable ones are staged by the runtime)
+  const struct { size_t off; const void *src; size_t n; } in[] = {
+      {H.q, q_host, (size_t)rows * 32 * kDim},
+      {H.k, k_host, (size_t)keys * kDim},
+      {H.g, scales_ue8m0_host, (size_t)keys * 4},
+      {H.w, weights_host, (size_t)rows * 32 * sizeof(float)},
+      {H.s, starts_host, (size_t)rows * sizeof(int32_t)},
+      {H.e, ends_host, (size_t)rows * sizeof(int32_t)}};
+  for (const auto &c : in) {
+    if (cudaMemcpyAsync(b + c.off, c.src, c.n, cudaMemcpyHostToDevice, st) != cudaSuccess) {
+      cudaGetLastError();
+      return MQA_ERR_CUDA;
+    }
+  }
+  if (launch_ue8m0_decode(b + H.g, reinterpret_cast<float *>(b + H.sc), keys, st) != cudaSuccess)
+    return MQA_ERR_CUDA;
+  rc = run_fused(b + H.q, b + H.k, reinterpret_cast<const float *>(b + H.sc),
+                 reinterpret_cast<const float *>(b + H.w), reinterpret_cast<const int32_t *>(b + H.s),
+                 reinterpret_cast<const int32_t *>(b + H.e), reinterpret_cast<int32_t *>(b + H.out), rows, keys, topk,
+                 32, b + H.ws, ws_bytes, stream, nullptr);
+  if (rc != MQA_OK) return rc;
+  if (cudaMemcpyAsync(out_host, b + H.out, (size_t)rows * topk * sizeof(int32_t), cudaMemcpyDeviceToHost, st) !=
+      cudaSuccess) {
+    cudaGetLastError();
+    return MQA_ERR_CUDA;
+  }
+  return MQA_OK;
+}
+
+int mqa_topk_host_get_status(const void *staging, int rows, int keys, int topk, int32_t *status, int32_t *stats,
+                             void *stream) {
+  if (!staging || rows < 1 || keys < 1 || keys > MQA_MAX_KEYS || !valid_topk(topk)) return MQA_ERR_INVALID_ARGUMENT;
+  const HostStaging H = host_staging(rows, keys, topk, 0);
+  return mqa_topk_get_status(reinterpret_cast<const uint8_t *>(staging) + H.ws, status, stats, stream);
+}
+
 int mqa_fp8_mma_probe(long long tiles_per_sm, int32_t *status, void *stream) {
   if (tiles_per_sm < 1 || tiles_per_sm > (1LL << 26) || !status) return MQA_ERR_INVALID_ARGUMENT;
   DeviceInfo d;

@@ -95,6 +95,25 @@ def test_ue8m0_argument_checks():
     assert L.mqa_ue8m0_decode(P(0x1001), P(0x2000), 5, None) == 2
 
 
+def test_host_entry_argument_checks():
+    """Argument errors of the host-buffer entry come back before any device
+    work (no GPU needed)."""
+    L = mqa.lib()
+    h = [P(0x1000 * i) for i in range(1, 8)]
+    # bad sizes and topk
+    assert L.mqa_topk_prefill_host(*h, 8, 0, 512, P(0x100000), 1 << 30, None) == 1
+    assert L.mqa_topk_prefill_host(*h, -1, 100, 512, P(0x100000), 1 << 30, None) == 1
+    assert L.mqa_topk_prefill_host(*h, 8, 100, 300, P(0x100000), 1 << 30, None) == 1
+    # zero rows is a no-op; null buffers and a misaligned staging buffer are rejected
+    assert L.mqa_topk_prefill_host(*h, 0, 100, 512, P(0x100000), 1 << 30, None) == 0
+    assert L.mqa_topk_prefill_host(None, *h[1:], 8, 100, 512, P(0x100000), 1 << 30, None) == 1
+    assert L.mqa_topk_prefill_host(*h, 8, 100, 512, None, 1 << 30, None) == 1
+    assert L.mqa_topk_prefill_host(*h, 8, 100, 512, P(0x100010), 1 << 30, None) == 2
+    n = ctypes.c_size_t()
+    assert L.mqa_topk_host_staging_bytes(0, 8, 100, 300, ctypes.byref(n)) == 1
+    assert L.mqa_topk_host_get_status(None, 8, 100, 512, None, None, None) == 1
+
+
 def test_logits_and_dense_argument_checks():
     L = mqa.lib()
     args = [P(0x1000), P(0x2000), P(0x3000), P(0x4000), P(0x5000), P(0x6000), P(0x7000), 8, 100]

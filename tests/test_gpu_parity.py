@@ -425,6 +425,24 @@ def test_two_level_source_then_consumer(mqa):
     assert_masked_parity(p, got, mask)
 
 
+def test_host_buffer_entry(mqa):
+    """mqa_topk_prefill_host: host inputs in, host indices out, through the C
+    ABI on one stream; two calls in a row on one staging buffer."""
+    import torch
+    for seed in (90, 91):
+        p = synth.random_small(seed, 40, 30000, 512)
+        pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()
+        staging = mqa.alloc_host_staging(p.rows, p.keys, p.topk)
+        out = torch.full((p.rows, p.topk), 7, dtype=torch.int32).pin_memory()
+        s = torch.cuda.Stream()
+        mqa.mqa_topk_prefill_host(pin(p.q), pin(p.k), pin(p.scales_ue8m0), pin(p.weights), pin(p.starts),
+                                  pin(p.ends), p.topk, staging, out, stream=s)
+        s.synchronize()
+        status, stats = mqa.host_get_status(staging, p.rows, p.keys, p.topk)
+        assert status == 0, stats
+        assert_parity(p, out.numpy())
+
+
 def test_fused_single_cta(mqa):
     """All blocks through one persistent CTA (job slots and slabs reused many times)."""
     p = synth.random_small(23, 64, 9000, 512)
