@@ -14,21 +14,24 @@
 // (exact, any order, then -1) is chosen in shared memory.
 //
 // Roles of one persistent CTA (one per SM, 20 warps):
-//  - warps 0-9 gather the job's K blocks into a 6-stage ring of tiles with
+//  - warps 0-7 gather the job's K blocks into a 5-stage ring of tiles with
 //    16-byte asynchronous copies (the copies a warp keeps in flight are
 //    bounded, so the gather rate grows with the loader warps: the 16,384-row,
 //    128K-key masked top-512 on random block lists took 14.2 ms with two
-//    loader warps, 10.9 ms with four, 9.7 ms with six and 8.1 ms with ten);
-//  - warp 10 issues the MMAs into 16 TMEM accumulators of 32 columns;
-//  - warp 11 claims rows, turns a row's block-mask words into lists of at
-//    most 1,024 blocks (a "job"; a row with more allowed blocks is several
-//    jobs) and loads the row's q;
-//  - warps 12-15 (one warp per TMEM lane quadrant) form each key's score and
+//    loader warps, 10.9 ms with four, 9.7 ms with six, 7.3 ms with eight
+//    or ten);
+//  - warps 8-11 (one warp per TMEM lane quadrant) form each key's score and
 //    store its order key in the job's score buffer, with the job's key count
 //    and order-key range;
-//  - warps 16-19 select: a value-bin histogram over that range, one pass that
+//  - warp 12 issues the MMAs into 16 TMEM accumulators of 32 columns;
+//  - warp 13 claims rows, turns a row's block-mask words into lists of at
+//    most 1,024 blocks (a "job"; a row with more allowed blocks is several
+//    jobs) and loads the row's q;
+//  - warps 14-19 select: a value-bin histogram over that range, one pass that
 //    emits the keys of the bins above the one holding the k-th largest and
-//    copies that bin out, and a radix select over the copy.
+//    copies that bin out, and a radix select over the copy.  With the source
+//    stage's own top blocks the selection sets the pace, so six warps select
+//    (against four with ten loader warps: 10.2 -> 9.7 ms at 128K keys).
 // Two job slots let a job's selection overlap the next job's scoring.
 #include <mutex>
 
@@ -41,9 +44,9 @@ namespace gather {
 
 constexpr int kBlk = 8;                      // keys per block
 constexpr int kTileBlocks = kTileKeys / kBlk;  // 16 blocks per 128-key tile
-constexpr int kStages = 6;                   // K ring depth
+constexpr int kStages = 5;                   // K ring depth
 #ifndef MQA_GATHER_LOADER_WARPS
-#define MQA_GATHER_LOADER_WARPS 10
+#define MQA_GATHER_LOADER_WARPS 8
 #endif
 constexpr int kLoaderWarps = MQA_GATHER_LOADER_WARPS;  // warps 0 .. kLoaderWarps - 1
 static_assert(kLoaderWarps % 2 == 0, "two loader warps per block of 8 keys");
@@ -58,14 +61,22 @@ constexpr int kList = 1024;                  // selection: threshold-bin keys co
 #define MQA_GATHER_EPI_SETS 1
 #endif
 #ifndef MQA_GATHER_SEL_WARPS
-#define MQA_GATHER_SEL_WARPS 4
+#define MQA_GATHER_SEL_WARPS 6
 #endif
 constexpr int kEpiSets = MQA_GATHER_EPI_SETS;
-constexpr int kMmaWarp = kLoaderWarps;
-constexpr int kBuilderWarp = kLoaderWarps + 1;
-constexpr int kEpiWarp0 = (kLoaderWarps + 2 + 3) / 4 * 4;  // a multiple of 4: warp % 4 is its TMEM quadrant
+// Warp layout: loaders first; the MMA issuer and the job builder fill the
+// gap before the epilogue warps (which must start at a multiple of 4, so that
+// warp % 4 is their TMEM lane quadrant) when there is one, else follow them;
+// the selection warps come last.
+#ifndef MQA_GATHER_LATE_ROLES
+#define MQA_GATHER_LATE_ROLES 1
+#endif
+constexpr bool kLateRoles = MQA_GATHER_LATE_ROLES != 0;
 constexpr int kEpiWarps = 4 * kEpiSets;
-constexpr int kSelWarp0 = kEpiWarp0 + kEpiWarps;
+constexpr int kEpiWarp0 = kLateRoles ? (kLoaderWarps + 3) / 4 * 4 : (kLoaderWarps + 2 + 3) / 4 * 4;
+constexpr int kMmaWarp = kLateRoles ? kEpiWarp0 + kEpiWarps : kLoaderWarps;
+constexpr int kBuilderWarp = kMmaWarp + 1;
+constexpr int kSelWarp0 = kLateRoles ? kBuilderWarp + 1 : kEpiWarp0 + kEpiWarps;
 constexpr int kSelWarps = MQA_GATHER_SEL_WARPS;
 constexpr int kHistCopies = kSelWarps;  // value-bin histograms, one per selection warp
 constexpr int kSelThreads = kSelWarps * 32;
