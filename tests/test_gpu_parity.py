@@ -353,6 +353,25 @@ def test_masked_gather_job_boundaries(mqa):
     assert_masked_parity(p, got, mask)
 
 
+def test_masked_gather_ties(mqa):
+    """Every key identical (one k row, one scale): each row's scores are all
+    equal, so the selection's value range is degenerate and it takes the
+    full radix select; half the keys identical in a second case, so the
+    threshold bin holds thousands of ties (more than the copy holds)."""
+    base = synth.random_small(94, 12, 20000, 512, empty_frac=0.0)
+    for frac in (1.0, 0.5):
+        k = base.k.copy()
+        g = base.scales_ue8m0.copy()
+        n = int(frac * base.keys)
+        k[:n] = k[0]
+        g[:n] = g[0]
+        p = synth.Problem(base.name, base.q, k, g, base.weights, base.starts, base.ends, base.topk)
+        mask, items = _full_mask(p)
+        got, status, stats = run_masked(mqa, p, mask, items)
+        assert status == 0, stats
+        assert_parity(p, got)
+
+
 def test_masked_gather_timeout_then_recovers(mqa):
     """A stalled gathering kernel ends at the time limit with the timeout bit;
     the next call on the same context is correct."""
@@ -484,6 +503,41 @@ def test_fused_max_keys(mqa):
         sub = synth.window(p, r)
         _, scores = oracle.run(sub, want_topk=False, want_scores=True)
         bad = check_topk_rows(got[r:r + 1], sub, np.array([0]), scores)
+        assert not bad, (r, bad[:5])
+
+
+def test_masked_gather_max_keys(mqa):
+    """The gathering kernel at 2^24 keys (K is 2 GiB): each row allows up to
+    3,000 random blocks of its range (ranges ending at the last key, one at
+    key 0, unaligned starts); every row is checked against the oracle on a
+    block-aligned window of its keys."""
+    p = synth.max_keys(topk=512)
+    keys = p.keys
+    rng = np.random.default_rng(93)
+    nb = ((p.ends.astype(np.int64) - 1) // 8 - p.starts.astype(np.int64) // 8 + 1).clip(min=1)
+    lists = np.full((p.rows, 3000), -1, np.int32)
+    for r in range(p.rows):
+        pick = rng.choice(int(nb[r]), size=min(3000, int(nb[r])), replace=False)
+        lists[r, :len(pick)] = pick
+    words = ((keys + 1023) // 1024) * 4
+    mask, items = numpy_block_mask(lists, p.starts, p.ends, keys, words)
+    got, status, stats = run_masked(mqa, p, mask, items)
+    assert status == 0, stats
+    assert stats["blocks_done"] == p.rows and stats["candidates"] == int(items.sum()), stats
+    for r in range(p.rows):
+        s, e = int(p.starts[r]), int(p.ends[r])
+        s8 = s - s % 8
+        sub = synth.Problem(f"{p.name}_w{r}", p.q[r:r + 1], p.k[s8:e], p.scales_ue8m0[s8:e], p.weights[r:r + 1],
+                            np.array([s - s8], np.int32), np.array([e - s8], np.int32), p.topk)
+        wk = e - s8
+        wwords = ((wk + 1023) // 1024) * 4
+        wmask = np.zeros((1, wwords), np.uint32)
+        b0 = s8 // 8
+        for b in range((wk + 7) // 8):
+            if (mask[r, (b0 + b) // 32] >> np.uint32((b0 + b) % 32)) & np.uint32(1):
+                wmask[0, b // 32] |= np.uint32(1 << (b % 32))
+        _, scores = oracle.run_masked(sub, wmask, want_topk=False, want_scores=True)
+        bad = check_masked_rows(got[r:r + 1], sub, np.array([0]), scores)
         assert not bad, (r, bad[:5])
 
 
