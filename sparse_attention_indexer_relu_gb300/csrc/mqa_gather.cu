@@ -25,14 +25,16 @@
 //    and order-key range;
 //  - warp 12 issues the MMAs into 16 TMEM accumulators of 32 columns;
 //  - warp 13 claims rows, turns a row's block-mask words into lists of at
-//    most 1,024 blocks (a "job"; a row with more allowed blocks is several
+//    most 768 blocks (a "job"; a row with more allowed blocks is several
 //    jobs) and loads the row's q;
 //  - warps 14-19 select: a value-bin histogram over that range, one pass that
 //    emits the keys of the bins above the one holding the k-th largest and
 //    copies that bin out, and a radix select over the copy.  With the source
 //    stage's own top blocks the selection sets the pace, so six warps select
 //    (against four with ten loader warps: 10.2 -> 9.7 ms at 128K keys).
-// Two job slots let a job's selection overlap the next job's scoring.
+// Three job slots let a job's selection overlap the scoring of the next two
+// (128K-key masked top-2048 on the source stage's own top blocks: two slots of
+// 1,024 blocks 9.7 ms, three of 768 7.9 ms, three or four of 512 8.0 ms).
 #include <mutex>
 
 #include "mqa_internal.h"
@@ -53,7 +55,16 @@ static_assert(kLoaderWarps % 2 == 0, "two loader warps per block of 8 keys");
 constexpr int kLoaderThreads = 32 * kLoaderWarps;
 constexpr int kBufs = 16;                    // TMEM accumulators (32 columns each)
 constexpr int kN = 32;                       // UMMA N: the row's heads
-constexpr int kSegBlocks = 1024;             // blocks per job
+#ifndef MQA_GATHER_JOB_SLOTS
+#define MQA_GATHER_JOB_SLOTS 3
+#endif
+#ifndef MQA_GATHER_SEG_BLOCKS
+#define MQA_GATHER_SEG_BLOCKS 768
+#endif
+constexpr int kJobSlots = MQA_GATHER_JOB_SLOTS;  // jobs in flight (score buffers, q, counters)
+constexpr int kLists = kJobSlots + 1;            // block lists: one more, so the next is built ahead
+constexpr int kSegBlocks = MQA_GATHER_SEG_BLOCKS;  // blocks per job
+static_assert(kSegBlocks % 16 == 0, "a job is whole 128-key tiles");
 constexpr int kSegKeys = kSegBlocks * kBlk;  // score-buffer entries per job
 constexpr int kMaxTopk = 2048;
 constexpr int kList = 1024;                  // selection: threshold-bin keys copied out
@@ -99,19 +110,19 @@ struct Job {
 
 struct Smem {
   alignas(1024) uint8_t kring[kStages][kTileKeys * kDim];
-  alignas(1024) uint8_t q[2][kQRowBytes];
-  uint32_t sbuf[2][kSegKeys];     // order keys of a job's gathered keys (0: not a visible key)
-  int32_t blist[3][kSegBlocks];   // job j's blocks (global block index, ascending) in list j % 3
+  alignas(1024) uint8_t q[kJobSlots][kQRowBytes];
+  uint32_t sbuf[kJobSlots][kSegKeys];  // order keys of a job's gathered keys (0: not a visible key)
+  int32_t blist[kLists][kSegBlocks];  // job j's blocks (global block index, ascending) in list j % kLists
   uint32_t ckey[2][kMaxTopk];     // the row's running top-k over its earlier jobs (ping-pong)
   int32_t cidx[2][kMaxTopk];
   int whist[kHistCopies][256];   // selection histograms
   int wabove[kSelWarps], win[kSelWarps];  // per selection warp: entries above / in the threshold bin
   uint32_t lkey[kList];           // selection: the keys of the threshold value bin
   int32_t lidx[kList];            // and their key indices
-  Job job[2];
+  Job job[kJobSlots];
   uint64_t k_full[kStages], k_empty[kStages];
   uint64_t t_full[kBufs], t_empty[kBufs];
-  uint64_t j_full[2], j_empty[2], s_full[2];
+  uint64_t j_full[kJobSlots], j_empty[kJobSlots], s_full[kJobSlots];
   uint64_t drain, stall_bar;
   uint32_t tmem_base;
   int abort_flag;
@@ -120,8 +131,8 @@ struct Smem {
   int sel_want, sel_bin, sel_inbin, sel_hb, list_n;
   int cnt_gt, cnt_eq;
   // a job's visible keys (count, order-key range), gathered by the epilogue
-  uint32_t jlo[2], jhi[2];
-  int jcnt[2];
+  uint32_t jlo[kJobSlots], jhi[kJobSlots];
+  int jcnt[kJobSlots];
 };
 
 constexpr size_t kSmemBytes = sizeof(Smem) + 1024;
@@ -277,20 +288,22 @@ __device__ void builder(Smem &S, const CUtensorMap *q_map, const GatherParams &p
     const float wl = done ? 0.f : __ldg(p.weights + (size_t)row * kN + lane);
     bool first = true;
     for (;;) {
-      const int slot = it & 1;
-      // The list of job `it` goes to blist[it % 3], last used by job it - 3,
-      // whose selection ended before job it - 1 was published; so it is built
-      // before the wait for job it - 2's slot, while that job is selected.
-      const int lb = it % 3;
+      const int slot = it % kJobSlots;
+      // The list of job `it` goes to blist[it % kLists], last used by job
+      // it - kLists, whose selection ended before job it - 1 was published;
+      // so it is built before the wait for job it - kJobSlots's slot, while
+      // that job is selected.
+      const int lb = it % kLists;
       int n = 0;
       if (!done) n = build_list(mrow, &wpos, wend, blo, bhi, S.blist[lb], lane);
       const bool last = wpos >= wend;
       bool ok = true;
-      if (lane == 0) ok = wait_bar(S, &S.j_empty[slot], ((it >> 1) & 1) ^ 1, p, 256);
+      if (lane == 0) ok = wait_bar(S, &S.j_empty[slot], ((it / kJobSlots) & 1) ^ 1, p, 256);
       if (!__shfl_sync(0xFFFFFFFFu, ok, 0)) {
         // unwinding: let the q loads of the last two jobs land before the CTA exits
         if (lane == 0)
-          for (int i = 1; i <= 2 && i <= it; ++i) drain_bar(&S.j_full[(it - i) & 1], ((it - i) >> 1) & 1, p.timeout_ns);
+          for (int i = 1; i <= kJobSlots && i <= it; ++i)
+            drain_bar(&S.j_full[(it - i) % kJobSlots], ((it - i) / kJobSlots) & 1, p.timeout_ns);
         return;
       }
       Job &J = S.job[slot];
@@ -361,8 +374,8 @@ __device__ void k_loader(Smem &S, const GatherParams &p, int lane, int lt) {
   int it = 0, kc = 0;
   bool ok = true;
   for (;;) {
-    const int slot = it & 1;
-    if (lane == 0) ok = wait_bar(S, &S.j_full[slot], (it >> 1) & 1, p, 128);
+    const int slot = it % kJobSlots;
+    if (lane == 0) ok = wait_bar(S, &S.j_full[slot], (it / kJobSlots) & 1, p, 128);
     if (!(ok = __shfl_sync(0xFFFFFFFFu, ok, 0))) break;
     const Job &J = S.job[slot];
     if (J.row < 0) break;
@@ -394,8 +407,8 @@ __device__ void mma_issuer(Smem &S, uint32_t tmem, const GatherParams &p) {
   int it = 0, kc = 0;
   const uint64_t a0 = sw128_kmajor_desc(smem_u32(&S.kring[0][0]));
   for (;;) {
-    const int slot = it & 1;
-    if (!wait_bar(S, &S.j_full[slot], (it >> 1) & 1, p, 64)) break;
+    const int slot = it % kJobSlots;
+    if (!wait_bar(S, &S.j_full[slot], (it / kJobSlots) & 1, p, 64)) break;
     const Job &J = S.job[slot];
     if (J.row < 0) break;
     const int ntiles = (J.nblocks + kTileBlocks - 1) / kTileBlocks;
@@ -433,8 +446,8 @@ __device__ void epilogue(Smem &S, uint32_t tmem, const GatherParams &p, int warp
   const uint32_t lane_addr = (uint32_t)(quad * 32) << 16;
   int it = 0, tc = 0;
   for (;;) {
-    const int slot = it & 1;
-    bool ok = wait_bar(S, &S.j_full[slot], (it >> 1) & 1, p, 64);
+    const int slot = it % kJobSlots;
+    bool ok = wait_bar(S, &S.j_full[slot], (it / kJobSlots) & 1, p, 64);
     if (!__all_sync(0xFFFFFFFFu, ok)) return;
     const Job &J = S.job[slot];
     if (J.row < 0) return;
@@ -824,12 +837,12 @@ __device__ void selection(Smem &S, const GatherParams &p, int warp, int lane) {
   int it = 0, cin = 0, cn = 0;
   uint32_t clo = 0u, chi = 0u;  // the running top-k's order-key range
   for (;;) {
-    const int slot = it & 1;
+    const int slot = it % kJobSlots;
     // the four selection warps leave together (each wait is bounded)
-    if (bar_or(kSelBar, kSelThreads, !wait_bar(S, &S.j_full[slot], (it >> 1) & 1, p, 256))) return;
+    if (bar_or(kSelBar, kSelThreads, !wait_bar(S, &S.j_full[slot], (it / kJobSlots) & 1, p, 256))) return;
     const Job &J = S.job[slot];
     if (J.row < 0) return;
-    if (bar_or(kSelBar, kSelThreads, !wait_bar(S, &S.s_full[slot], (it >> 1) & 1, p, 64))) return;
+    if (bar_or(kSelBar, kSelThreads, !wait_bar(S, &S.s_full[slot], (it / kJobSlots) & 1, p, 64))) return;
     if (J.first) cn = 0;
     const int topk = p.topk;
     const int nent = ((J.nblocks + kTileBlocks - 1) / kTileBlocks) * kTileKeys;
@@ -891,7 +904,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&S.t_full[i], 1);
       mbar_init(&S.t_empty[i], 4);  // the four warps of the set that owns the buffer
     }
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < kJobSlots; ++i) {
       mbar_init(&S.j_full[i], 1);
       // released by the loader warps, the MMA issuer (commit) and the selection warps
       mbar_init(&S.j_empty[i], kLoaderWarps + 1 + kSelWarps);

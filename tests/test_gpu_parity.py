@@ -290,8 +290,8 @@ def test_block_mask_kernel_bit_exact(mqa):
                                                       (73, 17, 90000, 1024, 0.05), (76, 13, 120000, 2048, 0.6)])
 def test_masked_selection_random_masks(mqa, seed, rows, keys, topk, frac, scan):
     """Top-k over the keys of each row's allowed blocks (random masks), by
-    the gathering kernel (rows of up to ~2,400 allowed blocks: up to three
-    1,024-block jobs and a running top-k) and by the masked scan."""
+    the gathering kernel (rows of up to ~2,400 allowed blocks: up to four
+    768-block jobs and a running top-k) and by the masked scan."""
     p = synth.random_small(seed, rows, keys, topk)
     rng = np.random.default_rng(seed)
     picks = rng.integers(0, keys // 8 + 1, (rows, 4096))  # relative block indices, many past the range
@@ -314,7 +314,7 @@ def _full_mask(p):
 
 def test_masked_gather_full_mask_equals_unmasked(mqa):
     """A mask that allows every block: the gathering kernel's selection is the
-    unmasked top-k (rows of up to 6,250 blocks, seven jobs each)."""
+    unmasked top-k (rows of up to 6,250 blocks, nine jobs each)."""
     p = synth.random_small(77, 20, 50000, 512)
     mask, items = _full_mask(p)
     got, status, stats = run_masked(mqa, p, mask, items)
@@ -324,14 +324,15 @@ def test_masked_gather_full_mask_equals_unmasked(mqa):
 
 
 def test_masked_gather_job_boundaries(mqa):
-    """Rows whose allowed blocks number exactly 1,024 (one full job), 1,025
-    (a second job of one block), 2,048, one, none, and blocks cut by the range
-    at both ends; one CTA serves every row, reusing both job slots."""
+    """Rows whose allowed blocks number exactly 768 (one full job), 769 (a
+    second job of one block), 1,536, 2,304 (three full jobs: every job slot
+    in use for one row), 1,024, 3,000, one, none, and blocks cut by the range
+    at both ends; one CTA serves every row, reusing each job slot."""
     rng = np.random.default_rng(78)
-    keys, rows = 60000, 8
+    keys, rows = 60000, 11
     p = synth.random_small(78, rows, keys, 512, empty_frac=0.0)
-    starts = np.array([3, 1001, 5, 17, 0, 999, 100, 50003], np.int32)
-    ends = np.array([59997, 41005, 30000, 59999, 60000, 999, 9000, 50013], np.int32)
+    starts = np.array([3, 1001, 5, 17, 0, 999, 100, 50003, 8, 2, 640], np.int32)
+    ends = np.array([59997, 41005, 30000, 59999, 60000, 999, 9000, 50013, 59000, 52001, 60000], np.int32)
     p = synth.Problem(p.name, p.q, p.k, p.scales_ue8m0, p.weights, starts, ends, 512)
     words = ((keys + 1023) // 1024) * 4
     mask = np.zeros((rows, words), np.uint32)
@@ -339,7 +340,7 @@ def test_masked_gather_job_boundaries(mqa):
     def allow(r, blocks):
         for b in blocks:
             mask[r, b // 32] |= np.uint32(1 << (b % 32))
-    for r, nb in ((0, 1024), (1, 1025), (2, 2048), (4, 3000)):
+    for r, nb in ((0, 768), (1, 769), (2, 1536), (4, 3000), (8, 2304), (9, 1024), (10, 2305)):
         lo, hi = int(starts[r]) // 8, (int(ends[r]) - 1) // 8
         allow(r, rng.choice(np.arange(lo, hi + 1), size=nb, replace=False))
     allow(3, [17 // 8])                          # one block, cut by the start
