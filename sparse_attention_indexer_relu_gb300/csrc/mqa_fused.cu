@@ -270,6 +270,85 @@ __device__ __forceinline__ bool wait_counter(Smem &S, int *flag, int target, con
 // of four to the ALU pipe was the fastest split measured (none, a quarter,
 // three eighths and a half were compared).
 constexpr int kHeadGroups = kHeads / 32;  // 32-column groups per row
+// Two thread layouts of a row's head sum.  The pair-helper compilation reads
+// the accumulators with 16x64b loads: per 32-column group, thread t holds
+// keys A = t/4 + 8 (t%2) and B = A + 16 (two loads, lanes 0-15 and 16-31 of
+// the quadrant) x the 16 heads of parity b = (t/2)%2 (registers 2i, 2i + 1 =
+// heads 4i + b, 4i + 2 + b), so partners t and t^2 hold the two halves of the
+// same keys and one exchange completes a key's sum.  That needs twice the
+// weight registers of the 16x256b layout below (4 lanes per key, two
+// exchange steps); it measured 3-4% faster on decode batches in the pair
+// compilation and 5% slower at 1M keys in the 8-row compilation, where the
+// extra registers spill.
+#if MQA_PAIR_HELPERS
+#define MQA_LD64 1
+#else
+#define MQA_LD64 0
+#endif
+#if MQA_LD64
+struct HeadW {
+  float2 w[8 * kHeadGroups];  // (w[4i + b], w[4i + 2 + b]) of group i / 8 (doubled for ALU chunks)
+};
+__device__ __forceinline__ bool alu_pair(int i) { return (i & 7) < 2 * MQA_RELU_ALU_CHUNKS; }
+__device__ __forceinline__ float2 head_w_pair(const float *w, int i, int lane) {
+  const int h = 32 * (i >> 3) + 4 * (i & 7) + ((lane >> 1) & 1);
+  const float2 v = make_float2(w[h], w[h + 2]);
+  return alu_pair(i) ? make_float2(2.f * v.x, 2.f * v.y) : v;
+}
+template <int kPair>
+__device__ __forceinline__ float2 relu2(uint32_t a, uint32_t b) {
+  const float2 x = make_float2(__uint_as_float(a), __uint_as_float(b));
+  if ((kPair & 7) < 2 * MQA_RELU_ALU_CHUNKS) return make_float2(fmaxf(x.x, 0.f), fmaxf(x.y, 0.f));
+  return __fadd2_rn(x, make_float2(fabsf(x.x), fabsf(x.y)));
+}
+template <int G>
+__device__ __forceinline__ void head_group(const uint32_t (&lo)[16], const uint32_t (&hi)[16], const HeadW &W,
+                                           float2 &aA, float2 &aB) {
+#define MQA_HEAD_PAIR(i)                                                      \
+  aA = __ffma2_rn(relu2<8 * G + i>(lo[2 * i], lo[2 * i + 1]), W.w[8 * G + i], aA); \
+  aB = __ffma2_rn(relu2<8 * G + i>(hi[2 * i], hi[2 * i + 1]), W.w[8 * G + i], aB);
+  MQA_HEAD_PAIR(0)
+  MQA_HEAD_PAIR(1)
+  MQA_HEAD_PAIR(2)
+  MQA_HEAD_PAIR(3)
+  MQA_HEAD_PAIR(4)
+  MQA_HEAD_PAIR(5)
+  MQA_HEAD_PAIR(6)
+  MQA_HEAD_PAIR(7)
+#undef MQA_HEAD_PAIR
+}
+// Lanes with bit 1 clear keep key A, the others key B.
+__device__ __forceinline__ float reduce_keys(float2 aA, float2 aB, int lane) {
+  const float pA = aA.x + aA.y, pB = aB.x + aB.y;
+  const bool second = lane & 2;
+  const float s = second ? pA : pB;
+  return (second ? pB : pA) + __shfl_xor_sync(0xFFFFFFFFu, s, 2);
+}
+__device__ __forceinline__ int owned_key(int lane) { return (lane >> 2) + 8 * (lane & 1) + 16 * ((lane >> 1) & 1); }
+__device__ __forceinline__ void score_rows(uint64_t *t_empty, uint32_t base, const HeadW (&W)[kRowsPerWarp],
+                                           float hsc, int lane, float (&out)[kRowsPerWarp]) {
+#pragma unroll
+  for (int rr = 0; rr < kRowsPerWarp; ++rr) {
+    uint32_t lo[kHeadGroups][16], hi[kHeadGroups][16];
+#pragma unroll
+    for (int g = 0; g < kHeadGroups; ++g) {
+      const uint32_t col = (uint32_t)(rr * kHeads + 32 * g);
+      tmem_ld_16x64b_x16(base + col, lo[g]);
+      tmem_ld_16x64b_x16(base + (16u << 16) + col, hi[g]);
+    }
+    tmem_ld_wait();
+    if (rr == kRowsPerWarp - 1) {
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(t_empty);
+    }
+    float2 aA = make_float2(0.f, 0.f), aB = aA;
+    head_group<0>(lo[0], hi[0], W[rr], aA, aB);
+    if constexpr (kHeadGroups > 1) head_group<1>(lo[1], hi[1], W[rr], aA, aB);
+    out[rr] = reduce_keys(aA, aB, lane) * hsc;
+  }
+}
+#else
 struct HeadW {
   float2 w[4 * kHeadGroups];  // weights of this thread's heads of one row, as pairs (doubled for ALU chunks)
 };
@@ -344,6 +423,8 @@ __device__ __forceinline__ void score_rows(uint64_t *t_empty, uint32_t base, con
     out[rr] = reduce_keys(aA, aB, aC, aD, lane) * hsc;
   }
 }
+
+#endif  // MQA_LD64
 
 #if MQA_FOLD
 // ------------------------------------------------------------------ scoring with the fold
@@ -1644,10 +1725,14 @@ __device__ void epilogue(Smem &S, uint32_t tmem, const FusedParams &p, int warp,
       tau[rr] = kLogits ? NEG_INF : S.tau[r];
       cnt[rr] = 0;
 #pragma unroll
+#if MQA_LD64
+      for (int i = 0; i < 8 * kHeadGroups; ++i) W[rr].w[i] = head_w_pair(J.w[r], i, lane);
+#else
       for (int i = 0; i < 4 * kHeadGroups; ++i) {
         const float2 wv = *reinterpret_cast<const float2 *>(&J.w[r][8 * i + 2 * (lane & 3)]);
         W[rr].w[i] = !kFold && i < MQA_RELU_ALU_CHUNKS ? make_float2(2.f * wv.x, 2.f * wv.y) : wv;
       }
+#endif
     }
     const int ns = J.ns, ns2 = 2 * J.ns, ntiles = 2 * J.ns + J.nt, mode = J.mode;
     const int block = J.block;
