@@ -95,7 +95,7 @@ typedef struct mqa_topk_debug_options {
   int force_gate;      /* 0: sampled gate; 1: gate at +inf (every non-empty row
                           under-fills and is rescanned); 2: no gate (rows longer
                           than the slab overflow and are rescanned) */
-  int slab_capacity;   /* candidate records per row; 0 = default (16384).  Must
+  int slab_capacity;   /* candidate records per row; 0 = default (13312).  Must
                           be a multiple of 128, at least 4 * (topk + 64), and
                           not above the default (the workspace is sized for it) */
   int stall;           /* nonzero: the producer first waits on a barrier that
@@ -120,13 +120,13 @@ typedef struct mqa_topk_debug_options {
  * on the API page):
  *  - a 256-byte header (claim counter, status, counters);
  *  - one persistent CTA per SM (at most 32 per block of rows), two slabs of
- *    8 rows x 16384 candidate records (8 B each) per CTA;
+ *    8 rows x 13312 candidate records (8 B each) per CTA;
  *  - the key-range split arrays: for the blocks whose key range several CTAs
  *    scan as chunks (every block when there are fewer blocks than CTAs, else
- *    the last partial wave of blocks), a slab of 8 rows x (16384 + 512)
+ *    the last partial wave of blocks), a slab of 8 rows x (13312 + 512)
  *    records (more per block at 4 or more chunks, for fewer blocks), the
  *    per-chunk segment counts and a finished-chunk counter per block.
- * 398.5 MB for 16,384 rows on 152 SMs.
+ * 323.8 MB for 16,384 rows on 152 SMs.
  * A workspace below this size but at least the header plus the per-CTA slabs
  * of min(blocks, SMs) CTAs still works: the call then splits no block. 
  * Returns MQA_ERR_NO_DEVICE / MQA_ERR_CUDA when the device cannot be queried. */
@@ -233,7 +233,7 @@ int mqa_topk_prefill_debug(const void *q, const void *k, const float *key_scales
  * whole device memory pool; latency-critical paths that must never wait on an
  * allocator).  Same inputs, output and result as mqa_topk_prefill, but no
  * workspace argument: the scratch is a static device array inside the library
- * of 256 B + 8 CTAs x 2 slots x 8 rows x 16384 records x 8 B (16 MiB + 256 B),
+ * of 256 B + 8 CTAs x 2 slots x 8 rows x 13312 records x 8 B (13 MiB + 256 B),
  * held by every GPU that loads the library until the process exits.  The call
  * therefore runs on at most 8 persistent CTAs (slower than mqa_topk_prefill on
  * big chunks).  Its scratch need does not grow with rows or keys, so every

@@ -22,7 +22,7 @@ HEADS = 32
 HEAD_DIM = 128
 TOPKS = (512, 1024, 2048)
 HEADER_BYTES = 256
-DEFAULT_SLAB_CAP = 16384
+DEFAULT_SLAB_CAP = 13312
 DEFAULT_LOGITS_BUDGET = 512 * 2 ** 20
 
 MQA_OK = 0

@@ -54,7 +54,7 @@ constexpr int kEpiWarp0 = 4;
 constexpr int kSelWarp0 = 2;
 constexpr int kQuads = 4;       // TMEM lane quadrants; each row's slab has one segment per quadrant
 
-constexpr int kDefaultSlabCap = 16384;  // candidate records per row per slot (4 segments)
+constexpr int kDefaultSlabCap = 13312;  // candidate records per row per slot (4 segments)
 constexpr int kSlots = 2;               // slab slots per CTA (scan one, select the other)
 constexpr int kMaxSortBlocks = 8192;    // heaviest-first order kept in smem up to this many blocks
 constexpr int kMaxKeys = 1 << 24;

@@ -363,6 +363,10 @@ int run_fused(const void *q, const void *k, const float *scales, const float *we
   p.mask = mask;
   p.mask_words = mask_words;
   p.cap = cap;
+  // The gate aims at 3k candidates per row, at most half the slab row.  At
+  // the default capacity a quadrant segment (cap / 4 = 3,328 records) holds
+  // 2.17x its expected share of a top-2048 row's 6,144; a row whose quadrant
+  // overflows is rescanned exactly.
   p.gate_target = 3 * topk < cap / 2 ? 3 * topk : cap / 2;
   // Masked rows see few of their range's keys, so a sample of the range holds
   // few gate-passing keys: a larger target keeps about 32 of them in the
