@@ -71,6 +71,18 @@ static_assert(MQA_HEADS == 32, "masked selection is built for 32 heads");
 namespace mqa {
 namespace MQA_KNS {
 
+// The gate's sample tiles are scored once in the pair-helper compilation (the
+// scores are kept in the job's slab slot for the gate's two histogram passes)
+// and twice elsewhere (a coarse pass, then a fine pass that scores them
+// again).  Scoring once shortened decode batches by 3-6%, but slowed the
+// 8-row compilation's main loop by 7% at 1M keys (the same work, different
+// code), so that compilation keeps the two passes.
+#if MQA_PAIR_HELPERS
+#define MQA_SAMPLE_ONCE 1
+#else
+#define MQA_SAMPLE_ONCE 0
+#endif
+constexpr int kSamplePasses = MQA_SAMPLE_ONCE ? 1 : 2;  // times each sample tile is scored
 constexpr uint32_t kIdesc = idesc_f8_e4m3_f32(kTileKeys, kCols);
 constexpr uint32_t kTmemAllocCols = 512;  // a power of two holding every accumulator buffer
 
@@ -149,7 +161,7 @@ struct Smem {
   int segcnt[kBlockRows][kQuads];
   int nsplit, nchunks;  // key-range split plan: the last nsplit blocks of the order, nchunks chunks each
   uint32_t ref[kBlockRows];
-  int ref_frozen[kBlockRows];
+  int ref_frozen[kBlockRows];  // two-pass sample: the reference is taken from the first tile
   int msample[kBlockRows];
   // gate refinement: the coarse bin that holds the target sample rank
   int g_on[kBlockRows], g_above[kBlockRows], g_j[kBlockRows];
@@ -1184,7 +1196,8 @@ __device__ void plan_split(Smem &S, const FusedParams &p, long long w_light) {
   if (items > p.gate_min) {
     long long want = (32LL * L + (long long)p.gate_target * kTileKeys - 1) / ((long long)p.gate_target * kTileKeys);
     want = want < 4 ? 4 : (want > 64 ? 64 : want);
-    sfrac = 2.f * (float)(want < nt ? want : nt) / (float)nt;
+    if (MQA_SAMPLE_ONCE && want > p.cap / 64) want = p.cap / 64;
+    sfrac = (float)kSamplePasses * (float)(want < nt ? want : nt) / (float)nt;
   }
   const float base = (float)((cand + ctas - 1) / ctas);
   float best = 0.97f * base;
@@ -1412,6 +1425,7 @@ __device__ void producer(Smem &S, const CUtensorMap *q_map, const CUtensorMap *k
           long long want = (32LL * L + (long long)p.gate_target * kTileKeys - 1) /
                            ((long long)p.gate_target * kTileKeys);
           want = want < 4 ? 4 : (want > 64 ? 64 : want);
+          if (MQA_SAMPLE_ONCE && want > p.cap / 64) want = p.cap / 64;  // the sample scores' room in the slab slot
           ns = (int)(want < nt ? want : nt);
         }
       }
@@ -1474,7 +1488,7 @@ __device__ void producer(Smem &S, const CUtensorMap *q_map, const CUtensorMap *k
         }
       }
 #endif
-      ntiles = 2 * ns + nt;
+      ntiles = kSamplePasses * ns + nt;
     } else if (lane == 0) {
       J.block = -1;
     }
@@ -1492,8 +1506,9 @@ __device__ void producer(Smem &S, const CUtensorMap *q_map, const CUtensorMap *k
     if (lane == 0) {
       const JobInfo &Jc = S.job[slot];
       for (int u = 0; u < ntiles; ++u) {
-        if (u >= 2 * Jc.ns && !tile_on(Jc, u - 2 * Jc.ns)) continue;
-        const int tile = u < 2 * Jc.ns ? sample_tile(Jc, u < Jc.ns ? u : u - Jc.ns) : Jc.lo_t + (u - 2 * Jc.ns);
+        if (u >= kSamplePasses * Jc.ns && !tile_on(Jc, u - kSamplePasses * Jc.ns)) continue;
+        const int tile = u < kSamplePasses * Jc.ns ? sample_tile(Jc, u < Jc.ns ? u : u - Jc.ns)
+                                                   : Jc.lo_t + (u - kSamplePasses * Jc.ns);
         const int stage = kcount % kKStages;
         const int sst = kcount % kSStages;
         if (!wait_bar(S, &S.k_empty[stage], ((kcount / kKStages) & 1) ^ 1, p, kBackoffIdle)) break;
@@ -1534,11 +1549,11 @@ __device__ void mma_issuer(Smem &S, uint32_t tmem, const FusedParams &p) {
     if (!wait_bar(S, &S.j_full[slot], (job_iter >> 1) & 1, p, kBackoffMma)) break;
     const JobInfo &J = S.job[slot];
     if (J.block < 0) break;
-    const int ntiles = 2 * J.ns + J.nt;
+    const int ntiles = kSamplePasses * J.ns + J.nt;
     const uint64_t b_desc = sw128_kmajor_desc(smem_u32(&S.q[slot][0]));
     bool ok = true;
     for (int u = 0; u < ntiles && ok; ++u) {
-      if (u >= 2 * J.ns && !tile_on(J, u - 2 * J.ns)) continue;
+      if (u >= kSamplePasses * J.ns && !tile_on(J, u - kSamplePasses * J.ns)) continue;
       ok = wait_bar(S, &S.k_full[stage], kphase, p, kBackoffMma) &&
            wait_bar(S, &S.t_empty[buf], tphase ^ 1, p, kBackoffMma);
       if (!ok) break;
@@ -1734,7 +1749,7 @@ __device__ void epilogue(Smem &S, uint32_t tmem, const FusedParams &p, int warp,
       }
 #endif
     }
-    const int ns = J.ns, ns2 = 2 * J.ns, ntiles = 2 * J.ns + J.nt, mode = J.mode;
+    const int ns = J.ns, ns2 = kSamplePasses * J.ns, ntiles = kSamplePasses * J.ns + J.nt, mode = J.mode;
     const int block = J.block;
     // this warp's candidate segment of row rbase; row rbase + rr's is rr * row_stride further.
     // Whole block: the CTA's slab slot, [rows][quadrant segments of seg].  Key
@@ -1823,6 +1838,213 @@ __device__ void epilogue(Smem &S, uint32_t tmem, const FusedParams &p, int warp,
       ++tcount;
       return ok;
     };
+#if MQA_SAMPLE_ONCE
+    // ---- sample tiles, scored once.  Each thread keeps its key's scores of
+    // the warp's rows in the job's slab slot (free until the main scan: the
+    // slot's last selection ended before the job began) and re-reads only what
+    // it wrote, so the gate's coarse and fine passes need neither a second
+    // scoring of the tiles nor a barrier per tile.  Row r's score of key k of
+    // sample tile u is word (r * ns + u) * kTileKeys + k; ns <= cap / 64 keeps
+    // the 8 rows inside the slot's 16 * cap words.
+    do {
+      if (ns == 0) break;
+      // this thread's words: row rbase + rr, sample tile u at samp[(rr * ns + u) * kTileKeys]
+      float *const samp = reinterpret_cast<float *>(p.slab + (size_t)(blockIdx.x * kSlots + slot) * 2 * kBlockRows * (size_t)cap) +
+                          (size_t)rbase * ns * kTileKeys + kown;
+      for (int u = 0; u < ns; ++u) {
+        float sv[kRowsPerWarp];
+        score_tile(sample_tile(J, u), sv);
+#pragma unroll
+        for (int rr = 0; rr < kRowsPerWarp; ++rr) samp[(rr * ns + u) * kTileKeys] = sv[rr];
+      }
+      // coarse pass, step A: each row's reference is its largest sample score
+#pragma unroll
+      for (int rr = 0; rr < kRowsPerWarp; ++rr) {
+        const int r = rbase + rr;
+        float mx = NEG_INF;
+        for (int u = 0; u < ns; ++u) mx = fmaxf(mx, samp[(rr * ns + u) * kTileKeys]);
+        const uint32_t m = __reduce_max_sync(0xFFFFFFFFu, mx > NEG_INF ? f2key(mx) : 0u);
+        if (act[rr] && lane == 0 && m) atomicMax(&S.ref[r], m);
+      }
+      if (bar_or(kEpiBarrier, kEpiThreads, aborted(S))) { bail = true; break; }
+      // step B: log-binned histogram of each sample score's distance to the reference
+#pragma unroll
+      for (int rr = 0; rr < kRowsPerWarp; ++rr) {
+        const int r = rbase + rr;
+        const uint32_t ref = S.ref[r];
+        int nvis = 0;
+        if (act[rr] && ref) {
+#pragma unroll 1
+          for (int u = 0; u < ns; ++u) {
+            const float v = samp[(rr * ns + u) * kTileKeys];
+            if (v > NEG_INF) {
+              atomicAdd(&S.hist[r][gate_bin(f2key(v), ref)], 1);
+              ++nvis;
+            }
+          }
+        }
+        nvis = __reduce_add_sync(0xFFFFFFFFu, nvis);
+        if (lane == 0 && nvis) atomicAdd(&S.msample[r], nvis);
+      }
+      if (bar_or(kEpiBarrier, kEpiThreads, aborted(S))) { bail = true; break; }
+      // coarse bin of row ew that holds the target sample rank j
+      if (gate_warp) {
+        const int r = ew;
+        const int n = J.items[r];
+        const int m = S.msample[r];
+        int on = 0, above = 0, jw = 0;
+        uint32_t klo = 0, khi = 0;
+        if (((J.mask >> r) & 1u) && n > p.gate_min && m > 0) {
+          jw = (int)max(1LL, ((long long)m * p.gate_target + n - 1) / n);
+          constexpr int kPer = kGateBins / 32;
+          int c[kPer], tot = 0;
+#pragma unroll
+          for (int j = 0; j < kPer; ++j) {
+            c[j] = S.hist[r][kPer * lane + j];
+            tot += c[j];
+          }
+          int incl = tot;
+#pragma unroll
+          for (int off = 1; off < 32; off <<= 1) {
+            const int vv = __shfl_up_sync(0xFFFFFFFFu, incl, off);
+            if (lane >= off) incl += vv;
+          }
+          const int excl = incl - tot;
+          const uint32_t bm = __ballot_sync(0xFFFFFFFFu, excl < jw && jw <= incl);
+          if (bm) {
+            const int src = __ffs(bm) - 1;
+            int bin = 0, run_before = 0;
+            if (lane == src) {
+              int run = excl;
+#pragma unroll
+              for (int j = 0; j < kPer; ++j) {
+                if (run + c[j] >= jw) { bin = kPer * lane + j; run_before = run; break; }
+                run += c[j];
+              }
+            }
+            bin = __shfl_sync(0xFFFFFFFFu, bin, src);
+            above = __shfl_sync(0xFFFFFFFFu, run_before, src);
+            const uint32_t ref = S.ref[r];
+            if (bin == 128) {
+              klo = khi = ref;
+            } else if (bin > 128) {  // keys ref - d for d in [lo, hi)
+              const uint64_t lo = dist_bin_lo(bin - 128), hi = dist_bin_hi(bin - 128);
+              khi = ref - (uint32_t)lo;
+              klo = (uint64_t)ref >= hi - 1 ? ref - (uint32_t)(hi - 1) : 0u;
+            } else {  // keys ref + d for d in [lo, hi)
+              const uint64_t lo = dist_bin_lo(128 - bin), hi = dist_bin_hi(128 - bin);
+              klo = ref + (uint32_t)lo;
+              khi = (uint64_t)ref + hi - 1 > 0xFFFFFFFFull ? 0xFFFFFFFFu : ref + (uint32_t)(hi - 1);
+            }
+            on = 1;
+          }
+        }
+        __syncwarp();
+        for (int b2 = lane; b2 < kGateBins; b2 += 32) S.hist[r][b2] = 0;
+        if (lane == 0) {
+          S.g_on[r] = on;
+          S.g_above[r] = above;
+          S.g_j[r] = jw;
+          S.g_klo[r] = klo;
+          S.g_khi[r] = khi;
+          S.tau[r] = NEG_INF;
+        }
+      }
+      if (bar_or(kEpiBarrier, kEpiThreads, aborted(S))) { bail = true; break; }
+      if (ew == 0 && lane == 0) atomicAdd(p.ws + kWsSampleTiles, ns);
+      // fine pass: 256 linear sub-bins of the coarse bin, so the gate lands on
+      // the target sample rank
+#pragma unroll
+      for (int rr = 0; rr < kRowsPerWarp; ++rr) {
+        const int r = rbase + rr;
+        if (!act[rr]) continue;
+        const bool on = S.g_on[r] != 0;
+        const uint32_t klo = S.g_klo[r], khi = S.g_khi[r];
+        const uint64_t width = (uint64_t)(khi - klo) + 1;
+        uint32_t mx = 0, mn = 0xFFFFFFFFu;
+#pragma unroll 1
+        for (int u = 0; u < ns; ++u) {
+          const float v = samp[(rr * ns + u) * kTileKeys];
+          if (v > NEG_INF) {
+            const uint32_t kv = f2key(v);
+            mx = max(mx, kv);
+            mn = min(mn, kv);
+            if (on && kv >= klo && kv <= khi) atomicAdd(&S.hist[r][(int)(((uint64_t)(khi - kv) * 256) / width)], 1);
+          }
+        }
+        mx = __reduce_max_sync(0xFFFFFFFFu, mx);
+        if (lane == 0 && mx) atomicMax(&S.smax[r], mx);
+        if constexpr (kFold) {
+          mn = __reduce_min_sync(0xFFFFFFFFu, mn);
+          if (lane == 0 && mn != 0xFFFFFFFFu) atomicMin(&S.smin[r], mn);
+        }
+      }
+      if (bar_or(kEpiBarrier, kEpiThreads, aborted(S))) { bail = true; break; }
+      if (gate_warp) {
+        const int r = ew;
+        float t = NEG_INF;
+        if (S.g_on[r]) {
+          const int need = S.g_j[r] - S.g_above[r];
+          const uint32_t klo = S.g_klo[r], khi = S.g_khi[r];
+          int c[8], tot = 0;
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            c[j] = S.hist[r][8 * lane + j];
+            tot += c[j];
+          }
+          int incl = tot;
+#pragma unroll
+          for (int off = 1; off < 32; off <<= 1) {
+            const int vv = __shfl_up_sync(0xFFFFFFFFu, incl, off);
+            if (lane >= off) incl += vv;
+          }
+          const int excl = incl - tot;
+          const uint32_t bm = __ballot_sync(0xFFFFFFFFu, excl < need && need <= incl);
+          if (bm) {
+            const int src = __ffs(bm) - 1;
+            int sub = 0;
+            if (lane == src) {
+              int run = excl;
+#pragma unroll
+              for (int j = 0; j < 8; ++j) {
+                run += c[j];
+                if (run >= need) { sub = 8 * lane + j; break; }
+              }
+            }
+            sub = __shfl_sync(0xFFFFFFFFu, sub, src);
+            // pass every key inside sub-bins 0..sub (and everything above the coarse bin)
+            const uint64_t width = (uint64_t)(khi - klo) + 1;
+            const uint64_t drop = ((uint64_t)(sub + 1) * width + 255) / 256;
+            t = (uint64_t)khi >= drop ? key2f(khi - (uint32_t)drop) : NEG_INF;
+          }
+        }
+#if MQA_FOLD
+        // A row that needs the fold (more visible keys than top-k) is
+        // classified from its samples' largest |score|; an unsafe row emits
+        // nothing, so it under-fills and is rescanned with the direct sum.
+        if (((J.mask >> r) & 1u) && J.mode == 0 && J.items[r] > p.topk && S.smax[r] != 0) {
+          // the largest |score| among the samples: at the top or the bottom
+          const float seen = fmaxf(fabsf(key2f(S.smax[r])), fabsf(key2f(S.smin[r])));
+          const bool safe = fold_safe(p, S.key_norm, J.beta[r], seen, J.chunk <= 0, lane);
+          if (!safe) t = INFINITY;
+          if (lane == 0) {
+            S.unsafe[r] = !safe;
+            S.classified[r] = 1;
+          }
+        }
+#endif
+        if (lane == 0) {
+          S.tau[r] = t;
+          // linear score bins from the gate to the largest sample score
+          const float smax = S.smax[r] ? key2f(S.smax[r]) : NEG_INF;
+          S.binv[r] = (t > NEG_INF && smax > t) ? __fdiv_rn((float)kScoreBins, __fsub_rn(smax, t)) : 0.f;
+        }
+      }
+      if (bar_or(kEpiBarrier, kEpiThreads, aborted(S))) { bail = true; break; }
+#pragma unroll
+      for (int rr = 0; rr < kRowsPerWarp; ++rr) tau[rr] = S.tau[rbase + rr];
+    } while (0);
+#else
     // ---- sample tiles: coarse then fine pass of the gate
     for (int u = 0; u < ns2 && !bail; ++u) {
       const int tile = sample_tile(J, u < ns ? u : u - ns);
@@ -2015,6 +2237,7 @@ __device__ void epilogue(Smem &S, uint32_t tmem, const FusedParams &p, int warp,
         continue;
       }
     }
+#endif
     // ---- main tiles
     for (int u = ns2; u < ntiles && !bail; ++u) {
       if (!tile_on(J, u - ns2)) continue;
