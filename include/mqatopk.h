@@ -125,7 +125,8 @@ typedef struct mqa_topk_debug_options {
  *    scan as chunks (every block when there are fewer blocks than CTAs, else
  *    the last partial wave of blocks), a slab of 8 rows x (13312 + 512)
  *    records (more per block at 4 or more chunks, for fewer blocks), the
- *    per-chunk segment counts and a finished-chunk counter per block.
+ *    per-chunk segment counts, a finished-chunk counter and a merge row
+ *    counter per block.
  * 323.8 MB for 16,384 rows on 152 SMs.
  * A workspace below this size but at least the header plus the per-CTA slabs
  * of min(blocks, SMs) CTAs still works: the call then splits no block. 

@@ -147,6 +147,8 @@ struct SelSlot {  // what the selection warps need from a finished scan
   float beta[kBlockRows];                    // fold: 2-norm of the row's fold residual
   int split;    // candidates are in the split slab of block bs, nseg segments of seglen per row
   int bs, nseg, seglen;
+  int dist;        // a spread merge: the block's rows are claimed from merge_next by every chunk CTA
+  int count_done;  // this slot counts the block finished (the block's last chunk)
   int segcnt[kBlockRows][32];  // records per (row, segment): 4 quadrant segments, or one run per key chunk
 };
 
@@ -190,6 +192,7 @@ struct Smem {
   int selnext[2];    // rows claimed over all uses of the selection slot
   uint32_t selfail[2];
   int prod_parked;   // the producer has issued its last job and waits for every job to retire
+  int grp_row;       // spread merge: the row the epilogue group selects next
   float key_norm;    // fold: largest key_scale * |k|_2 over the keys (this call)
   int unsafe[kBlockRows];  // fold: rows of the current scan whose fold error bound is too large
   int classified[kBlockRows];  // fold: rows of the current scan classified at the gate
@@ -255,6 +258,41 @@ __device__ __forceinline__ bool wait_counter(Smem &S, int *flag, int target, con
     }
     __nanosleep(64);
   }
+}
+
+// Spin until the global counter *addr >= target (written by other CTAs of
+// this launch); false on abort/timeout.
+__device__ __forceinline__ bool wait_global(Smem &S, const int *addr, int target, const FusedParams &p) {
+  const uint64_t t0 = globaltimer_ns();
+  for (;;) {
+    if (*(volatile const int *)addr >= target) {
+      __threadfence();
+      return true;
+    }
+    if (aborted(S)) return false;
+    if ((long long)(globaltimer_ns() - t0) > p.timeout_ns) {
+      raise_timeout(S, p);
+      return false;
+    }
+    __nanosleep(64);
+  }
+}
+
+// Spread merge (pair-helper compilation): when every block of the call is
+// split and there are no more key chunks than CTAs, CTA i scans chunk job i
+// and nothing else, so each CTA is parked once its chunk is scanned.  Every
+// chunk CTA of a block then waits for the block's last chunk and claims the
+// block's rows one at a time (merge_next), each row selected by its 16
+// epilogue warps together, instead of the last chunk's CTA selecting all 8.
+// A CTA waits on other CTAs only after it has no scan work left, and the
+// chunks it waits for are all assigned to running CTAs, so the wait ends (it
+// is also bounded by the call's time limit).
+__device__ __forceinline__ bool spread_merge(const Smem &S, const FusedParams &p) {
+#if MQA_PAIR_HELPERS
+  return S.nsplit > 0 && S.nsplit == p.nblocks && S.nsplit * S.nchunks <= (int)gridDim.x;
+#else
+  return false;
+#endif
 }
 
 // ------------------------------------------------------------------ scoring
@@ -1289,6 +1327,8 @@ __device__ void producer(Smem &S, const CUtensorMap *q_map, const CUtensorMap *k
   const int ktiles_all = (p.keys + kTileKeys - 1) / kTileKeys;
   int job_iter = 0, kcount = 0;
   bool exhausted = false;
+  const bool spread = !kLogits && spread_merge(S, p);
+  bool claimed = false;  // spread merge: this CTA's one chunk job was taken
   if (p.stall) {  // debug: a wait that nothing satisfies, ended by the time limit
     bool ok = true;
     if (lane == 0) ok = wait_bar(S, &S.stall_bar, 0, p);
@@ -1315,7 +1355,8 @@ __device__ void producer(Smem &S, const CUtensorMap *q_map, const CUtensorMap *k
         }
       }
       if (block < 0 && !exhausted) {
-        const int i = atomicAdd(p.ws + kWsClaim, 1);
+        const int i = spread ? (claimed ? total_jobs : (int)blockIdx.x) : atomicAdd(p.ws + kWsClaim, 1);
+        claimed = true;
         if (i < total_jobs) {
           if (kLogits) {
             block = i / p.key_chunks;
@@ -1635,9 +1676,15 @@ __device__ void work_slot_rows(Smem &S, const FusedParams &p, int slot, int use,
 #if MQA_PAIR_HELPERS
 __device__ void work_slot_rows_pair(Smem &S, const FusedParams &p, int slot, int use, int m, int member, int *hist,
                                     uint32_t *lk, int32_t *li, int lane);
+__device__ void work_slot_rows_group(Smem &S, const FusedParams &p, int slot, int ew, int lane);
 #endif
 // Scratch of one helping epilogue warp: a 256-bin histogram and the list.
 constexpr int kHelperScratchBytes = 1024 + 8 * kSelList;
+// The epilogue group of a spread merge: the leader's histogram and list, then
+// four histogram copies per warp.
+static_assert(kHelperScratchBytes + kEpiWarps * 4 * kScoreBins * (int)sizeof(int) <=
+                  (int)(sizeof(Smem::kring) + sizeof(Smem::q)),
+              "the group's scratch fits the idle K ring and q buffers");
 static_assert(kEpiWarps * kHelperScratchBytes <= (int)(sizeof(Smem::kring) + sizeof(Smem::q)),
               "helper scratch exceeds the K ring and q buffers");
 
@@ -1671,6 +1718,7 @@ __device__ void epilogue(Smem &S, uint32_t tmem, const FusedParams &p, int warp,
   const int quad = warp & 3;        // TMEM lane quadrant this warp may access
   const int rbase = kRowsPerWarp * (ew >> 2);  // this warp's rows: rbase .. rbase + kRowsPerWarp - 1
   const bool gate_warp = ew < kBlockRows;        // the first kBlockRows warps also own row ew's gate / compaction
+  const bool spread = !kLogits && spread_merge(S, p);
   const uint32_t lane_addr = (uint32_t)(quad * 32) << 16;
   const float NEG_INF = -INFINITY;
   const int cap = p.cap, seg = p.cap / kQuads;
@@ -2351,7 +2399,7 @@ __device__ void epilogue(Smem &S, uint32_t tmem, const FusedParams &p, int warp,
         // The CTA that finishes a split block's last chunk selects the block
         // over every chunk's run (one segment per chunk); the others hand the
         // selection warps an empty job.
-        bool merge = true;
+        bool merge = true, have = true;
         const bool packed = J.chunk >= 0 && J.nchunks > 8;
         const int nseg = J.chunk < 0 ? kQuads : (packed ? J.nchunks : kQuads * J.nchunks);
         if (J.chunk >= 0) {
@@ -2360,7 +2408,15 @@ __device__ void epilogue(Smem &S, uint32_t tmem, const FusedParams &p, int warp,
           if (lane == 0) old = atomicAdd(p.split_done + J.bs, 1);
           old = __shfl_sync(0xFFFFFFFFu, old, 0);
           merge = old == J.nchunks - 1;
-          if (merge) {
+          have = merge;
+          if (spread && !merge) {
+            // a spread merge: this chunk's CTA also selects rows of the block
+            // once its last chunk is in
+            bool okw = true;
+            if (lane == 0) okw = wait_global(S, p.split_done + J.bs, J.nchunks, p);
+            have = __shfl_sync(0xFFFFFFFFu, okw, 0) != 0;
+          }
+          if (have) {
             __threadfence();
             for (int i = lane; i < kBlockRows * nseg; i += 32)
               Q.segcnt[i / nseg][i % nseg] = __ldcg(cnt_g + (i / nseg) * 32 + i % nseg);
@@ -2384,8 +2440,10 @@ __device__ void epilogue(Smem &S, uint32_t tmem, const FusedParams &p, int warp,
           Q.block = J.block;
           Q.mode = J.mode;
           Q.mask = J.mask;
-          Q.nrows = merge ? J.nrows : 0;
+          Q.nrows = have ? J.nrows : 0;
           Q.split = J.chunk >= 0;
+          Q.dist = spread && J.chunk >= 0;
+          Q.count_done = merge;
           Q.bs = J.bs;
           Q.nseg = nseg;
           Q.seglen = J.chunk < 0 ? seg : (packed ? kQuads * seglen : seglen);
@@ -2394,6 +2452,21 @@ __device__ void epilogue(Smem &S, uint32_t tmem, const FusedParams &p, int warp,
         __syncwarp();
         if (lane == 0) mbar_arrive(&S.s_full[slot]);
       }
+#if MQA_PAIR_HELPERS
+      if (spread && J.chunk >= 0) {
+        // A spread merge: the producer parks after this CTA's one job (no
+        // TMA writes follow), then the epilogue warps select the block's rows
+        // as one group, with scratch in the idle K ring and q buffers.
+        bool okp = true;
+        if (ew == 0 && lane == 0) okp = wait_counter(S, &S.prod_parked, 1, p);
+        if (bar_or(kEpiBarrier, kEpiThreads, !okp || aborted(S))) break;
+        work_slot_rows_group(S, p, slot, ew, lane);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&S.j_empty[slot]);
+        ++job_iter;
+        continue;
+      }
+#endif
       // Once the producer has parked, the epilogue warps help select the
       // block just handed over, with scratch in the idle K ring and q buffers.
       const bool parked =
@@ -2438,25 +2511,33 @@ __device__ bool pair_sync(Smem &S, int m, const FusedParams &p, int lane) {
   return __shfl_sync(0xFFFFFFFFu, ok, 0) != 0;
 }
 
-// score_hist over the pieces of this member's batches, into this member's
-// four histogram copies (one per lane % 4: candidates crowd into the bins
-// just above the gate), already zeroed
-constexpr int kPairHistCopies = 8;  // 2 members x 4 lane groups
-__device__ void score_hist_half(const RowSlab &R, float lo, float inv, int *hcopies, int lane, int member) {
+// score_hist over the pieces of this member's batches (member i of kM takes
+// every kM-th batch), into this member's four histogram copies (one per lane
+// % 4: candidates crowd into the bins just above the gate), already zeroed
+// Pieces per batch of a member: a pair takes deep batches; a 16-warp group
+// spreads a row's few dozen pieces over all its warps.
+template <int kM>
+struct MultiDepth {
+  static constexpr int kHist = kM == 2 ? kHistDepth : 4;
+  static constexpr int kPass2 = kM == 2 ? kPass2Groups : 3;
+};
+template <int kM>
+__device__ void score_hist_part(const RowSlab &R, float lo, float inv, int *hcopies, int lane, int member) {
+  constexpr int kD = MultiDepth<kM>::kHist;
   int *hist = hcopies + (member * 4 + (lane & 3)) * kScoreBins;
   const PieceMap pm = piece_map(R, lane);
 #pragma unroll 1
-  for (int t0 = member * kHistDepth; t0 < pm.total; t0 += 2 * kHistDepth) {
-    int at[kHistDepth], lim[kHistDepth];
-    uint4 kk[kHistDepth];
+  for (int t0 = member * kD; t0 < pm.total; t0 += kM * kD) {
+    int at[kD], lim[kD];
+    uint4 kk[kD];
 #pragma unroll
-    for (int j = 0; j < kHistDepth; ++j) piece_at(R, pm, t0 + j, at[j], lim[j]);
+    for (int j = 0; j < kD; ++j) piece_at(R, pm, t0 + j, at[j], lim[j]);
 #pragma unroll
-    for (int j = 0; j < kHistDepth; ++j)
+    for (int j = 0; j < kD; ++j)
       kk[j] = 4 * lane < lim[j] ? __ldcg(reinterpret_cast<const uint4 *>(R.keys + at[j] + 4 * lane))
                                 : make_uint4(0, 0, 0, 0);
 #pragma unroll
-    for (int j = 0; j < kHistDepth; ++j) {
+    for (int j = 0; j < kD; ++j) {
       const int e = 4 * lane;
       if (e < lim[j]) atomicAdd(&hist[score_bin(key2f(kk[j].x), lo, inv)], 1);
       if (e + 1 < lim[j]) atomicAdd(&hist[score_bin(key2f(kk[j].y), lo, inv)], 1);
@@ -2468,31 +2549,52 @@ __device__ void score_hist_half(const RowSlab &R, float lo, float inv, int *hcop
 
 constexpr int kPairOut = 200, kPairList = 201;  // shared output / list counters in the leader's histogram
 
-// Returns the leader's written count, 0 for the other member, or -1 (both)
-// when the threshold bin does not fit the list.
-__device__ int pair_select_binned(Smem &S, const FusedParams &p, int m, int member, const RowSlab &R, int k,
-                                  float lo, float inv, int *hist, uint32_t *lk, int32_t *li, int32_t *out, int base,
-                                  int lane) {
-  // the histogram copies follow the pair's list in its scratch (the second
-  // member's share of the scratch is otherwise unused)
+// Selection of one row by kM warps (members 0 .. kM - 1; member 0 leads),
+// meeting at sync() (false: the call is aborting).  Returns the leader's
+// written count, 0 for the other members, -1 (all) when the threshold bin
+// does not fit the list, or -2 on abort.
+template <int kM, class Sync>
+__device__ int multi_select_binned(Sync &&sync, int member, const RowSlab &R, int k, float lo, float inv, int *hist,
+                                   uint32_t *lk, int32_t *li, int32_t *out, int base, int lane) {
+  // the histogram copies (4 per member) follow the leader's list in the
+  // members' scratch (the other members' own scratch is otherwise unused)
   int *hcopies = reinterpret_cast<int *>(li + kSelList);
   for (int b = lane; b < 4 * kScoreBins; b += 32) hcopies[member * 4 * kScoreBins + b] = 0;
   if (member == 0 && lane == 0) {
     hist[kPairOut] = 0;
     hist[kPairList] = 0;
   }
-  if (!pair_sync(S, m, p, lane)) return -2;
-  score_hist_half(R, lo, inv, hcopies, lane, member);
-  if (!pair_sync(S, m, p, lane)) return -2;
+  if (!sync()) return -2;
+  score_hist_part<kM>(R, lo, inv, hcopies, lane, member);
+  if (!sync()) return -2;
   int c[kBinsPerLane], tot = 0;
+  if constexpr (kM == 2) {
+    // each member sums the copies itself
 #pragma unroll
-  for (int j = 0; j < kBinsPerLane; ++j) {
-    const int b = kScoreBins - 1 - kBinsPerLane * lane - j;
-    int v = 0;
+    for (int j = 0; j < kBinsPerLane; ++j) {
+      const int b = kScoreBins - 1 - kBinsPerLane * lane - j;
+      int v = 0;
 #pragma unroll
-    for (int cp = 0; cp < kPairHistCopies; ++cp) v += hcopies[cp * kScoreBins + b];
-    c[j] = v;
-    tot += c[j];
+      for (int cp = 0; cp < 4 * kM; ++cp) v += hcopies[cp * kScoreBins + b];
+      c[j] = v;
+      tot += c[j];
+    }
+  } else {
+    // one thread per bin sums the copies into the leader's histogram
+    // (its first kScoreBins entries are free until the list radix)
+    const int t = member * 32 + lane;
+    if (t < kScoreBins) {
+      int v = 0;
+#pragma unroll 8
+      for (int cp = 0; cp < 4 * kM; ++cp) v += hcopies[cp * kScoreBins + t];
+      hist[t] = v;
+    }
+    if (!sync()) return -2;
+#pragma unroll
+    for (int j = 0; j < kBinsPerLane; ++j) {
+      c[j] = hist[kScoreBins - 1 - kBinsPerLane * lane - j];
+      tot += c[j];
+    }
   }
   int incl = tot;
 #pragma unroll
@@ -2521,16 +2623,17 @@ __device__ int pair_select_binned(Smem &S, const FusedParams &p, int m, int memb
   above = __shfl_sync(0xFFFFFFFFu, above, src);
   nB = __shfl_sync(0xFFFFFFFFu, nB, src);
   if (nB > kSelList || nB <= 0) return -1;
+  constexpr int kP2 = MultiDepth<kM>::kPass2;
   const PieceMap pm = piece_map(R, lane);
 #pragma unroll 1
-  for (int t0 = member * kPass2Groups; t0 < pm.total; t0 += 2 * kPass2Groups) {
-    int at[kPass2Groups], lim[kPass2Groups];
-    uint32_t kk[4 * kPass2Groups];
-    int32_t ii[4 * kPass2Groups];
+  for (int t0 = member * kP2; t0 < pm.total; t0 += kM * kP2) {
+    int at[kP2], lim[kP2];
+    uint32_t kk[4 * kP2];
+    int32_t ii[4 * kP2];
 #pragma unroll
-    for (int gi = 0; gi < kPass2Groups; ++gi) piece_at(R, pm, t0 + gi, at[gi], lim[gi]);
+    for (int gi = 0; gi < kP2; ++gi) piece_at(R, pm, t0 + gi, at[gi], lim[gi]);
 #pragma unroll
-    for (int gi = 0; gi < kPass2Groups; ++gi) {
+    for (int gi = 0; gi < kP2; ++gi) {
       uint4 kv = make_uint4(0, 0, 0, 0);
       int4 iv = make_int4(0, 0, 0, 0);
       if (4 * lane < lim[gi]) {
@@ -2543,7 +2646,7 @@ __device__ int pair_select_binned(Smem &S, const FusedParams &p, int m, int memb
     // the bin compared directly (the same monotone function as the count pass)
     uint32_t up = 0, in = 0;
 #pragma unroll
-    for (int j = 0; j < 4 * kPass2Groups; ++j) {
+    for (int j = 0; j < 4 * kP2; ++j) {
       const bool v = 4 * lane + (j & 3) < lim[j >> 2];
       const int bj = score_bin(key2f(kk[j]), lo, inv);
       if (v && bj > B) up |= 1u << j;
@@ -2567,7 +2670,7 @@ __device__ int pair_select_binned(Smem &S, const FusedParams &p, int m, int memb
     rl = __shfl_sync(0xFFFFFFFFu, rl, 0);
     int po = ro + (pexcl & 0xFFFF), pl = rl + (pexcl >> 16);
 #pragma unroll
-    for (int j = 0; j < 4 * kPass2Groups; ++j) {
+    for (int j = 0; j < 4 * kP2; ++j) {
       if ((up >> j) & 1u) {
         if (po < k) out[po] = out_index(ii[j], base);
         ++po;
@@ -2581,7 +2684,7 @@ __device__ int pair_select_binned(Smem &S, const FusedParams &p, int m, int memb
       }
     }
   }
-  if (!pair_sync(S, m, p, lane)) return -2;
+  if (!sync()) return -2;
   if (member != 0) return 0;
   int outc = hist[kPairOut];
   const int lc = min(hist[kPairList], kSelList);
@@ -2789,10 +2892,11 @@ __device__ void work_slot_rows(Smem &S, const FusedParams &p, int slot, int use,
 
 // ------------------------------------------------------------------ selection (warps 2-3)
 #if MQA_PAIR_HELPERS
-// Row r selected by pair m (member 0 leads); returns true when the row must
-// be rescanned.  Both members pass the same syncs on every path.
-__device__ bool select_row_pair(Smem &S, const FusedParams &p, int slot, int r, int m, int member, int *hist,
-                                uint32_t *lk, int32_t *li, int lane, bool &ok) {
+// Row r selected by kM warps (member 0 leads); returns true when the row
+// must be rescanned.  Every member passes the same syncs on every path.
+template <int kM, class Sync>
+__device__ bool select_row_multi(Smem &S, const FusedParams &p, int slot, int r, Sync &&sync, int member, int *hist,
+                                 uint32_t *lk, int32_t *li, int lane, bool &ok) {
   const SelSlot &Q = S.sel[slot];
   bool fail = false;
   if (r < Q.nrows && ((Q.mask >> r) & 1u)) {
@@ -2826,8 +2930,8 @@ __device__ bool select_row_pair(Smem &S, const FusedParams &p, int slot, int r, 
       int32_t *out = p.out + (size_t)(Q.block * kBlockRows + r) * topk;
       int wrote = -1;
       if (cnt > topk && Q.binned[r]) {
-        wrote = pair_select_binned(S, p, m, member, R, topk, Q.blo[r], Q.binv[r], hist, lk, li, out, Q.start[r],
-                                   lane);
+        wrote = multi_select_binned<kM>(sync, member, R, topk, Q.blo[r], Q.binv[r], hist, lk, li, out, Q.start[r],
+                                        lane);
         if (wrote == -2) {
           ok = false;
           return false;
@@ -2846,7 +2950,7 @@ __device__ bool select_row_pair(Smem &S, const FusedParams &p, int slot, int r, 
       }
     }
   }
-  ok = pair_sync(S, m, p, lane);
+  ok = sync();
   return fail;
 }
 
@@ -2877,7 +2981,8 @@ __device__ void work_slot_rows_pair(Smem &S, const FusedParams &p, int slot, int
       return;
     }
     bool ok = true;
-    const bool fail = select_row_pair(S, p, slot, r, m, member, hist, lk, li, lane, ok);
+    const bool fail = select_row_multi<2>(S, p, slot, r, [&]() { return pair_sync(S, m, p, lane); }, member, hist, lk,
+                                          li, lane, ok);
     if (!ok) return;
     if (member == 0 && lane == 0) {
       if (r < S.sel[slot].nrows && ((S.sel[slot].mask >> r) & 1u)) atomicAdd(p.ws + kWsPairRows, 1);
@@ -2903,6 +3008,45 @@ __device__ void work_slot_rows_pair(Smem &S, const FusedParams &p, int slot, int
   }
 }
 
+
+// A spread merge's rows, claimed one at a time from the block's merge_next
+// and selected by this CTA's 16 epilogue warps together (warp 0 leads); the
+// leader then releases the slot (rows to rescan go to this CTA's queue).
+__device__ void work_slot_rows_group(Smem &S, const FusedParams &p, int slot, int ew, int lane) {
+  const SelSlot &Q = S.sel[slot];
+  uint8_t *scr = &S.kring[0][0];
+  int *hist = reinterpret_cast<int *>(scr);
+  uint32_t *lk = reinterpret_cast<uint32_t *>(scr + 1024);
+  int32_t *li = reinterpret_cast<int32_t *>(scr + 1024 + 4 * kSelList);
+  auto sync = [&]() { return !bar_or(kEpiBarrier, kEpiThreads, aborted(S)); };
+  uint32_t fails = 0;
+  for (;;) {
+    if (ew == 0 && lane == 0)
+      *(volatile int *)&S.grp_row = Q.nrows > 0 ? atomicAdd(p.merge_next + Q.bs, 1) : kBlockRows;
+    if (!sync()) return;
+    const int r = *(volatile int *)&S.grp_row;
+    if (r >= kBlockRows) break;
+    bool ok = true;
+    const bool fail = select_row_multi<kEpiWarps>(S, p, slot, r, sync, ew, hist, lk, li, lane, ok);
+    if (!ok) return;
+    if (fail) fails |= 1u << r;
+    if (ew == 0 && lane == 0 && r < Q.nrows && ((Q.mask >> r) & 1u)) atomicAdd(p.ws + kWsPairRows, 1);
+  }
+  if (ew == 0 && lane == 0) {
+    if (fails) {
+      const int tail = S.fifo_tail;
+      S.fifo_block[tail & 7] = Q.block;
+      S.fifo_mask[tail & 7] = fails;
+      __threadfence_block();
+      *(volatile int *)&S.fifo_tail = tail + 1;
+    }
+    __threadfence_block();
+    if (Q.count_done) atomicAdd(p.ws + kWsBlocksDone, 1);
+    atomicAdd(&S.retired, 1);
+    mbar_arrive(&S.s_empty[slot]);
+  }
+}
+
 #endif
 
 __device__ void selection(Smem &S, const FusedParams &p, int warp, int lane) {
@@ -2915,7 +3059,9 @@ __device__ void selection(Smem &S, const FusedParams &p, int warp, int lane) {
     ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
     if (!ok) break;
     if (S.sel[slot].block < 0) break;
-    work_slot_rows(S, p, slot, job_iter >> 1, &S.selhist[sw][0], S.sel_lk[sw], S.sel_li[sw], lane);
+    // the epilogue group selects (and releases) a spread merge's slot
+    if (!S.sel[slot].dist)
+      work_slot_rows(S, p, slot, job_iter >> 1, &S.selhist[sw][0], S.sel_lk[sw], S.sel_li[sw], lane);
     ++job_iter;
   }
 }

@@ -112,6 +112,7 @@ struct FusedParams {
   uint32_t *split_slab;  // per split block: [rows 8][row capacity] keys, then same for indices
   int32_t *split_cnt;    // per split block: [rows 8][32] records per (chunk, quadrant) segment
   int32_t *split_done;   // per split block: chunks finished (zeroed with the header)
+  int32_t *merge_next;   // per split block: next row claimed in a spread merge (zeroed with the header)
   int split_max;         // split blocks the arrays above hold
   long long split_words; // uint32 words of split_slab
   const int32_t *row_items;  // masked selection: allowed keys per row

@@ -160,7 +160,8 @@ int split_max_blocks(int ctas, int rows, int brows) {
 FusedLayout mqa::fused_layout(int ctas, int cap, int split_max, int brows, int fold_rows) {
   FusedLayout L;
   L.done_off = kWsHeaderBytes;
-  L.slab_off = L.done_off + (((size_t)split_max * sizeof(int32_t) + 255) / 256) * 256;
+  // per split block: finished chunks, then the next row of a spread merge
+  L.slab_off = L.done_off + (((size_t)2 * split_max * sizeof(int32_t) + 255) / 256) * 256;
   L.split_off = L.slab_off + slab_bytes(ctas, cap, brows);
   long long rc = 0;
   if (split_max > 0) {
@@ -347,6 +348,7 @@ int run_fused(const void *q, const void *k, const float *scales, const float *we
   p.split_max = P.split_max;
   if (P.split_max > 0) {
     p.split_done = reinterpret_cast<int32_t *>(wsb + L.done_off);
+    p.merge_next = p.split_done + P.split_max;
     p.split_slab = reinterpret_cast<uint32_t *>(wsb + L.split_off);
     p.split_cnt = reinterpret_cast<int32_t *>(wsb + L.cnt_off);
     p.split_words = L.split_words;
