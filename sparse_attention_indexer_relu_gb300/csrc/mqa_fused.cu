@@ -71,17 +71,24 @@ static_assert(MQA_HEADS == 32, "masked selection is built for 32 heads");
 namespace mqa {
 namespace MQA_KNS {
 
-// The gate's sample tiles are scored once in the pair-helper compilation (the
-// scores are kept in the job's slab slot for the gate's two histogram passes)
-// and twice elsewhere (a coarse pass, then a fine pass that scores them
-// again).  Scoring once shortened decode batches by 3-6%, but slowed the
-// 8-row compilation's main loop by 7% at 1M keys (the same work, different
-// code), so that compilation keeps the two passes.
-#if MQA_PAIR_HELPERS
+// The gate's sample tiles are scored once in the 32-head key-selection
+// compilations (8-row and pair-helper: the scores are kept in the job's slab
+// slot for the gate's two histogram passes) and twice in the others (a coarse
+// pass, then a fine pass that scores them again).  Scoring once shortened
+// decode batches by 3-6% and, with the scan loop of gated jobs kept free of
+// the rescan code, the 1M-key chunk by 3.3%.
+#ifndef MQA_SAMPLE_ONCE
+#if MQA_HEADS == 32 && !MQA_BLOCKS && !MQA_MASKED && !MQA_FOLD
 #define MQA_SAMPLE_ONCE 1
 #else
 #define MQA_SAMPLE_ONCE 0
 #endif
+#endif
+// Gated scans skip the per-row ballots of a tile in which no key of the
+// warp's rows passes the gate (one vote over both rows).  That measured 2%
+// faster at 1M keys in the 8-row compilation and 1.5% slower on decode
+// batches in the pair-helper compilation, which leaves it out.
+constexpr bool kAnyGate = !MQA_PAIR_HELPERS;
 constexpr int kSamplePasses = MQA_SAMPLE_ONCE ? 1 : 2;  // times each sample tile is scored
 constexpr uint32_t kIdesc = idesc_f8_e4m3_f32(kTileKeys, kCols);
 constexpr uint32_t kTmemAllocCols = 512;  // a power of two holding every accumulator buffer
@@ -1598,7 +1605,8 @@ __device__ void producer(Smem &S, const CUtensorMap *q_map, const CUtensorMap *k
         const int stage = kcount % kKStages;
         const int sst = kcount % kSStages;
         if (!wait_bar(S, &S.k_empty[stage], ((kcount / kKStages) & 1) ^ 1, p, kBackoffIdle)) break;
-        // the tile's key scales (zero past the last key), released by the epilogue
+        // the tile's key scales (zero past the last key); a slot is released
+        // once every epilogue warp has read it
         if (!wait_bar(S, &S.sc_empty[sst], ((kcount / kSStages) & 1) ^ 1, p, kBackoffIdle)) break;
         if constexpr (kMasked) {
           mbar_arrive_expect_tx(&S.k_full[stage], kKTileBytes);
@@ -1631,6 +1639,7 @@ __device__ void mma_issuer(Smem &S, uint32_t tmem, const FusedParams &p) {
   int job_iter = 0;
   int stage = 0, kphase = 0;  // K ring slot and the parity its full barrier completes with
   int buf = 0, tphase = 0;    // accumulator buffer and the parity of its current use
+  int mcount = 0;  // tiles issued so far, over all jobs
   // Descriptors of the first K slot; a slot (and a 32-byte K step) moves the
   // start address field (bits 0-13, in 16-byte units) without carrying out of
   // it, since every shared address is below 2^18.
@@ -1656,6 +1665,13 @@ __device__ void mma_issuer(Smem &S, uint32_t tmem, const FusedParams &p) {
         umma_f8(d, a_desc + (uint64_t)(2 * kk), b_desc + (uint64_t)(2 * kk), kIdesc, kk > 0 ? 1u : 0u);
       umma_commit(&S.k_empty[stage]);
       umma_commit(&S.t_full[buf]);
+      // Every epilogue warp released this buffer's previous tile (two tiles
+      // back) and had read that tile's key scales before: free their slot
+      // here, after the MMAs are issued, instead of one arrival per epilogue
+      // warp and tile (1M keys: 0.7% faster with the separate gated-scan
+      // loop).  The masked scan's epilogue releases its slots itself.
+      if (!kMasked && mcount >= kTmemBufs) mbar_arrive(&S.sc_empty[(mcount - kTmemBufs) % kSStages]);
+      ++mcount;
       if (++stage == kKStages) {
         stage = 0;
         kphase ^= 1;
@@ -1900,7 +1916,7 @@ __device__ void epilogue(Smem &S, uint32_t tmem, const FusedParams &p, int warp,
 #pragma unroll
         for (int rr = 0; rr < kRowsPerWarp; ++rr) mw[rr] = S.mring[sst][rbase + rr][(tile >> 1) & 3];
       }
-      if (lane == 0) mbar_arrive(&S.sc_empty[sst]);
+      if (kMasked && lane == 0) mbar_arrive(&S.sc_empty[sst]);
       if (tile >= f_lo && tile < f_hi) {
         // the tile lies inside every row's range: no per-key mask
 #pragma unroll
@@ -2337,6 +2353,37 @@ __device__ void epilogue(Smem &S, uint32_t tmem, const FusedParams &p, int warp,
 #endif
     // ---- main tiles
     const int lo_t = J.lo_t;
+    if (!kLogits && mode == 0 && !bail) {
+      // Gated or plain scan: a loop of its own, without the rescan's
+      // compaction steps and bail-out test (1M keys: 0.7% faster).
+      for (int u = ns2; u < ntiles; ++u) {
+        if (!tile_on(J, u - ns2)) continue;
+        const int tile = lo_t + (u - ns2);
+        const int key = tile * kTileKeys + kown;
+        float sv[kRowsPerWarp];
+        score_tile(tile, sv);
+        if constexpr (kAnyGate) {
+          bool anyp = false;
+#pragma unroll
+          for (int rr = 0; rr < kRowsPerWarp; ++rr) anyp |= sv[rr] > tau[rr];
+          if (!__any_sync(0xFFFFFFFFu, anyp)) continue;
+        }
+#pragma unroll
+        for (int rr = 0; rr < kRowsPerWarp; ++rr) {
+          const bool pass = sv[rr] > tau[rr];
+          const uint32_t bal = __ballot_sync(0xFFFFFFFFu, pass);
+          if (bal) {
+            const int pos = cnt[rr] + __popc(bal & lt);
+            if (pass && pos < seglen) {
+              const int o = rr * row_stride + pos;
+              __stcg(&seg_keys[o], f2key(sv[rr]));
+              __stcg(&seg_idx[o], key);
+            }
+            cnt[rr] += __popc(bal);
+          }
+        }
+      }
+    } else
     for (int u = ns2; u < ntiles && !bail; ++u) {
       if (!tile_on(J, u - ns2)) continue;
       const int tile = lo_t + (u - ns2);
@@ -3134,7 +3181,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int i = 0; i < kSStages; ++i) {
       mbar_init(&S.sc_full[i], 1);
-      mbar_init(&S.sc_empty[i], kEpiWarps);
+      mbar_init(&S.sc_empty[i], kMasked ? kEpiWarps : 1);
     }
     for (int i = 0; i < kTmemBufs; ++i) {
       mbar_init(&S.t_full[i], 1);
