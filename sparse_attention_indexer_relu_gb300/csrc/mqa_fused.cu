@@ -71,14 +71,15 @@ static_assert(MQA_HEADS == 32, "masked selection is built for 32 heads");
 namespace mqa {
 namespace MQA_KNS {
 
-// The gate's sample tiles are scored once in the 32-head key-selection
-// compilations (8-row and pair-helper: the scores are kept in the job's slab
-// slot for the gate's two histogram passes) and twice in the others (a coarse
-// pass, then a fine pass that scores them again).  Scoring once shortened
-// decode batches by 3-6% and, with the scan loop of gated jobs kept free of
-// the rescan code, the 1M-key chunk by 3.3%.
+// The gate's sample tiles are scored once in the 32-head key and block
+// selection compilations (8-row, pair-helper and block: the scores are kept in
+// the job's slab slot for the gate's two histogram passes) and twice in the
+// others (a coarse pass, then a fine pass that scores them again).  Scoring
+// once shortened decode batches by 3-6% and, with the scan loop of gated jobs
+// kept free of the rescan code, the 1M-key chunk by 3.3% and the 1M-key block
+// selection by 0.7%.
 #ifndef MQA_SAMPLE_ONCE
-#if MQA_HEADS == 32 && !MQA_BLOCKS && !MQA_MASKED && !MQA_FOLD
+#if MQA_HEADS == 32 && !MQA_MASKED && !MQA_FOLD
 #define MQA_SAMPLE_ONCE 1
 #else
 #define MQA_SAMPLE_ONCE 0
@@ -88,7 +89,10 @@ namespace MQA_KNS {
 // warp's rows passes the gate (one vote over both rows).  That measured 2%
 // faster at 1M keys in the 8-row compilation and 1.5% slower on decode
 // batches in the pair-helper compilation, which leaves it out.
-constexpr bool kAnyGate = !MQA_PAIR_HELPERS;
+#ifndef MQA_ANY_GATE
+#define MQA_ANY_GATE (!MQA_PAIR_HELPERS)
+#endif
+constexpr bool kAnyGate = MQA_ANY_GATE;
 constexpr int kSamplePasses = MQA_SAMPLE_ONCE ? 1 : 2;  // times each sample tile is scored
 constexpr uint32_t kIdesc = idesc_f8_e4m3_f32(kTileKeys, kCols);
 constexpr uint32_t kTmemAllocCols = 512;  // a power of two holding every accumulator buffer
@@ -199,7 +203,8 @@ struct Smem {
   int selnext[2];    // rows claimed over all uses of the selection slot
   uint32_t selfail[2];
   int prod_parked;   // the producer has issued its last job and waits for every job to retire
-  int grp_row;       // spread merge: the row the epilogue group selects next
+  int grp_row[2];    // spread merge: the row each epilogue group selects next
+  unsigned grp_fails;  // spread merge: rows the groups failed (to rescan)
   float key_norm;    // fold: largest key_scale * |k|_2 over the keys (this call)
   int unsafe[kBlockRows];  // fold: rows of the current scan whose fold error bound is too large
   int classified[kBlockRows];  // fold: rows of the current scan classified at the gate
@@ -327,85 +332,6 @@ __device__ __forceinline__ bool spread_merge(const Smem &S, const FusedParams &p
 // of four to the ALU pipe was the fastest split measured (none, a quarter,
 // three eighths and a half were compared).
 constexpr int kHeadGroups = kHeads / 32;  // 32-column groups per row
-// Two thread layouts of a row's head sum.  The pair-helper compilation reads
-// the accumulators with 16x64b loads: per 32-column group, thread t holds
-// keys A = t/4 + 8 (t%2) and B = A + 16 (two loads, lanes 0-15 and 16-31 of
-// the quadrant) x the 16 heads of parity b = (t/2)%2 (registers 2i, 2i + 1 =
-// heads 4i + b, 4i + 2 + b), so partners t and t^2 hold the two halves of the
-// same keys and one exchange completes a key's sum.  That needs twice the
-// weight registers of the 16x256b layout below (4 lanes per key, two
-// exchange steps); it measured 3-4% faster on decode batches in the pair
-// compilation and 5% slower at 1M keys in the 8-row compilation, where the
-// extra registers spill.
-#if MQA_PAIR_HELPERS
-#define MQA_LD64 1
-#else
-#define MQA_LD64 0
-#endif
-#if MQA_LD64
-struct HeadW {
-  float2 w[8 * kHeadGroups];  // (w[4i + b], w[4i + 2 + b]) of group i / 8 (doubled for ALU chunks)
-};
-__device__ __forceinline__ bool alu_pair(int i) { return (i & 7) < 2 * MQA_RELU_ALU_CHUNKS; }
-__device__ __forceinline__ float2 head_w_pair(const float *w, int i, int lane) {
-  const int h = 32 * (i >> 3) + 4 * (i & 7) + ((lane >> 1) & 1);
-  const float2 v = make_float2(w[h], w[h + 2]);
-  return alu_pair(i) ? make_float2(2.f * v.x, 2.f * v.y) : v;
-}
-template <int kPair>
-__device__ __forceinline__ float2 relu2(uint32_t a, uint32_t b) {
-  const float2 x = make_float2(__uint_as_float(a), __uint_as_float(b));
-  if ((kPair & 7) < 2 * MQA_RELU_ALU_CHUNKS) return make_float2(fmaxf(x.x, 0.f), fmaxf(x.y, 0.f));
-  return __fadd2_rn(x, make_float2(fabsf(x.x), fabsf(x.y)));
-}
-template <int G>
-__device__ __forceinline__ void head_group(const uint32_t (&lo)[16], const uint32_t (&hi)[16], const HeadW &W,
-                                           float2 &aA, float2 &aB) {
-#define MQA_HEAD_PAIR(i)                                                      \
-  aA = __ffma2_rn(relu2<8 * G + i>(lo[2 * i], lo[2 * i + 1]), W.w[8 * G + i], aA); \
-  aB = __ffma2_rn(relu2<8 * G + i>(hi[2 * i], hi[2 * i + 1]), W.w[8 * G + i], aB);
-  MQA_HEAD_PAIR(0)
-  MQA_HEAD_PAIR(1)
-  MQA_HEAD_PAIR(2)
-  MQA_HEAD_PAIR(3)
-  MQA_HEAD_PAIR(4)
-  MQA_HEAD_PAIR(5)
-  MQA_HEAD_PAIR(6)
-  MQA_HEAD_PAIR(7)
-#undef MQA_HEAD_PAIR
-}
-// Lanes with bit 1 clear keep key A, the others key B.
-__device__ __forceinline__ float reduce_keys(float2 aA, float2 aB, int lane) {
-  const float pA = aA.x + aA.y, pB = aB.x + aB.y;
-  const bool second = lane & 2;
-  const float s = second ? pA : pB;
-  return (second ? pB : pA) + __shfl_xor_sync(0xFFFFFFFFu, s, 2);
-}
-__device__ __forceinline__ int owned_key(int lane) { return (lane >> 2) + 8 * (lane & 1) + 16 * ((lane >> 1) & 1); }
-__device__ __forceinline__ void score_rows(uint64_t *t_empty, uint32_t base, const HeadW (&W)[kRowsPerWarp],
-                                           float hsc, int lane, float (&out)[kRowsPerWarp]) {
-#pragma unroll
-  for (int rr = 0; rr < kRowsPerWarp; ++rr) {
-    uint32_t lo[kHeadGroups][16], hi[kHeadGroups][16];
-#pragma unroll
-    for (int g = 0; g < kHeadGroups; ++g) {
-      const uint32_t col = (uint32_t)(rr * kHeads + 32 * g);
-      tmem_ld_16x64b_x16(base + col, lo[g]);
-      tmem_ld_16x64b_x16(base + (16u << 16) + col, hi[g]);
-    }
-    tmem_ld_wait();
-    if (rr == kRowsPerWarp - 1) {
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(t_empty);
-    }
-    float2 aA = make_float2(0.f, 0.f), aB = aA;
-    head_group<0>(lo[0], hi[0], W[rr], aA, aB);
-    if constexpr (kHeadGroups > 1) head_group<1>(lo[1], hi[1], W[rr], aA, aB);
-    out[rr] = reduce_keys(aA, aB, lane) * hsc;
-  }
-}
-#else
 struct HeadW {
   float2 w[4 * kHeadGroups];  // weights of this thread's heads of one row, as pairs (doubled for ALU chunks)
 };
@@ -525,8 +451,6 @@ __device__ __forceinline__ void score_rows(uint64_t *t_empty, uint32_t base, con
   }
 }
 #endif  // MQA_HEADS
-
-#endif  // MQA_LD64
 
 #if MQA_FOLD
 // ------------------------------------------------------------------ scoring with the fold
@@ -1854,14 +1778,10 @@ __device__ void epilogue(Smem &S, uint32_t tmem, const FusedParams &p, int warp,
       tau[rr] = kLogits ? NEG_INF : S.tau[r];
       cnt[rr] = 0;
 #pragma unroll
-#if MQA_LD64
-      for (int i = 0; i < 8 * kHeadGroups; ++i) W[rr].w[i] = head_w_pair(J.w[r], i, lane);
-#else
       for (int i = 0; i < 4 * kHeadGroups; ++i) {
         const float2 wv = *reinterpret_cast<const float2 *>(&J.w[r][8 * i + 2 * (lane & 3)]);
         W[rr].w[i] = !kFold && i < MQA_RELU_ALU_CHUNKS ? make_float2(2.f * wv.x, 2.f * wv.y) : wv;
       }
-#endif
     }
     const int ns = J.ns, ns2 = kSamplePasses * J.ns, ntiles = kSamplePasses * J.ns + J.nt, mode = J.mode;
     const int block = J.block;
@@ -3107,27 +3027,52 @@ __device__ void work_slot_rows_pair(Smem &S, const FusedParams &p, int slot, int
 
 
 // A spread merge's rows, claimed one at a time from the block's merge_next
-// and selected by this CTA's 16 epilogue warps together (warp 0 leads); the
-// leader then releases the slot (rows to rescan go to this CTA's queue).
-__device__ void work_slot_rows_group(Smem &S, const FusedParams &p, int slot, int ew, int lane) {
+// and selected by a group of this CTA's epilogue warps together (the group's
+// first warp leads).  With fewer key chunks per block than rows, each chunk's
+// CTA has several rows to select, and two groups of 8 warps take two rows side
+// by side (32 x 8 rows x 64K keys, 4 chunks per block: 153.5 -> 147.4 us);
+// with more chunks than rows all 16 warps take one row (4 x 8 rows x 256K
+// keys, 32 chunks: 106.5 us against 112.5 with two groups).  The CTA's first
+// warp then releases the slot (rows to rescan go to this CTA's queue).
+template <int kGroups>
+__device__ void merge_group_rows(Smem &S, const FusedParams &p, int slot, int ew, int lane) {
+  constexpr int kGroupWarps = kEpiWarps / kGroups;
+  constexpr int kGroupScratch =
+      (kHelperScratchBytes + kGroupWarps * 4 * kScoreBins * (int)sizeof(int) + 127) / 128 * 128;
+  static_assert(kGroups * kGroupScratch <= (int)(sizeof(Smem::kring) + sizeof(Smem::q)),
+                "the groups' scratch fits the idle K ring and q buffers");
   const SelSlot &Q = S.sel[slot];
-  uint8_t *scr = &S.kring[0][0];
+  const int g = ew / kGroupWarps, gm = ew % kGroupWarps;
+  uint8_t *scr = &S.kring[0][0] + (size_t)g * kGroupScratch;
   int *hist = reinterpret_cast<int *>(scr);
   uint32_t *lk = reinterpret_cast<uint32_t *>(scr + 1024);
   int32_t *li = reinterpret_cast<int32_t *>(scr + 1024 + 4 * kSelList);
-  auto sync = [&]() { return !bar_or(kEpiBarrier, kEpiThreads, aborted(S)); };
+  auto sync = [&]() {
+    if (kGroups == 1) return !bar_or(kEpiBarrier, kEpiThreads, aborted(S));
+    return g == 0 ? !bar_or(kEpiBarrier + 1, kGroupWarps * 32, aborted(S))
+                  : !bar_or(kEpiBarrier + 2, kGroupWarps * 32, aborted(S));
+  };
   uint32_t fails = 0;
   for (;;) {
-    if (ew == 0 && lane == 0)
-      *(volatile int *)&S.grp_row = Q.nrows > 0 ? atomicAdd(p.merge_next + Q.bs, 1) : kBlockRows;
+    if (gm == 0 && lane == 0)
+      *(volatile int *)&S.grp_row[g] = Q.nrows > 0 ? atomicAdd(p.merge_next + Q.bs, 1) : kBlockRows;
     if (!sync()) return;
-    const int r = *(volatile int *)&S.grp_row;
+    const int r = *(volatile int *)&S.grp_row[g];
     if (r >= kBlockRows) break;
     bool ok = true;
-    const bool fail = select_row_multi<kEpiWarps>(S, p, slot, r, sync, ew, hist, lk, li, lane, ok);
+    const bool fail = select_row_multi<kGroupWarps>(S, p, slot, r, sync, gm, hist, lk, li, lane, ok);
     if (!ok) return;
     if (fail) fails |= 1u << r;
-    if (ew == 0 && lane == 0 && r < Q.nrows && ((Q.mask >> r) & 1u)) atomicAdd(p.ws + kWsPairRows, 1);
+    if (gm == 0 && lane == 0 && r < Q.nrows && ((Q.mask >> r) & 1u)) atomicAdd(p.ws + kWsPairRows, 1);
+  }
+  if constexpr (kGroups > 1) {
+    // both groups are done with the slot before it is released
+    if (gm == 0 && lane == 0 && fails) atomicOr(&S.grp_fails, fails);
+    if (bar_or(kEpiBarrier, kEpiThreads, aborted(S))) return;
+    if (ew == 0 && lane == 0) {
+      fails = *(volatile unsigned *)&S.grp_fails;
+      S.grp_fails = 0;
+    }
   }
   if (ew == 0 && lane == 0) {
     if (fails) {
@@ -3142,6 +3087,10 @@ __device__ void work_slot_rows_group(Smem &S, const FusedParams &p, int slot, in
     atomicAdd(&S.retired, 1);
     mbar_arrive(&S.s_empty[slot]);
   }
+}
+__device__ void work_slot_rows_group(Smem &S, const FusedParams &p, int slot, int ew, int lane) {
+  if (S.nchunks < kBlockRows) merge_group_rows<2>(S, p, slot, ew, lane);
+  else merge_group_rows<1>(S, p, slot, ew, lane);
 }
 
 #endif
@@ -3202,6 +3151,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     S.fifo_head = 0;
     S.fifo_tail = 0;
     S.retired = 0;
+    S.grp_fails = 0;
     S.nsplit = 0;
     S.nchunks = 1;
     S.prod_parked = 0;
