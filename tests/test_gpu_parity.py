@@ -189,6 +189,25 @@ def test_fused_key_split_overflow_rescans(mqa):
     assert_parity(p, got)
 
 
+@pytest.mark.parametrize("force_gate", [0, 1])
+def test_fused_spread_merge_two_groups(mqa, force_gate):
+    """Four row blocks on 16 CTAs: every block is cut into 4 key chunks, fewer
+    than its 8 rows, so each chunk's CTA merges its rows with two groups of 8
+    epilogue warps side by side.  With the gate forced to +inf every row
+    under-fills, and the rows the groups fail go to the exact rescan.  Either
+    way the result must be the exact top-k."""
+    p = _causal(synth.random_small(30, 32, 40000, 512, empty_frac=0.0), 40000)
+    got, status, stats = run_fused(mqa, p, debug={"force_gate": force_gate, "max_ctas": 16})
+    assert status == 0, stats
+    assert stats["split_blocks"] == 4, stats
+    assert stats["pair_rows"] >= 32, stats
+    if force_gate:
+        assert stats["rows_rescanned"] == 32, stats
+    else:
+        assert stats["gated_rows"] == 32 and stats["rows_rescanned"] == 0, stats
+    assert_parity(p, got)
+
+
 @pytest.mark.parametrize("seed,rows,keys,topk", [(40, 3, 700, 512), (41, 13, 5000, 1024), (42, 37, 20000, 2048)])
 def test_fused_64_heads_random_ranges(mqa, seed, rows, keys, topk):
     """64 index heads per row (4-row blocks): arbitrary ranges, exact top-k."""
