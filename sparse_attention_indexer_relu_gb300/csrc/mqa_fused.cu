@@ -172,7 +172,8 @@ struct Smem {
   SelSlot sel[2];
   float tau[kBlockRows];
   int segcnt[kBlockRows][kQuads];
-  int nsplit, nchunks;  // key-range split plan: the last nsplit blocks of the order, nchunks chunks each
+  int nsplit, nchunks;  // key-range split plan: nsplit blocks of the order, nchunks chunks each
+  int split_first;      // the split blocks are the first nsplit of the order (else the last)
   uint32_t ref[kBlockRows];
   int ref_frozen[kBlockRows];  // two-pass sample: the reference is taken from the first tile
   int msample[kBlockRows];
@@ -1198,21 +1199,29 @@ __device__ MQA_SEL_FN int warp_select_binned(const RowSlab &R, int k, float lo, 
 // before it as well measured no faster and doubled the split's workspace).  Costs
 // are counted in units of the lightest block's scan; each chunk also scores
 // the block's whole sample again (fraction sfrac of a block).
-__device__ void plan_split(Smem &S, const FusedParams &p, long long w_light) {
+// Sample tiles of a block whose rows see `L` keys on average (as the producer
+// plans them), times the passes that score them.
+__device__ long long plan_sample_tiles(const FusedParams &p, long long L) {
+  const long long items = kBlocks ? L / 8 : L;
+  const long long nt = (L + kTileKeys - 1) / kTileKeys;
+  if (items <= p.gate_min) return 0;
+  long long want = (32LL * L + (long long)p.gate_target * kTileKeys - 1) / ((long long)p.gate_target * kTileKeys);
+  want = want < 4 ? 4 : (want > 64 ? 64 : want);
+  if (MQA_SAMPLE_ONCE && want > p.cap / 64) want = p.cap / 64;
+  return (long long)kSamplePasses * (want < nt ? want : nt);
+}
+
+// `key` holds the blocks' weights (visible keys summed over the block's rows,
+// in the high 32 bits) in heaviest-first order.
+__device__ void plan_split(Smem &S, const FusedParams &p, const uint64_t *key) {
   const int nb = p.nblocks, ctas = gridDim.x;
+  const long long w_light = (long long)(key[nb - 1] >> 32);
   const int cand = nb < ctas ? nb : nb % ctas;
   if (cand == 0 || cand > p.split_max) return;
   const long long L = w_light / kBlockRows;  // mean visible keys per row of the lightest block
-  const long long items = kBlocks ? L / 8 : L;  // and the items it selects from
   const long long nt = (L + kTileKeys - 1) / kTileKeys;
   if (nt < 8) return;  // too short to be worth a second sample pass
-  float sfrac = 0.f;
-  if (items > p.gate_min) {
-    long long want = (32LL * L + (long long)p.gate_target * kTileKeys - 1) / ((long long)p.gate_target * kTileKeys);
-    want = want < 4 ? 4 : (want > 64 ? 64 : want);
-    if (MQA_SAMPLE_ONCE && want > p.cap / 64) want = p.cap / 64;
-    sfrac = (float)kSamplePasses * (float)(want < nt ? want : nt) / (float)nt;
-  }
+  const float sfrac = (float)plan_sample_tiles(p, L) / (float)nt;
   const float base = (float)((cand + ctas - 1) / ctas);
   float best = 0.97f * base;
   int best_c = 1;
@@ -1228,6 +1237,48 @@ __device__ void plan_split(Smem &S, const FusedParams &p, long long w_light) {
   if (best_c > 1) {
     S.nsplit = cand;
     S.nchunks = best_c;
+  }
+  if (nb >= ctas) return;
+  // Fewer blocks than CTAs, of different lengths (a mixed decode batch): the
+  // time is the heaviest block's.  Splitting only the heaviest blocks, into
+  // more chunks, can shorten it where one chunk count for every block cannot
+  // (the lightest block limits it).  Tiles of the i-th heaviest block, and
+  // the one-wave time of a plan, in tiles:
+  // (divisions by constants and float arithmetic only: thread 0 runs this
+  // while the CTA waits)
+  auto tiles = [&](int i) -> float {
+    return (float)(((key[i] >> 32) / (uint64_t)kBlockRows + kTileKeys - 1) / (uint64_t)kTileKeys);
+  };
+  const float gt = (float)p.gate_target;
+  auto samp = [&](int i) -> float {
+    const float Li = (float)((key[i] >> 32) / (uint64_t)kBlockRows);
+    if (Li <= (float)p.gate_min) return 0.f;
+    const float want = fminf(fmaxf(ceilf(Li / (4.f * gt)), 4.f), MQA_SAMPLE_ONCE ? fminf(64.f, (float)(p.cap / 64)) : 64.f);
+    return (float)kSamplePasses * fminf(want, ceilf(Li / (float)kTileKeys));
+  };
+  const float t0 = tiles(0), s0 = samp(0);
+  if (t0 < 1.25f * tiles(nb - 1)) return;  // lengths near uniform: the uniform plan is as good
+  const float uniform = best_c > 1 ? base * (t0 / best_c + s0) : t0 + s0;  // base = 1 wave here
+  float best_first = 0.9f * uniform;
+  int bf_n = 0, bf_c = 1;
+  for (int c = 2; c <= kMaxChunks; c *= 2) {
+    for (int ns = 1; ns < nb; ++ns) {
+      if (nb - ns + ns * c > ctas) break;
+      if ((long long)ns * 2 * kBlockRows * split_row_capacity(p.cap, c) > p.split_words) break;
+      if (tiles(ns - 1) / c < 4.f) break;
+      const float rest = tiles(ns) + samp(ns);
+      const float t = fmaxf(t0 / c + s0, rest);
+      if (t < best_first) {
+        best_first = t;
+        bf_n = ns;
+        bf_c = c;
+      }
+    }
+  }
+  if (bf_n > 0) {
+    S.nsplit = bf_n;
+    S.nchunks = bf_c;
+    S.split_first = 1;
   }
 }
 
@@ -1267,7 +1318,7 @@ __device__ void build_order(Smem &S, const FusedParams &p) {
     }
   }
   for (int b = threadIdx.x; b < nb; b += blockDim.x) S.order[b] = (uint16_t)(0xFFFFFFFFu - (uint32_t)key[b]);
-  if (threadIdx.x == 0 && p.split_max > 0) plan_split(S, p, (long long)(key[nb - 1] >> 32));
+  if (threadIdx.x == 0 && p.split_max > 0) plan_split(S, p, key);
   __syncthreads();
 }
 
@@ -1298,6 +1349,7 @@ __device__ void producer(Smem &S, const CUtensorMap *q_map, const CUtensorMap *k
   const uint64_t pol_k = policy_evict_last(), pol_q = policy_evict_first();
   // claim order: whole blocks, then nsplit blocks as nchunks consecutive key chunks each
   const int nsplit = kLogits ? 0 : S.nsplit, nchunks = kLogits ? 1 : S.nchunks;
+  const bool split_first = !kLogits && S.split_first;
   const int nwhole = p.nblocks - nsplit;
   const int total_jobs = kLogits ? p.nblocks * p.key_chunks : nwhole + nsplit * nchunks;
   const int ktiles_all = (p.keys + kTileKeys - 1) / kTileKeys;
@@ -1339,7 +1391,15 @@ __device__ void producer(Smem &S, const CUtensorMap *q_map, const CUtensorMap *k
             chunk = i % p.key_chunks;
           } else {
             int oi = i;
-            if (i >= nwhole) {  // a key chunk of a split block
+            if (split_first) {  // the heaviest blocks' key chunks first, then the whole blocks
+              if (i < nsplit * nchunks) {
+                bs = i / nchunks;
+                kchunk = i % nchunks;
+                oi = bs;
+              } else {
+                oi = nsplit + (i - nsplit * nchunks);
+              }
+            } else if (i >= nwhole) {  // a key chunk of a split block
               bs = (i - nwhole) / nchunks;
               kchunk = (i - nwhole) % nchunks;
               oi = nwhole + bs;
@@ -3153,6 +3213,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     S.retired = 0;
     S.grp_fails = 0;
     S.nsplit = 0;
+    S.split_first = 0;
     S.nchunks = 1;
     S.prod_parked = 0;
     // fold: the per-call preparation wrote the keys' largest scale * |k|_2

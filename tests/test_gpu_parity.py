@@ -208,6 +208,21 @@ def test_fused_spread_merge_two_groups(mqa, force_gate):
     assert_parity(p, got)
 
 
+@pytest.mark.parametrize("max_ctas", [0, 16])
+def test_fused_split_heaviest_blocks_first(mqa, max_ctas):
+    """Eight requests of 8 rows with 64K, 8K and 4K keys: fewer blocks than
+    CTAs and of very different lengths, so only the heaviest blocks are cut
+    into key chunks (6 blocks x 16 chunks on every SM, 2 x 4 on 16 CTAs), and
+    their chunks are claimed before the whole blocks.  Exact top-k."""
+    p = synth.make_multi("split_first", (65536, 65536, 8192, 8192, 8192, 8192, 4096, 4096), (8,) * 8, 512, seed=3)
+    debug = {"max_ctas": max_ctas} if max_ctas else None
+    got, status, stats = run_fused(mqa, p, debug=debug)
+    assert status == 0, stats
+    assert 0 < stats["split_blocks"] < 8, stats
+    assert stats["rows_rescanned"] == 0, stats
+    assert_parity(p, got)
+
+
 @pytest.mark.parametrize("seed,rows,keys,topk", [(40, 3, 700, 512), (41, 13, 5000, 1024), (42, 37, 20000, 2048)])
 def test_fused_64_heads_random_ranges(mqa, seed, rows, keys, topk):
     """64 index heads per row (4-row blocks): arbitrary ranges, exact top-k."""
