@@ -35,6 +35,19 @@ def assert_parity(p, got, rows=None):
     assert not bad, bad[:10]
 
 
+# ---------------------------------------------------------------- workspace
+def test_workspace_bytes_for_a_16k_row_chunk(mqa):
+    """The fixed workspace of a 16,384-row chunk: per-SM slab slots plus the
+    key-range split's slab.  On a 152-SM GB300 it stays within 330 MB."""
+    import ctypes
+    import torch
+    n = ctypes.c_size_t(0)
+    assert mqa.lib().mqa_topk_workspace_bytes(0, 16384, ctypes.byref(n)) == 0
+    assert n.value > 0
+    if torch.cuda.get_device_properties(0).multi_processor_count == 152:
+        assert n.value <= 330 * 10 ** 6, n.value
+
+
 # ---------------------------------------------------------------- UE8M0 decode
 @pytest.mark.parametrize("keys", [1, 3, 256, 1001, 65536 + 5])
 def test_ue8m0_decode_bit_exact(mqa, keys):
