@@ -124,7 +124,7 @@ struct JobInfo {
   int block;      // row block (-1: no more work)
   int mode;       // 0 gated scan, 1 exact rescan
   int lo_t, nt;   // main tiles [lo_t, lo_t + nt)
-  int ns;         // sample tiles; scored twice (coarse, then fine gate pass) before the main tiles
+  int ns;         // sample tiles, scored before the main tiles (once, or twice: coarse, then fine gate pass)
   uint32_t mask;  // rows taking part
   int nrows;      // valid rows in the block
   int chunk;      // key chunk of a split block (-1: the whole block)
