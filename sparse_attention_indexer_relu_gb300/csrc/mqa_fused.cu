@@ -1252,7 +1252,7 @@ __device__ void plan_split(Smem &S, const FusedParams &p, const uint64_t *key) {
   const float gt = (float)p.gate_target;
   auto samp = [&](int i) -> float {
     const float Li = (float)((key[i] >> 32) / (uint64_t)kBlockRows);
-    if (Li <= (float)p.gate_min) return 0.f;
+    if ((kBlocks ? Li / 8.f : Li) <= (float)p.gate_min) return 0.f;
     const float want = fminf(fmaxf(ceilf(Li / (4.f * gt)), 4.f), MQA_SAMPLE_ONCE ? fminf(64.f, (float)(p.cap / 64)) : 64.f);
     return (float)kSamplePasses * fminf(want, ceilf(Li / (float)kTileKeys));
   };
@@ -1262,9 +1262,10 @@ __device__ void plan_split(Smem &S, const FusedParams &p, const uint64_t *key) {
   float best_first = 0.9f * uniform;
   int bf_n = 0, bf_c = 1;
   for (int c = 2; c <= kMaxChunks; c *= 2) {
+    const long long row_words = 2LL * kBlockRows * split_row_capacity(p.cap, c);
     for (int ns = 1; ns < nb; ++ns) {
       if (nb - ns + ns * c > ctas) break;
-      if ((long long)ns * 2 * kBlockRows * split_row_capacity(p.cap, c) > p.split_words) break;
+      if ((long long)ns * row_words > p.split_words) break;
       if (tiles(ns - 1) / c < 4.f) break;
       const float rest = tiles(ns) + samp(ns);
       const float t = fmaxf(t0 / c + s0, rest);
